@@ -1,0 +1,82 @@
+"""Work accounting for the decoder block: parameters, FLOPs and bytes.
+
+Conventions (each one is pinned by ``tests/test_accounting.py`` against the
+numbers the pages print):
+
+* One multiply-add is 2 FLOPs, so a weight matrix costs 2 FLOPs per parameter
+  per token ("Transformer block" page, "How it works", FLOPs paragraph;
+  "The Transformer" GenerativeAIDocs section 4).  The "Transformer
+  Architecture" page counts a multiply-add as one FLOP; that convention is not
+  used.
+* Attention costs 2·T·d for q·kᵀ and 2·T·d for the weighted sum of v per token
+  when the full T×T matrix is counted; a causal kernel that skips masked work
+  does about half ("Transformer block" page, FLOPs paragraph).  Here the causal
+  count is exact: query i meets i+1 keys.
+* KV-cache bytes per token are 2·L·Hkv·dh·bytes ("Transformer block" page,
+  KV-cache paragraph; "09 The Transformer", "Counting everything").
+"""
+from __future__ import annotations
+
+from typing import Iterable
+
+
+def block_matrix_params(d: int, H: int, Hkv: int, dh: int, f: int) -> int:
+    """Parameters of the block's weight matrices: Wq, Wk, Wv, Wo, W1, W3, W2."""
+    return d * (H + 2 * Hkv) * dh + H * dh * d + 3 * d * f
+
+
+def block_params(d: int, H: int, Hkv: int, dh: int, f: int) -> int:
+    """All parameters of one block, the two RMSNorm gain vectors included."""
+    return block_matrix_params(d, H, Hkv, dh, f) + 2 * d
+
+
+def gemm_flops(d: int, H: int, Hkv: int, dh: int, f: int, tokens: int) -> int:
+    """FLOPs of the block's projections for ``tokens`` tokens: 2 per parameter."""
+    return 2 * block_matrix_params(d, H, Hkv, dh, f) * tokens
+
+
+def gemm_flops_each(d: int, H: int, Hkv: int, dh: int, f: int, tokens: int) -> dict:
+    """FLOPs of each GEMM of the block (QKV, Wo, W1/W3, W2)."""
+    return {
+        "qkv": 2 * tokens * d * (H + 2 * Hkv) * dh,
+        "wo": 2 * tokens * H * dh * d,
+        "w13": 2 * tokens * d * 2 * f,
+        "w2": 2 * tokens * f * d,
+    }
+
+
+def causal_attn_flops(B: int, H: int, dh: int, T: int) -> int:
+    """Exact causal attention FLOPs of a prefill: 4·dh per (query head, visible
+    pair), T(T+1)/2 visible pairs per head and sequence."""
+    return 4 * B * H * dh * (T * (T + 1) // 2)
+
+
+def full_attn_flops(B: int, H: int, dh: int, T: int) -> int:
+    """Attention FLOPs counting the whole T×T square (the pages' 4·T·d per token)."""
+    return 4 * B * H * dh * T * T
+
+
+def decode_attn_flops(H: int, dh: int, keys: Iterable[int]) -> int:
+    """Decode attention FLOPs: each query head meets every attended key once."""
+    return 4 * H * dh * sum(int(k) for k in keys)
+
+
+def kv_bytes_per_token(L: int, Hkv: int, dh: int, bytes_per_value: int) -> int:
+    """KV-cache bytes per token: K and V, every layer, Hkv heads of dh values."""
+    return 2 * L * Hkv * dh * bytes_per_value
+
+
+def decode_kv_bytes(lens: Iterable[int], Hkv: int, dh: int, bytes_per_value: int) -> int:
+    """KV bytes one decode step must read: lens[b] cached rows plus the appended
+    one, for K and V, per sequence."""
+    return sum(int(n) + 1 for n in lens) * kv_bytes_per_token(1, Hkv, dh, bytes_per_value)
+
+
+def weight_bytes(d: int, H: int, Hkv: int, dh: int, f: int, bytes_per_value: int) -> int:
+    """Bytes of the block's weight matrices (what a decode step must stream)."""
+    return block_matrix_params(d, H, Hkv, dh, f) * bytes_per_value
+
+
+def forward_flops_per_token(N: int, L: int, T: int, d: int) -> int:
+    """The pages' rule 2N + 4·L·T·d forward FLOPs per token (full square)."""
+    return 2 * N + 4 * L * T * d

@@ -1,0 +1,17 @@
+"""fp64 CPU oracle of the Llama-layout pre-norm decoder block.
+
+TEST INFRASTRUCTURE, not part of the product.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import
+it.  It shares no code with the CUDA library and never imports it.
+
+Every function is pinned by ``tests/test_oracle_pins.py`` against what the
+pages and the mathematics fix (closed forms, invariants, a library
+cross-check, brute force on tiny inputs); none is "parity unpinned".
+"""
+from .block import (Cfg, rms_norm, rope_angles, rope, silu, softmax_rows, causal_attention,
+                    qkv_heads, mlp_branch, block_prefill_seq, block_prefill, block_decode_seq,
+                    block_decode)
+
+__all__ = ["Cfg", "rms_norm", "rope_angles", "rope", "silu", "softmax_rows", "causal_attention",
+           "qkv_heads", "mlp_branch", "block_prefill_seq", "block_prefill", "block_decode_seq",
+           "block_decode"]
