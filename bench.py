@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the decoder block: prefill tokens/s with attention and GEMM
+TFLOP/s, and decode KV-cache GB/s, on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tb|reference]
+
+One step is one full prefill of the block (RMSNorm, QKV + RoPE, causal GQA
+attention, Wo + residual, RMSNorm, SwiGLU, W2 + residual) over one batch of the
+prefill workload (default gqa_8k: B=4, T=8192, d=4096, H=32, Hkv=8, dh=128,
+f=14336).  The decode workload (gqa_decode: 32 sequences, cache lengths
+uniform in [1024, 16383]) is timed after it and reported under "decode".
+
+Inputs are seeded synthetic tensors resident in HBM before timing; each one is
+larger than L2 (x 268 MB, weights 436 MB, decode KV 1.1 GB), so no L2 flush is
+needed between steps.  Device time comes from CUDA events on the launching
+stream; per-kernel times from the library's stage trace (events recorded
+between launches on the same stream).  Under torchrun every rank runs its own
+replica (the block has no exchange step) and the slowest rank's time counts.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores (the only reference that exists for this path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        mx = max(num(r[2]) for r in rows)
+        power = [num(r[3]) for r in rows]
+        pmax = max(power)
+        loaded = [c for c, p in zip(sm, power) if p >= 0.5 * pmax] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": pmax}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline field)
+# ---------------------------------------------------------------------------
+
+def time_oracle_prefill(s, tokens: int, seed: int = 0):
+    """The fp64 oracle on the first `tokens` tokens of sequence 0 of the
+    workload (a causal prefix is a complete prefill of its own).  Returns
+    (seconds, tokens)."""
+    import oracle
+    import workloads
+    inp = workloads.make_block_inputs(s.with_(B=1), seed=seed, x_tokens=tokens)
+    w = {n: workloads.to_f64(inp[n]) for n in workloads.WEIGHT_NAMES}
+    cfg = oracle.Cfg(s.d, s.H, s.Hkv, s.dh, s.f, s.rope_base, s.eps)
+    x = workloads.to_f64(inp["x"][0])
+    t0 = time.perf_counter()
+    oracle.block_prefill_seq(x, w, cfg)
+    return time.perf_counter() - t0, tokens
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    import workloads
+    if rank != 0:
+        return
+    s = workloads.CONFIGS[args.workload]
+    tokens = args.ref_tokens
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, _ = time_oracle_prefill(s, tokens)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = tokens * len(times) / total
+    sample = f"fp64 oracle prefill of the first {tokens} tokens of one sequence of {s.name}, per step"
+    line = {
+        "impl": "reference", "metric": "prefill tokens/s per block", "value": value, "unit": "tok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(s),
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def workload_config(s):
+    return {"workload": s.name, "B": s.B, "T": s.T, "d": s.d, "H": s.H, "Hkv": s.Hkv, "dh": s.dh, "f": s.f,
+            "rope_base": s.rope_base, "eps": s.eps, "storage": s.dtype, "accumulate": "f32",
+            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def stage_stats(traces):
+    """Mean ms of each stage over the traced calls."""
+    acc = {}
+    for tr in traces:
+        for name, ms in tr:
+            acc.setdefault(name, []).append(ms)
+    return {k: sum(v) / len(v) for k, v in acc.items()}
+
+
+def prefill_stage_work(s):
+    from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
+    M = s.B * s.T
+    g = acc.gemm_flops_each(s.d, s.H, s.Hkv, s.dh, s.f, M)
+    return {
+        "qkv": ("tensor", g["qkv"]), "attn": ("tensor", acc.causal_attn_flops(s.B, s.H, s.dh, s.T)),
+        "wo": ("tensor", g["wo"]), "w13": ("tensor", g["w13"]), "w2": ("tensor", g["w2"]),
+        "rms": ("hbm", M * s.d * 2 + M * 8),
+    }
+
+
+def bench_prefill(args, s, world, peaks):
+    import torch
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    from causal_gqa_attention_rmsnorm_gb300 import binding
+    import workloads
+
+    inp = workloads.make_block_inputs(s, seed=0)
+    dev = {n: t.cuda() for n, t in inp.items()}
+    cfg = tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, s.T, s.rope_base, s.eps, tb.TB_BF16)
+    packed = tb.tb_pack_weights(cfg, dev)
+    x = dev["x"]
+    y = torch.empty((s.B, s.T, s.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tb.tb_workspace_bytes(cfg, s.B, s.T, 0), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tb.tb_block_prefill(cfg, packed, x, y=y, ws=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert tb.tb_get_device_error(clear=True) == 0
+
+    binding.tbx_trace_enable(args.steps)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    traces = [binding.tbx_trace_read(i) for i in range(args.steps)]
+    binding.tbx_trace_enable(0)
+    assert tb.tb_get_device_error(clear=True) == 0
+    assert torch.isfinite(y).all().item()
+    ms_total = max_over_ranks(ms_total, world)
+    stages = stage_stats(traces)
+
+    # end to end through the public call with host buffers: pinned x in, y out
+    e2e = None
+    if not args.no_e2e:
+        xh = inp["x"].pin_memory()
+        yh = torch.empty((s.B, s.T, s.d), dtype=torch.float32).pin_memory()
+        for _ in range(2):
+            x.copy_(xh, non_blocking=True)
+            step()
+            yh.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            x.copy_(xh, non_blocking=True)
+            step()
+            yh.copy_(y, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world)
+        e2e = {"value": world * s.B * s.T * args.steps / (e2e_ms * 1e-3), "unit": "tok/s",
+               "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+               "d2h_bytes_per_step": yh.numel() * yh.element_size(), "ms_per_step": e2e_ms / args.steps}
+    del ws
+    return {"ms_total": ms_total, "stages": stages, "clocks": clk, "e2e": e2e, "launches_per_step": 6}
+
+
+def roofline_entry(stages, work, peaks, peak_src):
+    name = max(stages, key=lambda k: stages[k])
+    bound, amount = work[name]
+    ms = stages[name]
+    if bound == "tensor":
+        achieved = amount / (ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+    else:
+        achieved = amount / (ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    return {"kernel": name, "bound": "tensor" if bound == "tensor" else "hbm", "achieved": achieved, "peak": peak,
+            "unit": unit, "frac": achieved / peak, "traffic": None, "ms": ms,
+            "peak_source": f"{peak_src} ({'bf16 sustained' if bound == 'tensor' else 'hbm copy'})"}
+
+
+def bench_decode(args, world, peaks):
+    import torch
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
+    from causal_gqa_attention_rmsnorm_gb300 import binding
+    import workloads
+
+    s = workloads.CONFIGS[args.decode_workload]
+    inp = workloads.make_block_inputs(s, seed=0)
+    dev = {n: t.cuda() for n, t in inp.items()}
+    lens = workloads.make_lens(s, seed=0)
+    kc, vc = workloads.make_decode_cache(s, 0, lens, fill=0.0, device="cuda")
+    lens0 = lens.cuda()
+    kv = tb.KVCache(kc, vc, lens0.clone())
+    cfg = tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, s.T, s.rope_base, s.eps, tb.TB_BF16)
+    packed = tb.tb_pack_weights(cfg, dev)
+    y = torch.empty((s.B, 1, s.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tb.tb_workspace_bytes(cfg, s.B, s.T, 1), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kv.lens.copy_(lens0, non_blocking=True)      # every step decodes at the same positions
+        tb.tb_block_decode(cfg, packed, dev["x"], kv, y=y, ws=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert tb.tb_get_device_error(clear=True) == 0
+    n = max(args.steps, 20)
+    binding.tbx_trace_enable(n)
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world) / n
+    stages = stage_stats([binding.tbx_trace_read(i) for i in range(n)])
+    binding.tbx_trace_enable(0)
+    assert torch.isfinite(y).all().item()
+    kv_bytes = acc.decode_kv_bytes(lens.tolist(), s.Hkv, s.dh, 2)
+    w_bytes = acc.weight_bytes(s.d, s.H, s.Hkv, s.dh, s.f, 2)
+    attn_ms = stages["attn"]
+    kv_gbs = kv_bytes / (attn_ms * 1e-3) / 1e9
+    return {
+        "workload": s.name, "B": s.B, "T_max": s.T, "kv_bytes": kv_bytes, "weight_bytes": w_bytes,
+        "kv_gbs": kv_gbs, "kv_frac_hbm": kv_gbs / peaks["hbm_gbs"], "attn_ms": attn_ms, "step_ms": ms,
+        "tok_s": world * s.B / (ms * 1e-3), "stages_ms": stages, "gpu_launches": 7 * n,
+        "step_hbm_gbs": (kv_bytes + w_bytes) / (ms * 1e-3) / 1e9,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["tb", "reference"], default="tb")
+    ap.add_argument("--workload", default="gqa_8k")
+    ap.add_argument("--decode-workload", default="gqa_decode")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
+    ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample size for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import workloads
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    peaks, peak_src = load_peaks()
+    s = workloads.CONFIGS[args.workload]
+
+    pre = bench_prefill(args, s, world, peaks)
+    dec = None if args.no_decode else bench_decode(args, world, peaks)
+
+    from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
+    tokens = s.B * s.T
+    ms_step = pre["ms_total"] / args.steps
+    value = world * tokens * args.steps / (pre["ms_total"] * 1e-3)
+    work = prefill_stage_work(s)
+    stages = pre["stages"]
+    attn_tflops = work["attn"][1] / (stages["attn"] * 1e-3) / 1e12
+    gemm_ms = sum(stages[k] for k in ("qkv", "wo", "w13", "w2"))
+    gemm_tflops = sum(work[k][1] for k in ("qkv", "wo", "w13", "w2")) / (gemm_ms * 1e-3) / 1e12
+    line = {
+        "metric": "prefill tokens/s per block (attention TFLOP/s, GEMM TFLOP/s; decode KV GB/s)",
+        "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(1,0.1) gains)",
+        "config": workload_config(s),
+        "attn_tflops": attn_tflops, "attn_frac_bf16": attn_tflops / peaks["bf16_tflops_sustained"],
+        "gemm_tflops": gemm_tflops, "gemm_frac_bf16": gemm_tflops / peaks["bf16_tflops_sustained"],
+        "stages_ms": stages,
+        "stage_tflops": {k: work[k][1] / (stages[k] * 1e-3) / 1e12 for k in stages if work.get(k, ("", 0))[0] == "tensor"},
+        "roofline": roofline_entry(stages, work, peaks, peak_src),
+        "gpu_launches": pre["launches_per_step"] * args.steps,
+        "clocks": pre["clocks"],
+        "e2e": pre["e2e"],
+        "decode": dec,
+        "peaks": {"source": peak_src, "bf16_tflops": peaks["bf16_tflops"],
+                  "bf16_tflops_sustained": peaks["bf16_tflops_sustained"], "hbm_gbs": peaks["hbm_gbs"]},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, n = time_oracle_prefill(s, args.cpu_tokens)
+        line["cpu_baseline"] = {
+            "value": n / dt, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 oracle prefill of the first {n} tokens of one sequence of {s.name} "
+                      f"({dt:.1f} s; a causal prefix has less attention work per token than T={s.T})"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,128 @@
+// Shared device helpers and the internal launcher interface of libtb.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tb.h"
+
+namespace tb {
+
+using bf16 = __nv_bfloat16;
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<bf16>(bf16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// 16-byte vector of T: 4 floats or 8 bf16.
+template <typename T> struct Vec16 {
+  static constexpr int N = 16 / sizeof(T);
+  uint4 raw;
+  __device__ __forceinline__ float get(int i) const {
+    if constexpr (sizeof(T) == 4) {
+      return __uint_as_float((&raw.x)[i]);
+    } else {
+      uint32_t w = (&raw.x)[i >> 1];
+      return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
+    }
+  }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// Everything a launcher needs to know about one block call.
+struct Dims {
+  int d, H, Hkv, dh, f;
+  float eps;
+  int max_pos;
+};
+
+// Views into the packed weight blob (device pointers).
+struct Packed {
+  const void* wqkv;   // [(H+2Hkv)·dh, d]  gain-folded, transposed
+  const void* wo;     // [d, H·dh]
+  const void* w13;    // [2f, d]           gain-folded, rows 2j = W1[:,j], 2j+1 = W3[:,j]
+  const void* w2;     // [d, f]
+  const float2* rope; // [max_pos, dh/2]   (cos, sin)
+};
+
+}  // namespace tb
+
+// ---------------------------------------------------------------------------
+// Launchers (host functions, one translation unit each group).  All return a
+// cudaError_t from cudaGetLastError after their launches.
+// ---------------------------------------------------------------------------
+namespace tb {
+
+// tb_api.cu: device address of the per-device error word (TB_DEVERR_* bits)
+int* device_error_word();
+
+// elementwise.cu
+cudaError_t launch_pack(int dtype, const Dims& D, const tb_block_weights& w, void* packed,
+                        const Packed& P, float rope_base, cudaStream_t s);
+cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, float* r,
+                             float* ssq_zero, int T, int32_t* lens_set, int32_t* lens_bump,
+                             int32_t* pos_out, int T_max, int* err, cudaStream_t s);
+cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new,
+                             int n, int* err, cudaStream_t s);
+
+// GEMM epilogue argument bundles.
+struct QKVArgs {
+  const float* r;          // [M] RMSNorm-1 inverse RMS of each token
+  const float2* rope;      // [max_pos, dh/2]
+  void* q;                 // [B, H, Tq, dh]
+  void* k;                 // [B, Hkv, kv_stride, dh]
+  void* v;
+  int T;                   // tokens per sequence (1 for decode)
+  int kv_stride;           // rows per (b, kv head) in k/v
+  const int32_t* pos;      // decode: position of sequence b (-1: skip); prefill: nullptr
+};
+struct WoArgs {
+  const void* x;           // [M, d] residual input (cfg dtype)
+  float* h;                // [M, d] fp32 residual stream after attention
+  void* hb;                // [M, d] cfg dtype copy of h (A operand of W1/W3), may be == h for f32
+  float* ssq;              // [M] Σ h² (accumulated)
+};
+struct W13Args {
+  const float* ssq;        // [M] Σ h²
+  void* a;                 // [M, f] SiLU(gate)·up
+};
+struct W2Args {
+  const float* h;          // [M, d]
+  void* y;                 // [M, d]
+  int y_dtype;
+};
+
+// gemm_simt.cu (fp32 path)
+cudaError_t gemm_simt_qkv(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
+                          const QKVArgs& e, cudaStream_t s);
+cudaError_t gemm_simt_wo(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
+                         const WoArgs& e, cudaStream_t s);
+cudaError_t gemm_simt_w13(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
+                          const W13Args& e, cudaStream_t s);
+cudaError_t gemm_simt_w2(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
+                         const W2Args& e, cudaStream_t s);
+
+// attn_simt.cu (fp32 path)
+cudaError_t attn_prefill_simt(int dtype, const void* q, const void* k, const void* v, void* o, int B,
+                              int T, int H, int Hkv, int dh, int kv_stride, cudaStream_t s);
+
+// attn_decode.cu
+int decode_chunk_keys();
+size_t decode_part_floats(int B, int H, int dh, int nchunk_max);
+cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos,
+                        int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max,
+                        void* o, cudaStream_t s);
+
+}  // namespace tb

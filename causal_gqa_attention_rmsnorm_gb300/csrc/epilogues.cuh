@@ -1,0 +1,141 @@
+// GEMM epilogues of the block, shared by the fp32 SIMT GEMM and the bf16
+// tcgen05 GEMM.  Each functor receives 4 consecutive output columns
+// [col, col+4) of one row with col % 4 == 0, in fp32, and returns a value the
+// caller sums over the row's columns when kRowReduce is set.
+//
+// Steps ("Transformer block" page, tirogla.com, "How it works" step 2-3):
+//   QKV  : × r (RMSNorm-1 row scale), RoPE on q and k, scatter q / k / v
+//   Wo   : h = x + o·Wo  (first residual add), Σ h² for RMSNorm-2
+//   W1W3 : a = SiLU(r2·gate) ⊙ (r2·up)  (columns come interleaved gate, up)
+//   W2   : y = h + a·W2 (second residual add)
+#pragma once
+
+#include "common.cuh"
+
+namespace tb {
+
+template <typename T> __device__ __forceinline__ void store4(T* p, const float v[4]);
+template <> __device__ __forceinline__ void store4<float>(float* p, const float v[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <> __device__ __forceinline__ void store4<bf16>(bf16* p, const float v[4]) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+template <typename T> __device__ __forceinline__ void load4(const T* p, float v[4]);
+template <> __device__ __forceinline__ void load4<float>(const float* p, float v[4]) {
+  const float4 f = *reinterpret_cast<const float4*>(p);
+  v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+}
+template <> __device__ __forceinline__ void load4<bf16>(const bf16* p, float v[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+  v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+template <typename T> __device__ __forceinline__ void store2(T* p, float a, float b);
+template <> __device__ __forceinline__ void store2<float>(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+template <> __device__ __forceinline__ void store2<bf16>(bf16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+
+// RoPE rotation of one adjacent pair by the angle whose (cos, sin) is cs.
+__device__ __forceinline__ void rope_pair(float& a, float& b, float2 cs) {
+  const float x = a, y = b;
+  a = x * cs.x - y * cs.y;
+  b = x * cs.y + y * cs.x;
+}
+
+template <typename T>
+struct EpiQKV {
+  static constexpr bool kRowReduce = false;
+  QKVArgs a;
+  int H, Hkv, dh;
+  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
+    int b, t, qt;
+    if (a.pos) {
+      b = row; t = a.pos[row]; qt = 0;
+    } else {
+      b = row / a.T; t = row - b * a.T; qt = t;
+    }
+    const float rr = a.r[row];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] *= rr;
+    const int qn = H * dh, kn = Hkv * dh;
+    const int e = col % dh;
+    if (col < qn + kn && t >= 0) {
+      const float2* cs = a.rope + (size_t)t * (dh >> 1) + (e >> 1);
+      rope_pair(v[0], v[1], cs[0]);
+      rope_pair(v[2], v[3], cs[1]);
+    }
+    if (col < qn) {
+      const int h = col / dh;
+      store4<T>((T*)a.q + (((size_t)b * H + h) * a.T + qt) * dh + e, v);
+    } else if (t >= 0) {
+      const bool is_k = col < qn + kn;
+      const int h = (col - (is_k ? qn : qn + kn)) / dh;
+      T* base = (T*)(is_k ? a.k : a.v);
+      store4<T>(base + (((size_t)b * Hkv + h) * a.kv_stride + t) * dh + e, v);
+    }
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_reduce(int, float) const {}
+};
+
+template <typename T>
+struct EpiWo {
+  static constexpr bool kRowReduce = true;
+  WoArgs a;
+  int d;
+  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
+    float x[4];
+    load4<T>((const T*)a.x + (size_t)row * d + col, x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] += x[i];
+    store4<float>(a.h + (size_t)row * d + col, v);
+    if ((void*)a.hb != (void*)a.h) store4<T>((T*)a.hb + (size_t)row * d + col, v);
+    return v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+  }
+  __device__ __forceinline__ void row_reduce(int row, float s) const { atomicAdd(a.ssq + row, s); }
+};
+
+template <typename T>
+struct EpiW13 {
+  static constexpr bool kRowReduce = false;
+  W13Args a;
+  int d, f;
+  float eps;
+  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
+    const float r2 = 1.0f / sqrtf(a.ssq[row] / (float)d + eps);
+    const float o0 = silu_f(v[0] * r2) * (v[1] * r2);
+    const float o1 = silu_f(v[2] * r2) * (v[3] * r2);
+    store2<T>((T*)a.a + (size_t)row * f + (col >> 1), o0, o1);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_reduce(int, float) const {}
+};
+
+struct EpiW2 {
+  static constexpr bool kRowReduce = false;
+  W2Args a;
+  int d;
+  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
+    float h[4];
+    load4<float>(a.h + (size_t)row * d + col, h);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] += h[i];
+    if (a.y_dtype == TB_F32)
+      store4<float>((float*)a.y + (size_t)row * d + col, v);
+    else
+      store4<bf16>((bf16*)a.y + (size_t)row * d + col, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_reduce(int, float) const {}
+};
+
+}  // namespace tb

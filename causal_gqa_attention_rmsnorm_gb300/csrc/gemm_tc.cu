@@ -1,0 +1,325 @@
+// bf16 GEMM on the 5th-generation tensor cores: C = A·Bᵀ, A [M, K] (tokens ×
+// reduction), B [N, K] (packed weights, reduction axis contiguous), fp32
+// accumulation in tensor memory, and the block's fused epilogues.
+//
+// Persistent, warp-specialised, one CTA per SM:
+//   warp 0      TMA producer: A and B tiles (128-byte swizzle) into a ring of
+//               shared-memory stages, completion tracked by mbarriers;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M = 128, N = BN,
+//               K = 16) into one of two TMEM accumulators, and commits each
+//               stage back to the producer when the tensor core is done with it;
+//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (each warp
+//               owns its 32-lane quarter of TMEM, i.e. 32 rows), the fused
+//               epilogue, global stores; then the accumulator is released, so
+//               the next tile's MMAs overlap this tile's epilogue.
+// Tiles are visited n-fastest so that the CTAs running together share the A
+// row block and the weight panel stays resident in L2.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "epilogues.cuh"
+#include "gemm_tc.cuh"
+#include "sm100_ptx.cuh"
+
+namespace tb {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128, BK = 64;
+
+template <int BN> struct TcCfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+// fp32 output of the raw product (test hook).
+struct EpiF32 {
+  static constexpr bool kRowReduce = false;
+  float* C;
+  int N;
+  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
+    *reinterpret_cast<float4*>(C + (size_t)row * N + col) = make_float4(v[0], v[1], v[2], v[3]);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_reduce(int, float) const {}
+};
+#pragma nv_diag_suppress 177
+
+template <int BN, class Epi>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
+              uint32_t a_box_bytes, Epi epi, int* err) {
+  using C = TcCfg<BN>;
+  constexpr int STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
+  const int tiles = m_tiles * n_tiles;
+  const int kblocks = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued[STAGES];
+      uint32_t last_phase[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0, last_phase[s] = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+        const int mt = tile / n_tiles, nt = tile - mt * n_tiles;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          // the A box is shorter than the tile when M < 128; rows past it are never stored
+          mbar_arrive_expect_tx(&full[stage], a_box_bytes + C::B_BYTES);
+          tma_load_2d(&tmA, sa, &full[stage], kb * BK, mt * BM);
+          tma_load_2d(&tmB, sa + C::A_BYTES, &full[stage], kb * BK, nt * BN);
+          issued[stage] = 1;
+          last_phase[stage] = phase;
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+      }
+      // every copy issued must have landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s]) {
+          volatile int no_abort = 0;
+          mbar_wait(&full[s], last_phase[s], &no_abort, err);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16_ss(d_tmem, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), idesc,
+                        (kb | k) != 0);
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+        if (ok) mma_commit(&tfull[acc]);
+      }
+      // all MMAs must be done before TMEM is released
+      mma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort, err);
+    }
+  } else {
+    const int quad = warp & 3;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, err)) break;
+      tc_fence_after();
+      const int mt = tile / n_tiles, nt = tile - mt * n_tiles;
+      const int row = mt * BM + quad * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
+      float rsum = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + c, r);
+        tmem_wait_ld();
+        if (row < M) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int col = nt * BN + c + 4 * g;
+            if (col < N) {
+              float v[4] = {__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]), __uint_as_float(r[4 * g + 2]),
+                            __uint_as_float(r[4 * g + 3])};
+              rsum += epi(row, col, v);
+            }
+          }
+        }
+      }
+      if constexpr (Epi::kRowReduce) {
+        if (row < M) epi.row_reduce(row, rsum);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+template <int BN, class Epi>
+cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& epi, cudaStream_t s) {
+  using C = TcCfg<BN>;
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  CUtensorMap ta, tbm;
+  const uint32_t a_rows = M >= BM ? BM : (uint32_t)((M + 7) / 8 * 8);
+  cudaError_t e = make_tmap_2d_bf16(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)K, BK, a_rows);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d_bf16(&tbm, B, (uint64_t)N, (uint64_t)K, (uint64_t)K, BK, BN);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(k_gemm_tc<BN, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  k_gemm_tc<BN, Epi><<<grid, 192, C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, epi, device_error_word());
+  return cudaGetLastError();
+}
+
+// Narrow N tiles when the grid would not fill the GPU.
+template <class Epi>
+cudaError_t run_auto(const void* A, const void* B, int M, int N, int K, const Epi& epi, cudaStream_t s) {
+  const long tiles256 = (long)((M + BM - 1) / BM) * ((N + 255) / 256);
+  if (tiles256 >= 2L * sm_count()) return run<256, Epi>(A, B, M, N, K, epi, s);
+  return run<128, Epi>(A, B, M, N, K, epi, s);
+}
+
+}  // namespace
+
+int sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 1;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 1;
+  }
+  return n[dev];
+}
+
+cudaError_t make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                              uint64_t row_stride_elems, uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_stride_elems * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
+                              uint64_t row_stride_elems, uint64_t plane_stride_elems, uint32_t box_cols,
+                              uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {cols, rows, planes};
+  const cuuint64_t strides[2] = {row_stride_elems * 2, plane_stride_elems * 2};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
+                        cudaStream_t s) {
+  return run_auto(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh}, s);
+}
+cudaError_t gemm_tc_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
+                       cudaStream_t s) {
+  return run_auto(A, B, M, N, K, EpiWo<bf16>{e, D.d}, s);
+}
+cudaError_t gemm_tc_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
+                        cudaStream_t s) {
+  return run_auto(A, B, M, N, K, EpiW13<bf16>{e, D.d, D.f, D.eps}, s);
+}
+cudaError_t gemm_tc_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
+                       cudaStream_t s) {
+  return run_auto(A, B, M, N, K, EpiW2{e, D.d}, s);
+}
+cudaError_t gemm_tc_f32out(const void* A, const void* B, float* Cp, int M, int N, int K, int bn, cudaStream_t s) {
+  if (bn == 256) return run<256>(A, B, M, N, K, EpiF32{Cp, N}, s);
+  return run<128>(A, B, M, N, K, EpiF32{Cp, N}, s);
+}
+
+}  // namespace tb

@@ -1,0 +1,469 @@
+// C ABI of libtb: argument checks, buffer carving and the launch sequences of
+// the prefill and decode steps.  Declarations and contracts are in tb.h.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "common.cuh"
+#include "gemm_tc.cuh"
+
+namespace tb {
+namespace {
+
+__device__ int g_device_error;  // TB_DEVERR_* bits
+
+thread_local char g_msg[512] = "";
+
+tb_status fail(tb_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+tb_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(TB_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+// Device address of the error word on the current device.
+int* device_error_word() {
+  static int* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = (int*)p;
+  }
+  return ptrs[dev];
+}
+
+namespace {
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+size_t esize(int dtype) { return dtype == TB_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+tb_status check_cfg(const tb_block_cfg* c) {
+  if (!c) return fail(TB_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->d <= 0 || c->H <= 0 || c->Hkv <= 0 || c->dh <= 0 || c->f <= 0)
+    return fail(TB_ERR_INVALID_ARG, "d, H, Hkv, dh and f must be positive");
+  if (c->H % c->Hkv) return fail(TB_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", c->H, c->Hkv);
+  if ((long long)c->H * c->dh != c->d)
+    return fail(TB_ERR_INVALID_ARG, "dh (%d) must equal d/H (%d/%d)", c->dh, c->d, c->H);
+  if (c->dh % 2) return fail(TB_ERR_INVALID_ARG, "dh must be even (RoPE rotates pairs)");
+  if (c->max_pos <= 0) return fail(TB_ERR_INVALID_ARG, "max_pos must be positive");
+  if (!(c->rope_base > 0.f)) return fail(TB_ERR_INVALID_ARG, "rope_base must be positive");
+  if (!(c->eps >= 0.f)) return fail(TB_ERR_INVALID_ARG, "eps must be non-negative");
+  if (c->dtype != TB_F32 && c->dtype != TB_BF16) return fail(TB_ERR_INVALID_ARG, "unknown dtype %d", c->dtype);
+  if (c->dh != 16 && c->dh != 32 && c->dh != 64 && c->dh != 128)
+    return fail(TB_ERR_UNSUPPORTED, "dh %d: attention kernels exist for 16, 32, 64 and 128", c->dh);
+  const int G = c->H / c->Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(TB_ERR_UNSUPPORTED, "H/Hkv = %d: decode kernels exist for 1, 2, 4 and 8", G);
+  if (c->f % 2) return fail(TB_ERR_UNSUPPORTED, "f must be even");
+  if (c->dtype == TB_BF16) {
+    if (c->d % 64 || c->f % 64)
+      return fail(TB_ERR_UNSUPPORTED, "bf16 tensor-core path needs d and f multiples of 64 (d=%d f=%d)", c->d,
+                  c->f);
+  }
+  return TB_OK;
+}
+
+Dims dims_of(const tb_block_cfg* c) { return Dims{c->d, c->H, c->Hkv, c->dh, c->f, c->eps, c->max_pos}; }
+
+// Packed weight blob: four matrices and the RoPE table, 1 KiB aligned.
+struct PackedLayout {
+  size_t wqkv, wo, w13, w2, rope, total;
+};
+PackedLayout packed_layout(const tb_block_cfg* c) {
+  const size_t es = esize(c->dtype);
+  PackedLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 1024);
+    return o;
+  };
+  const size_t nqkv = (size_t)(c->H + 2 * c->Hkv) * c->dh;
+  L.wqkv = take(nqkv * c->d * es);
+  L.wo = take((size_t)c->d * c->H * c->dh * es);
+  L.w13 = take((size_t)2 * c->f * c->d * es);
+  L.w2 = take((size_t)c->d * c->f * es);
+  L.rope = take((size_t)c->max_pos * (c->dh / 2) * sizeof(float2));
+  L.total = off;
+  return L;
+}
+
+Packed packed_views(const tb_block_cfg* c, const void* blob) {
+  const PackedLayout L = packed_layout(c);
+  const char* b = (const char*)blob;
+  return Packed{b + L.wqkv, b + L.wo, b + L.w13, b + L.w2, (const float2*)(b + L.rope)};
+}
+
+// Workspace carving.  Prefill keeps K/V in the workspace when no cache is given.
+struct Work {
+  float* r;
+  float* ssq;
+  int32_t* pos;
+  void* q;
+  void* k;
+  void* v;
+  void* o;
+  float* h;
+  void* hb;
+  void* a;
+  float* part;
+  int nchunk_max;
+  size_t total;
+};
+
+Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
+  const size_t es = esize(c->dtype);
+  char* p = (char*)base;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* r = p ? (void*)(p + off) : nullptr;
+    off = align_up(off + bytes, 256);
+    return r;
+  };
+  Work w{};
+  const size_t M = (size_t)B * (mode == 0 ? T : 1);
+  const size_t hd = (size_t)c->H * c->dh, kvd = (size_t)c->Hkv * c->dh;
+  w.r = (float*)take(M * 4);
+  w.ssq = (float*)take(M * 4);
+  w.pos = (int32_t*)take((size_t)B * 4);
+  w.q = take(M * hd * es);
+  if (mode == 0) {
+    w.k = take(M * kvd * es);
+    w.v = take(M * kvd * es);
+  }
+  w.o = take(M * hd * es);
+  w.h = (float*)take(M * c->d * 4);
+  w.hb = c->dtype == TB_F32 ? (void*)w.h : take(M * c->d * es);
+  w.a = take(M * c->f * es);
+  if (mode == 1) {
+    w.nchunk_max = (T + decode_chunk_keys() - 1) / decode_chunk_keys();
+    w.part = (float*)take(decode_part_floats(B, c->H, c->dh, w.nchunk_max) * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+tb_status check_kv(const tb_block_cfg* c, const tb_kvcache* kv, int B) {
+  if (!kv->k || !kv->v || !kv->lens) return fail(TB_ERR_INVALID_ARG, "kv cache pointers must be non-NULL");
+  if (kv->B != B) return fail(TB_ERR_INVALID_ARG, "kv->B (%d) differs from B (%d)", kv->B, B);
+  if (kv->Hkv != c->Hkv || kv->dh != c->dh)
+    return fail(TB_ERR_INVALID_ARG, "kv cache heads/width (%d, %d) differ from cfg (%d, %d)", kv->Hkv, kv->dh,
+                c->Hkv, c->dh);
+  if (kv->dtype != c->dtype) return fail(TB_ERR_INVALID_ARG, "kv cache dtype differs from cfg dtype");
+  if (kv->T_max <= 0) return fail(TB_ERR_INVALID_ARG, "kv->T_max must be positive");
+  if (!aligned16(kv->k) || !aligned16(kv->v) || ((uintptr_t)kv->lens & 3u))
+    return fail(TB_ERR_INVALID_ARG, "kv cache pointers must be 16-byte aligned (lens 4-byte)");
+  return TB_OK;
+}
+
+// Per-stage CUDA-event trace (test and benchmark hook).  When enabled, each
+// prefill/decode call takes the next slot of a ring of `slots` calls and
+// records one event before each of its stages and one after the last, on the
+// call's own stream, so stage durations are device times of exactly those
+// launches.
+struct Trace {
+  bool on = false;
+  int slots = 0, next = 0, stages = 0;
+  std::vector<cudaEvent_t> ev;       // slots × (kMaxStages + 1)
+  std::vector<int> used;             // stages recorded per slot
+  std::vector<const char*> names;    // stage names of the last traced call
+};
+constexpr int kMaxStages = 8;
+Trace g_trace;
+
+struct StageRecorder {
+  cudaStream_t s;
+  int slot = -1, n = 0;
+  explicit StageRecorder(cudaStream_t st) : s(st) {
+    if (g_trace.on && g_trace.slots > 0) {
+      slot = g_trace.next;
+      g_trace.next = (g_trace.next + 1) % g_trace.slots;
+      g_trace.names.clear();
+    }
+  }
+  void stage(const char* name) {
+    if (slot < 0 || n >= kMaxStages) return;
+    cudaEventRecord(g_trace.ev[(size_t)slot * (kMaxStages + 1) + n], s);
+    g_trace.names.push_back(name);
+    ++n;
+  }
+  ~StageRecorder() {
+    if (slot < 0) return;
+    cudaEventRecord(g_trace.ev[(size_t)slot * (kMaxStages + 1) + n], s);
+    g_trace.used[slot] = n;
+  }
+};
+
+#define TB_TRY(expr)                              \
+  do {                                            \
+    cudaError_t e_ = (expr);                      \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #expr); \
+  } while (0)
+
+}  // namespace
+}  // namespace tb
+
+using namespace tb;
+
+extern "C" {
+
+size_t tb_packed_weights_bytes(const tb_block_cfg* cfg) {
+  if (check_cfg(cfg) != TB_OK) return 0;
+  return packed_layout(cfg).total;
+}
+
+tb_status tb_pack_weights(const tb_block_cfg* cfg, const tb_block_weights* w, void* packed, size_t packed_bytes,
+                          void* stream) {
+  tb_status st = check_cfg(cfg);
+  if (st != TB_OK) return st;
+  if (!w || !packed) return fail(TB_ERR_INVALID_ARG, "weights and packed must be non-NULL");
+  const void* ptrs[9] = {w->g_attn, w->wq, w->wk, w->wv, w->wo, w->g_mlp, w->w1, w->w3, w->w2};
+  for (const void* p : ptrs)
+    if (!p) return fail(TB_ERR_INVALID_ARG, "a weight pointer is NULL");
+  if ((uintptr_t)packed & 255u) return fail(TB_ERR_INVALID_ARG, "packed must be 256-byte aligned");
+  if (packed_bytes < packed_layout(cfg).total)
+    return fail(TB_ERR_INVALID_ARG, "packed buffer too small: %zu < %zu", packed_bytes, packed_layout(cfg).total);
+  const Packed P = packed_views(cfg, packed);
+  TB_TRY(launch_pack(cfg->dtype, dims_of(cfg), *w, packed, P, cfg->rope_base, (cudaStream_t)stream));
+  return TB_OK;
+}
+
+size_t tb_workspace_bytes(const tb_block_cfg* cfg, int32_t B, int32_t T, int32_t mode) {
+  if (check_cfg(cfg) != TB_OK || B < 0 || T < 0 || (mode != 0 && mode != 1)) return 0;
+  return carve(cfg, B, T, mode, nullptr).total;
+}
+
+tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const void* x, void* y, int32_t y_dtype,
+                           int32_t B, int32_t T, const tb_kvcache* kv, void* ws, size_t ws_bytes, void* stream) {
+  tb_status st = check_cfg(cfg);
+  if (st != TB_OK) return st;
+  if (B < 0 || T < 0) return fail(TB_ERR_INVALID_ARG, "B and T must be non-negative");
+  if (y_dtype != TB_F32 && !(y_dtype == TB_BF16 && cfg->dtype == TB_BF16))
+    return fail(TB_ERR_INVALID_ARG, "y_dtype must be TB_F32, or TB_BF16 for a bf16 block");
+  if (kv) {
+    st = check_kv(cfg, kv, B);
+    if (st != TB_OK) return st;
+    if (T > kv->T_max) return fail(TB_ERR_INVALID_ARG, "T (%d) exceeds kv->T_max (%d)", T, kv->T_max);
+  }
+  if (B == 0 || T == 0) return TB_OK;
+  if (T > cfg->max_pos) return fail(TB_ERR_INVALID_ARG, "T (%d) exceeds cfg->max_pos (%d)", T, cfg->max_pos);
+  if ((long long)B * T > (1LL << 30)) return fail(TB_ERR_UNSUPPORTED, "B·T above 2^30 tokens");
+  if (!packed || !x || !y || !ws) return fail(TB_ERR_INVALID_ARG, "packed, x, y and ws must be non-NULL");
+  if (!aligned16(x) || !aligned16(y) || ((uintptr_t)packed & 255u) || ((uintptr_t)ws & 255u))
+    return fail(TB_ERR_INVALID_ARG, "x, y must be 16-byte aligned; packed, ws 256-byte aligned");
+  if (x == y) return fail(TB_ERR_INVALID_ARG, "y may not alias x");
+  const Work W = carve(cfg, B, T, 0, ws);
+  if (ws_bytes < W.total) return fail(TB_ERR_INVALID_ARG, "workspace too small: %zu < %zu", ws_bytes, W.total);
+  int* err = device_error_word();
+  if (!err) return fail(TB_ERR_CUDA, "cannot resolve the device error word");
+
+  cudaStream_t s = (cudaStream_t)stream;
+  const Dims D = dims_of(cfg);
+  const Packed P = packed_views(cfg, packed);
+  const int M = B * T;
+  const int dt = cfg->dtype;
+  const int nqkv = (cfg->H + 2 * cfg->Hkv) * cfg->dh;
+  void* kbuf = kv ? kv->k : W.k;
+  void* vbuf = kv ? kv->v : W.v;
+  const int kv_stride = kv ? kv->T_max : T;
+
+  StageRecorder rec(s);
+  rec.stage("rms");
+  TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, W.ssq, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
+                          err, s));
+  const QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr};
+  const WoArgs wa{x, W.h, W.hb, W.ssq};
+  const W13Args ga{W.ssq, W.a};
+  const W2Args ya{W.h, y, y_dtype};
+  if (dt == TB_F32) {
+    rec.stage("qkv");
+    TB_TRY(gemm_simt_qkv(dt, x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
+    rec.stage("attn");
+    TB_TRY(attn_prefill_simt(dt, W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, s));
+    rec.stage("wo");
+    TB_TRY(gemm_simt_wo(dt, W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    rec.stage("w13");
+    TB_TRY(gemm_simt_w13(dt, W.hb, P.w13, M, 2 * cfg->f, cfg->d, D, ga, s));
+    rec.stage("w2");
+    TB_TRY(gemm_simt_w2(dt, W.a, P.w2, M, cfg->d, cfg->f, D, ya, s));
+  } else {
+    rec.stage("qkv");
+    TB_TRY(gemm_tc_qkv(x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
+    rec.stage("attn");
+    TB_TRY(attn_prefill_simt(dt, W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, s));
+    rec.stage("wo");
+    TB_TRY(gemm_tc_wo(W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    rec.stage("w13");
+    TB_TRY(gemm_tc_w13(W.hb, P.w13, M, 2 * cfg->f, cfg->d, D, ga, s));
+    rec.stage("w2");
+    TB_TRY(gemm_tc_w2(W.a, P.w2, M, cfg->d, cfg->f, D, ya, s));
+  }
+  return TB_OK;
+}
+
+tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const void* x, void* y, int32_t y_dtype,
+                          const tb_kvcache* kv, void* ws, size_t ws_bytes, void* stream) {
+  tb_status st = check_cfg(cfg);
+  if (st != TB_OK) return st;
+  if (!kv) return fail(TB_ERR_INVALID_ARG, "decode needs a kv cache");
+  if (kv->B < 0) return fail(TB_ERR_INVALID_ARG, "kv->B must be non-negative");
+  st = check_kv(cfg, kv, kv->B);
+  if (st != TB_OK) return st;
+  if (y_dtype != TB_F32 && !(y_dtype == TB_BF16 && cfg->dtype == TB_BF16))
+    return fail(TB_ERR_INVALID_ARG, "y_dtype must be TB_F32, or TB_BF16 for a bf16 block");
+  if (kv->T_max > cfg->max_pos)
+    return fail(TB_ERR_INVALID_ARG, "kv->T_max (%d) exceeds cfg->max_pos (%d)", kv->T_max, cfg->max_pos);
+  const int B = kv->B;
+  if (B == 0) return TB_OK;
+  if (!packed || !x || !y || !ws) return fail(TB_ERR_INVALID_ARG, "packed, x, y and ws must be non-NULL");
+  if (!aligned16(x) || !aligned16(y) || ((uintptr_t)packed & 255u) || ((uintptr_t)ws & 255u))
+    return fail(TB_ERR_INVALID_ARG, "x, y must be 16-byte aligned; packed, ws 256-byte aligned");
+  if (x == y) return fail(TB_ERR_INVALID_ARG, "y may not alias x");
+  const Work W = carve(cfg, B, kv->T_max, 1, ws);
+  if (ws_bytes < W.total) return fail(TB_ERR_INVALID_ARG, "workspace too small: %zu < %zu", ws_bytes, W.total);
+  int* err = device_error_word();
+  if (!err) return fail(TB_ERR_CUDA, "cannot resolve the device error word");
+
+  cudaStream_t s = (cudaStream_t)stream;
+  const Dims D = dims_of(cfg);
+  const Packed P = packed_views(cfg, packed);
+  const int dt = cfg->dtype;
+  const int nqkv = (cfg->H + 2 * cfg->Hkv) * cfg->dh;
+
+  StageRecorder rec(s);
+  rec.stage("rms");
+  TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, W.ssq, 1, nullptr, kv->lens, W.pos, kv->T_max, err, s));
+  const QKVArgs qa{W.r, P.rope, W.q, kv->k, kv->v, 1, kv->T_max, W.pos};
+  const WoArgs wa{x, W.h, W.hb, W.ssq};
+  const W13Args ga{W.ssq, W.a};
+  const W2Args ya{W.h, y, y_dtype};
+  if (dt == TB_F32) {
+    rec.stage("qkv");
+    TB_TRY(gemm_simt_qkv(dt, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
+    rec.stage("attn");
+    TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
+                       W.nchunk_max, W.o, s));
+    rec.stage("wo");
+    TB_TRY(gemm_simt_wo(dt, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    rec.stage("w13");
+    TB_TRY(gemm_simt_w13(dt, W.hb, P.w13, B, 2 * cfg->f, cfg->d, D, ga, s));
+    rec.stage("w2");
+    TB_TRY(gemm_simt_w2(dt, W.a, P.w2, B, cfg->d, cfg->f, D, ya, s));
+  } else {
+    rec.stage("qkv");
+    TB_TRY(gemm_tc_qkv(x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
+    rec.stage("attn");
+    TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
+                       W.nchunk_max, W.o, s));
+    rec.stage("wo");
+    TB_TRY(gemm_tc_wo(W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    rec.stage("w13");
+    TB_TRY(gemm_tc_w13(W.hb, P.w13, B, 2 * cfg->f, cfg->d, D, ga, s));
+    rec.stage("w2");
+    TB_TRY(gemm_tc_w2(W.a, P.w2, B, cfg->d, cfg->f, D, ya, s));
+  }
+  return TB_OK;
+}
+
+tb_status tb_kvcache_append(const tb_kvcache* kv, const void* k_new, const void* v_new, int32_t n, void* stream) {
+  if (!kv) return fail(TB_ERR_INVALID_ARG, "kv is NULL");
+  if (n < 0) return fail(TB_ERR_INVALID_ARG, "n must be non-negative");
+  if (kv->dtype != TB_F32 && kv->dtype != TB_BF16) return fail(TB_ERR_INVALID_ARG, "unknown kv dtype");
+  if (kv->B < 0 || kv->Hkv <= 0 || kv->dh <= 0 || kv->T_max <= 0)
+    return fail(TB_ERR_INVALID_ARG, "kv shape must be positive (B may be 0)");
+  if ((kv->dh * (int)esize(kv->dtype)) % 16) return fail(TB_ERR_UNSUPPORTED, "dh·sizeof must be a multiple of 16");
+  if (n == 0 || kv->B == 0) return TB_OK;
+  if (n > kv->T_max) return fail(TB_ERR_CACHE_FULL, "n (%d) exceeds T_max (%d)", n, kv->T_max);
+  if (!kv->k || !kv->v || !kv->lens || !k_new || !v_new)
+    return fail(TB_ERR_INVALID_ARG, "cache and new-row pointers must be non-NULL");
+  if (!aligned16(kv->k) || !aligned16(kv->v) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(TB_ERR_INVALID_ARG, "cache and new-row pointers must be 16-byte aligned");
+  int* err = device_error_word();
+  if (!err) return fail(TB_ERR_CUDA, "cannot resolve the device error word");
+  TB_TRY(launch_kv_append(kv->dtype, *kv, k_new, v_new, n, err, (cudaStream_t)stream));
+  return TB_OK;
+}
+
+tb_status tb_get_device_error(void* stream, int32_t* err_out, int32_t clear) {
+  if (!err_out) return fail(TB_ERR_INVALID_ARG, "err_out is NULL");
+  TB_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+  int* err = device_error_word();
+  if (!err) return fail(TB_ERR_CUDA, "cannot resolve the device error word");
+  int v = 0;
+  TB_TRY(cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost));
+  *err_out = v;
+  if (clear) TB_TRY(cudaMemset(err, 0, sizeof(int)));
+  return TB_OK;
+}
+
+const char* tb_status_string(tb_status s) {
+  switch (s) {
+    case TB_OK: return "ok";
+    case TB_ERR_INVALID_ARG: return "invalid argument";
+    case TB_ERR_UNSUPPORTED: return "unsupported shape";
+    case TB_ERR_CUDA: return "CUDA error";
+    case TB_ERR_CACHE_FULL: return "KV cache full";
+    case TB_ERR_TIMEOUT: return "timeout";
+  }
+  return "unknown status";
+}
+
+const char* tb_last_error_message(void) { return g_msg; }
+
+// Trace hooks (not part of the public header).  tbx_trace_enable(slots)
+// creates `slots` × 9 events on the current device and turns tracing on;
+// slots = 0 turns it off.  tbx_trace_read(slot, ms, n) synchronises the slot's
+// last event and writes up to n stage durations; it returns the number of
+// stages recorded in that slot (0 if none), or -1 on a CUDA error.
+TB_API int32_t tbx_trace_enable(int32_t slots) {
+  for (cudaEvent_t e : g_trace.ev) cudaEventDestroy(e);
+  g_trace = Trace{};
+  if (slots <= 0) return 0;
+  g_trace.ev.resize((size_t)slots * (kMaxStages + 1));
+  for (auto& e : g_trace.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return -1;
+  g_trace.used.assign(slots, 0);
+  g_trace.slots = slots;
+  g_trace.on = true;
+  return 0;
+}
+
+TB_API int32_t tbx_trace_read(int32_t slot, float* ms, int32_t n) {
+  if (slot < 0 || slot >= g_trace.slots) return 0;
+  const int used = g_trace.used[slot];
+  cudaEvent_t* ev = &g_trace.ev[(size_t)slot * (kMaxStages + 1)];
+  if (used == 0) return 0;
+  if (cudaEventSynchronize(ev[used]) != cudaSuccess) return -1;
+  for (int i = 0; i < used && i < n; ++i)
+    if (cudaEventElapsedTime(&ms[i], ev[i], ev[i + 1]) != cudaSuccess) return -1;
+  return used;
+}
+
+TB_API const char* tbx_trace_stage_name(int32_t i) {
+  return (i >= 0 && i < (int)g_trace.names.size()) ? g_trace.names[i] : "";
+}
+
+// Test hook (not part of the public header): C[M, N] = A[M, K]·B[N, K]ᵀ in
+// fp32 through the bf16 tcgen05 main loop, N-tile width bn (128 or 256).
+TB_API tb_status tbx_gemm_bf16(const void* A, const void* B, float* Cp, int32_t M, int32_t N, int32_t K, int32_t bn,
+                        void* stream) {
+  if (!A || !B || !Cp || M < 0 || N <= 0 || K <= 0 || K % 64 || N % 4 || (bn != 128 && bn != 256))
+    return fail(TB_ERR_INVALID_ARG, "tbx_gemm_bf16: bad arguments");
+  TB_TRY(gemm_tc_f32out(A, B, Cp, M, N, K, bn, (cudaStream_t)stream));
+  return TB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,172 @@
+/*
+ * tb.h — C ABI of the GB300 (sm_103a) Llama-layout pre-norm decoder block.
+ *
+ * One block forward pass, as the "Transformer block" page (tirogla.com,
+ * section "How it works": dataflow diagram and steps 2-3) defines it:
+ *
+ *   h = x + Wo · concat_h softmax(q_h·k_{h/G}ᵀ/√dh + causal) · v_{h/G}
+ *       with q, k, v = RMSNorm(x)·Wq, ·Wk, ·Wv and RoPE on q and k
+ *   y = h + W2 · (SiLU(hn·W1) ⊙ hn·W3),   hn = RMSNorm(h)
+ *
+ * in two modes: full-sequence prefill, and one decode step over a KV cache of
+ * post-RoPE keys and values [B, Hkv, T_max, dh] (same page, KV-cache paragraph;
+ * "Transformers", engineering.msaqlain.com, section 5.2).  Notation follows the
+ * pages: B batch, T sequence, d width, H query heads, Hkv KV heads (G = H/Hkv
+ * query heads share one KV head), dh = d/H head width, f MLP width.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are CUDA device pointers on the current device;
+ *    "host" pointers are ordinary host memory.  The caller owns every buffer;
+ *    the library allocates no device memory.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream) except tb_get_device_error, which synchronises it.
+ *  - Arguments are checked on the host before anything is launched.  A bad
+ *    argument returns TB_ERR_INVALID_ARG (or TB_ERR_UNSUPPORTED for a valid
+ *    but unimplemented shape) and launches nothing; tb_last_error_message()
+ *    then says which argument.
+ *  - Conditions only the device can see (a sequence whose cache is full) set
+ *    a bit in a per-device error word, skip the affected rows and never trap;
+ *    tb_get_device_error reads it.  No kernel waits without a time limit: a
+ *    wait that runs out sets TB_DEVERR_TIMEOUT and the kernel returns.
+ *  - Row-major layouts throughout; weights are [in, out] (y = x·W), as in the
+ *    "Transformer block" page's Rust block.
+ */
+#ifndef TB_H_
+#define TB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TB_API __attribute__((visibility("default")))
+#else
+#define TB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TB_OK = 0,
+  TB_ERR_INVALID_ARG = 1,   /* a null/misaligned pointer, inconsistent shape, too small a buffer */
+  TB_ERR_UNSUPPORTED = 2,   /* a valid shape this build has no kernel for */
+  TB_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+  TB_ERR_CACHE_FULL = 4,    /* host-visible cache overflow (append of n rows past T_max) */
+  TB_ERR_TIMEOUT = 5        /* reserved for a host-side wait that ran out */
+} tb_status;
+
+typedef enum { TB_F32 = 0, TB_BF16 = 1 } tb_dtype;
+
+/* Bits of the device error word (tb_get_device_error). */
+#define TB_DEVERR_CACHE_FULL 1  /* a decode/append row found lens[b] + n > T_max; that row was skipped */
+#define TB_DEVERR_TIMEOUT    2  /* a kernel's bounded wait ran out; its output is not valid */
+
+/* Block hyper-parameters.
+ *  d, H, Hkv, dh, f : widths in the pages' notation; H·dh must equal d, H a
+ *                     multiple of Hkv, dh even (RoPE rotates pairs).
+ *  max_pos          : number of positions the packed RoPE table covers
+ *                     (prefill T and every decode position must be below it).
+ *  rope_base        : RoPE base; pair i of a head turns by t·base^(-2i/dh)
+ *                     at 0-based position t ("Transformer block" page, RoPE).
+ *  eps              : RMSNorm eps, added to the mean square inside the root.
+ *  dtype            : tb_dtype of x, the weights, the gains and the KV cache.
+ *                     TB_BF16 computes with bf16 tensor-core operands, fp32
+ *                     accumulation, fp32 softmax and norms; TB_F32 computes in
+ *                     fp32 throughout. */
+typedef struct {
+  int32_t d, H, Hkv, dh, f;
+  int32_t max_pos;
+  float rope_base;
+  float eps;
+  int32_t dtype;
+} tb_block_cfg;
+
+/* Unpacked weights, device pointers of cfg.dtype, [in, out] row-major:
+ *  g_attn [d], wq [d, H·dh], wk [d, Hkv·dh], wv [d, Hkv·dh], wo [H·dh, d],
+ *  g_mlp [d], w1 [d, f] (gate), w3 [d, f] (up), w2 [f, d].
+ * Head h of q is column block [h·dh, (h+1)·dh) of x·Wq (likewise k, v). */
+typedef struct {
+  const void *g_attn, *wq, *wk, *wv, *wo, *g_mlp, *w1, *w3, *w2;
+} tb_block_weights;
+
+/* KV cache of post-RoPE keys and values.
+ *  k, v  : device, cfg.dtype, [B, Hkv, T_max, dh] each, row-major.
+ *  lens  : device int32 [B], the number of valid rows of each sequence.
+ * Rows at or beyond lens[b] are never read. */
+typedef struct {
+  void *k, *v;
+  int32_t *lens;
+  int32_t B, Hkv, T_max, dh;
+  int32_t dtype;
+} tb_kvcache;
+
+/* Bytes the packed weight blob of tb_pack_weights needs. */
+TB_API size_t tb_packed_weights_bytes(const tb_block_cfg *cfg);
+
+/* Pack a weight set once for the kernels: the RMSNorm gains are folded into
+ * the rows of the input dimension (RMSNorm(x)·W = r·(x·(diag(g)·W)), r the
+ * per-token inverse RMS, so the norm becomes a per-row scale in the GEMM
+ * epilogue), the matrices are stored transposed ([out, in], reduction axis
+ * contiguous) with Wq|Wk|Wv fused and W1/W3 interleaved column by column
+ * (the fused GEMMs of the "Transformer block" page's implementation notes),
+ * and a [max_pos, dh/2] cos/sin table is built in fp64 and stored in fp32
+ * (the same notes suggest precomputing it).
+ *  w      : unpacked weights (device).
+ *  packed : device, at least tb_packed_weights_bytes(cfg) bytes, 256-B aligned.
+ * The packed blob depends only on cfg and w; it is read-only afterwards. */
+TB_API tb_status tb_pack_weights(const tb_block_cfg *cfg, const tb_block_weights *w,
+                          void *packed, size_t packed_bytes, void *stream);
+
+/* Workspace bytes a call needs: mode 0 = prefill of B×T tokens (with K/V kept
+ * in the workspace when no cache is passed, which is the larger case), mode 1
+ * = decode of B sequences whose cache holds up to T positions (T = T_max). */
+TB_API size_t tb_workspace_bytes(const tb_block_cfg *cfg, int32_t B, int32_t T, int32_t mode);
+
+/* Full-sequence prefill of B sequences of T tokens.
+ *  packed  : device blob from tb_pack_weights for this cfg.
+ *  x       : device [B, T, d] cfg.dtype.
+ *  y       : device [B, T, d] y_dtype (TB_F32, or TB_BF16 when cfg.dtype is
+ *            TB_BF16).  y may not alias x.
+ *  kv      : NULL, or a cache with kv->B == B, T ≤ kv->T_max: its rows [0, T)
+ *            receive the post-RoPE K and V of every position and lens[b] is
+ *            set to T.
+ *  ws      : device workspace of ws_bytes ≥ tb_workspace_bytes(cfg, B, T, 0).
+ * B == 0 or T == 0 is an empty call that returns TB_OK. */
+TB_API tb_status tb_block_prefill(const tb_block_cfg *cfg, const void *packed, const void *x, void *y,
+                           int32_t y_dtype, int32_t B, int32_t T, const tb_kvcache *kv,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* One decode step of kv->B sequences.  Token b sits at position p = lens[b]:
+ * its k and v are rotated at p and written to cache row p, its query attends
+ * over rows 0..p, and lens[b] becomes p + 1.
+ *  x  : device [B, 1, d] cfg.dtype;  y : device [B, 1, d] y_dtype.
+ *  kv : required; kv->T_max ≤ cfg->max_pos.
+ *  ws : device workspace of ws_bytes ≥ tb_workspace_bytes(cfg, B, kv->T_max, 1).
+ * A sequence with lens[b] ≥ T_max sets TB_DEVERR_CACHE_FULL, keeps its cache
+ * and length unchanged, and gets an unspecified y row. */
+TB_API tb_status tb_block_decode(const tb_block_cfg *cfg, const void *packed, const void *x, void *y,
+                          int32_t y_dtype, const tb_kvcache *kv, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/* Append n post-RoPE rows per sequence: k_new, v_new are device
+ * [B, Hkv, n, dh] of kv->dtype; rows go to [lens[b], lens[b]+n) and lens[b]
+ * grows by n.  A sequence with lens[b] + n > T_max sets TB_DEVERR_CACHE_FULL
+ * and is left unchanged.  n == 0 is a no-op. */
+TB_API tb_status tb_kvcache_append(const tb_kvcache *kv, const void *k_new, const void *v_new, int32_t n,
+                            void *stream);
+
+/* Synchronise `stream` and read the current device's error word (TB_DEVERR_*
+ * bits, 0 = none) into *err_out; `clear` != 0 resets it to 0. */
+TB_API tb_status tb_get_device_error(void *stream, int32_t *err_out, int32_t clear);
+
+/* Short text for a status code (static storage). */
+TB_API const char *tb_status_string(tb_status s);
+
+/* Detail of the last non-OK status returned on the calling thread. */
+TB_API const char *tb_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TB_H_ */

@@ -1,0 +1,61 @@
+"""Shared test plumbing: run the CUDA path through the C ABI and the oracle on
+the same seeded inputs, and measure the difference.
+
+The tolerances are the ones the block is held to:
+  * fp32 storage: normwise max relative error max|Δ| / max|y_ref| ≤ 1e-4;
+  * bf16 storage (fp32 accumulate, fp32 softmax and norms): relative L2 error
+    ≤ 1e-2 and max absolute error ≤ 3e-2, against the oracle run in fp64 on
+    the bf16-rounded inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+from workloads import BlockShape
+
+F32_NORMWISE_TOL = 1e-4
+BF16_REL_L2_TOL = 1e-2
+BF16_MAX_ABS_TOL = 3e-2
+
+
+def oracle_cfg(s: BlockShape) -> oracle.Cfg:
+    return oracle.Cfg(s.d, s.H, s.Hkv, s.dh, s.f, s.rope_base, s.eps)
+
+
+def oracle_weights(inp):
+    return {n: workloads.to_f64(inp[n]) for n in workloads.WEIGHT_NAMES}
+
+
+def block_config(s: BlockShape, max_pos: int):
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    return tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, max_pos, s.rope_base, s.eps,
+                          tb.TB_F32 if s.dtype == "f32" else tb.TB_BF16)
+
+
+def to_device(inp, device="cuda"):
+    return {n: t.to(device) for n, t in inp.items()}
+
+
+def errors(got: np.ndarray, ref: np.ndarray) -> dict:
+    d = np.asarray(got, np.float64) - np.asarray(ref, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return {
+        "max_abs": float(np.max(np.abs(d))) if d.size else 0.0,
+        "rel_l2": float(np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-300)) if d.size else 0.0,
+        "normwise": float(np.max(np.abs(d)) / max(np.max(np.abs(ref)), 1e-300)) if d.size else 0.0,
+        "finite": bool(np.isfinite(np.asarray(got, np.float64)).all()),
+    }
+
+
+def assert_close(got, ref, dtype: str, what: str = "y", max_abs_tol: float = BF16_MAX_ABS_TOL):
+    e = errors(got, ref)
+    assert e["finite"], f"{what}: non-finite values"
+    if dtype == "f32":
+        assert e["normwise"] <= F32_NORMWISE_TOL, f"{what}: {e}"
+    else:
+        assert e["rel_l2"] <= BF16_REL_L2_TOL, f"{what}: {e}"
+        assert e["max_abs"] <= max_abs_tol, f"{what}: {e}"
+    return e

@@ -1,0 +1,28 @@
+"""The bf16 tcgen05 GEMM main loop against a plain fp32 product of the same
+bf16 operands (C = A·Bᵀ), over tile-aligned, ragged and small shapes."""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("M,N,K,bn", [
+    (128, 256, 64, 256),        # one tile, one k-block
+    (256, 512, 1024, 256),      # several tiles and stages
+    (300, 260, 192, 128),       # ragged M and N
+    (32, 6144, 4096, 128),      # decode-shaped (M = 32)
+    (1000, 768, 768, 256),      # ragged M, N multiple of 256 with K 768
+    (4096, 2304, 768, 256),     # many tiles per CTA (persistent loop, accumulator ping-pong)
+])
+def test_gemm_bf16_matches_fp32_product(M, N, K, bn):
+    from causal_gqa_attention_rmsnorm_gb300 import binding
+    g = torch.Generator(device="cpu").manual_seed(M * 7 + N * 3 + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
+    B = (0.05 * torch.randn(N, K, generator=g)).to(torch.bfloat16).cuda()
+    C = binding.tbx_gemm_bf16(A, B, bn=bn)
+    torch.cuda.synchronize()
+    ref = A.double() @ B.double().T
+    err = (C.double() - ref).abs().max().item()
+    scale = ref.abs().max().item()
+    # fp32 accumulation of K products: rounding ~ K·2^-24·max|a·b|
+    assert err <= 1e-4 * max(scale, 1.0), (err, scale)

@@ -1,0 +1,153 @@
+"""Prefill parity: the CUDA path through the C ABI against the fp64 oracle on
+the same seeded inputs (bf16 cases: the oracle sees the bf16-rounded values).
+
+Small cases span several tiles and a ragged tail; the full workloads run in
+the launch configuration the benchmark times, with every row checked where
+the oracle is quick and sampled rows (computed exactly, by causality, from
+all keys before them) where it is not."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import (assert_close, block_config, errors, oracle_cfg, oracle_weights, to_device)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    # fp32 storage, GQA 4/2, the tiny workload itself
+    "tiny_fp32": workloads.CONFIGS["tiny_fp32"],
+    # fp32, MQA, ragged T, two sequences
+    "fp32_mqa_ragged": workloads.CONFIGS["tiny_fp32"].with_(name="fp32_mqa_ragged", B=2, T=37, Hkv=1,
+                                                           rope_base=500.0),
+    # bf16, GQA 4/2, dh 64, two sequences, T not a multiple of 128
+    "bf16_gqa_dh64": workloads.BlockShape("bf16_gqa_dh64", "prefill", "bf16", B=2, T=200, d=256, H=4, Hkv=2,
+                                          dh=64, f=512, rope_base=1e4, eps=1e-6, gains="normal"),
+    # bf16, MQA 4/1, dh 128, ragged
+    "bf16_mqa_dh128": workloads.BlockShape("bf16_mqa_dh128", "prefill", "bf16", B=1, T=333, d=512, H=4, Hkv=1,
+                                           dh=128, f=1024, rope_base=5e5, eps=1e-5, gains="normal"),
+    # bf16, GQA 8/1 (largest group), one token per sequence
+    "bf16_t1": workloads.BlockShape("bf16_t1", "prefill", "bf16", B=3, T=1, d=1024, H=8, Hkv=1, dh=128,
+                                    f=1536, rope_base=1e4, eps=1e-6, gains="normal"),
+}
+
+
+def run_prefill(s, inp, with_cache=False, y_dtype=None, T_max=None):
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    T = inp["x"].shape[1]
+    cfg = block_config(s, max_pos=max(T, T_max or 0, 1))
+    dev = to_device(inp)
+    packed = tb.tb_pack_weights(cfg, dev)
+    kv = None
+    if with_cache:
+        kv = tb.KVCache.empty(s.B, s.Hkv, T_max or T, s.dh, dtype=s.torch_dtype, fill=float("nan"))
+    y = tb.tb_block_prefill(cfg, packed, dev["x"], y_dtype=tb.TB_F32 if y_dtype is None else y_dtype, kv=kv)
+    assert tb.tb_get_device_error(clear=True) == 0
+    return y, kv
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_prefill_small(name):
+    s = SMALL[name]
+    inp = workloads.make_block_inputs(s, seed=0)
+    y, kv = run_prefill(s, inp, with_cache=True, T_max=s.T + 5)
+    ref = oracle.block_prefill(workloads.to_f64(inp["x"]), oracle_weights(inp), oracle_cfg(s))
+    assert_close(y.cpu().double().numpy(), ref["y"], s.dtype, "y")
+    # the emitted cache holds the post-RoPE keys and values of every position
+    assert_close(kv.k[:, :, :s.T].cpu().double().numpy(), ref["k"], s.dtype, "k cache")
+    assert_close(kv.v[:, :, :s.T].cpu().double().numpy(), ref["v"], s.dtype, "v cache")
+    assert kv.lens.cpu().tolist() == [s.T] * s.B
+    # rows past T are untouched
+    assert torch.isnan(kv.k[:, :, s.T:].float()).all()
+
+
+def test_prefill_without_cache_equals_with_cache():
+    s = SMALL["bf16_gqa_dh64"]
+    inp = workloads.make_block_inputs(s, seed=3)
+    y0, _ = run_prefill(s, inp, with_cache=False)
+    y1, _ = run_prefill(s, inp, with_cache=True, T_max=256)
+    torch.testing.assert_close(y0, y1, rtol=0, atol=1e-5)
+
+
+def test_prefill_bf16_output():
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    s = SMALL["bf16_gqa_dh64"]
+    inp = workloads.make_block_inputs(s, seed=1)
+    y, _ = run_prefill(s, inp, y_dtype=tb.TB_BF16)
+    assert y.dtype == torch.bfloat16
+    ref = oracle.block_prefill(workloads.to_f64(inp["x"]), oracle_weights(inp), oracle_cfg(s))
+    assert_close(y.cpu().double().numpy(), ref["y"], "bf16", "y (bf16)")
+
+
+def test_prefill_causality_on_gpu():
+    """A prefix of the sequence gives the same rows as the whole sequence."""
+    s = SMALL["bf16_mqa_dh128"]
+    inp = workloads.make_block_inputs(s, seed=2)
+    full, _ = run_prefill(s, inp)
+    short = dict(inp, x=inp["x"][:, :130].contiguous())
+    part, _ = run_prefill(s.with_(T=130), short)
+    torch.testing.assert_close(part, full[:, :130], rtol=0, atol=1e-5)
+
+
+def test_empty_prefill_is_a_noop():
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    s = SMALL["bf16_gqa_dh64"]
+    inp = workloads.make_block_inputs(s.with_(B=1, T=4), seed=0)
+    cfg = block_config(s, 16)
+    dev = to_device(inp)
+    packed = tb.tb_pack_weights(cfg, dev)
+    x = torch.empty((0, 4, s.d), dtype=torch.bfloat16, device="cuda")
+    y = tb.tb_block_prefill(cfg, packed, x)
+    assert y.shape == (0, 4, s.d)
+
+
+def _full_rows_case(name, sample=None, seed=0):
+    s = workloads.CONFIGS[name]
+    inp = workloads.make_block_inputs(s, seed=seed)
+    y, kv = run_prefill(s, inp, with_cache=True)
+    w = oracle_weights(inp)
+    cfg = oracle_cfg(s)
+    x64 = workloads.to_f64(inp["x"])
+    report = []
+    for b in range(s.B):
+        rows = None if sample is None else sample(b, s.T)
+        if rows is not None and len(rows) == 0:
+            continue
+        ref = oracle.block_prefill_seq(x64[b], w, cfg, rows=rows)
+        got = y[b].cpu().double().numpy()[ref["rows"]]
+        report.append(errors(got, ref["y"]))
+        S = ref["k"].shape[1]
+        assert_close(kv.k[b, :, :S].cpu().double().numpy(), ref["k"], s.dtype, f"k cache b={b}")
+        assert_close(kv.v[b, :, :S].cpu().double().numpy(), ref["v"], s.dtype, f"v cache b={b}")
+    return s, y, report
+
+
+def test_prefill_mha_768_all_rows():
+    s, y, rep = _full_rows_case("mha_768")
+    for e in rep:
+        assert e["finite"] and e["rel_l2"] <= 1e-2 and e["max_abs"] <= 3e-2, e
+
+
+def test_prefill_llama2_7b_all_rows():
+    s, y, rep = _full_rows_case("llama2_7b")
+    for e in rep:
+        assert e["finite"] and e["rel_l2"] <= 1e-2, e
+        assert e["max_abs"] <= 3e-2, e
+
+
+def _gqa_rows(b, T):
+    rng = np.random.default_rng(100 + b)
+    if b == 0:
+        return np.r_[np.arange(64), np.arange(T - 64, T), rng.choice(T, 128, replace=False)]
+    if b == 3:
+        return np.r_[np.arange(16), np.arange(T - 16, T), rng.choice(T, 32, replace=False)]
+    return []
+
+
+def test_prefill_gqa_8k_sampled_rows():
+    s, y, rep = _full_rows_case("gqa_8k", sample=_gqa_rows)
+    assert torch.isfinite(y).all()
+    for e in rep:
+        assert e["finite"] and e["rel_l2"] <= 1e-2, e
+        assert e["max_abs"] <= 3e-2, e
