@@ -19,6 +19,12 @@ from workloads import BlockShape
 F32_NORMWISE_TOL = 1e-4
 BF16_REL_L2_TOL = 1e-2
 BF16_MAX_ABS_TOL = 3e-2
+# Max-abs bound used for d = 4096 workloads.  A CPU fp32 model of the bf16
+# path's rounding points (tests/rounding_model.py) reaches 7.2e-2 against the
+# oracle on a 1024-token slice of gqa_8k (4.2M outputs); the full workload has
+# ~32x more outputs, whose Gaussian-tail maximum is sqrt(ln(1.3e8)/ln(4.2e6))
+# ≈ 1.1x larger, so 1e-1 leaves ~25% headroom over pure rounding noise.
+D4096_MAX_ABS_BOUND = 1e-1
 
 
 def oracle_cfg(s: BlockShape) -> oracle.Cfg:
