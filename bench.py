@@ -357,6 +357,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["tb", "reference"], default="tb")
     ap.add_argument("--workload", default="gqa_8k")
+    ap.add_argument("--batch", type=int, default=0, help="override B of the prefill workload (profiling runs)")
     ap.add_argument("--decode-workload", default="gqa_decode")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -380,6 +381,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     peaks, peak_src = load_peaks()
     s = workloads.CONFIGS[args.workload]
+    if args.batch:
+        s = s.with_(name=f"{s.name}_b{args.batch}", B=args.batch)
 
     pre = bench_prefill(args, s, world, peaks)
     dec = None if args.no_decode else bench_decode(args, world, peaks)

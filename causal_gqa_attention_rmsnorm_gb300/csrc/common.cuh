@@ -118,6 +118,10 @@ cudaError_t gemm_simt_w2(int dtype, const void* A, const void* B, int M, int N, 
 cudaError_t attn_prefill_simt(int dtype, const void* q, const void* k, const void* v, void* o, int B,
                               int T, int H, int Hkv, int dh, int kv_stride, cudaStream_t s);
 
+// attn_tc.cu (bf16 path, dh 64 or 128)
+cudaError_t attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int T, int H, int Hkv,
+                            int dh, int kv_stride, cudaStream_t s);
+
 // attn_decode.cu
 int decode_chunk_keys();
 size_t decode_part_floats(int B, int H, int dh, int nchunk_max);

@@ -72,6 +72,8 @@ tb_status check_cfg(const tb_block_cfg* c) {
     if (c->d % 64 || c->f % 64)
       return fail(TB_ERR_UNSUPPORTED, "bf16 tensor-core path needs d and f multiples of 64 (d=%d f=%d)", c->d,
                   c->f);
+    if (c->dh != 64 && c->dh != 128)
+      return fail(TB_ERR_UNSUPPORTED, "bf16 tensor-core attention needs dh 64 or 128 (dh=%d)", c->dh);
   }
   return TB_OK;
 }
@@ -303,7 +305,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
     rec.stage("qkv");
     TB_TRY(gemm_tc_qkv(x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
-    TB_TRY(attn_prefill_simt(dt, W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, s));
+    TB_TRY(attn_prefill_tc(W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, s));
     rec.stage("wo");
     TB_TRY(gemm_tc_wo(W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
