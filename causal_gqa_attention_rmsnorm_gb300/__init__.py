@@ -6,9 +6,9 @@ the build step (``build``) and the work accounting used by the benchmark
 (``accounting``).
 """
 from .binding import (TB_BF16, TB_F32, TB_DEVERR_CACHE_FULL, TB_DEVERR_TIMEOUT, BlockConfig, KVCache, TbError,
-                      tb_block_decode, tb_block_prefill, tb_get_device_error, tb_kvcache_append,
+                      tb_block_decode, tb_block_decode_noalloc, tb_block_prefill, tb_get_device_error, tb_kvcache_append,
                       tb_pack_weights, tb_packed_weights_bytes, tb_status_string, tb_workspace_bytes)
 
 __all__ = ["TB_BF16", "TB_F32", "TB_DEVERR_CACHE_FULL", "TB_DEVERR_TIMEOUT", "BlockConfig", "KVCache", "TbError",
-           "tb_block_decode", "tb_block_prefill", "tb_get_device_error", "tb_kvcache_append", "tb_pack_weights",
+           "tb_block_decode", "tb_block_decode_noalloc", "tb_block_prefill", "tb_get_device_error", "tb_kvcache_append", "tb_pack_weights",
            "tb_packed_weights_bytes", "tb_status_string", "tb_workspace_bytes"]

@@ -24,7 +24,7 @@ STATUS = {0: "TB_OK", 1: "TB_ERR_INVALID_ARG", 2: "TB_ERR_UNSUPPORTED", 3: "TB_E
           4: "TB_ERR_CACHE_FULL", 5: "TB_ERR_TIMEOUT"}
 WEIGHT_FIELDS = ("g_attn", "wq", "wk", "wv", "wo", "g_mlp", "w1", "w3", "w2")
 EXPORTED = ("tb_packed_weights_bytes", "tb_pack_weights", "tb_workspace_bytes", "tb_block_prefill",
-            "tb_block_decode", "tb_kvcache_append", "tb_get_device_error", "tb_status_string",
+            "tb_block_decode", "tb_block_decode_noalloc", "tb_kvcache_append", "tb_get_device_error", "tb_status_string",
             "tb_last_error_message")
 
 
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
                                        P(tb_kvcache), c_void_p, c_size_t, c_void_p]
         L.tb_block_decode.argtypes = [P(tb_block_cfg), c_void_p, c_void_p, c_void_p, c_int32, P(tb_kvcache),
                                       c_void_p, c_size_t, c_void_p]
+        L.tb_block_decode_noalloc.argtypes = [P(tb_block_cfg), c_void_p, c_void_p, c_void_p, c_int32,
+                                              P(tb_kvcache), c_void_p]
         L.tb_kvcache_append.argtypes = [P(tb_kvcache), c_void_p, c_void_p, c_int32, c_void_p]
         L.tb_get_device_error.argtypes = [c_void_p, P(c_int32), c_int32]
         L.tb_status_string.argtypes = [c_int32]
@@ -82,7 +84,8 @@ def lib() -> ctypes.CDLL:
         L.tbx_trace_read.restype = c_int32
         L.tbx_trace_stage_name.argtypes = [c_int32]
         L.tbx_trace_stage_name.restype = ctypes.c_char_p
-        for fn in ("tb_pack_weights", "tb_block_prefill", "tb_block_decode", "tb_kvcache_append",
+        for fn in ("tb_pack_weights", "tb_block_prefill", "tb_block_decode", "tb_block_decode_noalloc",
+                   "tb_kvcache_append",
                    "tb_get_device_error", "tbx_gemm_bf16"):
             getattr(L, fn).restype = c_int32
         _lib = L
@@ -231,6 +234,24 @@ def tb_block_decode(cfg: BlockConfig, packed: torch.Tensor, x: torch.Tensor, kv:
     _check("tb_block_decode", lib().tb_block_decode(ctypes.byref(cfg.c()), packed.data_ptr(), x.data_ptr(),
                                                     y.data_ptr(), y_dtype, ctypes.byref(kvs), ws.data_ptr(),
                                                     ws_bytes, _stream(stream)))
+    return y
+
+
+def tb_block_decode_noalloc(cfg: BlockConfig, packed: torch.Tensor, x: torch.Tensor, kv: KVCache,
+                            y: Optional[torch.Tensor] = None, y_dtype: int = TB_F32, stream=None) -> torch.Tensor:
+    """tb_block_decode without a workspace argument: the library uses its own
+    fixed 64 MiB device scratch, for callers that cannot allocate device
+    memory.  Calls that may overlap on the GPU must be serialised."""
+    kvs = kv.c()
+    B = kvs.B
+    _need(x, "x", cfg.torch_dtype, (B, 1, cfg.d))
+    ydt = torch.float32 if y_dtype == TB_F32 else torch.bfloat16
+    if y is None:
+        y = torch.empty((B, 1, cfg.d), dtype=ydt, device=x.device)
+    _need(y, "y", ydt, (B, 1, cfg.d))
+    _check("tb_block_decode_noalloc", lib().tb_block_decode_noalloc(ctypes.byref(cfg.c()), packed.data_ptr(),
+                                                                    x.data_ptr(), y.data_ptr(), y_dtype,
+                                                                    ctypes.byref(kvs), _stream(stream)))
     return y
 
 

@@ -67,6 +67,8 @@ namespace tb {
 
 // tb_api.cu: device address of the per-device error word (TB_DEVERR_* bits)
 int* device_error_word();
+// tb_api.cu: record the message tb_last_error_message() returns; returns st.
+tb_status report(tb_status st, const char* fmt, ...);
 
 // elementwise.cu
 cudaError_t launch_pack(int dtype, const Dims& D, const tb_block_weights& w, void* packed,

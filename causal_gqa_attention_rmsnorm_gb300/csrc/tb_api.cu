@@ -30,6 +30,14 @@ tb_status cuda_fail(cudaError_t e, const char* where) {
 
 }  // namespace
 
+tb_status report(tb_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
 // Device address of the error word on the current device.
 int* device_error_word() {
   static int* ptrs[64] = {nullptr};

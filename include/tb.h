@@ -149,6 +149,28 @@ TB_API tb_status tb_block_decode(const tb_block_cfg *cfg, const void *packed, co
                           int32_t y_dtype, const tb_kvcache *kv, void *ws, size_t ws_bytes,
                           void *stream);
 
+/* tb_block_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for callers that must
+ * not call cudaMalloc or a framework allocator on their hot path (allocation
+ * can synchronise the device and take unbounded time), plugins whose host
+ * framework hands out no device memory, and runtimes without a device
+ * allocator.  It runs exactly tb_block_decode with the workspace taken from a
+ * file-scope device array of 64 MiB (enough for 32 sequences, a 16384-row
+ * cache, d = 4096, f = 14336) that every GPU loading the library holds until
+ * the process exits; the call allocates nothing.
+ *  Arguments and behaviour are those of tb_block_decode minus ws/ws_bytes.
+ *  A step whose tb_workspace_bytes(cfg, kv->B, kv->T_max, 1) exceeds 64 MiB
+ *  returns TB_ERR_INVALID_ARG and launches nothing.
+ *  The first call on each device looks up the array's device address
+ *  (cudaGetSymbolAddress) with that device current; make that first call
+ *  before any stream capture.
+ *  All calls share the one array and its contents persist between calls (the
+ *  step zeroes what it accumulates into), so calls that may overlap on the
+ *  GPU — on different streams, or from different threads — race; serialise
+ *  them, e.g. on one stream. */
+TB_API tb_status tb_block_decode_noalloc(const tb_block_cfg *cfg, const void *packed, const void *x, void *y,
+                                         int32_t y_dtype, const tb_kvcache *kv, void *stream);
+
 /* Append n post-RoPE rows per sequence: k_new, v_new are device
  * [B, Hkv, n, dh] of kv->dtype; rows go to [lens[b], lens[b]+n) and lens[b]
  * grows by n.  A sequence with lens[b] + n > T_max sets TB_DEVERR_CACHE_FULL

@@ -109,6 +109,19 @@ def test_decode_argument_checks(lib):
     assert lib.tb_block_decode(ctypes.byref(c), FAKE, FAKE, FAKE + 4096, 0, ctypes.byref(kv), FAKE, 0, None) == 0
 
 
+def test_noalloc_decode_rejects_steps_beyond_its_scratch(lib):
+    # 64 sequences of a 16384-row cache at d = 4096 need more than the 64 MiB scratch
+    c = cfg(d=4096, H=32, Hkv=8, dh=128, f=14336, max_pos=16384)
+    assert lib.tb_workspace_bytes(ctypes.byref(c), 64, 16384, 1) > 64 << 20
+    kv = binding.tb_kvcache(FAKE, FAKE, FAKE, 64, 8, 16384, 128, 1)
+    st = lib.tb_block_decode_noalloc(ctypes.byref(c), FAKE, FAKE, FAKE + 4096, 0, ctypes.byref(kv), None)
+    assert st == 1 and b"static scratch" in lib.tb_last_error_message()
+    # a step that fits is not rejected for its size (its bad pointers are, later)
+    assert lib.tb_workspace_bytes(ctypes.byref(c), 32, 16384, 1) <= 64 << 20
+    st = lib.tb_block_decode_noalloc(ctypes.byref(c), FAKE, None, FAKE + 4096, 0, ctypes.byref(kv), None)
+    assert st == 1
+
+
 def test_append_argument_checks(lib):
     kv = binding.tb_kvcache(FAKE, FAKE, FAKE, 2, 2, 16, 64, 1)
     assert lib.tb_kvcache_append(ctypes.byref(kv), FAKE, FAKE, -1, None) == 1
