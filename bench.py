@@ -360,6 +360,7 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override B of the prefill workload (profiling runs)")
     ap.add_argument("--decode-workload", default="gqa_decode")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling runs); prints the decode object")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
@@ -384,6 +385,11 @@ def main():
     if args.batch:
         s = s.with_(name=f"{s.name}_b{args.batch}", B=args.batch)
 
+    if args.no_prefill:
+        dec = bench_decode(args, world, peaks)
+        if rank == 0:
+            print(json.dumps({"decode": dec}))
+        return
     pre = bench_prefill(args, s, world, peaks)
     dec = None if args.no_decode else bench_decode(args, world, peaks)
 

@@ -8,16 +8,19 @@
 // section 6 describes, which never materialises the T×T matrix.
 //
 // One CTA per (query head, sequence, 128-query tile), heaviest tiles first:
-//   warp 4      TMA: the Q tile once, then K and V tiles of 128 keys through a
+//   warp 8      TMA: the Q tile once, then K and V tiles of 128 keys through a
 //               two-stage ring (3-D tensor maps, so keys past T read as zero);
-//   warp 5      MMA issuer: S_j = Q·K_jᵀ into one of two TMEM buffers
+//   warp 9      MMA issuer: S_j = Q·K_jᵀ into one of two TMEM buffers
 //               (M = 128, N = 128, K = dh), then O += P_j·V_j into a TMEM
 //               accumulator (M = 128, N = dh, K = 128; V is the MN-major
 //               operand, read in place from its [keys, dh] tile);
-//   warps 0..3  softmax: thread i owns query row i (TMEM lane i), so row max
-//               and row sum need no shuffles; fp32 online softmax in base 2
-//               with the scale folded in, bf16 P written to shared memory in
-//               the 128-byte-swizzled K-major layout the MMA reads.
+//   warps 0..7  softmax: query row i is TMEM lane i; warps w and w+4 share the
+//               32 rows of lane quarter w%4, each exponentiating half of the
+//               128 key columns (and owning half of O's columns); both read
+//               the whole row from TMEM for its maximum, so they agree on it
+//               without exchanging anything.  fp32 online softmax in base 2,
+//               scale and max folded into one FMA, bf16 P written to shared
+//               memory in the 128-byte-swizzled K-major layout the MMA reads.
 // Key tiles past the query tile's last row are never loaded (causal skip);
 // only the diagonal tile is masked element by element.  O is rescaled only
 // when a row maximum grows by more than 2^8 over the one in use: with a stale
@@ -48,8 +51,17 @@ template <int DH> struct AttnCfg {
   static constexpr uint32_t TMEM_O = 2 * kBN;              // S buffers at columns 0 and 128
 };
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Named barrier for the 64 threads of one softmax warp pair.
+__device__ __forceinline__ void pair_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
 template <int DH>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out, int T, int H, int Hkv, int n_qtiles,
               float scale_log2, int* err) {
@@ -86,8 +98,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&s_free[i], 8);
+      mbar_init(&p_full[i], 8);
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(o_full, 1);
@@ -95,7 +107,7 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -104,7 +116,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       prefetch_tmap(&tmQ);
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait(&v_full[j & 1], (j >> 1) & 1, &no_abort, err);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN);
@@ -191,45 +203,62 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(drain, 0, &no_abort, err);
     }
   } else {
-    // ---------------- softmax (warps 0..3, one query row per thread) ----------------
-    const int r = warp * 32 + lane;
+    // ---------------- softmax (warps 0..7, half a query row per thread) ----------------
+    constexpr int HC = kBN / 2;          // key columns per thread
+    constexpr int HO = DH / 2;           // O columns per thread
+    const int quad = warp & 3, half = warp >> 2;
+    const int r = quad * 32 + lane;
     const int qi = q0 + r;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     uint8_t* pbase = smem + C::OFF_P;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int st = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait(&s_full[st], ph, abort_flag, err)) {
+      if (!mbar_wait_warp(&s_full[st], ph, abort_flag, err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[kBN];
+      float s[HC];
 #pragma unroll
-      for (int c = 0; c < kBN; c += 16) {
+      for (int c = 0; c < HC; c += 16) {
         uint32_t u[16];
-        tmem_ld16(lane_base + st * kBN + c, u);
+        tmem_ld16(lane_base + st * kBN + half * HC + c, u);
 #pragma unroll
         for (int i = 0; i < 16; ++i) s[c + i] = __uint_as_float(u[i]);
       }
       tmem_wait_ld();
+      // raw row maximum over all 128 columns (own half kept in s, the other
+      // half only scanned); only the diagonal tile masks future keys
+      const bool diag = (j == nkv - 1);
+      const int lim = qi - j * kBN;                     // column c is a future key iff c > lim
+      float mx = -INFINITY;
+      if (diag) {
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+          if (half * HC + c > lim) s[c] = -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < HC; ++c) mx = fmaxf(mx, s[c]);
+      }
+#pragma unroll 1
+      for (int c = 0; c < HC; c += 16) {
+        uint32_t u[16];
+        tmem_ld16(lane_base + st * kBN + (half ^ 1) * HC + c, u);
+        tmem_wait_ld();
+        const int c0 = (half ^ 1) * HC + c;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, (diag && c0 + i > lim) ? -INFINITY : __uint_as_float(u[i]));
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[st]);
 
-      const bool diag = (j == nkv - 1);
-      const int key0 = j * kBN;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        float v = s[c] * scale_log2;
-        if (diag && key0 + c > qi) v = -INFINITY;
-        s[c] = v;
-        mx = fmaxf(mx, v);
-      }
-      const float m_new = fmaxf(m_used, mx);
+      const float m_new = fmaxf(m_used, mx * scale_log2);
       bool need = false;
       if (j == 0) {
         m_used = m_new;
@@ -238,20 +267,20 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (__any_sync(0xffffffffu, need)) {
         // the previous P·V must be finished before O is read and rewritten
-        if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, err)) {
+        if (!mbar_wait_warp(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float factor = need ? exp2f(m_used - m_new) : 1.f;
+        const float factor = need ? ex2(m_used - m_new) : 1.f;
 #pragma unroll 1
-        for (int c = 0; c < DH; c += 16) {
+        for (int c = 0; c < HO; c += 16) {
           uint32_t u[16];
-          tmem_ld16(lane_base + C::TMEM_O + c, u);
+          tmem_ld16(lane_base + C::TMEM_O + half * HO + c, u);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * factor);
-          tmem_st16(lane_base + C::TMEM_O + c, u);
+          tmem_st16(lane_base + C::TMEM_O + half * HO + c, u);
         }
         tmem_wait_st();
         if (need) {
@@ -261,18 +290,18 @@ __global__ void __launch_bounds__(192, 1)
       }
       const float msub = m_used == -INFINITY ? 0.f : m_used;
       // P buffer st is free once the P·V two tiles back has finished
-      if (j >= 2 && !mbar_wait(&pv_done[st], ((j - 2) >> 1) & 1, abort_flag, err)) {
+      if (j >= 2 && !mbar_wait_warp(&pv_done[st], ((j - 2) >> 1) & 1, abort_flag, err)) {
         ok = false;
         break;
       }
-      uint8_t* prow = pbase + st * C::P_BYTES + r * 128;
+      uint8_t* prow = pbase + st * C::P_BYTES + half * (kBM * 128) + r * 128;
       float rowsum = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBN; c += 8) {
+      for (int c = 0; c < HC; c += 8) {
         float p[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          p[i] = exp2f(s[c + i] - msub);
+          p[i] = ex2(fmaf(s[c + i], scale_log2, -msub));
           rowsum += p[i];
         }
         uint4 w;
@@ -282,8 +311,7 @@ __global__ void __launch_bounds__(192, 1)
         w.y = *reinterpret_cast<uint32_t*>(&t1);
         w.z = *reinterpret_cast<uint32_t*>(&t2);
         w.w = *reinterpret_cast<uint32_t*>(&t3);
-        const int blk = c >> 6, chunk = (c & 63) >> 3;
-        *reinterpret_cast<uint4*>(prow + blk * (kBM * 128) + ((chunk ^ (r & 7)) << 4)) = w;
+        *reinterpret_cast<uint4*>(prow + (((c >> 3) ^ (r & 7)) << 4)) = w;
       }
       l += rowsum;
       fence_proxy_async();    // generic-proxy P stores -> visible to the tensor core
@@ -291,14 +319,22 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[st]);
     }
-    if (ok && mbar_wait(o_full, 0, abort_flag, err)) {
+    const bool have_o = ok && mbar_wait_warp(o_full, 0, abort_flag, err);
+    // both halves' sums share the same maximum: add them (the P buffers are
+    // free once the last P·V has finished).  Every softmax thread reaches the
+    // pair barrier, whether or not its waits succeeded.
+    float* red = reinterpret_cast<float*>(pbase);
+    if (have_o) red[half * 128 + r] = l;
+    pair_sync(1 + quad);
+    if (have_o) {
       tc_fence_after();
+      l += red[(half ^ 1) * 128 + r];
       const float inv = l > 0.f ? 1.0f / l : 0.f;
-      bf16* orow = out + ((size_t)b * T + qi) * (size_t)H * DH + (size_t)h * DH;
+      bf16* orow = out + ((size_t)b * T + qi) * (size_t)H * DH + (size_t)h * DH + half * HO;
 #pragma unroll 1
-      for (int c = 0; c < DH; c += 16) {
+      for (int c = 0; c < HO; c += 16) {
         uint32_t u[16];
-        tmem_ld16(lane_base + C::TMEM_O + c, u);
+        tmem_ld16(lane_base + C::TMEM_O + half * HO + c, u);
         tmem_wait_ld();
         if (qi < T) {
           uint4 w[2];
@@ -318,7 +354,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -345,7 +381,7 @@ cudaError_t run(const void* q, const void* k, const void* v, void* o, int B, int
   }
   const int nq = (T + kBM - 1) / kBM;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
-  k_attn_tc<DH><<<dim3(H, B, nq), 192, C::SMEM, s>>>(tq, tk, tv, (bf16*)o, T, H, Hkv, nq, scale_log2,
+  k_attn_tc<DH><<<dim3(H, B, nq), 320, C::SMEM, s>>>(tq, tk, tv, (bf16*)o, T, H, Hkv, nq, scale_log2,
                                                     device_error_word());
   return cudaGetLastError();
 }

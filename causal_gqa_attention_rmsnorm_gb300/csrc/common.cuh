@@ -75,7 +75,7 @@ cudaError_t launch_pack(int dtype, const Dims& D, const tb_block_weights& w, voi
                         const Packed& P, float rope_base, cudaStream_t s);
 cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, float* r,
                              float* ssq_zero, int T, int32_t* lens_set, int32_t* lens_bump,
-                             int32_t* pos_out, int T_max, int* err, cudaStream_t s);
+                             int32_t* pos_out, int T_max, int* zero_word, int* err, cudaStream_t s);
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new,
                              int n, int* err, cudaStream_t s);
 
@@ -129,6 +129,6 @@ int decode_chunk_keys();
 size_t decode_part_floats(int B, int H, int dh, int nchunk_max);
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos,
                         int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max,
-                        void* o, cudaStream_t s);
+                        int* work_counter, void* o, cudaStream_t s);
 
 }  // namespace tb

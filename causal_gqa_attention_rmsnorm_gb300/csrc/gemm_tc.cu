@@ -51,10 +51,31 @@ struct EpiF32 {
 };
 #pragma nv_diag_suppress 177
 
+// Tile index -> (m, n) tile.  group_m == 0 walks n fastest (CTAs running
+// together share one A row block and stream the whole B panel, best when B
+// is reused from L2 or K is long).  Otherwise tiles go in groups of group_m
+// row blocks, m fastest inside a group, so the CTAs running together touch
+// group_m A blocks and a few B blocks: both stay in L2 even when the B panel
+// is larger than L2.
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int group_m, int& mt, int& nt) {
+  if (group_m <= 0) {
+    mt = tile / n_tiles;
+    nt = tile - mt * n_tiles;
+    return;
+  }
+  const int per_group = group_m * n_tiles;
+  const int g = tile / per_group;
+  const int first_m = g * group_m;
+  const int gm = min(group_m, m_tiles - first_m);
+  const int local = tile - g * per_group;
+  mt = first_m + local % gm;
+  nt = local / gm;
+}
+
 template <int BN, class Epi>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
-              uint32_t a_box_bytes, Epi epi, int* err) {
+              uint32_t a_box_bytes, int group_m, Epi epi, int* err) {
   using C = TcCfg<BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -105,7 +126,8 @@ __global__ void __launch_bounds__(192, 1)
       for (int s = 0; s < STAGES; ++s) issued[s] = 0, last_phase[s] = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
-        const int mt = tile / n_tiles, nt = tile - mt * n_tiles;
+        int mt, nt;
+        tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) {
             ok = false;
@@ -169,9 +191,10 @@ __global__ void __launch_bounds__(192, 1)
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, err)) break;
+      if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, err)) break;
       tc_fence_after();
-      const int mt = tile / n_tiles, nt = tile - mt * n_tiles;
+      int mt, nt;
+      tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
       const int row = mt * BM + quad * 32 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
       float rsum = 0.f;
@@ -243,9 +266,15 @@ cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& ep
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int m_tiles = (M + BM - 1) / BM;
+  const int tiles = m_tiles * ((N + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  k_gemm_tc<BN, Epi><<<grid, 192, C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, epi, device_error_word());
+  // Short K with a B panel beyond what L2 keeps: group 32 row blocks (32 MB of
+  // A at K = 4096).  Otherwise n fastest.
+  const size_t b_bytes = (size_t)N * K * 2;
+  const int group_m = (K <= 8192 && b_bytes > (size_t(48) << 20) && m_tiles > 32) ? 32 : 0;
+  k_gemm_tc<BN, Epi><<<grid, 192, C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
+                                                device_error_word());
   return cudaGetLastError();
 }
 

@@ -122,6 +122,7 @@ struct Work {
   float* r;
   float* ssq;
   int32_t* pos;
+  int* counter;
   void* q;
   void* k;
   void* v;
@@ -149,6 +150,7 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
   w.r = (float*)take(M * 4);
   w.ssq = (float*)take(M * 4);
   w.pos = (int32_t*)take((size_t)B * 4);
+  w.counter = (int*)take(4);
   w.q = take(M * hd * es);
   if (mode == 0) {
     w.k = take(M * kvd * es);
@@ -293,7 +295,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
   StageRecorder rec(s);
   rec.stage("rms");
   TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, W.ssq, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
-                          err, s));
+                          nullptr, err, s));
   const QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr};
   const WoArgs wa{x, W.h, W.hb, W.ssq};
   const W13Args ga{W.ssq, W.a};
@@ -355,7 +357,8 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
 
   StageRecorder rec(s);
   rec.stage("rms");
-  TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, W.ssq, 1, nullptr, kv->lens, W.pos, kv->T_max, err, s));
+  TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, W.ssq, 1, nullptr, kv->lens, W.pos, kv->T_max,
+                          W.counter, err, s));
   const QKVArgs qa{W.r, P.rope, W.q, kv->k, kv->v, 1, kv->T_max, W.pos};
   const WoArgs wa{x, W.h, W.hb, W.ssq};
   const W13Args ga{W.ssq, W.a};
@@ -365,7 +368,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(gemm_simt_qkv(dt, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                       W.nchunk_max, W.o, s));
+                       W.nchunk_max, W.counter, W.o, s));
     rec.stage("wo");
     TB_TRY(gemm_simt_wo(dt, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
@@ -377,7 +380,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(gemm_tc_qkv(x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                       W.nchunk_max, W.o, s));
+                       W.nchunk_max, W.counter, W.o, s));
     rec.stage("wo");
     TB_TRY(gemm_tc_wo(W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
