@@ -9,13 +9,14 @@
 // chunks whose partial softmax states (running max m, sum l, unnormalised o)
 // a second kernel merges by log-sum-exp.
 //
-// bf16 (k_decode_stream): persistent warps take 256-key chunks from a global
+// bf16 (k_decode_mma): persistent warps take 256-key chunks from a global
 // counter, so the grid has no idle CTAs and the tail is one chunk.  Each warp
-// streams its chunk in 32-key stages through two shared-memory slots with
-// TMA (128-byte swizzle), the next stage always in flight while the current
-// one is computed.  q·k: lane = key, the swizzle makes the 32 rows' reads
-// conflict-free and q is a broadcast; p·v: lane = 4 (or 2) head dimensions,
-// p a broadcast; all products as packed fp32x2 FMAs.
+// streams its chunks in 16-key stages through three shared-memory slots with
+// TMA (128-byte swizzle), two stages always in flight while one is computed.
+// The two small contractions (G query heads against 16 keys) run as
+// warp-level m16n8k16 MMAs on fragments read with ldmatrix, which keeps the
+// instruction count per key far below the SIMT form so the kernel can run at
+// the rate the cache streams in; the softmax stays in fp32 registers.
 // fp32 (k_decode_split): one CTA per 256-key chunk, lanes read 16-byte pieces
 // of consecutive rows straight from global memory.
 // Rows at or beyond lens[b]+1 never reach the result.
@@ -28,7 +29,8 @@
 namespace tb {
 namespace {
 
-constexpr int kChunk = 256;  // keys per CTA
+constexpr int kChunk = 256;  // keys per CTA (fp32 kernel) and per work item (bf16 kernel)
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the running max grows by more than 2^8
 constexpr int kWarps = 4;
 
 template <int DH>
@@ -224,279 +226,303 @@ __global__ void k_decode_combine(const float* __restrict__ part, const int32_t* 
 // bf16 streaming kernel
 // ---------------------------------------------------------------------------
 
-constexpr int kSChunk = 256;   // keys per work item
-constexpr int kSKeys = 32;     // keys per stage (one per lane)
-constexpr int kSWarps = 6;
+constexpr int kMChunk = 256;   // keys per work item (one partial state per head)
+constexpr int kMKeys = 16;     // keys per stage
+constexpr int kMSlots = 3;     // stages in shared memory per warp: the current one + 2 in flight
+constexpr int kMWarps = 8;
 
-template <int DH, int G> struct StreamCfg {
-  static constexpr int NB = DH / 64;                           // 128-byte boxes per row
-  static constexpr uint32_t HALF_BYTES = kSKeys * 128;         // one box: 32 rows x 128 B
-  static constexpr uint32_t KV_BYTES = NB * HALF_BYTES;        // K (or V) of one stage
-  static constexpr uint32_t SLOT_BYTES = 2 * KV_BYTES;         // K then V
-  static constexpr uint32_t WARP_SLOTS = 2 * SLOT_BYTES;
-  static constexpr uint32_t Q_FLOATS = G * DH;
-  static constexpr uint32_t OFF_Q = kSWarps * WARP_SLOTS;
-  static constexpr uint32_t OFF_P = OFF_Q + kSWarps * Q_FLOATS * 4;
-  static constexpr uint32_t OFF_BAR = OFF_P + kSWarps * kSKeys * G * 4;
-  static constexpr uint32_t OFF_PRE = OFF_BAR + kSWarps * 2 * 8;
+template <int DH> struct MCfg {
+  static constexpr int NB = DH / 64;                          // 128-byte boxes per row
+  static constexpr uint32_t BOX = kMKeys * 128;               // 16 rows x 128 B
+  static constexpr uint32_t KV_BYTES = NB * BOX;              // K (or V) of one stage
+  static constexpr uint32_t SLOT = 2 * KV_BYTES;              // K then V
+  static constexpr uint32_t WARP_BYTES = kMSlots * SLOT;
+  static constexpr uint32_t OFF_BAR = kMWarps * WARP_BYTES;
+  static constexpr uint32_t OFF_PRE = OFF_BAR + kMWarps * kMSlots * 8;
 };
 
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
 }
 
+// D = A·B + D, m16n8k16, bf16 inputs, fp32 accumulators (warp-level MMA).
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// Address of the 16-byte piece holding dims [8·chunk, 8·chunk+8) of stage row
+// `row` in a K or V stage written by TMA with the 128-byte swizzle.
+template <int DH>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
+  return base + (chunk >> 3) * MCfg<DH>::BOX + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+// Each warp owns a stream of work items (a sequence, a KV head, 256 keys) taken
+// from a global counter, and walks it in 16-key stages.  Per stage:
+//   S[16 × 16] = Q·Kᵀ with Q the G query heads padded to 16 rows (held as
+//   bf16 MMA fragments in registers for the whole item) and K fragments read
+//   with ldmatrix from the swizzled stage; lane (g, t) then holds four scores
+//   of head g, so the row max is a two-step shuffle within its quad;
+//   O[16 × dh] += P·V with P built in registers from the score fragments and
+//   V fragments read with ldmatrix.trans.
+// The tensor cores only shrink the instruction count; the kernel is bound by
+// reading K and V from HBM.
 template <int DH, int G>
-__global__ void __launch_bounds__(kSWarps * 32, 1)
-    k_decode_stream(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const bf16* __restrict__ q, const int32_t* __restrict__ pos_arr, int B, int Hkv,
-                    float* __restrict__ part, int nchunk_max, int* __restrict__ counter, float scale_log2,
-                    int* err) {
-  using C = StreamCfg<DH, G>;
+__global__ void __launch_bounds__(kMWarps * 32, 1)
+    k_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const bf16* __restrict__ q, const int32_t* __restrict__ pos_arr, int B, int Hkv,
+                 float* __restrict__ part, int nchunk_max, int* __restrict__ counter, float scale_log2, int* err) {
+  using C = MCfg<DH>;
   using namespace ptx;
+  static_assert(G <= 8, "at most 8 query heads per KV head");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);       // [B+1] item prefix over sequences
+  const int g = lane >> 2, t = lane & 3;     // MMA fragment row (query head) and column pair
+  int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
   __shared__ int abort_word;
 
-  // items of sequence b: Hkv x ceil((pos+1)/chunk), in (b, kv head, chunk) order
   if (threadIdx.x == 0) {
     int acc = 0;
     for (int b = 0; b < B; ++b) {
       pre[b] = acc;
       const int p = pos_arr[b];
-      acc += p < 0 ? 0 : Hkv * ((p + kSChunk) / kSChunk);
+      acc += p < 0 ? 0 : Hkv * ((p + kMChunk) / kMChunk);
     }
     pre[B] = acc;
     abort_word = 0;
   }
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * kMSlots;
   if (lane == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int i = 0; i < kMSlots; ++i) mbar_init(&full[i], 1);
     fence_barrier_init();
   }
   __syncthreads();
   volatile int* abort_flag = &abort_word;
   const int total = pre[B];
   const int H = Hkv * G;
-
-  uint8_t* slots = smem + warp * C::WARP_SLOTS;
-  float* qs = reinterpret_cast<float*>(smem + C::OFF_Q) + warp * C::Q_FLOATS;
-  float* ps = reinterpret_cast<float*>(smem + C::OFF_P) + warp * kSKeys * G;
+  uint8_t* slots = smem + warp * C::WARP_BYTES;
+  const uint32_t slots_u32 = smem_u32(slots);
 
   struct Item { int b, kvh, c, key0, nkeys; };
-  auto decode = [&](int t) {
-    int lo = 0, hi = B - 1;                 // last b with pre[b] <= t
+  auto decode = [&](int id) {
+    int lo = 0, hi = B - 1;                    // last b with pre[b] <= id
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= t) lo = mid; else hi = mid - 1;
+      if (pre[mid] <= id) lo = mid; else hi = mid - 1;
     }
-    const int b = lo;
-    const int n = pos_arr[b] + 1;
-    const int nch = (n + kSChunk - 1) / kSChunk;
-    const int r = t - pre[b];
+    const int n = pos_arr[lo] + 1;
+    const int nch = (n + kMChunk - 1) / kMChunk;
+    const int r = id - pre[lo];
     Item it;
-    it.b = b;
+    it.b = lo;
     it.kvh = r / nch;
     it.c = r - it.kvh * nch;
-    it.key0 = it.c * kSChunk;
-    it.nkeys = min(kSChunk, n - it.key0);
+    it.key0 = it.c * kMChunk;
+    it.nkeys = min(kMChunk, n - it.key0);
     return it;
   };
-  // lane 0: TMA of stage `st` of item `it` into slot `sl` (K and V, all boxes)
-  auto issue = [&](const Item& it, int st, int sl) {
-    uint8_t* base = slots + sl * C::SLOT_BYTES;
-    mbar_arrive_expect_tx(&full[sl], C::SLOT_BYTES);
-    const int y = it.key0 + st * kSKeys, z = it.b * Hkv + it.kvh;
+
+  // ---- lane 0: item queue and stage producer ----
+  int queue[4] = {0, 0, 0, 0};
+  int qn = 0, reserve = 0, pidx = 0, pst = 0;
+  uint32_t issued = 0, consumed = 0;
+  bool stream_done = false;
+  auto push = [&]() {
+    queue[qn++] = reserve;
+    reserve = atomicAdd(counter, 1);          // the reply is needed only at the next push
+  };
+  auto issue_one = [&]() {
+    while (!stream_done) {
+      if (pidx >= qn) push();
+      const int id = queue[pidx];
+      if (id >= total) {
+        stream_done = true;
+        return;
+      }
+      const Item it = decode(id);
+      const int nst = (it.nkeys + kMKeys - 1) / kMKeys;
+      if (pst < nst) {
+        const int sl = issued % kMSlots;
+        uint8_t* base = slots + sl * C::SLOT;
+        fence_proxy_async();       // earlier generic writes to the slot, before the TMA overwrite
+        mbar_arrive_expect_tx(&full[sl], C::SLOT);
+        const int y = it.key0 + pst * kMKeys, z = it.b * Hkv + it.kvh;
 #pragma unroll
-    for (int h = 0; h < C::NB; ++h) {
-      tma_load_3d(&tmK, base + h * C::HALF_BYTES, &full[sl], h * 64, y, z);
-      tma_load_3d(&tmV, base + C::KV_BYTES + h * C::HALF_BYTES, &full[sl], h * 64, y, z);
+        for (int hb = 0; hb < C::NB; ++hb) {
+          tma_load_3d(&tmK, base + hb * C::BOX, &full[sl], hb * 64, y, z);
+          tma_load_3d(&tmV, base + C::KV_BYTES + hb * C::BOX, &full[sl], hb * 64, y, z);
+        }
+        ++pst;
+        ++issued;
+        return;
+      }
+      ++pidx;
+      pst = 0;
     }
   };
-
-  int cur = 0, nxt = 0;
   if (lane == 0) {
-    cur = atomicAdd(counter, 1);
-    nxt = atomicAdd(counter, 1);
+    reserve = atomicAdd(counter, 1);
+    push();
   }
-  cur = __shfl_sync(0xffffffffu, cur, 0);
-  nxt = __shfl_sync(0xffffffffu, nxt, 0);
-  uint32_t use = 0;            // stages consumed so far by this warp
-  int pending = -1;            // slot with a load in flight that no one will consume (abort path)
-  if (cur < total && lane == 0) issue(decode(cur), 0, 0);
-  bool ok = true;
 
-  while (ok && cur < total) {
+  bool ok = true;
+  while (ok) {
+    const int cur = __shfl_sync(0xffffffffu, queue[0], 0);
+    if (cur >= total) break;
     const Item it = decode(cur);
-    const int nst = (it.nkeys + kSKeys - 1) / kSKeys;
-    // q of the G heads of this KV head, in fp32, pre-scaled to base-2 logits
-    for (int i = lane; i < G * DH / 8; i += 32) {
-      const int g = i / (DH / 8), e = (i % (DH / 8)) * 8;
-      const uint4 raw = *reinterpret_cast<const uint4*>(q + ((size_t)it.b * H + it.kvh * G + g) * DH + e);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    const int nst = (it.nkeys + kMKeys - 1) / kMKeys;
+    // Q fragments: rows = query heads of this KV head (rows >= G are zero)
+    uint32_t qa0[DH / 16], qa2[DH / 16];
+    {
+      const bf16* qrow = q + ((size_t)it.b * H + it.kvh * G + (g < G ? g : 0)) * DH;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = bf2_to_f2(w[k]);
-        qs[g * DH + e + 2 * k] = f.x * scale_log2;
-        qs[g * DH + e + 2 * k + 1] = f.y * scale_log2;
+      for (int ks = 0; ks < DH / 16; ++ks) {
+        qa0[ks] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t) : 0u;
+        qa2[ks] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t) : 0u;
       }
     }
-    __syncwarp();
-    float m[G], lsum[G];
-    float2 o[G][DH / 64];
+    float o[DH / 8][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-      lsum[g] = 0.f;
-#pragma unroll
-      for (int k = 0; k < DH / 64; ++k) o[g][k] = make_float2(0.f, 0.f);
-    }
-    for (int st = 0; st < nst; ++st, ++use) {
-      const int sl = use & 1;
-      if (lane == 0) {             // prefetch the next stage of the stream into the other slot
-        if (st + 1 < nst) {
-          issue(it, st + 1, sl ^ 1);
-          pending = sl ^ 1;
-        } else if (nxt < total) {
-          issue(decode(nxt), 0, sl ^ 1);
-          pending = sl ^ 1;
-        } else {
-          pending = -1;
-        }
-      }
-      if (!mbar_wait_warp(&full[sl], (use >> 1) & 1, abort_flag, err)) {
+    for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_used = -INFINITY, lsum = 0.f;
+
+    for (int st = 0; st < nst; ++st) {
+      if (lane == 0)
+        while (!stream_done && issued < consumed + kMSlots) issue_one();
+      const int sl = consumed % kMSlots;
+      if (!mbar_wait_warp(&full[sl], (consumed / kMSlots) & 1, abort_flag, err)) {
         ok = false;
         break;
       }
-      const uint8_t* ks = slots + sl * C::SLOT_BYTES;
-      const uint8_t* vs = ks + C::KV_BYTES;
-      const int nvalid = min(kSKeys, it.nkeys - st * kSKeys);
+      const uint32_t ks_base = slots_u32 + sl * C::SLOT, vs_base = ks_base + C::KV_BYTES;
+      const int nvalid = min(kMKeys, it.nkeys - st * kMKeys);
+      if (nvalid < kMKeys) {
+        // V rows past the sequence hold whatever the cache holds there; P is 0
+        // for them, but 0·NaN is NaN inside an MMA, so zero them first
+        uint8_t* vrows = slots + sl * C::SLOT + C::KV_BYTES;
+        for (int i = lane; i < (kMKeys - nvalid) * C::NB * 8; i += 32) {
+          const int row = nvalid + i / (C::NB * 8), piece = i % (C::NB * 8);
+          *reinterpret_cast<uint4*>(vrows + (piece >> 3) * C::BOX + row * 128 + (piece & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
 
-      // q·k, lane = key
-      float2 acc[G];
+      // S = Q·Kᵀ for two 8-key column tiles
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int mi = lane >> 3, row = 8 * (mi >> 1) + (lane & 7);
 #pragma unroll
-      for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < DH / 8; ++c) {
-        const int h = c >> 3, cc = c & 7;
-        const uint4 kr = *reinterpret_cast<const uint4*>(ks + h * C::HALF_BYTES + lane * 128 + ((cc ^ (lane & 7)) << 4));
-        const float2 k0 = bf2_to_f2(kr.x), k1 = bf2_to_f2(kr.y), k2 = bf2_to_f2(kr.z), k3 = bf2_to_f2(kr.w);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 qa = *reinterpret_cast<const float4*>(qs + g * DH + c * 8);
-          const float4 qb = *reinterpret_cast<const float4*>(qs + g * DH + c * 8 + 4);
-          acc[g] = __ffma2_rn(make_float2(qa.x, qa.y), k0, acc[g]);
-          acc[g] = __ffma2_rn(make_float2(qa.z, qa.w), k1, acc[g]);
-          acc[g] = __ffma2_rn(make_float2(qb.x, qb.y), k2, acc[g]);
-          acc[g] = __ffma2_rn(make_float2(qb.z, qb.w), k3, acc[g]);
+        for (int ks = 0; ks < DH / 16; ++ks) {
+          uint32_t kb[4];
+          ldsm_x4(swz<DH>(ks_base, row, 2 * ks + (mi & 1)), kb);
+          mma16816(s0, qa0[ks], 0u, qa2[ks], 0u, kb[0], kb[1]);
+          mma16816(s1, qa0[ks], 0u, qa2[ks], 0u, kb[2], kb[3]);
         }
       }
-      // online softmax over the stage: lane = key
-      float pv[G];
+      // online softmax of head g over the stage's keys (raw scores; scale folded into the exponent)
+      const int k0 = 2 * t, k1 = 2 * t + 1, k2 = 8 + 2 * t, k3 = 9 + 2 * t;
+      float r0 = k0 < nvalid ? s0[0] : -INFINITY, r1 = k1 < nvalid ? s0[1] : -INFINITY;
+      float r2 = k2 < nvalid ? s1[0] : -INFINITY, r3 = k3 < nvalid ? s1[1] : -INFINITY;
+      float mx = fmaxf(fmaxf(r0, r1), fmaxf(r2, r3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_used, mx * scale_log2);     // finite: the stage has a visible key
+      if (m_new > m_used + kRescaleLog2 || m_used == -INFINITY) {
+        const float f = m_used == -INFINITY ? 0.f : ex2_approx(m_used - m_new);
+        lsum *= f;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float sc = lane < nvalid ? acc[g].x + acc[g].y : -INFINITY;
-        float mx = sc;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float mn = fmaxf(m[g], mx);             // finite: the stage has a visible key
-        const float corr = ex2_approx(m[g] - mn);
-        pv[g] = ex2_approx(sc - mn);
-        lsum[g] = lsum[g] * corr + pv[g];
-#pragma unroll
-        for (int k = 0; k < DH / 64; ++k) o[g][k] = __fmul2_rn(o[g][k], make_float2(corr, corr));
-        m[g] = mn;
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) ps[lane * G + g] = pv[g];
-      __syncwarp();
-      // p·v, lane = head dimensions [lane·DH/32, +DH/32)
-      const int vh = (lane * (DH / 32)) >> 6;               // which 64-column box
-      const int vc = ((lane * (DH / 32)) & 63) >> 3;        // 16-byte chunk in the row
-      const int vo = ((lane * (DH / 32)) & 7) * 2;          // byte offset in the chunk
-      for (int jj = 0; jj < nvalid; ++jj) {
-        const uint8_t* vrow = vs + vh * C::HALF_BYTES + jj * 128 + ((vc ^ (jj & 7)) << 4) + vo;
-        float2 v[DH / 64];
-        if constexpr (DH == 128) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(vrow);
-          v[0] = bf2_to_f2(raw.x);
-          v[1] = bf2_to_f2(raw.y);
-        } else {
-          v[0] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(vrow));
+        for (int i = 0; i < DH / 8; ++i) {
+          o[i][0] *= f;
+          o[i][1] *= f;
         }
-        float pj[G];
-        if constexpr (G % 4 == 0) {
-#pragma unroll
-          for (int g = 0; g < G; g += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(ps + jj * G + g);
-            pj[g] = t.x; pj[g + 1] = t.y; pj[g + 2] = t.z; pj[g + 3] = t.w;
-          }
-        } else {
-#pragma unroll
-          for (int g = 0; g < G; ++g) pj[g] = ps[jj * G + g];
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int k = 0; k < DH / 64; ++k) o[g][k] = __ffma2_rn(make_float2(pj[g], pj[g]), v[k], o[g][k]);
+        m_used = m_new;
       }
-      __syncwarp();                // the slot and p may be rewritten after this
+      const float p0 = ex2_approx(fmaf(r0, scale_log2, -m_used)), p1 = ex2_approx(fmaf(r1, scale_log2, -m_used));
+      const float p2 = ex2_approx(fmaf(r2, scale_log2, -m_used)), p3 = ex2_approx(fmaf(r3, scale_log2, -m_used));
+      lsum += (p0 + p1) + (p2 + p3);
+      const uint32_t pa0 = pack_bf16(p0, p1), pa2 = pack_bf16(p2, p3);
+      // O += P·V over eight-dimension column tiles, two per ldmatrix
+      {
+        const int mi = lane >> 3, row = 8 * (mi & 1) + (lane & 7);
+#pragma unroll
+        for (int dt = 0; dt < DH / 8; dt += 2) {
+          uint32_t vb[4];
+          ldsm_x4_t(swz<DH>(vs_base, row, dt + (mi >> 1)), vb);
+          mma16816(o[dt], pa0, 0u, pa2, 0u, vb[0], vb[1]);
+          mma16816(o[dt + 1], pa0, 0u, pa2, 0u, vb[2], vb[3]);
+        }
+      }
+      __syncwarp();           // the slot may be refilled after this
+      ++consumed;
     }
     if (!ok) break;
-    // write this chunk's partial states
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float l = lsum[g];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    // partial state of each query head of this chunk
+    float l = lsum;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (g < G) {
       float* pr = part + (((size_t)it.b * H + it.kvh * G + g) * nchunk_max + it.c) * PartLayout<DH>::stride;
-      float* po = pr + 4 + lane * (DH / 32);
-      if constexpr (DH == 128) {
-        *reinterpret_cast<float4*>(po) = make_float4(o[g][0].x, o[g][0].y, o[g][1].x, o[g][1].y);
-      } else {
-        *reinterpret_cast<float2*>(po) = o[g][0];
-      }
-      if (lane == 0) {
-        pr[0] = m[g];
+#pragma unroll
+      for (int i = 0; i < DH / 8; ++i)
+        *reinterpret_cast<float2*>(pr + 4 + 8 * i + 2 * t) = make_float2(o[i][0], o[i][1]);
+      if (t == 0) {
+        pr[0] = m_used;
         pr[1] = l;
       }
     }
-    cur = nxt;
-    if (lane == 0 && cur < total) nxt = atomicAdd(counter, 1);
-    nxt = __shfl_sync(0xffffffffu, nxt, 0);
-    pending = -1;
+    if (lane == 0) {          // drop the finished item from the queue
+      queue[0] = queue[1];
+      queue[1] = queue[2];
+      queue[2] = queue[3];
+      --qn;
+      --pidx;
+    }
   }
-  // on an aborted wait, the copies in flight (the stage waited for and the one
-  // issued ahead) must land before the CTA exits
-  pending = __shfl_sync(0xffffffffu, pending, 0);
+  // copies issued but not consumed (only after an aborted wait) must land before the CTA exits
+  issued = __shfl_sync(0xffffffffu, issued, 0);
   if (!ok && lane == 0) {
     volatile int no_abort = 0;
-    mbar_wait(&full[use & 1], (use >> 1) & 1, &no_abort, err);
-    if (pending >= 0) mbar_wait(&full[pending], ((use + 1) >> 1) & 1, &no_abort, err);
+    for (uint32_t k = consumed; k < issued; ++k)
+      mbar_wait(&full[k % kMSlots], (k / kMSlots) & 1, &no_abort, err);
   }
 }
 
 template <int DH, int G>
 cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
                        float* part, int nchunk_max, int* counter, void* o, cudaStream_t s) {
-  using C = StreamCfg<DH, G>;
+  using C = MCfg<DH>;
   CUtensorMap tk, tv;
-  cudaError_t e = make_tmap_3d_bf16(&tk, kc, (uint64_t)B * Hkv, T_max, DH, DH, (uint64_t)T_max * DH, 64, kSKeys);
+  cudaError_t e = make_tmap_3d_bf16(&tk, kc, (uint64_t)B * Hkv, T_max, DH, DH, (uint64_t)T_max * DH, 64, kMKeys);
   if (e != cudaSuccess) return e;
-  e = make_tmap_3d_bf16(&tv, vc, (uint64_t)B * Hkv, T_max, DH, DH, (uint64_t)T_max * DH, 64, kSKeys);
+  e = make_tmap_3d_bf16(&tv, vc, (uint64_t)B * Hkv, T_max, DH, DH, (uint64_t)T_max * DH, 64, kMKeys);
   if (e != cudaSuccess) return e;
   const size_t smem = C::OFF_PRE + (size_t)(B + 1) * 4 + 1024;
   if (smem > 232448) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(k_decode_stream<DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(k_decode_mma<DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
-  k_decode_stream<DH, G><<<sm_count(), kSWarps * 32, smem, s>>>(tk, tv, (const bf16*)q, pos, B, Hkv, part,
-                                                                nchunk_max, counter, scale_log2,
-                                                                device_error_word());
+  k_decode_mma<DH, G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, (const bf16*)q, pos, B, Hkv, part,
+                                                             nchunk_max, counter, scale_log2, device_error_word());
   k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), DH < 128 ? DH : 128, 0, s>>>(part, pos, Hkv * G, nchunk_max,
-                                                                             kSChunk, (bf16*)o);
+                                                                             kMChunk, (bf16*)o);
   return cudaGetLastError();
 }
 
