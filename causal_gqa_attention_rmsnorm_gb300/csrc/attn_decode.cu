@@ -196,9 +196,17 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restric
 }
 
 // o[b, h·DH + e] = Σ_c acc_c[e]·2^(m_c - M) / Σ_c l_c·2^(m_c - M), M = max_c m_c.
+// One CTA per (head, sequence): the chunk maxima and sums are read in
+// parallel into shared memory, every thread forms the weights from there, and
+// each output dimension sums its chunks with independent loads.
+constexpr int kCombineMaxChunks = 1024;
+
 template <typename T, int DH>
-__global__ void k_decode_combine(const float* __restrict__ part, const int32_t* __restrict__ pos_arr, int H,
-                                 int nchunk_max, int chunk, T* __restrict__ o) {
+__global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict__ part,
+                                                        const int32_t* __restrict__ pos_arr, int H, int nchunk_max,
+                                                        int chunk, T* __restrict__ o) {
+  __shared__ float w_s[kCombineMaxChunks];
+  __shared__ float red[128 / 32];
   const int h = blockIdx.x, b = blockIdx.y;
   const int pos = pos_arr[b];
   T* orow = o + ((size_t)b * H + h) * DH;
@@ -206,19 +214,51 @@ __global__ void k_decode_combine(const float* __restrict__ part, const int32_t* 
     for (int e = threadIdx.x; e < DH; e += blockDim.x) orow[e] = from_f<T>(0.f);
     return;
   }
-  const int nc = (pos + 1 + chunk - 1) / chunk;
+  const int nc = min((pos + 1 + chunk - 1) / chunk, kCombineMaxChunks);
   constexpr int P = PartLayout<DH>::stride;
   const float* pr = part + ((size_t)b * H + h) * nchunk_max * P;
-  float M = -INFINITY;
-  for (int c = 0; c < nc; ++c) M = fmaxf(M, pr[(size_t)c * P]);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // M = max_c m_c
+  float mx = -INFINITY;
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+    const float m = pr[(size_t)c * P];
+    w_s[c] = m;
+    mx = fmaxf(mx, m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int i = 1; i < 128 / 32; ++i) M = fmaxf(M, red[i]);
+  __syncthreads();
+  // weights w_c = 2^(m_c - M) and L = Σ_c l_c·w_c
+  float Lp = 0.f;
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+    const float w = exp2f(w_s[c] - M);
+    w_s[c] = w;
+    Lp += pr[(size_t)c * P + 1] * w;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, off);
+  if (lane == 0) red[warp] = Lp;
+  __syncthreads();
+  float L = 0.f;
+#pragma unroll
+  for (int i = 0; i < 128 / 32; ++i) L += red[i];
+  const float inv = 1.0f / L;
   for (int e = threadIdx.x; e < DH; e += blockDim.x) {
-    float L = 0.f, A = 0.f;
-    for (int c = 0; c < nc; ++c) {
-      const float sc = exp2f(pr[(size_t)c * P] - M);
-      L += pr[(size_t)c * P + 1] * sc;
-      A += pr[(size_t)c * P + 4 + e] * sc;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int c = 0;
+    for (; c + 4 <= nc; c += 4) {
+      a0 += pr[(size_t)c * P + 4 + e] * w_s[c];
+      a1 += pr[(size_t)(c + 1) * P + 4 + e] * w_s[c + 1];
+      a2 += pr[(size_t)(c + 2) * P + 4 + e] * w_s[c + 2];
+      a3 += pr[(size_t)(c + 3) * P + 4 + e] * w_s[c + 3];
     }
-    orow[e] = from_f<T>(A / L);
+    for (; c < nc; ++c) a0 += pr[(size_t)c * P + 4 + e] * w_s[c];
+    orow[e] = from_f<T>(((a0 + a1) + (a2 + a3)) * inv);
   }
 }
 
@@ -521,7 +561,7 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_mma<DH, G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, (const bf16*)q, pos, B, Hkv, part,
                                                              nchunk_max, counter, scale_log2, device_error_word());
-  k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), DH < 128 ? DH : 128, 0, s>>>(part, pos, Hkv * G, nchunk_max,
+  k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), 128, 0, s>>>(part, pos, Hkv * G, nchunk_max,
                                                                              kMChunk, (bf16*)o);
   return cudaGetLastError();
 }
@@ -544,7 +584,7 @@ cudaError_t run(const void* q, const void* kc, const void* vc, const int32_t* po
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_split<T, DH, G><<<dim3(nchunk_max, Hkv, B), kWarps * 32, 0, s>>>(
       (const T*)q, (const T*)kc, (const T*)vc, pos, Hkv, T_max, part, nchunk_max, scale_log2);
-  k_decode_combine<T, DH><<<dim3(Hkv * G, B), DH < 128 ? DH : 128, 0, s>>>(part, pos, Hkv * G, nchunk_max,
+  k_decode_combine<T, DH><<<dim3(Hkv * G, B), 128, 0, s>>>(part, pos, Hkv * G, nchunk_max,
                                                                           kChunk, (T*)o);
   return cudaGetLastError();
 }

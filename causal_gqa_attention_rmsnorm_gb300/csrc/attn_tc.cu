@@ -11,20 +11,21 @@
 //   warp 8      TMA: the Q tile once, then K and V tiles of 128 keys through a
 //               two-stage ring (3-D tensor maps, so keys past T read as zero);
 //   warp 9      MMA issuer: S_j = Q·K_jᵀ into one of two TMEM buffers
-//               (M = 128, N = 128, K = dh), then O += P_j·V_j into a TMEM
-//               accumulator (M = 128, N = dh, K = 128; V is the MN-major
-//               operand, read in place from its [keys, dh] tile);
+//               (M = 128, N = 128, K = dh; both operands in shared memory),
+//               then O += P_j·V_j into a TMEM accumulator (M = 128, N = dh,
+//               K = 128) with P read from tensor memory and V, the MN-major
+//               operand, read in place from its [keys, dh] tile;
 //   warps 0..7  softmax: query row i is TMEM lane i; warps w and w+4 share the
-//               32 rows of lane quarter w%4, each exponentiating half of the
-//               128 key columns (and owning half of O's columns); both read
-//               the whole row from TMEM for its maximum, so they agree on it
-//               without exchanging anything.  fp32 online softmax in base 2,
-//               scale and max folded into one FMA, bf16 P written to shared
-//               memory in the 128-byte-swizzled K-major layout the MMA reads.
-// Key tiles past the query tile's last row are never loaded (causal skip);
-// only the diagonal tile is masked element by element.  O is rescaled only
-// when a row maximum grows by more than 2^8 over the one in use: with a stale
-// maximum every weight stays ≤ 256, and the final O/l is exact either way.
+//               32 rows of lane quarter w%4, each taking half of the 128 key
+//               columns and half of O's columns, and agree on the row maximum
+//               through shared memory.  fp32 online softmax in base 2 with
+//               the scale and maximum in one FMA; P goes back to tensor
+//               memory as bf16 over the S columns it came from.
+// P never touches shared memory, which leaves shared-memory bandwidth to the
+// operands of Q·Kᵀ and to V.  Key tiles past the query tile are never loaded
+// (causal skip); only the diagonal tile is masked element by element.  O is
+// rescaled only when a row maximum grows by more than 2^8 over the one in use:
+// with a stale maximum every weight stays ≤ 2^8, and O/l is exact either way.
 #include <math.h>
 
 #include "gemm_tc.cuh"
@@ -42,20 +43,13 @@ template <int DH> struct AttnCfg {
   static constexpr int NB = DH / 64;                       // 64-column swizzle blocks per row
   static constexpr uint32_t Q_BYTES = kBM * DH * 2;
   static constexpr uint32_t KV_BYTES = kBN * DH * 2;
-  static constexpr uint32_t P_BYTES = kBM * kBN * 2;
   static constexpr uint32_t OFF_K = Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t TMEM_O = 2 * kBN;              // S buffers at columns 0 and 128
+  static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
+  static constexpr uint32_t OFF_RED = OFF_BAR + 256;      // [2 buffers][2 halves][128 rows] fp32
+  static constexpr size_t SMEM = OFF_RED + 2 * 2 * 128 * 4 + 1024;
+  static constexpr uint32_t TMEM_O = 2 * kBN;              // S/P buffers at columns 0 and 128
 };
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Named barrier for the 64 threads of one softmax warp pair.
 __device__ __forceinline__ void pair_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
@@ -75,13 +69,13 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* v_full = bars + 5;
   uint64_t* v_empty = bars + 7;
   uint64_t* s_full = bars + 9;
-  uint64_t* s_free = bars + 11;
-  uint64_t* p_full = bars + 13;
-  uint64_t* pv_done = bars + 15;
-  uint64_t* o_full = bars + 17;
-  uint64_t* drain = bars + 18;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  uint64_t* p_full = bars + 11;
+  uint64_t* pv_done = bars + 13;
+  uint64_t* o_full = bars + 15;
+  uint64_t* drain = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, b = blockIdx.y;
@@ -98,7 +92,6 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 8);
       mbar_init(&p_full[i], 8);
       mbar_init(&pv_done[i], 1);
     }
@@ -157,17 +150,18 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
+    // tcgen05.mma operations of one thread execute in issue order, so S_{j+1}
+    // may be issued into the columns P_{j-1} occupied once P·V_{j-1} is issued.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN);
       constexpr uint32_t idesc_pv = idesc_bf16(kBM, DH, false, true);
       const uint32_t sQ = smem_u32(smem);
-      const uint32_t sK = sQ + C::OFF_K, sV = sQ + C::OFF_V, sP = sQ + C::OFF_P;
+      const uint32_t sK = sQ + C::OFF_K, sV = sQ + C::OFF_V;
       bool ok = mbar_wait(q_full, 0, abort_flag, err);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
         if (!mbar_wait(&k_full[st], ph, abort_flag, err)) return false;
-        if (!mbar_wait(&s_free[st], ph ^ 1u, abort_flag, err)) return false;
         tc_fence_after();
         const uint32_t kb = sK + st * C::KV_BYTES;
 #pragma unroll
@@ -187,13 +181,11 @@ __global__ void __launch_bounds__(320, 1)
         if (!mbar_wait(&p_full[st], ph, abort_flag, err)) break;
         if (!mbar_wait(&v_full[st], ph, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t pb = sP + st * C::P_BYTES, vb = sV + st * C::KV_BYTES;
+        const uint32_t vb = sV + st * C::KV_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::TMEM_O, desc_kmajor_sw128(pb + aoff),
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(tmem + C::TMEM_O, tmem + st * kBN + kk * 8,
                       desc_mnmajor_sw128(vb + kk * 16 * 128, kBN * 128, 1024), idesc_pv, (j | kk) != 0);
-        }
         mma_commit(&pv_done[st]);
         mma_commit(&v_empty[st]);
         if (j == nkv - 1) mma_commit(o_full);
@@ -210,7 +202,6 @@ __global__ void __launch_bounds__(320, 1)
     const int r = quad * 32 + lane;
     const int qi = q0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    uint8_t* pbase = smem + C::OFF_P;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
@@ -230,34 +221,26 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < 16; ++i) s[c + i] = __uint_as_float(u[i]);
       }
       tmem_wait_ld();
-      // raw row maximum over all 128 columns (own half kept in s, the other
-      // half only scanned); only the diagonal tile masks future keys
-      const bool diag = (j == nkv - 1);
-      const int lim = qi - j * kBN;                     // column c is a future key iff c > lim
+      // raw maximum of this thread's columns; only the diagonal tile masks
       float mx = -INFINITY;
-      if (diag) {
+      if (j == nkv - 1) {
+        const int lim = qi - (j * kBN + half * HC);     // column c is a future key iff c > lim
 #pragma unroll
         for (int c = 0; c < HC; ++c) {
-          if (half * HC + c > lim) s[c] = -INFINITY;
+          if (c > lim) s[c] = -INFINITY;
           mx = fmaxf(mx, s[c]);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < HC; ++c) mx = fmaxf(mx, s[c]);
       }
-#pragma unroll 1
-      for (int c = 0; c < HC; c += 16) {
-        uint32_t u[16];
-        tmem_ld16(lane_base + st * kBN + (half ^ 1) * HC + c, u);
-        tmem_wait_ld();
-        const int c0 = (half ^ 1) * HC + c;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, (diag && c0 + i > lim) ? -INFINITY : __uint_as_float(u[i]));
-      }
+      // agree with the partner thread on the row maximum; the barrier also
+      // orders both threads' reads of S before either writes P over it
+      red[(st * 2 + half) * 128 + r] = mx;
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[st]);
-
+      pair_sync(1 + quad);
+      tc_fence_after();
+      mx = fmaxf(mx, red[(st * 2 + (half ^ 1)) * 128 + r]);
       const float m_new = fmaxf(m_used, mx * scale_log2);
       bool need = false;
       if (j == 0) {
@@ -272,7 +255,7 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after();
-        const float factor = need ? ex2(m_used - m_new) : 1.f;
+        const float factor = need ? ex2_approx(m_used - m_new) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < HO; c += 16) {
           uint32_t u[16];
@@ -289,41 +272,34 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       const float msub = m_used == -INFINITY ? 0.f : m_used;
-      // P buffer st is free once the P·V two tiles back has finished
-      if (j >= 2 && !mbar_wait_warp(&pv_done[st], ((j - 2) >> 1) & 1, abort_flag, err)) {
-        ok = false;
-        break;
-      }
-      uint8_t* prow = pbase + st * C::P_BYTES + half * (kBM * 128) + r * 128;
-      float rowsum = 0.f;
+      // p = 2^(s·scale − m), in pairs; bf16 P back into this S buffer's columns
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-msub, -msub);
+      float2 sum2 = make_float2(0.f, 0.f);
+      uint32_t pk[HC / 2];
 #pragma unroll
-      for (int c = 0; c < HC; c += 8) {
-        float p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          p[i] = ex2(fmaf(s[c + i], scale_log2, -msub));
-          rowsum += p[i];
-        }
-        uint4 w;
-        __nv_bfloat162 t0 = __floats2bfloat162_rn(p[0], p[1]), t1 = __floats2bfloat162_rn(p[2], p[3]);
-        __nv_bfloat162 t2 = __floats2bfloat162_rn(p[4], p[5]), t3 = __floats2bfloat162_rn(p[6], p[7]);
-        w.x = *reinterpret_cast<uint32_t*>(&t0);
-        w.y = *reinterpret_cast<uint32_t*>(&t1);
-        w.z = *reinterpret_cast<uint32_t*>(&t2);
-        w.w = *reinterpret_cast<uint32_t*>(&t3);
-        *reinterpret_cast<uint4*>(prow + (((c >> 3) ^ (r & 7)) << 4)) = w;
+      for (int c = 0; c < HC; c += 2) {
+        const float2 arg = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+        const float2 p = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+        sum2 = __fadd2_rn(sum2, p);
+        __nv_bfloat162 t = __floats2bfloat162_rn(p.x, p.y);
+        pk[c / 2] = *reinterpret_cast<uint32_t*>(&t);
       }
-      l += rowsum;
-      fence_proxy_async();    // generic-proxy P stores -> visible to the tensor core
-      tc_fence_before();      // order any O rescale (tcgen05.st) before the next MMA
+      l += sum2.x + sum2.y;
+#pragma unroll
+      for (int c = 0; c < HC / 2; c += 16) {
+        uint32_t u[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) u[i] = pk[c + i];
+        tmem_st16(lane_base + st * kBN + half * (HC / 2) + c, u);
+      }
+      tmem_wait_st();
+      tc_fence_before();      // P (and any O rescale) before the next MMA
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[st]);
     }
     const bool have_o = ok && mbar_wait_warp(o_full, 0, abort_flag, err);
-    // both halves' sums share the same maximum: add them (the P buffers are
-    // free once the last P·V has finished).  Every softmax thread reaches the
-    // pair barrier, whether or not its waits succeeded.
-    float* red = reinterpret_cast<float*>(pbase);
+    // both halves' sums share the same maximum: add them.  Every softmax
+    // thread reaches the pair barrier, whether or not its waits succeeded.
     if (have_o) red[half * 128 + r] = l;
     pair_sync(1 + quad);
     if (have_o) {

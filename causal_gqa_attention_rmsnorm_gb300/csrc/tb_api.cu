@@ -338,6 +338,9 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     return fail(TB_ERR_INVALID_ARG, "y_dtype must be TB_F32, or TB_BF16 for a bf16 block");
   if (kv->T_max > cfg->max_pos)
     return fail(TB_ERR_INVALID_ARG, "kv->T_max (%d) exceeds cfg->max_pos (%d)", kv->T_max, cfg->max_pos);
+  if (kv->T_max > 1024 * decode_chunk_keys())
+    return fail(TB_ERR_UNSUPPORTED, "kv->T_max (%d) above the %d rows the decode merge supports", kv->T_max,
+                1024 * decode_chunk_keys());
   const int B = kv->B;
   if (B == 0) return TB_OK;
   if (!packed || !x || !y || !ws) return fail(TB_ERR_INVALID_ARG, "packed, x, y and ws must be non-NULL");
