@@ -35,7 +35,10 @@ template <int BN> struct TcCfg {
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
+  static constexpr uint32_t OFF_EPI = OFF_BAR + 256;                // 4 warps x [32 rows][36] fp32
+  static constexpr uint32_t EPI_STRIDE = 36;                        // 32 columns + 4 pad: conflict-free both ways
+  static constexpr size_t SMEM = OFF_EPI + 4 * 32 * EPI_STRIDE * 4 + 1024;
 };
 
 // fp32 output of the raw product (test hook).
@@ -80,7 +83,7 @@ __global__ void __launch_bounds__(192, 1)
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -186,7 +189,13 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(drain, 0, &no_abort, err);
     }
   } else {
+    // Epilogue: each warp reads its 32 TMEM lanes (32 rows) 32 columns at a
+    // time, turns the chunk around in shared memory, and then lets lane l
+    // handle columns [4·(l%8), +4) of rows (l/8) + 4·i, so every global access
+    // of a warp instruction covers four contiguous row segments.
     const int quad = warp & 3;
+    float* stage = reinterpret_cast<float*>(smem + C::OFF_EPI) + (warp - 2) * 32 * C::EPI_STRIDE;
+    const int sub_row = lane >> 3, sub_col = 4 * (lane & 7);
     int local = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
       const int acc = local & 1;
@@ -195,32 +204,54 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       int mt, nt;
       tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
-      const int row = mt * BM + quad * 32 + lane;
+      const int row0 = mt * BM + quad * 32;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
-      float rsum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 16) {
-        uint32_t r[16];
-        tmem_ld16(taddr + c, r);
-        tmem_wait_ld();
-        if (row < M) {
+      float rsum[8];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int col = nt * BN + c + 4 * g;
-            if (col < N) {
-              float v[4] = {__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]), __uint_as_float(r[4 * g + 2]),
-                            __uint_as_float(r[4 * g + 3])};
-              rsum += epi(row, col, v);
-            }
-          }
+      for (int i = 0; i < 8; ++i) rsum[i] = 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(taddr + c0, r0);
+        tmem_ld16(taddr + c0 + 16, r1);
+        tmem_wait_ld();
+        if (c0 + 32 == BN) {     // the accumulator is free once its last columns are in registers
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
         }
+        float* my = stage + lane * C::EPI_STRIDE;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          *reinterpret_cast<float4*>(my + 4 * i) = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
+                                                               __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
+          *reinterpret_cast<float4*>(my + 16 + 4 * i) =
+              make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
+                          __uint_as_float(r1[4 * i + 3]));
+        }
+        __syncwarp();
+        const int col = nt * BN + c0 + sub_col;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rl = sub_row + 4 * i;
+          const float4 t = *reinterpret_cast<const float4*>(stage + rl * C::EPI_STRIDE + sub_col);
+          float v[4] = {t.x, t.y, t.z, t.w};
+          const int row = row0 + rl;
+          if (row < M && col < N) rsum[i] += epi(row, col, v);
+        }
+        __syncwarp();            // before the next chunk overwrites the stage
       }
       if constexpr (Epi::kRowReduce) {
-        if (row < M) epi.row_reduce(row, rsum);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float t = rsum[i];
+          t += __shfl_xor_sync(0xffffffffu, t, 1);
+          t += __shfl_xor_sync(0xffffffffu, t, 2);
+          t += __shfl_xor_sync(0xffffffffu, t, 4);
+          const int row = row0 + sub_row + 4 * i;
+          if ((lane & 7) == 0 && row < M) epi.row_reduce(row, t);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
     }
   }
 
