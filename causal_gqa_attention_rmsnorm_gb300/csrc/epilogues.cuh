@@ -51,36 +51,57 @@ __device__ __forceinline__ void rope_pair(float& a, float& b, float2 cs) {
   b = x * cs.y + y * cs.x;
 }
 
+// Every epilogue reads its global inputs in two steps ahead of any store, so a
+// caller processing several (row, 4-column) items can issue all their loads
+// before the first store:
+//   RowAux row_aux(row)            inputs that depend on the row only (once per tile)
+//   Aux    aux(row, col, RowAux)   inputs of the 4 columns
+//   float  operator()(row, col, v, RowAux, Aux)   compute and store; returns the
+//                                  item's share of a row reduction (kRowReduce)
+
 template <typename T>
 struct EpiQKV {
   static constexpr bool kRowReduce = false;
   QKVArgs a;
   int H, Hkv, dh;
-  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
-    int b, t, qt;
+  struct RowAux { float r; int b, t, qt; };
+  struct Aux { float2 c0, c1; };
+  __device__ __forceinline__ RowAux row_aux(int row) const {
+    RowAux ra;
     if (a.pos) {
-      b = row; t = a.pos[row]; qt = 0;
+      ra.b = row; ra.t = a.pos[row]; ra.qt = 0;
     } else {
-      b = row / a.T; t = row - b * a.T; qt = t;
+      ra.b = row / a.T; ra.t = row - ra.b * a.T; ra.qt = ra.t;
     }
-    const float rr = a.r[row];
+    ra.r = a.r[row];
+    return ra;
+  }
+  __device__ __forceinline__ Aux aux(int, int col, const RowAux& ra) const {
+    Aux x;
+    if (col < (H + Hkv) * dh && ra.t >= 0) {
+      const float2* cs = a.rope + (size_t)ra.t * (dh >> 1) + ((col % dh) >> 1);
+      x.c0 = cs[0];
+      x.c1 = cs[1];
+    } else {
+      x.c0 = x.c1 = make_float2(1.f, 0.f);
+    }
+    return x;
+  }
+  __device__ __forceinline__ float operator()(int, int col, float v[4], const RowAux& ra, const Aux& x) const {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] *= rr;
+    for (int i = 0; i < 4; ++i) v[i] *= ra.r;
     const int qn = H * dh, kn = Hkv * dh;
     const int e = col % dh;
-    if (col < qn + kn && t >= 0) {
-      const float2* cs = a.rope + (size_t)t * (dh >> 1) + (e >> 1);
-      rope_pair(v[0], v[1], cs[0]);
-      rope_pair(v[2], v[3], cs[1]);
-    }
+    rope_pair(v[0], v[1], x.c0);        // identity rotation for v columns
+    rope_pair(v[2], v[3], x.c1);
     if (col < qn) {
       const int h = col / dh;
-      store4<T>((T*)a.q + (((size_t)b * H + h) * a.T + qt) * dh + e, v);
-    } else if (t >= 0) {
+      store4<T>((T*)a.q + (((size_t)ra.b * H + h) * a.T + ra.qt) * dh + e, v);
+    } else if (ra.t >= 0) {
       const bool is_k = col < qn + kn;
       const int h = (col - (is_k ? qn : qn + kn)) / dh;
       T* base = (T*)(is_k ? a.k : a.v);
-      store4<T>(base + (((size_t)b * Hkv + h) * a.kv_stride + t) * dh + e, v);
+      store4<T>(base + (((size_t)ra.b * Hkv + h) * a.kv_stride + ra.t) * dh + e, v);
     }
     return 0.f;
   }
@@ -92,11 +113,17 @@ struct EpiWo {
   static constexpr bool kRowReduce = true;
   WoArgs a;
   int d;
-  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
-    float x[4];
-    load4<T>((const T*)a.x + (size_t)row * d + col, x);
+  struct RowAux {};
+  struct Aux { float x[4]; };
+  __device__ __forceinline__ RowAux row_aux(int) const { return RowAux{}; }
+  __device__ __forceinline__ Aux aux(int row, int col, const RowAux&) const {
+    Aux x;
+    load4<T>((const T*)a.x + (size_t)row * d + col, x.x);
+    return x;
+  }
+  __device__ __forceinline__ float operator()(int row, int col, float v[4], const RowAux&, const Aux& x) const {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] += x[i];
+    for (int i = 0; i < 4; ++i) v[i] += x.x[i];
     store4<float>(a.h + (size_t)row * d + col, v);
     if ((void*)a.hb != (void*)a.h) store4<T>((T*)a.hb + (size_t)row * d + col, v);
     return v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
@@ -110,8 +137,14 @@ struct EpiW13 {
   W13Args a;
   int d, f;
   float eps;
-  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
-    const float r2 = 1.0f / sqrtf(a.ssq[row] / (float)d + eps);
+  struct RowAux { float r2; };
+  struct Aux {};
+  __device__ __forceinline__ RowAux row_aux(int row) const {
+    return RowAux{1.0f / sqrtf(a.ssq[row] / (float)d + eps)};
+  }
+  __device__ __forceinline__ Aux aux(int, int, const RowAux&) const { return Aux{}; }
+  __device__ __forceinline__ float operator()(int row, int col, float v[4], const RowAux& ra, const Aux&) const {
+    const float r2 = ra.r2;
     const float o0 = silu_f(v[0] * r2) * (v[1] * r2);
     const float o1 = silu_f(v[2] * r2) * (v[3] * r2);
     store2<T>((T*)a.a + (size_t)row * f + (col >> 1), o0, o1);
@@ -124,11 +157,17 @@ struct EpiW2 {
   static constexpr bool kRowReduce = false;
   W2Args a;
   int d;
-  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
-    float h[4];
-    load4<float>(a.h + (size_t)row * d + col, h);
+  struct RowAux {};
+  struct Aux { float h[4]; };
+  __device__ __forceinline__ RowAux row_aux(int) const { return RowAux{}; }
+  __device__ __forceinline__ Aux aux(int row, int col, const RowAux&) const {
+    Aux x;
+    load4<float>(a.h + (size_t)row * d + col, x.h);
+    return x;
+  }
+  __device__ __forceinline__ float operator()(int row, int col, float v[4], const RowAux&, const Aux& x) const {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] += h[i];
+    for (int i = 0; i < 4; ++i) v[i] += x.h[i];
     if (a.y_dtype == TB_F32)
       store4<float>((float*)a.y + (size_t)row * d + col, v);
     else

@@ -53,7 +53,10 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const T* __restrict__ A, cons
   for (int i = 0; i < 4; ++i) {
     const int row = m0 + ty * 4 + i;
     float part = 0.f;
-    if (row < M && col < N) part = epi(row, col, acc[i]);
+    if (row < M && col < N) {
+      const auto ra = epi.row_aux(row);
+      part = epi(row, col, acc[i], ra, epi.aux(row, col, ra));
+    }
     if constexpr (Epi::kRowReduce) {
       // the 16 threads of a half-warp share this row
 #pragma unroll

@@ -42,17 +42,21 @@ template <int BN> struct TcCfg {
 };
 
 // fp32 output of the raw product (test hook).
+#pragma nv_diag_suppress 177
 struct EpiF32 {
   static constexpr bool kRowReduce = false;
   float* C;
   int N;
-  __device__ __forceinline__ float operator()(int row, int col, float v[4]) const {
+  struct RowAux {};
+  struct Aux {};
+  __device__ __forceinline__ RowAux row_aux(int) const { return RowAux{}; }
+  __device__ __forceinline__ Aux aux(int, int, const RowAux&) const { return Aux{}; }
+  __device__ __forceinline__ float operator()(int row, int col, float v[4], const RowAux&, const Aux&) const {
     *reinterpret_cast<float4*>(C + (size_t)row * N + col) = make_float4(v[0], v[1], v[2], v[3]);
     return 0.f;
   }
   __device__ __forceinline__ void row_reduce(int, float) const {}
 };
-#pragma nv_diag_suppress 177
 
 // Tile index -> (m, n) tile.  group_m == 0 walks n fastest (CTAs running
 // together share one A row block and stream the whole B panel, best when B
@@ -207,8 +211,13 @@ __global__ void __launch_bounds__(192, 1)
       const int row0 = mt * BM + quad * 32;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
       float rsum[8];
+      typename Epi::RowAux ra[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rsum[i] = 0.f;
+      for (int i = 0; i < 8; ++i) {
+        rsum[i] = 0.f;
+        const int row = row0 + sub_row + 4 * i;
+        if (row < M) ra[i] = epi.row_aux(row);
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r0[16], r1[16];
@@ -231,13 +240,20 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
         const int col = nt * BN + c0 + sub_col;
+        // all global inputs of the chunk first, then compute and store
+        typename Epi::Aux ax[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = row0 + sub_row + 4 * i;
+          if (row < M && col < N) ax[i] = epi.aux(row, col, ra[i]);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int rl = sub_row + 4 * i;
           const float4 t = *reinterpret_cast<const float4*>(stage + rl * C::EPI_STRIDE + sub_col);
           float v[4] = {t.x, t.y, t.z, t.w};
           const int row = row0 + rl;
-          if (row < M && col < N) rsum[i] += epi(row, col, v);
+          if (row < M && col < N) rsum[i] += epi(row, col, v, ra[i], ax[i]);
         }
         __syncwarp();            // before the next chunk overwrites the stage
       }
