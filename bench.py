@@ -117,13 +117,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: every rank contributes x, all get the maximum."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(world: int, units_per_rank_step: int, steps: int, ms_total_max: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: every rank processes the
+    same units per step; the slowest rank's time bounds the job."""
+    return world * units_per_rank_step * steps / (ms_total_max * 1e-3)
 
 
 # ---------------------------------------------------------------------------
@@ -338,6 +346,29 @@ def bench_decode(args, world, peaks):
     stages = stage_stats([binding.tbx_trace_read(i) for i in range(n)])
     binding.tbx_trace_enable(0)
     assert torch.isfinite(y).all().item()
+    # the same step captured once as a CUDA graph and replayed (no per-launch host work)
+    graph_ms = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()                                    # warm the capture stream
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        a.record(stream)
+        for _ in range(n):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = max_over_ranks(a.elapsed_time(b), world) / n
+        assert torch.isfinite(y).all().item()
     kv_bytes = acc.decode_kv_bytes(lens.tolist(), s.Hkv, s.dh, 2)
     w_bytes = acc.weight_bytes(s.d, s.H, s.Hkv, s.dh, s.f, 2)
     attn_ms = stages["attn"]
@@ -346,6 +377,8 @@ def bench_decode(args, world, peaks):
         "workload": s.name, "B": s.B, "T_max": s.T, "kv_bytes": kv_bytes, "weight_bytes": w_bytes,
         "kv_gbs": kv_gbs, "kv_frac_hbm": kv_gbs / peaks["hbm_gbs"], "attn_ms": attn_ms, "step_ms": ms,
         "tok_s": world * s.B / (ms * 1e-3), "stages_ms": stages, "gpu_launches": 7 * n,
+        "graph_step_ms": graph_ms,
+        "graph_tok_s": None if graph_ms is None else world * s.B / (graph_ms * 1e-3),
         "step_hbm_gbs": (kv_bytes + w_bytes) / (ms * 1e-3) / 1e9,
     }
 
@@ -363,6 +396,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling runs); prints the decode object")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the decode step")
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
     ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample size for cpu_baseline")
     args = ap.parse_args()
@@ -396,7 +430,7 @@ def main():
     from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
     tokens = s.B * s.T
     ms_step = pre["ms_total"] / args.steps
-    value = world * tokens * args.steps / (pre["ms_total"] * 1e-3)
+    value = aggregate_rate(world, tokens, args.steps, pre["ms_total"])
     work = prefill_stage_work(s)
     stages = pre["stages"]
     attn_tflops = work["attn"][1] / (stages["attn"] * 1e-3) / 1e12

@@ -556,8 +556,17 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
   if (e != cudaSuccess) return e;
   const size_t smem = C::OFF_PRE + (size_t)(B + 1) * 4 + 1024;
   if (smem > 232448) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(k_decode_mma<DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // raise the kernel's dynamic shared-memory limit only when a launch needs
+  // more than this device has been given so far (no attribute call in the
+  // steady state, e.g. while a stream is being captured)
+  static size_t attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || attr_set[dev] < smem) {
+    e = cudaFuncSetAttribute(k_decode_mma<DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = smem;
+  }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_mma<DH, G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, (const bf16*)q, pos, B, Hkv, part,
                                                              nchunk_max, counter, scale_log2, device_error_word());
