@@ -54,11 +54,49 @@ template <int DH> struct AttnCfg {
   static constexpr uint32_t TMEM_O = 2 * kBN;              // S/P of slot g at g·128, O of slot g at 256 + g·DH
 };
 
+// One work item: two query tiles of one sequence that share a KV head.
+struct Item {
+  int b, h0, h1, qb0, qb1, nkv0, nkv1, nkv, kvh;
+};
+
+// Items are numbered heaviest first: all items of the last query block (or
+// block pair) come first, then the next one down.
+__device__ __forceinline__ Item decode_item(int w, int B, int H, int Hkv, int nq, int head_pairs) {
+  Item it;
+  if (head_pairs) {
+    const int P = H / 2, per = B * P;
+    const int level = w / per, r = w - level * per;
+    it.b = r / P;
+    it.h0 = 2 * (r - it.b * P);
+    it.h1 = it.h0 + 1;
+    it.qb0 = it.qb1 = nq - 1 - level;
+  } else {
+    const int per = B * H, npair = (nq + 1) / 2;
+    const int level = w / per, r = w - level * per;
+    it.b = r / H;
+    it.h0 = it.h1 = r - it.b * H;
+    it.qb0 = 2 * (npair - 1 - level);
+    it.qb1 = it.qb0 + 1;
+  }
+  it.kvh = it.h0 / (H / Hkv);
+  it.nkv0 = it.qb0 + 1;                          // key tiles 0..qb hold every visible key
+  it.nkv1 = it.qb1 < nq ? it.qb1 + 1 : 0;        // 0: slot 1 empty
+  it.nkv = it.nkv0 > it.nkv1 ? it.nkv0 : it.nkv1;
+  return it;
+}
+
+// The k-th item of CTA c: rounds of gridDim.x items, alternating direction, so
+// every CTA gets a near-equal share of the decreasing item sizes.
+__device__ __forceinline__ int item_of(int k) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
 template <int DH>
 __global__ void __launch_bounds__(320, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out, int T, int H, int Hkv, int n_qtiles,
-              int head_pairs, float scale_log2, int* err) {
+              const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out, int B, int T, int H, int Hkv,
+              int n_qtiles, int head_pairs, int n_items, float scale_log2, int* err) {
   using C = AttnCfg<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -71,32 +109,17 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* s_full = bars + 9;     // [slot]
   uint64_t* p_full = bars + 11;    // [slot]
   uint64_t* pv_done = bars + 13;   // [slot]
-  uint64_t* o_full = bars + 15;
-  uint64_t* drain = bars + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* o_full = bars + 15;    // [slot]
+  uint64_t* drain = bars + 17;
+  uint64_t* q_empty = bars + 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
-  const int G = H / Hkv;
-  // the two slots: heads h0, h1 at query blocks qb0, qb1; heaviest work first
-  int h0, h1, qb0, qb1;
-  if (head_pairs) {
-    h0 = 2 * blockIdx.x;
-    h1 = h0 + 1;
-    qb0 = qb1 = n_qtiles - 1 - (int)blockIdx.z;
-  } else {
-    h0 = h1 = blockIdx.x;
-    qb0 = 2 * ((int)gridDim.z - 1 - (int)blockIdx.z);
-    qb1 = qb0 + 1;
-  }
-  const int kvh = h0 / G;
-  const int nkv0 = qb0 + 1;                         // key tiles 0..qb hold every visible key
-  const int nkv1 = qb1 < n_qtiles ? qb1 + 1 : 0;    // 0: slot 1 empty
-  const int nkv = nkv0 > nkv1 ? nkv0 : nkv1;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -105,8 +128,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&o_full[i], 1);
     }
-    mbar_init(o_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -120,47 +143,65 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Barrier phases run on across items: K/V stages by the CTA's running key
+  // tile count, s_full / p_full / pv_done by each slot's running tile count,
+  // q_full / q_empty by the item count, o_full by the count of items in which
+  // the slot has work.
   if (warp == 8) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      const int nq_slots = nkv1 > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, nq_slots * C::Q_BYTES);
-      for (int g = 0; g < nq_slots; ++g)
+      int nk_issued = 0, nv_issued = 0, nq_issued = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k);
+        if (w >= n_items) break;
+        const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs);
+        // the previous item's last S must be done with the Q tiles
+        if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, abort_flag, err)) break;
+        const int nq_slots = it.nkv1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(q_full, nq_slots * C::Q_BYTES);
+        for (int g = 0; g < nq_slots; ++g)
 #pragma unroll
-        for (int blk = 0; blk < C::NB; ++blk)
-          tma_load_3d(&tmQ, smem + g * C::Q_BYTES + blk * kBM * 128, q_full, blk * 64, (g ? qb1 : qb0) * kBM,
-                      b * H + (g ? h1 : h0));
-      int last = -1;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, err)) break;
-        mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
+          for (int blk = 0; blk < C::NB; ++blk)
+            tma_load_3d(&tmQ, smem + g * C::Q_BYTES + blk * kBM * 128, q_full, blk * 64,
+                        (g ? it.qb1 : it.qb0) * kBM, it.b * H + (g ? it.h1 : it.h0));
+        ++nq_issued;
+        for (int j = 0; j < it.nkv; ++j) {
+          const int t = nk_issued, st = t & 1;
+          const uint32_t ph = (t >> 1) & 1;
+          if (!mbar_wait(&k_empty[st], ph ^ 1u, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
 #pragma unroll
-        for (int blk = 0; blk < C::NB; ++blk)
-          tma_load_3d(&tmK, smem + C::OFF_K + st * C::KV_BYTES + blk * kBN * 128, &k_full[st], blk * 64, j * kBN,
-                      b * Hkv + kvh);
-        if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, err)) {
-          last = j;
-          break;
+          for (int blk = 0; blk < C::NB; ++blk)
+            tma_load_3d(&tmK, smem + C::OFF_K + st * C::KV_BYTES + blk * kBN * 128, &k_full[st], blk * 64, j * kBN,
+                        it.b * Hkv + it.kvh);
+          ++nk_issued;
+          if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
+#pragma unroll
+          for (int blk = 0; blk < C::NB; ++blk)
+            tma_load_3d(&tmV, smem + C::OFF_V + st * C::KV_BYTES + blk * kBN * 128, &v_full[st], blk * 64, j * kBN,
+                        it.b * Hkv + it.kvh);
+          ++nv_issued;
         }
-        mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
-#pragma unroll
-        for (int blk = 0; blk < C::NB; ++blk)
-          tma_load_3d(&tmV, smem + C::OFF_V + st * C::KV_BYTES + blk * kBN * 128, &v_full[st], blk * 64, j * kBN,
-                      b * Hkv + kvh);
-        last = j;
       }
-      // every copy issued must land before the CTA may exit
+      // every copy issued must land before the CTA may exit (earlier copies
+      // into the same buffers were consumed, hence complete)
       volatile int no_abort = 0;
-      mbar_wait(q_full, 0, &no_abort, err);
-      for (int j = last - 1 < 0 ? 0 : last - 1; j <= last; ++j) {
-        mbar_wait(&k_full[j & 1], (j >> 1) & 1, &no_abort, err);
-        mbar_wait(&v_full[j & 1], (j >> 1) & 1, &no_abort, err);
-      }
+      if (nq_issued > 0) mbar_wait(q_full, (nq_issued - 1) & 1, &no_abort, err);
+      for (int t = nk_issued - 2 < 0 ? 0 : nk_issued - 2; t < nk_issued; ++t)
+        mbar_wait(&k_full[t & 1], (t >> 1) & 1, &no_abort, err);
+      for (int t = nv_issued - 2 < 0 ? 0 : nv_issued - 2; t < nv_issued; ++t)
+        mbar_wait(&v_full[t & 1], (t >> 1) & 1, &no_abort, err);
     }
   } else if (warp == 9) {
     // ---------------- MMA issuer ----------------
@@ -170,60 +211,88 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN);
       constexpr uint32_t idesc_pv = idesc_bf16(kBM, DH, false, true);
+      // Every operand descriptor is formed once: the issuing thread shares its
+      // sub-partition with two softmax warps, so each MMA must cost it as few
+      // instructions as possible.  A descriptor's address field is the byte
+      // address / 16, and no block crosses 256 KB, so offsetting a block is a
+      // plain add to the descriptor.
       const uint32_t sQ = smem_u32(smem);
-      const uint32_t sK = sQ + C::OFF_K, sV = sQ + C::OFF_V;
-      auto issue_s = [&](int g, int j) {
-        const uint32_t qb = sQ + g * C::Q_BYTES, kb = sK + (j & 1) * C::KV_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          mma_bf16_ss(tmem + g * kBN, desc_kmajor_sw128(qb + off), desc_kmajor_sw128(kb + off), idesc_qk, kk > 0);
-        }
+      const uint64_t dq0 = desc_kmajor_sw128(sQ), dq1 = desc_kmajor_sw128(sQ + C::Q_BYTES);
+      const uint64_t dk0 = desc_kmajor_sw128(sQ + C::OFF_K), dk1 = desc_kmajor_sw128(sQ + C::OFF_K + C::KV_BYTES);
+      const uint64_t dv0 = desc_mnmajor_sw128(sQ + C::OFF_V, kBN * 128, 1024);
+      const uint64_t dv1 = desc_mnmajor_sw128(sQ + C::OFF_V + C::KV_BYTES, kBN * 128, 1024);
+      auto issue_s = [&](int g, int t) {
+        const uint64_t qd = g ? dq1 : dq0, kd = (t & 1) ? dk1 : dk0;
+        mma_tile_ss<DH / 16>(tmem + g * kBN, qd, kd, idesc_qk);
         mma_commit(&s_full[g]);
       };
-      auto issue_pv = [&](int g, int j) {
-        const uint32_t vb = sV + (j & 1) * C::KV_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ts(tmem + C::TMEM_O + g * DH, tmem + g * kBN + kk * 8,
-                      desc_mnmajor_sw128(vb + kk * 16 * 128, kBN * 128, 1024), idesc_pv, (j | kk) != 0);
+      auto issue_pv = [&](int g, int t, bool acc) {
+        const uint64_t vd = (t & 1) ? dv1 : dv0;
+        mma_tile_ts128(tmem + C::TMEM_O + g * DH, tmem + g * kBN, vd, idesc_pv, acc ? 1u : 0u);
         mma_commit(&pv_done[g]);
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, err) && mbar_wait(&k_full[0], 0, abort_flag, err);
-      if (ok) {
+      int kt = 0, c0 = 0, c1 = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int w = item_of(k);
+        if (w >= n_items) break;
+        const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs);
+        if (!mbar_wait(q_full, k & 1, abort_flag, err) ||
+            !mbar_wait(&k_full[kt & 1], (kt >> 1) & 1, abort_flag, err)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        issue_s(0, 0);
-        if (nkv1 > 0) issue_s(1, 0);
-        mma_commit(&k_empty[0]);
-      }
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int vst = j & 1;
-        const uint32_t vph = (j >> 1) & 1;
-        const bool next = j + 1 < nkv;
-        if (!mbar_wait(&v_full[vst], vph, abort_flag, err)) break;
-        // slot 0: P·V of tile j, then S of tile j+1
-        if (j < nkv0) {
-          if (!mbar_wait(&p_full[0], j & 1, abort_flag, err)) break;
-          tc_fence_after();
-          issue_pv(0, j);
+        issue_s(0, kt);
+        if (it.nkv1 > 0) issue_s(1, kt);
+        mma_commit(&k_empty[kt & 1]);
+        if (it.nkv == 1) mma_commit(q_empty);
+        for (int j = 0; j < it.nkv; ++j) {
+          const int t = kt + j;
+          const bool next = j + 1 < it.nkv;
+          if (!mbar_wait(&v_full[t & 1], (t >> 1) & 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          // slot 0: P·V of tile j, then S of tile j+1
+          if (j < it.nkv0) {
+            if (!mbar_wait(&p_full[0], c0 & 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            ++c0;
+            tc_fence_after();
+            issue_pv(0, t, j > 0);
+            if (j + 1 == it.nkv0) mma_commit(&o_full[0]);
+          }
+          if (next) {
+            if (!mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (j + 1 < it.nkv0) issue_s(0, t + 1);
+          }
+          // slot 1: P·V of tile j, then S of tile j+1
+          if (j < it.nkv1) {
+            if (!mbar_wait(&p_full[1], c1 & 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            ++c1;
+            tc_fence_after();
+            issue_pv(1, t, j > 0);
+            if (j + 1 == it.nkv1) mma_commit(&o_full[1]);
+          }
+          if (next) {
+            if (j + 1 < it.nkv1) issue_s(1, t + 1);
+            mma_commit(&k_empty[(t + 1) & 1]);
+            if (j + 2 == it.nkv) mma_commit(q_empty);     // the item's last S is issued
+          }
+          mma_commit(&v_empty[t & 1]);
         }
-        if (next) {
-          if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, err)) break;
-          tc_fence_after();
-          if (j + 1 < nkv0) issue_s(0, j + 1);
-        }
-        // slot 1: P·V of tile j, then S of tile j+1
-        if (j < nkv1) {
-          if (!mbar_wait(&p_full[1], j & 1, abort_flag, err)) break;
-          tc_fence_after();
-          issue_pv(1, j);
-        }
-        if (next) {
-          if (j + 1 < nkv1) issue_s(1, j + 1);
-          mma_commit(&k_empty[(j + 1) & 1]);
-        }
-        mma_commit(&v_empty[vst]);
-        if (j == nkv - 1) mma_commit(o_full);
+        if (!ok) break;
+        kt += it.nkv;
       }
       mma_commit(drain);
       volatile int no_abort = 0;
@@ -233,117 +302,135 @@ __global__ void __launch_bounds__(320, 1)
     // ---------------- softmax (warps 0..7, one query row per thread) ----------------
     const int g = warp >> 2, quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int nk = g == 0 ? nkv0 : nkv1;
-    const int qb = g ? qb1 : qb0;
-    const int qi = qb * kBM + r;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t s_col = lane_base + g * kBN, o_col = lane_base + C::TMEM_O + g * DH;
-    float m_used = -INFINITY, l = 0.f;
+    int c = 0;                                  // this slot's running tile count
+    int nitem = 0;                              // items in which this slot had work
     bool ok = true;
-    for (int j = 0; j < nk; ++j) {
-      if (!mbar_wait_warp(&s_full[g], j & 1, abort_flag, err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 16) {
-        uint32_t u[16];
-        tmem_ld16(s_col + c, u);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) s[c + i] = __uint_as_float(u[i]);
-      }
-      tmem_wait_ld();
-      // raw row maximum, four independent chains; only the diagonal tile masks
-      if (j == qb) {
-        const int lim = qi - j * kBN;          // column c is a future key iff c > lim
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c > lim) s[c] = -INFINITY;
-      }
-      float m4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-      for (int c = 4; c < kBN; c += 4)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m4[i] = fmaxf(m4[i], s[c + i]);
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      const float m_new = fmaxf(m_used, mx * scale_log2);
-      bool need = false;
-      if (j == 0) {
-        m_used = m_new;
-      } else {
-        need = m_new > m_used + kRescaleLog2;
-      }
-      if (__any_sync(0xffffffffu, need)) {
-        // the previous P·V of this slot must be finished before O is rewritten
-        if (!mbar_wait_warp(&pv_done[g], (j - 1) & 1, abort_flag, err)) {
+    for (int k = 0; ok; ++k) {
+      const int w = item_of(k);
+      if (w >= n_items) break;
+      const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs);
+      const int nk = g ? it.nkv1 : it.nkv0;
+      if (nk == 0) continue;
+      const int qb = g ? it.qb1 : it.qb0;
+      const int qi = qb * kBM + r;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < nk; ++j, ++c) {
+        if (!mbar_wait_warp(&s_full[g], c & 1, abort_flag, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float factor = need ? ex2_approx(m_used - m_new) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < DH; c += 8) {
-          uint32_t u[8];
-          tmem_ld8(o_col + c, u);
-          tmem_wait_ld();
+        float s[kBN];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * factor);
-          tmem_st8(o_col + c, u);
-        }
-        tmem_wait_st();
-        if (need) {
-          l *= factor;
-          m_used = m_new;
-        }
-      }
-      const float msub = m_used == -INFINITY ? 0.f : m_used;
-      // p = 2^(s·scale − m), in pairs; bf16 P back over the first 64 S columns
-      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-msub, -msub);
-      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        for (int cc = 0; cc < kBN; cc += 16) {
+          uint32_t u[16];
+          tmem_ld16(s_col + cc, u);
 #pragma unroll
-      for (int c = 0; c < kBN; c += 16) {
-        uint32_t u[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float2 arg = __ffma2_rn(make_float2(s[c + 2 * i], s[c + 2 * i + 1]), sc2, nm2);
-          const float2 p = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
-          sum2[i & 1] = __fadd2_rn(sum2[i & 1], p);
-          __nv_bfloat162 t = __floats2bfloat162_rn(p.x, p.y);
-          u[i] = *reinterpret_cast<uint32_t*>(&t);
+          for (int i = 0; i < 16; ++i) s[cc + i] = __uint_as_float(u[i]);
         }
-        tmem_st8(s_col + c / 2, u);
-      }
-      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]);
-      l += s01.x + s01.y;
-      tmem_wait_st();
-      tc_fence_before();      // P (and any O rescale) before the next MMA
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[g]);
-    }
-    if (nk > 0 && ok && mbar_wait_warp(o_full, 0, abort_flag, err)) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
-      bf16* orow = out + ((size_t)b * T + qi) * (size_t)H * DH + (size_t)(g ? h1 : h0) * DH;
-#pragma unroll 1
-      for (int c = 0; c < DH; c += 16) {
-        uint32_t u[16];
-        tmem_ld16(o_col + c, u);
         tmem_wait_ld();
-        if (qi < T) {
-          uint4 w[2];
-          uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+        // raw row maximum, four chains of three-input maxima; only the
+        // diagonal tile masks future keys
+        if (j == qb) {
+          const int lim = qi - j * kBN;          // column cc is a future key iff cc > lim
+#pragma unroll
+          for (int cc = 0; cc < kBN; ++cc)
+            if (cc > lim) s[cc] = -INFINITY;
+        }
+        float m4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float m = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+          for (int cc = 8 + 2 * i; cc < kBN; cc += 8) m = fmax3(m, s[cc], s[cc + 1]);
+          m4[i] = m;
+        }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        const float m_new = fmaxf(m_used, mx * scale_log2);
+        bool need = false;
+        if (j == 0) {
+          m_used = m_new;
+        } else {
+          need = m_new > m_used + kRescaleLog2;
+        }
+        if (__any_sync(0xffffffffu, need)) {
+          // the previous P·V of this slot must be finished before O is rewritten
+          if (!mbar_wait_warp(&pv_done[g], (c - 1) & 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float factor = need ? ex2_approx(m_used - m_new) : 1.f;
+#pragma unroll 1
+          for (int cc = 0; cc < DH; cc += 8) {
+            uint32_t u[8];
+            tmem_ld8(o_col + cc, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * factor);
+            tmem_st8(o_col + cc, u);
+          }
+          tmem_wait_st();
+          if (need) {
+            l *= factor;
+            m_used = m_new;
+          }
+        }
+        const float msub = m_used == -INFINITY ? 0.f : m_used;
+        // p = 2^(s·scale − m), in pairs; bf16 P back over the first 64 S columns
+        const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-msub, -msub);
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int cc = 0; cc < kBN; cc += 16) {
+          uint32_t u[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(u[2 * i]) * inv,
-                                                     __uint_as_float(u[2 * i + 1]) * inv);
+            const float2 arg = __ffma2_rn(make_float2(s[cc + 2 * i], s[cc + 2 * i + 1]), sc2, nm2);
+            const float2 p = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+            sum2[i & 1] = __fadd2_rn(sum2[i & 1], p);
+            __nv_bfloat162 t = __floats2bfloat162_rn(p.x, p.y);
+            u[i] = *reinterpret_cast<uint32_t*>(&t);
+          }
+          tmem_st8(s_col + cc / 2, u);
+        }
+        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]);
+        l += s01.x + s01.y;
+        tmem_wait_st();
+        tc_fence_before();      // P (and any O rescale) before the next MMA
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[g]);
+      }
+      if (!ok || !mbar_wait_warp(&o_full[g], nitem & 1, abort_flag, err)) {
+        ok = false;
+        break;
+      }
+      ++nitem;
+      // O of this item; the next item's first P·V into these columns waits for
+      // this slot's next P, which these warps write only after this drain
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      bf16* orow = out + ((size_t)it.b * T + qi) * (size_t)H * DH + (size_t)(g ? it.h1 : it.h0) * DH;
+      uint32_t u[DH];
+#pragma unroll
+      for (int cc = 0; cc < DH; cc += 16) tmem_ld16(o_col + cc, *reinterpret_cast<uint32_t(*)[16]>(u + cc));
+      tmem_wait_ld();
+      if (qi < T) {
+#pragma unroll
+        for (int cc = 0; cc < DH; cc += 8) {
+          uint4 wv;
+          uint32_t* wp = reinterpret_cast<uint32_t*>(&wv);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(u[cc + 2 * i]) * inv,
+                                                     __uint_as_float(u[cc + 2 * i + 1]) * inv);
             wp[i] = *reinterpret_cast<uint32_t*>(&t);
           }
-          *reinterpret_cast<uint4*>(orow + c) = w[0];
-          *reinterpret_cast<uint4*>(orow + c + 8) = w[1];
+          *reinterpret_cast<uint4*>(orow + cc) = wv;
         }
       }
+      tc_fence_before();
     }
   }
 
@@ -377,8 +464,11 @@ cudaError_t run(const void* q, const void* k, const void* v, void* o, int B, int
   const int nq = (T + kBM - 1) / kBM;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   const int head_pairs = ((H / Hkv) % 2 == 0) ? 1 : 0;
-  const dim3 grid = head_pairs ? dim3(H / 2, B, nq) : dim3(H, B, (nq + 1) / 2);
-  k_attn_tc<DH><<<grid, 320, C::SMEM, s>>>(tq, tk, tv, (bf16*)o, T, H, Hkv, nq, head_pairs, scale_log2,
+  const long long items = head_pairs ? (long long)nq * B * (H / 2) : (long long)((nq + 1) / 2) * B * H;
+  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  const int n_items = (int)items;
+  const int grid = n_items < sm_count() ? n_items : sm_count();
+  k_attn_tc<DH><<<grid, 320, C::SMEM, s>>>(tq, tk, tv, (bf16*)o, B, T, H, Hkv, nq, head_pairs, n_items, scale_log2,
                                            device_error_word());
   return cudaGetLastError();
 }

@@ -115,6 +115,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input form of max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // ---- tcgen05 -------------------------------------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
@@ -153,6 +160,65 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+
+// Batched issue of the MMAs of one tile, for an issuing thread that must spend
+// as few instructions per MMA as possible: descriptors are passed as their low
+// and high 32-bit words, each MMA's operand offset is an immediate added to the
+// low word (the address field never carries into the high word below 256 KB of
+// shared memory), and one predicate serves every MMA after the first.
+//
+// S += Q·Kᵀ over dh = 16·NK: both operands K-major with the 128-byte swizzle,
+// 64-element column blocks 16 KB apart (128 rows of 128 bytes).
+#define TB_MMA_SS_STEP(OFF, PRED)                                              \
+  "add.u32 la, %1, " #OFF ";\n\t"                                             \
+  "add.u32 lb, %3, " #OFF ";\n\t"                                             \
+  "mov.b64 da, {la, %2};\n\t"                                                 \
+  "mov.b64 db, {lb, %4};\n\t"                                                 \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, " #PRED ";\n\t"
+template <int NK>
+__device__ __forceinline__ void mma_tile_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  static_assert(NK == 4 || NK == 8, "dh 64 or 128");
+  const uint32_t alo = (uint32_t)adesc, ahi = (uint32_t)(adesc >> 32);
+  const uint32_t blo = (uint32_t)bdesc, bhi = (uint32_t)(bdesc >> 32);
+  if constexpr (NK == 4) {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        TB_MMA_SS_STEP(0, pf) TB_MMA_SS_STEP(2, pt) TB_MMA_SS_STEP(4, pt) TB_MMA_SS_STEP(6, pt) "}" ::"r"(d_tmem),
+        "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        TB_MMA_SS_STEP(0, pf) TB_MMA_SS_STEP(2, pt) TB_MMA_SS_STEP(4, pt) TB_MMA_SS_STEP(6, pt)
+        TB_MMA_SS_STEP(1024, pt) TB_MMA_SS_STEP(1026, pt) TB_MMA_SS_STEP(1028, pt) TB_MMA_SS_STEP(1030, pt) "}" ::"r"(d_tmem),
+        "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc)
+        : "memory");
+  }
+}
+#undef TB_MMA_SS_STEP
+
+// O (+)= P·V over 128 keys: P (bf16 pairs) in tensor memory at a_tmem, 8
+// columns per 16 keys; V MN-major with 16-key slices 2 KB apart.  `acc` = 0
+// overwrites O with the first slice's product.
+#define TB_MMA_TS_STEP(K, PRED)                                                \
+  "add.u32 ta, %1, " #K "*8;\n\t"                                             \
+  "add.u32 lb, %2, " #K "*128;\n\t"                                           \
+  "mov.b64 db, {lb, %3};\n\t"                                                 \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, " #PRED ";\n\t"
+__device__ __forceinline__ void mma_tile_ts128(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t acc) {
+  const uint32_t blo = (uint32_t)bdesc, bhi = (uint32_t)(bdesc >> 32);
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b32 ta, lb;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 pf, %5, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      TB_MMA_TS_STEP(0, pf) TB_MMA_TS_STEP(1, pt) TB_MMA_TS_STEP(2, pt) TB_MMA_TS_STEP(3, pt)
+      TB_MMA_TS_STEP(4, pt) TB_MMA_TS_STEP(5, pt) TB_MMA_TS_STEP(6, pt) TB_MMA_TS_STEP(7, pt) "}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+#undef TB_MMA_TS_STEP
 
 // Arrive on `bar` once every tcgen05 op this thread issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
