@@ -35,6 +35,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Token count up to which each bf16 GEMM runs as a K-split kernel plus a
+# partial-sum epilogue kernel (two launches instead of one).
+FEW_TOKENS = 64
+
+
+def decode_launches(B: int) -> int:
+    """Kernels one decode step launches: row statistics, the two attention
+    kernels, and the four GEMMs."""
+    return 3 + 4 * (2 if B <= FEW_TOKENS else 1)
 
 
 def load_peaks():
@@ -284,7 +293,8 @@ def bench_prefill(args, s, world, peaks):
                "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                "d2h_bytes_per_step": yh.numel() * yh.element_size(), "ms_per_step": e2e_ms / args.steps}
     del ws
-    return {"ms_total": ms_total, "stages": stages, "clocks": clk, "e2e": e2e, "launches_per_step": 6}
+    return {"ms_total": ms_total, "stages": stages, "clocks": clk, "e2e": e2e,
+            "launches_per_step": 6 if s.B * s.T > FEW_TOKENS else 10}
 
 
 # DRAM bytes (read + write) per launch of a kernel at the benchmark workload,
@@ -392,7 +402,7 @@ def bench_decode(args, world, peaks):
     return {
         "workload": s.name, "B": s.B, "T_max": s.T, "kv_bytes": kv_bytes, "weight_bytes": w_bytes,
         "kv_gbs": kv_gbs, "kv_frac_hbm": kv_gbs / peaks["hbm_gbs"], "attn_ms": attn_ms, "step_ms": ms,
-        "tok_s": world * s.B / (ms * 1e-3), "stages_ms": stages, "gpu_launches": 7 * n,
+        "tok_s": world * s.B / (ms * 1e-3), "stages_ms": stages, "gpu_launches": decode_launches(s.B) * n,
         "graph_step_ms": graph_ms,
         "graph_tok_s": None if graph_ms is None else world * s.B / (graph_ms * 1e-3),
         "step_hbm_gbs": (kv_bytes + w_bytes) / (ms * 1e-3) / 1e9,

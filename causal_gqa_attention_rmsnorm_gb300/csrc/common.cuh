@@ -116,6 +116,19 @@ cudaError_t gemm_simt_w13(int dtype, const void* A, const void* B, int M, int N,
 cudaError_t gemm_simt_w2(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
                          const W2Args& e, cudaStream_t s);
 
+// gemm_skinny.cu (bf16, M ≤ skinny_max_tokens(): K-split tcgen05 GEMM plus a
+// partial-sum epilogue kernel; `part` holds skinny_part_floats(M, N) floats)
+int skinny_max_tokens();
+size_t skinny_part_floats(int M, int max_n);
+cudaError_t gemm_skinny_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
+                            float* part, cudaStream_t s);
+cudaError_t gemm_skinny_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
+                           float* part, cudaStream_t s);
+cudaError_t gemm_skinny_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
+                            float* part, cudaStream_t s);
+cudaError_t gemm_skinny_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
+                           float* part, cudaStream_t s);
+
 // attn_simt.cu (fp32 path)
 cudaError_t attn_prefill_simt(int dtype, const void* q, const void* k, const void* v, void* o, int B,
                               int T, int H, int Hkv, int dh, int kv_stride, cudaStream_t s);

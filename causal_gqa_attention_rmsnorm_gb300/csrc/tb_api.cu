@@ -132,6 +132,7 @@ struct Work {
   void* a;
   float* part;
   int nchunk_max;
+  float* skpart;             // K-split partial sums of the few-token GEMMs (bf16, M ≤ 64)
   size_t total;
 };
 
@@ -164,8 +165,33 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
     w.nchunk_max = (T + decode_chunk_keys() - 1) / decode_chunk_keys();
     w.part = (float*)take(decode_part_floats(B, c->H, c->dh, w.nchunk_max) * 4);
   }
+  if (c->dtype == TB_BF16 && M <= (size_t)skinny_max_tokens()) {
+    int max_n = (c->H + 2 * c->Hkv) * c->dh;
+    if (c->d > max_n) max_n = c->d;
+    if (2 * c->f > max_n) max_n = 2 * c->f;
+    w.skpart = (float*)take(skinny_part_floats((int)M, max_n) * 4);
+  }
   w.total = off;
   return w;
+}
+
+// bf16 GEMMs: few tokens go to the K-split GEMM, which streams the weights
+// with every SM; more tokens to the persistent tile GEMM.
+cudaError_t mm_qkv(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D,
+                   const QKVArgs& e, cudaStream_t s) {
+  return W.skpart ? gemm_skinny_qkv(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_qkv(A, Bw, M, N, K, D, e, s);
+}
+cudaError_t mm_wo(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D, const WoArgs& e,
+                  cudaStream_t s) {
+  return W.skpart ? gemm_skinny_wo(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_wo(A, Bw, M, N, K, D, e, s);
+}
+cudaError_t mm_w13(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D,
+                   const W13Args& e, cudaStream_t s) {
+  return W.skpart ? gemm_skinny_w13(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_w13(A, Bw, M, N, K, D, e, s);
+}
+cudaError_t mm_w2(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D, const W2Args& e,
+                  cudaStream_t s) {
+  return W.skpart ? gemm_skinny_w2(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_w2(A, Bw, M, N, K, D, e, s);
 }
 
 tb_status check_kv(const tb_block_cfg* c, const tb_kvcache* kv, int B) {
@@ -313,15 +339,15 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
     TB_TRY(gemm_simt_w2(dt, W.a, P.w2, M, cfg->d, cfg->f, D, ya, s));
   } else {
     rec.stage("qkv");
-    TB_TRY(gemm_tc_qkv(x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
+    TB_TRY(mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_prefill_tc(W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, s));
     rec.stage("wo");
-    TB_TRY(gemm_tc_wo(W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    TB_TRY(mm_wo(W, W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
-    TB_TRY(gemm_tc_w13(W.hb, P.w13, M, 2 * cfg->f, cfg->d, D, ga, s));
+    TB_TRY(mm_w13(W, W.hb, P.w13, M, 2 * cfg->f, cfg->d, D, ga, s));
     rec.stage("w2");
-    TB_TRY(gemm_tc_w2(W.a, P.w2, M, cfg->d, cfg->f, D, ya, s));
+    TB_TRY(mm_w2(W, W.a, P.w2, M, cfg->d, cfg->f, D, ya, s));
   }
   return TB_OK;
 }
@@ -380,16 +406,16 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(gemm_simt_w2(dt, W.a, P.w2, B, cfg->d, cfg->f, D, ya, s));
   } else {
     rec.stage("qkv");
-    TB_TRY(gemm_tc_qkv(x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
+    TB_TRY(mm_qkv(W, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
                        W.nchunk_max, W.counter, W.o, s));
     rec.stage("wo");
-    TB_TRY(gemm_tc_wo(W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    TB_TRY(mm_wo(W, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
-    TB_TRY(gemm_tc_w13(W.hb, P.w13, B, 2 * cfg->f, cfg->d, D, ga, s));
+    TB_TRY(mm_w13(W, W.hb, P.w13, B, 2 * cfg->f, cfg->d, D, ga, s));
     rec.stage("w2");
-    TB_TRY(gemm_tc_w2(W.a, P.w2, B, cfg->d, cfg->f, D, ya, s));
+    TB_TRY(mm_w2(W, W.a, P.w2, B, cfg->d, cfg->f, D, ya, s));
   }
   return TB_OK;
 }

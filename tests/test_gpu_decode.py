@@ -66,6 +66,32 @@ def test_decode_small(name):
             assert torch.isnan(kv.k[b, :, pos + 1:].float()).all()
 
 
+# Few-token GEMMs: token counts padded to 16, 32, 48 and 64 (65 takes the tile
+# GEMM), output widths that end in a partial 128-row weight tile (960, 320),
+# and weight matrices long enough in K to be split unevenly over CTAs.
+FEW_TOKENS = {
+    "ragged_n": workloads.BlockShape("few_ragged_n", "decode", "bf16", B=1, T=0, d=320, H=5, Hkv=5, dh=64,
+                                     f=192, rope_base=1e4, eps=1e-6, gains="normal"),
+    "split_k": workloads.BlockShape("few_split_k", "decode", "bf16", B=1, T=0, d=1024, H=8, Hkv=8, dh=128,
+                                    f=2752, rope_base=5e5, eps=1e-5, gains="normal"),
+}
+
+
+@pytest.mark.parametrize("B", [1, 17, 40, 64, 65])
+@pytest.mark.parametrize("name", list(FEW_TOKENS))
+def test_decode_token_counts(name, B):
+    T_max = 64
+    lens = np.random.default_rng(100 + B).integers(0, T_max - 1, size=B).tolist()
+    s, inp, kv, y, err = _decode_case(FEW_TOKENS[name].with_(B=B), 21 + B, lens, T_max)
+    assert err == 0
+    assert kv.lens.cpu().tolist() == [n + 1 for n in lens]
+    for b, pos in enumerate(lens):
+        ref = _oracle_step(s, inp, kv, b, pos)
+        assert_close(y[b, 0].cpu().double().numpy(), ref["y"], s.dtype, f"y b={b}")
+        assert_close(kv.k[b, :, pos].cpu().double().numpy(), ref["k"], s.dtype, f"k row b={b}")
+        assert_close(kv.v[b, :, pos].cpu().double().numpy(), ref["v"], s.dtype, f"v row b={b}")
+
+
 def test_decode_continues_a_prefill():
     """Prefill T-1 tokens into the cache, decode token T-1: equals row T-1 of
     the oracle prefill of all T tokens (decode with a cache is the same
