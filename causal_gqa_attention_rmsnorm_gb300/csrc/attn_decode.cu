@@ -202,11 +202,17 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restric
 constexpr int kCombineMaxChunks = 1024;
 
 template <typename T, int DH>
-__global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict__ part,
+__global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict__ part,
                                                         const int32_t* __restrict__ pos_arr, int H, int nchunk_max,
                                                         int chunk, T* __restrict__ o) {
+  // Thread (e, g) sums output column e over chunks g, g + NG, ... with eight
+  // independent loads in flight, so the merge costs a few L2 round trips.
+  static_assert(256 % DH == 0, "head width must divide the block");
+  constexpr int NG = 256 / DH;
+  constexpr int U = 8;
   __shared__ float w_s[kCombineMaxChunks];
-  __shared__ float red[128 / 32];
+  __shared__ float red[256 / 32];
+  __shared__ float acc_s[NG][DH];
   const int h = blockIdx.x, b = blockIdx.y;
   const int pos = pos_arr[b];
   T* orow = o + ((size_t)b * H + h) * DH;
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict_
   __syncthreads();
   float M = red[0];
 #pragma unroll
-  for (int i = 1; i < 128 / 32; ++i) M = fmaxf(M, red[i]);
+  for (int i = 1; i < 256 / 32; ++i) M = fmaxf(M, red[i]);
   __syncthreads();
   // weights w_c = 2^(m_c - M) and L = Σ_c l_c·w_c
   float Lp = 0.f;
@@ -246,19 +252,30 @@ __global__ void __launch_bounds__(128) k_decode_combine(const float* __restrict_
   __syncthreads();
   float L = 0.f;
 #pragma unroll
-  for (int i = 0; i < 128 / 32; ++i) L += red[i];
-  const float inv = 1.0f / L;
-  for (int e = threadIdx.x; e < DH; e += blockDim.x) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int c = 0;
-    for (; c + 4 <= nc; c += 4) {
-      a0 += pr[(size_t)c * P + 4 + e] * w_s[c];
-      a1 += pr[(size_t)(c + 1) * P + 4 + e] * w_s[c + 1];
-      a2 += pr[(size_t)(c + 2) * P + 4 + e] * w_s[c + 2];
-      a3 += pr[(size_t)(c + 3) * P + 4 + e] * w_s[c + 3];
-    }
-    for (; c < nc; ++c) a0 += pr[(size_t)c * P + 4 + e] * w_s[c];
-    orow[e] = from_f<T>(((a0 + a1) + (a2 + a3)) * inv);
+  for (int i = 0; i < 256 / 32; ++i) L += red[i];
+  const int e = threadIdx.x % DH, g = threadIdx.x / DH;
+  float a[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) a[u] = 0.f;
+  int c = g;
+  for (; c + (U - 1) * NG < nc; c += U * NG) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = pr[(size_t)(c + u * NG) * P + 4 + e];
+#pragma unroll
+    for (int u = 0; u < U; ++u) a[u] = fmaf(v[u], w_s[c + u * NG], a[u]);
+  }
+  for (; c < nc; c += NG) a[0] = fmaf(pr[(size_t)c * P + 4 + e], w_s[c], a[0]);
+  float t = 0.f;
+#pragma unroll
+  for (int u = 0; u < U; ++u) t += a[u];
+  acc_s[g][e] = t;
+  __syncthreads();
+  if (g == 0) {
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < NG; ++i) sum += acc_s[i][e];
+    orow[e] = from_f<T>(sum / L);
   }
 }
 
@@ -570,7 +587,7 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_mma<DH, G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, (const bf16*)q, pos, B, Hkv, part,
                                                              nchunk_max, counter, scale_log2, device_error_word());
-  k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), 128, 0, s>>>(part, pos, Hkv * G, nchunk_max,
+  k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max,
                                                                              kMChunk, (bf16*)o);
   return cudaGetLastError();
 }
@@ -593,7 +610,7 @@ cudaError_t run(const void* q, const void* kc, const void* vc, const int32_t* po
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_split<T, DH, G><<<dim3(nchunk_max, Hkv, B), kWarps * 32, 0, s>>>(
       (const T*)q, (const T*)kc, (const T*)vc, pos, Hkv, T_max, part, nchunk_max, scale_log2);
-  k_decode_combine<T, DH><<<dim3(Hkv * G, B), 128, 0, s>>>(part, pos, Hkv * G, nchunk_max,
+  k_decode_combine<T, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max,
                                                                           kChunk, (T*)o);
   return cudaGetLastError();
 }

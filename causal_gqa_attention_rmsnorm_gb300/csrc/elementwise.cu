@@ -62,8 +62,23 @@ __global__ void k_row_stats(const T* __restrict__ x, int M, int d, float eps, fl
   float s = 0.f;
   constexpr int V = Vec16<T>::N;
   if ((d % V) == 0) {
+    // four 16-byte loads in flight per lane
     const uint4* p = reinterpret_cast<const uint4*>(xr);
-    for (int i = lane; i < d / V; i += 32) {
+    const int nv = d / V;
+    int i = lane;
+    for (; i + 96 < nv; i += 128) {
+      Vec16<T> v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u].raw = __ldg(p + i + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+          const float f = v[u].get(j);
+          s = fmaf(f, f, s);
+        }
+    }
+    for (; i < nv; i += 32) {
       Vec16<T> v;
       v.raw = __ldg(p + i);
 #pragma unroll

@@ -4,17 +4,20 @@
 // With M tokens and N outputs, C = X·Wᵀ is bound by streaming the weight
 // matrix W [N, K] from HBM.  The product is computed transposed, Cᵀ = W·Xᵀ, so
 // that 128 weight rows form the MMA's M dimension and the (padded) tokens its N
-// dimension: no MMA lane is wasted on padding rows.  Each CTA owns one
-// 128-row weight tile and one contiguous range of K; enough K ranges are used
-// that about two CTAs per SM stream weights at once.
+// dimension: no MMA lane is wasted on padding rows.  A work item is one
+// 128-row weight tile over one contiguous range of K; persistent CTAs, two per
+// SM, walk the items with one continuous stage ring, so every SM streams
+// weights from the first cycle to the last.
 //   warp 0      TMA: the weight tile [128, 64] and the token tile [NT, 64]
 //               of each K block into a ring of shared-memory stages;
 //   warp 1      MMA issuer: D[128, NT] += W_blk · X_blkᵀ (tcgen05, fp32 in
 //               tensor memory);
 //   warps 2..5  drain: each warp's 32 TMEM lanes are 32 output features; the
-//               fp32 partial sums go to part[split][token][feature].
-// A second kernel adds the K-range partials and applies the block's fused
-// epilogue (the same functors as the large GEMMs) to 4 outputs per thread.
+//               fp32 partial sums go to part[split][token][feature] while the
+//               next item accumulates into the other TMEM buffer.
+// A second kernel adds the K-range partials (from L2) and applies the block's
+// fused epilogue, the same functors as the large GEMMs, to 4 outputs per
+// thread.
 #include "epilogues.cuh"
 #include "gemm_tc.cuh"
 #include "sm100_ptx.cuh"
@@ -27,7 +30,7 @@ using namespace ptx;
 constexpr int kRows = 128;       // weight rows per CTA: the MMA's M
 constexpr int kBK = 64;          // K per stage (one 128-byte swizzle row)
 constexpr int kMaxTok = 64;
-constexpr int kMaxCtas = 320;    // tiles × splits target bound; sizes the partial buffer
+constexpr int kMaxItems = 1024;  // (weight tile, K range) items; sizes the partial buffer
 
 template <int NT> struct SkCfg {
   static constexpr int STAGES = NT <= 32 ? 5 : 4;           // two CTAs per SM
@@ -36,35 +39,46 @@ template <int NT> struct SkCfg {
   static constexpr uint32_t STAGE_BYTES = W_BYTES + X_BYTES;
   static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
   static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t TMEM_COLS = NT <= 32 ? 32 : 64;
+  static constexpr uint32_t ACC_COLS = 64;                   // two accumulators of NT ≤ 64 columns
+  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 };
 
+// Persistent: CTA c takes work items c, c + gridDim.x, ...; item w is weight
+// tile w % tiles over K range w / tiles.  The stage ring runs on across items
+// and the accumulators alternate, so one item's drain overlaps the next
+// item's loads and MMAs.
 template <int NT>
 __global__ void __launch_bounds__(192)
     k_gemm_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N,
-                  int kblocks, int splits, float* __restrict__ part, int* err) {
+                  int tiles, int kblocks, int splits, float* __restrict__ part, int* err) {
   using C = SkCfg<NT>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* drain = tfull + 1;
+  uint64_t* tfull = empty + STAGES;     // [2]
+  uint64_t* tempty = tfull + 2;         // [2]
+  uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kRows, sp = blockIdx.y;
-  const int kb0 = (int)((long long)kblocks * sp / splits);
-  const int nkb = (int)((long long)kblocks * (sp + 1) / splits) - kb0;   // ≥ 1: splits ≤ kblocks
+  const int items = tiles * splits;
+  auto krange = [&](int sp, int& kb0, int& nkb) {
+    kb0 = (int)((long long)kblocks * sp / splits);
+    nkb = (int)((long long)kblocks * (sp + 1) / splits) - kb0;   // ≥ 1: splits ≤ kblocks
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -82,57 +96,82 @@ __global__ void __launch_bounds__(192)
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int st = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (!mbar_wait(&empty[st], ph ^ 1u, abort_flag, err)) break;
-        uint8_t* sw = smem + st * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
-        tma_load_2d(&tmW, sw, &full[st], (kb0 + i) * kBK, n0);
-        tma_load_2d(&tmX, sw + C::W_BYTES, &full[st], (kb0 + i) * kBK, 0);
-        ++issued;
+      int i = 0;                                  // running K-block count: stage i % STAGES
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+        const int tile = w % tiles;
+        int kb0, nkb;
+        krange(w / tiles, kb0, nkb);
+        for (int j = 0; j < nkb; ++j, ++i) {
+          const int st = i % STAGES;
+          if (!mbar_wait(&empty[st], ((i / STAGES) & 1) ^ 1u, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sw = smem + st * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+          tma_load_2d(&tmW, sw, &full[st], (kb0 + j) * kBK, tile * kRows);
+          tma_load_2d(&tmX, sw + C::W_BYTES, &full[st], (kb0 + j) * kBK, 0);
+        }
       }
-      // every copy issued must land before the CTA may exit
+      // every copy issued must land before the CTA may exit (earlier copies
+      // into the same stages were consumed, hence complete)
       volatile int no_abort = 0;
-      for (int i = issued - STAGES < 0 ? 0 : issued - STAGES; i < issued; ++i)
-        mbar_wait(&full[i % STAGES], (i / STAGES) & 1, &no_abort, err);
+      for (int t = i - STAGES < 0 ? 0 : i - STAGES; t < i; ++t)
+        mbar_wait(&full[t % STAGES], (t / STAGES) & 1, &no_abort, err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kRows, NT);
+      int i = 0, local = 0;
       bool ok = true;
-      for (int i = 0; i < nkb; ++i) {
-        const int st = i % STAGES;
-        if (!mbar_wait(&full[st], (i / STAGES) & 1, abort_flag, err)) {
-          ok = false;
-          break;
-        }
+      for (int w = blockIdx.x; ok && w < items; w += gridDim.x, ++local) {
+        int kb0, nkb;
+        krange(w / tiles, kb0, nkb);
+        const int acc = local & 1;
+        if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1u, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t w0 = smem_u32(smem + st * C::STAGE_BYTES), x0 = w0 + C::W_BYTES;
+        const uint32_t d = tmem + acc * C::ACC_COLS;
+        for (int j = 0; j < nkb; ++j, ++i) {
+          const int st = i % STAGES;
+          if (!mbar_wait(&full[st], (i / STAGES) & 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w0 = smem_u32(smem + st * C::STAGE_BYTES), x0 = w0 + C::W_BYTES;
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)
-          mma_bf16_ss(tmem, desc_kmajor_sw128(w0 + k * 32), desc_kmajor_sw128(x0 + k * 32), idesc, (i | k) != 0);
-        mma_commit(&empty[st]);
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss(d, desc_kmajor_sw128(w0 + k * 32), desc_kmajor_sw128(x0 + k * 32), idesc, (j | k) != 0);
+          mma_commit(&empty[st]);
+        }
+        if (ok) mma_commit(&tfull[acc]);
       }
-      if (ok) mma_commit(tfull);
       mma_commit(drain);
       volatile int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, err);
     }
   } else {
-    // lane l of warp w holds output feature n0 + 32·(w%4) + l for all NT tokens
+    // lane l of warp w holds output feature 32·(w%4) + l of the tile for all
+    // NT tokens; the accumulator is released as soon as it is in registers
     const int quad = warp & 3;
-    if (mbar_wait_warp(tfull, 0, abort_flag, err)) {
+    int local = 0;
+    for (int w = blockIdx.x; w < items; w += gridDim.x, ++local) {
+      const int acc = local & 1;
+      if (!mbar_wait_warp(&tfull[acc], (local >> 1) & 1, abort_flag, err)) break;
       tc_fence_after();
       uint32_t u[NT];
 #pragma unroll
       for (int c = 0; c < NT; c += 16)
-        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c, *reinterpret_cast<uint32_t(*)[16]>(u + c));
+        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + acc * C::ACC_COLS + c,
+                  *reinterpret_cast<uint32_t(*)[16]>(u + c));
       tmem_wait_ld();
-      const int n = n0 + quad * 32 + lane;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      const int n = (w % tiles) * kRows + quad * 32 + lane;
       if (n < N) {
-        float* dst = part + (size_t)sp * M * N + n;
+        float* dst = part + (size_t)(w / tiles) * M * N + n;
 #pragma unroll
         for (int m = 0; m < NT; ++m)
           if (m < M) dst[(size_t)m * N] = __uint_as_float(u[m]);
@@ -158,17 +197,36 @@ __global__ void __launch_bounds__(256)
   const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   float r = 0.f;
   if (col < N) {
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* p = part + (size_t)m * N + col;
-    for (int s = 0; s < splits; ++s) {
-      const float4 t = *reinterpret_cast<const float4*>(p + (size_t)s * M * N);
-      v[0] += t.x;
-      v[1] += t.y;
-      v[2] += t.z;
-      v[3] += t.w;
-    }
+    // the epilogue's own inputs first, then the partials eight at a time
     const auto ra = epi.row_aux(m);
-    r = epi(m, col, v, ra, epi.aux(m, col, ra));
+    const auto ax = epi.aux(m, col, ra);
+    constexpr int U = 8;
+    float4 a[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* p = part + (size_t)m * N + col;
+    const size_t stride = (size_t)M * N;
+    int sp = 0;
+    for (; sp + U <= splits; sp += U) {
+      float4 t[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) t[u] = *reinterpret_cast<const float4*>(p + (size_t)(sp + u) * stride);
+#pragma unroll
+      for (int u = 0; u < U; ++u) a[u] = make_float4(a[u].x + t[u].x, a[u].y + t[u].y, a[u].z + t[u].z, a[u].w + t[u].w);
+    }
+    for (int u = 0; sp < splits; ++sp, ++u) {
+      const float4 t = *reinterpret_cast<const float4*>(p + (size_t)sp * stride);
+      a[u] = make_float4(a[u].x + t.x, a[u].y + t.y, a[u].z + t.z, a[u].w + t.w);
+    }
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      v[0] += a[u].x;
+      v[1] += a[u].y;
+      v[2] += a[u].z;
+      v[3] += a[u].w;
+    }
+    r = epi(m, col, v, ra, ax);
   }
   if constexpr (Epi::kRowReduce) {
     r = warp_sum(r);
@@ -176,13 +234,23 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// K ranges per weight tile.  Items are equal in size, so the time is the
+// number of item waves over the resident CTAs (two per SM): take the split
+// count whose item count fills its last wave best (fewest splits on a tie),
+// with at least 4 K blocks (64 KB of weights) per item.  The partials
+// (items × 128 × M floats) stay in L2 between the two kernels.
 int split_count(int tiles, int kblocks) {
-  int target = 2 * sm_count();
-  if (target > kMaxCtas) target = kMaxCtas;
-  int sp = target / tiles;
-  const int cap = kblocks / 8 > 0 ? kblocks / 8 : 1;     // at least 8 K blocks (1 MB of W) per CTA
-  if (sp > cap) sp = cap;
-  return sp < 1 ? 1 : sp;
+  const long long slots = 2LL * sm_count();
+  int spmax = kblocks / 4;
+  if (spmax > kMaxItems / tiles) spmax = kMaxItems / tiles;
+  int best = 1;
+  double best_fill = 0.0;
+  for (int sp = 1; sp <= spmax; ++sp) {
+    const long long items = (long long)tiles * sp, waves = (items + slots - 1) / slots;
+    const double fill = (double)items / (double)(waves * slots);
+    if (fill > best_fill + 1e-3) best = sp, best_fill = fill;
+  }
+  return best;
 }
 
 template <int NT, class Epi>
@@ -203,8 +271,9 @@ cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi&
   }
   const int tiles = (N + kRows - 1) / kRows, kblocks = K / kBK;
   const int splits = split_count(tiles, kblocks);
-  k_gemm_skinny<NT><<<dim3(tiles, splits), 192, C::SMEM, s>>>(tw, tx, M, N, kblocks, splits, part,
-                                                              device_error_word());
+  const int items = tiles * splits, slots = 2 * sm_count();
+  k_gemm_skinny<NT><<<items < slots ? items : slots, 192, C::SMEM, s>>>(tw, tx, M, N, tiles, kblocks, splits, part,
+                                                                       device_error_word());
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k_splitk_epilogue<Epi><<<dim3((N / 4 + 255) / 256, M), 256, 0, s>>>(part, splits, M, N, epi);
@@ -226,8 +295,8 @@ cudaError_t run(const void* X, const void* W, int M, int N, int K, const Epi& ep
 int skinny_max_tokens() { return kMaxTok; }
 
 size_t skinny_part_floats(int M, int max_n) {
-  const int tiles = (max_n + kRows - 1) / kRows;
-  return (size_t)M * kRows * (size_t)(tiles > kMaxCtas ? tiles : kMaxCtas);
+  const size_t tiles = (size_t)(max_n + kRows - 1) / kRows;
+  return (size_t)M * kRows * (tiles > (size_t)kMaxItems ? tiles : (size_t)kMaxItems);
 }
 
 cudaError_t gemm_skinny_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
