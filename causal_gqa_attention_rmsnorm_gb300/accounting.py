@@ -45,10 +45,19 @@ def gemm_flops_each(d: int, H: int, Hkv: int, dh: int, f: int, tokens: int) -> d
     }
 
 
-def causal_attn_flops(B: int, H: int, dh: int, T: int) -> int:
+def visible_pairs(T: int, window: int = 0) -> int:
+    """(query, key) pairs a causal prefill of T tokens attends: query i meets
+    i+1 keys, or min(i+1, W) with a sliding window W > 0 ("09 The Transformer"
+    §5, sliding-window attention)."""
+    if window <= 0 or window >= T:
+        return T * (T + 1) // 2
+    return window * (window + 1) // 2 + (T - window) * window
+
+
+def causal_attn_flops(B: int, H: int, dh: int, T: int, window: int = 0) -> int:
     """Exact causal attention FLOPs of a prefill: 4·dh per (query head, visible
-    pair), T(T+1)/2 visible pairs per head and sequence."""
-    return 4 * B * H * dh * (T * (T + 1) // 2)
+    pair)."""
+    return 4 * B * H * dh * visible_pairs(T, window)
 
 
 def full_attn_flops(B: int, H: int, dh: int, T: int) -> int:
@@ -66,10 +75,16 @@ def kv_bytes_per_token(L: int, Hkv: int, dh: int, bytes_per_value: int) -> int:
     return 2 * L * Hkv * dh * bytes_per_value
 
 
-def decode_kv_bytes(lens: Iterable[int], Hkv: int, dh: int, bytes_per_value: int) -> int:
-    """KV bytes one decode step must read: lens[b] cached rows plus the appended
-    one, for K and V, per sequence."""
-    return sum(int(n) + 1 for n in lens) * kv_bytes_per_token(1, Hkv, dh, bytes_per_value)
+def attended_keys(lens: Iterable[int], window: int = 0) -> int:
+    """Keys one decode step attends over all sequences: lens[b] cached rows plus
+    the appended one, at most W of them with a sliding window W > 0 (the pages:
+    the KV cache a sliding window needs is capped at W)."""
+    return sum(min(int(n) + 1, window) if window > 0 else int(n) + 1 for n in lens)
+
+
+def decode_kv_bytes(lens: Iterable[int], Hkv: int, dh: int, bytes_per_value: int, window: int = 0) -> int:
+    """KV bytes one decode step must read: the attended rows of K and V."""
+    return attended_keys(lens, window) * kv_bytes_per_token(1, Hkv, dh, bytes_per_value)
 
 
 def weight_bytes(d: int, H: int, Hkv: int, dh: int, f: int, bytes_per_value: int) -> int:

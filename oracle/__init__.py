@@ -8,10 +8,11 @@ Every function is pinned by ``tests/test_oracle_pins.py`` against what the
 pages and the mathematics fix (closed forms, invariants, a library
 cross-check, brute force on tiny inputs); none is "parity unpinned".
 """
-from .block import (Cfg, rms_norm, rope_angles, rope, silu, softmax_rows, causal_attention,
+from .block import (Cfg, rms_norm, rope_angles, rope, silu, softmax_rows, visible_keys,
+                    causal_attention,
                     qkv_heads, mlp_branch, block_prefill_seq, block_prefill, block_decode_seq,
                     block_decode)
 
-__all__ = ["Cfg", "rms_norm", "rope_angles", "rope", "silu", "softmax_rows", "causal_attention",
+__all__ = ["Cfg", "rms_norm", "rope_angles", "rope", "silu", "softmax_rows", "visible_keys", "causal_attention",
            "qkv_heads", "mlp_branch", "block_prefill_seq", "block_prefill", "block_decode_seq",
            "block_decode"]

@@ -47,10 +47,13 @@ class Cfg:
     f: int
     rope_base: float
     eps: float
+    window: int = 0            # sliding-window width W; 0 is full causal attention
 
     def __post_init__(self):
         if self.H % self.Hkv:
             raise ValueError("H must be a multiple of Hkv")
+        if self.window < 0:
+            raise ValueError("window must be non-negative")
         if self.dh % 2:
             raise ValueError("RoPE rotates pairs: dh must be even")
 
@@ -112,21 +115,37 @@ def softmax_rows(s: np.ndarray) -> np.ndarray:
     return e / np.sum(e, axis=-1, keepdims=True)
 
 
+def visible_keys(q_pos: Sequence[int], S: int, window: int = 0) -> np.ndarray:
+    """Mask [Tq, S]: key position j is visible to the query at position i.
+
+    Causal: j ≤ i ("Transformers" 5.1).  With a sliding window W > 0 the
+    query also drops every key older than its W most recent positions, its own
+    included: j > i - W ("09 The Transformer" §5, sliding-window attention:
+    with W = 4096, token 10000 attends to tokens 5905..10000).
+    """
+    j = np.arange(S)[None, :]
+    i = np.asarray(q_pos)[:, None]
+    mask = j <= i
+    if window > 0:
+        mask = mask & (j > i - window)
+    return mask
+
+
 def causal_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
-                     q_pos: Sequence[int]) -> np.ndarray:
+                     q_pos: Sequence[int], window: int = 0) -> np.ndarray:
     """Causal GQA scaled dot-product attention.
 
     q [Tq, H, dh] at positions q_pos; k, v [S, Hkv, dh] at positions 0..S-1.
-    Query head h reads KV head h // (H/Hkv).  Query i sees keys j ≤ q_pos[i]
-    ("Transformers" 5.1: scores for j > i are -inf before the softmax).
+    Query head h reads KV head h // (H/Hkv).  Query i sees the keys
+    ``visible_keys`` allows (j ≤ q_pos[i], and within the window when
+    window > 0); the others score -inf before the softmax.
     Returns o [Tq, H, dh].
     """
     q, k, v = (np.asarray(a, F64) for a in (q, k, v))
     Tq, H, dh = q.shape
     S, Hkv, _ = k.shape
     G = H // Hkv
-    q_pos = np.asarray(q_pos)
-    visible = np.arange(S)[None, :] <= q_pos[:, None]          # [Tq, S]
+    visible = visible_keys(q_pos, S, window)                     # [Tq, S]
     o = np.empty((Tq, H, dh), F64)
     for h in range(H):
         kv = h // G
@@ -166,7 +185,8 @@ def block_prefill_seq(x: np.ndarray, w, cfg: Cfg, rows: Optional[Sequence[int]] 
 
     Returns dict(y [R, d], k [Hkv, S, dh], v [Hkv, S, dh]) where R are the
     requested rows (all T by default) and S = 1 + max(rows): causality means a
-    row needs only the keys at or before it, so any subset of rows is exact.
+    row needs only the keys at or before it, so any subset of rows is exact
+    (a sliding window only removes keys).
     """
     w = _f64_weights(w)
     x = np.asarray(x, F64)
@@ -175,7 +195,7 @@ def block_prefill_seq(x: np.ndarray, w, cfg: Cfg, rows: Optional[Sequence[int]] 
     S = int(rows.max()) + 1
     xn = rms_norm(x[:S], w["g_attn"], cfg.eps)
     q, k, v = qkv_heads(xn, w, cfg, range(S))
-    o = causal_attention(q[rows], k, v, rows).reshape(len(rows), cfg.H * cfg.dh)
+    o = causal_attention(q[rows], k, v, rows, cfg.window).reshape(len(rows), cfg.H * cfg.dh)
     h = x[rows] + o @ w["wo"]
     y = mlp_branch(h, w, cfg)
     return {"y": y, "rows": rows, "k": k.transpose(1, 0, 2), "v": v.transpose(1, 0, 2)}
@@ -193,8 +213,9 @@ def block_decode_seq(x: np.ndarray, w, cfg: Cfg, k_cache: np.ndarray, v_cache: n
 
     x [d] is the new token at position ``pos``; k_cache, v_cache [Hkv, >=pos, dh]
     hold the post-RoPE keys and values of positions 0..pos-1.  The new token's
-    k, v are rotated at ``pos`` and appended, and its query attends over all
-    pos+1 keys (Transformer block page, KV-cache paragraph).  Returns
+    k, v are rotated at ``pos`` and appended, and its query attends over the
+    pos+1 keys (Transformer block page, KV-cache paragraph), the last
+    cfg.window of them when a sliding window is set.  Returns
     dict(y [d], k [Hkv, dh], v [Hkv, dh]) with k, v the appended rows.
     """
     w = _f64_weights(w)
@@ -203,7 +224,7 @@ def block_decode_seq(x: np.ndarray, w, cfg: Cfg, k_cache: np.ndarray, v_cache: n
     q, k_new, v_new = qkv_heads(xn, w, cfg, [pos])
     k_all = np.concatenate([np.asarray(k_cache, F64)[:, :pos].transpose(1, 0, 2), k_new], axis=0)
     v_all = np.concatenate([np.asarray(v_cache, F64)[:, :pos].transpose(1, 0, 2), v_new], axis=0)
-    o = causal_attention(q, k_all, v_all, [pos]).reshape(1, cfg.H * cfg.dh)
+    o = causal_attention(q, k_all, v_all, [pos], cfg.window).reshape(1, cfg.H * cfg.dh)
     h = x + o @ w["wo"]
     y = mlp_branch(h, w, cfg)
     return {"y": y[0], "k": k_new[0], "v": v_new[0]}

@@ -90,3 +90,17 @@ def test_decode_kv_bytes():
     # GQA decode reads lens+1 rows of K and V per KV head
     assert acc.decode_kv_bytes([3, 0], Hkv=8, dh=128, bytes_per_value=2) == (4 + 1) * 2 * 8 * 128 * 2
     assert acc.kv_bytes_per_token(1, 8, 128, 2) == 4096
+
+
+def test_window_pairs_and_keys():
+    # the pages' example: with W = 4096 token 10000 meets 4096 keys, without a window 10001
+    assert acc.attended_keys([10000], 4096) == 4096 and acc.attended_keys([10000]) == 10001
+    # brute force over queries, for windows inside and beyond the sequence
+    for T in (1, 5, 37):
+        for W in (0, 1, 2, 7, 37, 50):
+            want = sum(min(i + 1, W) if W > 0 else i + 1 for i in range(T))
+            assert acc.visible_pairs(T, W) == want
+    # the KV read of a windowed decode is capped at W rows per sequence
+    lens = [3, 0, 9000, 4095]
+    assert acc.decode_kv_bytes(lens, 8, 128, 2, window=4096) == (4 + 1 + 4096 + 4096) * 4096
+    assert acc.decode_kv_bytes(lens, 8, 128, 2, window=100000) == acc.decode_kv_bytes(lens, 8, 128, 2)

@@ -182,6 +182,82 @@ def check_attention_brute_force():
 
 
 # ----------------------------------------------------------------------------
+# Sliding window: "09 The Transformer" §5, sliding-window attention.
+# ----------------------------------------------------------------------------
+
+def _golden_rows(name):
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    rows = []
+    with open(path) as fh:
+        for line in fh:
+            if line.strip() and not line.startswith("#"):
+                rows.append([int(x) for x in line.split()])
+    return rows
+
+
+def check_window_worked_example():
+    # the pages' example: with W = 4096 token 10000 sees exactly tokens 5905..10000
+    for W, i, first, last in _golden_rows("window_example.tsv"):
+        idx = np.nonzero(ob.visible_keys([i], i + 1, W)[0])[0]
+        assert idx[0] == first and idx[-1] == last and len(idx) == last - first + 1, (W, i, idx[[0, -1]])
+
+
+def check_window_reductions():
+    T, H, Hkv, dh = 12, 4, 2, 6
+    G = H // Hkv
+    q = RNG.standard_normal((T, H, dh)); k = RNG.standard_normal((T, Hkv, dh))
+    v = RNG.standard_normal((T, Hkv, dh))
+    full = ob.causal_attention(q, k, v, np.arange(T))
+    # a window at least as long as the sequence is full causal attention
+    for W in (T, T + 3):
+        np.testing.assert_array_equal(ob.causal_attention(q, k, v, np.arange(T), W), full)
+    # W = 1: every query sees only itself
+    o1 = ob.causal_attention(q, k, v, np.arange(T), 1)
+    for h in range(H):
+        np.testing.assert_allclose(o1[:, h], v[:, h // G], rtol=1e-15)
+    # zero queries: o_i is the mean of v over the last min(i + 1, W) positions
+    W = 4
+    o = ob.causal_attention(np.zeros((T, H, dh)), k, v, np.arange(T), W)
+    for i in range(T):
+        lo = max(0, i - W + 1)
+        for h in range(H):
+            np.testing.assert_allclose(o[i, h], v[lo:i + 1, h // G].mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def check_window_brute_force():
+    # scalar loops: key j visible to query i iff i - W < j <= i
+    T, H, Hkv, dh, W = 7, 2, 1, 3, 3
+    q = RNG.standard_normal((T, H, dh)); k = RNG.standard_normal((T, Hkv, dh))
+    v = RNG.standard_normal((T, Hkv, dh))
+    got = ob.causal_attention(q, k, v, list(range(T)), W)
+    for i in range(T):
+        js = range(max(0, i - W + 1), i + 1)
+        for h in range(H):
+            g = h // (H // Hkv)
+            w = [math.exp(sum(q[i, h, e] * k[j, g, e] for e in range(dh)) / math.sqrt(dh)) for j in js]
+            for e in range(dh):
+                want = sum(wj * v[j, g, e] for wj, j in zip(w, js)) / sum(w)
+                assert abs(got[i, h, e] - want) < 1e-12
+
+
+def check_window_decode_matches_prefill():
+    # decoding token T-1 over the windowed cache equals row T-1 of the windowed prefill
+    base = _cfg()
+    for W in (1, 3, 8):
+        cfg = ob.Cfg(base.d, base.H, base.Hkv, base.dh, base.f, base.rope_base, base.eps, W)
+        w = _weights(cfg, RNG)
+        T = 11
+        x = RNG.standard_normal((T, cfg.d))
+        pre = ob.block_prefill_seq(x, w, cfg)
+        dec = ob.block_decode_seq(x[T - 1], w, cfg, pre["k"], pre["v"], T - 1)
+        np.testing.assert_allclose(dec["y"], pre["y"][T - 1], rtol=1e-12, atol=1e-12)
+        # and differs from full attention's row
+        full = ob.block_prefill_seq(x, w, _cfg())
+        assert np.max(np.abs(pre["y"][T - 1] - full["y"][T - 1])) > 1e-6
+
+
+# ----------------------------------------------------------------------------
 # Block-level: residual wiring, GQA sharing, causality, decode vs prefill.
 # ----------------------------------------------------------------------------
 
@@ -268,7 +344,9 @@ def check_swiglu_closed_form():
 CHECKS = [check_rope_closed_form, check_swiglu_closed_form, check_rope_invariants, check_rmsnorm, check_silu, check_softmax,
           check_attention_vs_library, check_attention_closed_forms, check_attention_brute_force,
           check_block_zero_branches, check_block_uniform_attention_closed_form,
-          check_gqa_equals_duplicated_mha, check_causality_prefix, check_decode_matches_prefill]
+          check_gqa_equals_duplicated_mha, check_causality_prefix, check_decode_matches_prefill,
+          check_window_worked_example, check_window_reductions, check_window_brute_force,
+          check_window_decode_matches_prefill]
 
 
 def _run(check):
@@ -305,10 +383,12 @@ def _orig(name):
 
 def mut_diagonal(monkeypatch):
     # mask built with j < i
-    def attn(q, k, v, q_pos):
+    def attn(q, k, v, q_pos, window=0):
         q, k, v = (np.asarray(a, float) for a in (q, k, v))
         G = q.shape[1] // k.shape[1]
         vis = np.arange(k.shape[0])[None, :] < np.asarray(q_pos)[:, None]
+        if window > 0:
+            vis = vis & (np.arange(k.shape[0])[None, :] > np.asarray(q_pos)[:, None] - window)
         o = np.empty_like(q)
         for h in range(q.shape[1]):
             s = np.where(vis, q[:, h] @ k[:, h // G].T / math.sqrt(q.shape[2]), -np.inf)
@@ -375,10 +455,10 @@ def mut_eps_outside(monkeypatch):
 
 
 def mut_gqa_modulo(monkeypatch):
-    def attn(q, k, v, q_pos):
+    def attn(q, k, v, q_pos, window=0):
         q, k, v = (np.asarray(a, float) for a in (q, k, v))
         Hkv = k.shape[1]
-        vis = np.arange(k.shape[0])[None, :] <= np.asarray(q_pos)[:, None]
+        vis = ob.visible_keys(q_pos, k.shape[0], window)
         o = np.empty_like(q)
         for h in range(q.shape[1]):
             s = np.where(vis, q[:, h] @ k[:, h % Hkv].T / math.sqrt(q.shape[2]), -np.inf)
@@ -389,8 +469,8 @@ def mut_gqa_modulo(monkeypatch):
 
 def mut_scale_dh(monkeypatch):
     orig = _orig("causal_attention")
-    def attn(q, k, v, q_pos):
-        return orig(np.asarray(q) / math.sqrt(np.asarray(q).shape[-1]), k, v, q_pos)
+    def attn(q, k, v, q_pos, window=0):
+        return orig(np.asarray(q) / math.sqrt(np.asarray(q).shape[-1]), k, v, q_pos, window)
     monkeypatch.setattr(ob, "causal_attention", attn)
 
 
@@ -412,7 +492,25 @@ def mut_gate_up_swapped(monkeypatch):
     monkeypatch.setattr(ob, "mlp_branch", mlp)
 
 
-MUTANTS = [mut_diagonal, mut_rope_on_v, mut_cache_pre_rope, mut_no_max, mut_rope_halves,
+def mut_window_one_more(monkeypatch):
+    # window keeps j >= i - W (W + 1 keys)
+    def vis(q_pos, S, window=0):
+        j = np.arange(S)[None, :]; i = np.asarray(q_pos)[:, None]
+        m = j <= i
+        return m & (j >= i - window) if window > 0 else m
+    monkeypatch.setattr(ob, "visible_keys", vis)
+
+
+def mut_window_decode_ignored(monkeypatch):
+    # decode attends over the whole cache whatever the window
+    orig = _orig("block_decode_seq")
+    def dec(x, w, cfg, k_cache, v_cache, pos):
+        full = ob.Cfg(cfg.d, cfg.H, cfg.Hkv, cfg.dh, cfg.f, cfg.rope_base, cfg.eps, 0)
+        return orig(x, w, full, k_cache, v_cache, pos)
+    monkeypatch.setattr(ob, "block_decode_seq", dec)
+
+
+MUTANTS = [mut_window_one_more, mut_window_decode_ignored, mut_diagonal, mut_rope_on_v, mut_cache_pre_rope, mut_no_max, mut_rope_halves,
            mut_rope_freq, mut_rope_sign, mut_eps_outside, mut_gqa_modulo, mut_scale_dh,
            mut_no_residual, mut_silu_sign, mut_gate_up_swapped]
 
