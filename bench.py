@@ -410,6 +410,79 @@ def bench_decode(args, world, peaks):
     }
 
 
+def bench_window(args, world, peaks):
+    """The sliding-window path at W = args.window: one prefill of the benchmark
+    workload and one decode step of the decode workload, each timed over
+    args.steps live steps, with the windowed pair and byte counts."""
+    import torch
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
+    from causal_gqa_attention_rmsnorm_gb300 import binding
+    import workloads
+
+    W = args.window
+    n = max(args.steps, 5)
+
+    def timed(step):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        assert tb.tb_get_device_error(clear=True) == 0
+        binding.tbx_trace_enable(n)
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            step()
+        b.record()
+        torch.cuda.synchronize()
+        stages = stage_stats([binding.tbx_trace_read(i) for i in range(n)])
+        binding.tbx_trace_enable(0)
+        assert tb.tb_get_device_error(clear=True) == 0
+        return max_over_ranks(a.elapsed_time(b), world) / n, stages
+
+    s = workloads.CONFIGS[args.workload]
+    if args.batch:
+        s = s.with_(B=args.batch)
+    s = s.with_(window=W)
+    inp = workloads.make_block_inputs(s, seed=0)
+    dev = {k: t.cuda() for k, t in inp.items()}
+    cfg = tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, s.T, s.rope_base, s.eps, tb.TB_BF16, W)
+    packed = tb.tb_pack_weights(cfg, dev)
+    y = torch.empty((s.B, s.T, s.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tb.tb_workspace_bytes(cfg, s.B, s.T, 0), dtype=torch.uint8, device="cuda")
+    ms, st = timed(lambda: tb.tb_block_prefill(cfg, packed, dev["x"], y=y, ws=ws))
+    assert torch.isfinite(y).all().item()
+    fl = acc.causal_attn_flops(s.B, s.H, s.dh, s.T, W)
+    pre = {"workload": s.name, "ms_per_step": ms, "tok_s": world * s.B * s.T / (ms * 1e-3),
+           "attn_ms": st["attn"], "attn_flops": fl, "attn_tflops": fl / (st["attn"] * 1e-3) / 1e12,
+           "attn_frac_bf16": fl / (st["attn"] * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+    del dev, packed, y, ws
+
+    s = workloads.CONFIGS[args.decode_workload].with_(window=W)
+    inp = workloads.make_block_inputs(s, seed=0)
+    dev = {k: t.cuda() for k, t in inp.items()}
+    lens = workloads.make_lens(s, seed=0)
+    kc, vc = workloads.make_decode_cache(s, 0, lens, fill=0.0, device="cuda")
+    lens0 = lens.cuda()
+    kv = tb.KVCache(kc, vc, lens0.clone())
+    cfg = tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, s.T, s.rope_base, s.eps, tb.TB_BF16, W)
+    packed = tb.tb_pack_weights(cfg, dev)
+    y = torch.empty((s.B, 1, s.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tb.tb_workspace_bytes(cfg, s.B, s.T, 1), dtype=torch.uint8, device="cuda")
+
+    def dstep():
+        kv.lens.copy_(lens0, non_blocking=True)
+        tb.tb_block_decode(cfg, packed, dev["x"], kv, y=y, ws=ws)
+    ms, st = timed(dstep)
+    assert torch.isfinite(y).all().item()
+    kv_bytes = acc.decode_kv_bytes(lens.tolist(), s.Hkv, s.dh, 2, W)
+    dec = {"workload": s.name, "step_ms": ms, "tok_s": world * s.B / (ms * 1e-3), "attn_ms": st["attn"],
+           "kv_bytes": kv_bytes, "kv_gbs": kv_bytes / (st["attn"] * 1e-3) / 1e9,
+           "kv_frac_hbm": kv_bytes / (st["attn"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    return {"window": W, "prefill": pre, "decode": dec, "gpu_launches": (6 + decode_launches(s.B)) * n}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -424,6 +497,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the decode step")
+    ap.add_argument("--window", type=int, default=4096, help="sliding-window width of the extra window line (0: skip)")
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
     ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample size for cpu_baseline")
     args = ap.parse_args()
@@ -453,6 +527,7 @@ def main():
         return
     pre = bench_prefill(args, s, world, peaks)
     dec = None if args.no_decode else bench_decode(args, world, peaks)
+    win = None if (args.window <= 0 or args.no_decode) else bench_window(args, world, peaks)
 
     from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
     tokens = s.B * s.T
@@ -480,6 +555,7 @@ def main():
         "clocks": pre["clocks"],
         "e2e": pre["e2e"],
         "decode": dec,
+        "sliding_window": win,
         "peaks": {"source": peak_src, "bf16_tflops": peaks["bf16_tflops"],
                   "bf16_tflops_sustained": peaks["bf16_tflops_sustained"], "hbm_gbs": peaks["hbm_gbs"]},
     }

@@ -30,7 +30,8 @@ EXPORTED = ("tb_packed_weights_bytes", "tb_pack_weights", "tb_workspace_bytes", 
 
 class tb_block_cfg(ctypes.Structure):
     _fields_ = [("d", c_int32), ("H", c_int32), ("Hkv", c_int32), ("dh", c_int32), ("f", c_int32),
-                ("max_pos", c_int32), ("rope_base", c_float), ("eps", c_float), ("dtype", c_int32)]
+                ("max_pos", c_int32), ("rope_base", c_float), ("eps", c_float), ("dtype", c_int32),
+                ("window", c_int32)]
 
 
 class tb_block_weights(ctypes.Structure):
@@ -109,10 +110,11 @@ class BlockConfig:
     rope_base: float
     eps: float
     dtype: int = TB_BF16
+    window: int = 0          # sliding-window width W (0: full causal)
 
     def c(self) -> tb_block_cfg:
         return tb_block_cfg(self.d, self.H, self.Hkv, self.dh, self.f, self.max_pos, self.rope_base, self.eps,
-                            self.dtype)
+                            self.dtype, self.window)
 
     @property
     def torch_dtype(self) -> torch.dtype:

@@ -38,12 +38,18 @@ struct PartLayout {
   static constexpr int stride = DH + 4;  // m, l, pad, pad, acc[DH]  (16-byte rows)
 };
 
+// First key a decode query at position n-1 attends: 0, or n - W with a
+// sliding window W > 0 ("09 The Transformer", infra.pidoku.co.in, §5,
+// sliding-window attention: the query sees its W most recent positions).
+// Chunk c of a sequence covers keys [first + c·chunk, ...).
+__device__ __forceinline__ int window_first(int n, int window) { return window > 0 && n > window ? n - window : 0; }
+
 template <typename T, int DH, int G>
 __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restrict__ q, const T* __restrict__ kc,
                                                               const T* __restrict__ vc,
                                                               const int32_t* __restrict__ pos_arr, int Hkv,
                                                               int T_max, float* __restrict__ part, int nchunk_max,
-                                                              float scale_log2) {
+                                                              int window, float scale_log2) {
   constexpr int VEC = 16 / sizeof(T);
   constexpr int LPK = DH / VEC;   // lanes per key row
   static_assert(LPK >= 1 && LPK <= 32 && (32 % LPK) == 0, "row must split evenly over lanes");
@@ -55,7 +61,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restric
   const int pos = pos_arr[b];
   if (pos < 0) return;
   const int n = pos + 1;
-  const int j0 = c * kChunk;
+  const int j0 = window_first(n, window) + c * kChunk;
   if (j0 >= n) return;
   const int j1 = min(n, j0 + kChunk);
   const int H = Hkv * G;
@@ -204,7 +210,7 @@ constexpr int kCombineMaxChunks = 1024;
 template <typename T, int DH>
 __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict__ part,
                                                         const int32_t* __restrict__ pos_arr, int H, int nchunk_max,
-                                                        int chunk, T* __restrict__ o) {
+                                                        int chunk, int window, T* __restrict__ o) {
   // Thread (e, g) sums output column e over chunks g, g + NG, ... with eight
   // independent loads in flight, so the merge costs a few L2 round trips.
   static_assert(256 % DH == 0, "head width must divide the block");
@@ -220,7 +226,8 @@ __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict_
     for (int e = threadIdx.x; e < DH; e += blockDim.x) orow[e] = from_f<T>(0.f);
     return;
   }
-  const int nc = min((pos + 1 + chunk - 1) / chunk, kCombineMaxChunks);
+  const int nkeys = pos + 1 - window_first(pos + 1, window);
+  const int nc = min((nkeys + chunk - 1) / chunk, kCombineMaxChunks);
   constexpr int P = PartLayout<DH>::stride;
   const float* pr = part + ((size_t)b * H + h) * nchunk_max * P;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -344,7 +351,8 @@ template <int DH, int G>
 __global__ void __launch_bounds__(kMWarps * 32, 1)
     k_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const bf16* __restrict__ q, const int32_t* __restrict__ pos_arr, int B, int Hkv,
-                 float* __restrict__ part, int nchunk_max, int* __restrict__ counter, float scale_log2, int* err) {
+                 float* __restrict__ part, int nchunk_max, int* __restrict__ counter, int window, float scale_log2,
+                 int* err) {
   using C = MCfg<DH>;
   using namespace ptx;
   static_assert(G <= 8, "at most 8 query heads per KV head");
@@ -360,7 +368,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
     for (int b = 0; b < B; ++b) {
       pre[b] = acc;
       const int p = pos_arr[b];
-      acc += p < 0 ? 0 : Hkv * ((p + kMChunk) / kMChunk);
+      acc += p < 0 ? 0 : Hkv * ((p + 1 - window_first(p + 1, window) + kMChunk - 1) / kMChunk);
     }
     pre[B] = acc;
     abort_word = 0;
@@ -385,13 +393,14 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
       if (pre[mid] <= id) lo = mid; else hi = mid - 1;
     }
     const int n = pos_arr[lo] + 1;
-    const int nch = (n + kMChunk - 1) / kMChunk;
+    const int first = window_first(n, window);
+    const int nch = (n - first + kMChunk - 1) / kMChunk;
     const int r = id - pre[lo];
     Item it;
     it.b = lo;
     it.kvh = r / nch;
     it.c = r - it.kvh * nch;
-    it.key0 = it.c * kMChunk;
+    it.key0 = first + it.c * kMChunk;
     it.nkeys = min(kMChunk, n - it.key0);
     return it;
   };
@@ -564,7 +573,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
 
 template <int DH, int G>
 cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
-                       float* part, int nchunk_max, int* counter, void* o, cudaStream_t s) {
+                       float* part, int nchunk_max, int* counter, int window, void* o, cudaStream_t s) {
   using C = MCfg<DH>;
   CUtensorMap tk, tv;
   cudaError_t e = make_tmap_3d_bf16(&tk, kc, (uint64_t)B * Hkv, T_max, DH, DH, (uint64_t)T_max * DH, 64, kMKeys);
@@ -586,55 +595,55 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_mma<DH, G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, (const bf16*)q, pos, B, Hkv, part,
-                                                             nchunk_max, counter, scale_log2, device_error_word());
-  k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max,
-                                                                             kMChunk, (bf16*)o);
+                                                             nchunk_max, counter, window, scale_log2,
+                                                             device_error_word());
+  k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kMChunk, window,
+                                                               (bf16*)o);
   return cudaGetLastError();
 }
 
 template <int DH>
 cudaError_t stream_by_g(int G, const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv,
-                        int T_max, float* part, int nchunk_max, int* counter, void* o, cudaStream_t s) {
+                        int T_max, float* part, int nchunk_max, int* counter, int window, void* o, cudaStream_t s) {
   switch (G) {
-    case 1: return run_stream<DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, o, s);
-    case 2: return run_stream<DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, o, s);
-    case 4: return run_stream<DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, o, s);
-    case 8: return run_stream<DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, o, s);
+    case 1: return run_stream<DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, o, s);
+    case 2: return run_stream<DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, o, s);
+    case 4: return run_stream<DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, o, s);
+    case 8: return run_stream<DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, o, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T, int DH, int G>
 cudaError_t run(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
-                float* part, int nchunk_max, void* o, cudaStream_t s) {
+                float* part, int nchunk_max, int window, void* o, cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_split<T, DH, G><<<dim3(nchunk_max, Hkv, B), kWarps * 32, 0, s>>>(
-      (const T*)q, (const T*)kc, (const T*)vc, pos, Hkv, T_max, part, nchunk_max, scale_log2);
-  k_decode_combine<T, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max,
-                                                                          kChunk, (T*)o);
+      (const T*)q, (const T*)kc, (const T*)vc, pos, Hkv, T_max, part, nchunk_max, window, scale_log2);
+  k_decode_combine<T, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kChunk, window, (T*)o);
   return cudaGetLastError();
 }
 
 template <typename T, int DH>
 cudaError_t by_g(int G, const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv,
-                 int T_max, float* part, int nchunk_max, void* o, cudaStream_t s) {
+                 int T_max, float* part, int nchunk_max, int window, void* o, cudaStream_t s) {
   switch (G) {
-    case 1: return run<T, DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
-    case 2: return run<T, DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
-    case 4: return run<T, DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
-    case 8: return run<T, DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
+    case 1: return run<T, DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+    case 2: return run<T, DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+    case 4: return run<T, DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+    case 8: return run<T, DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T>
 cudaError_t by_dh(int dh, int G, const void* q, const void* kc, const void* vc, const int32_t* pos, int B,
-                  int Hkv, int T_max, float* part, int nchunk_max, void* o, cudaStream_t s) {
+                  int Hkv, int T_max, float* part, int nchunk_max, int window, void* o, cudaStream_t s) {
   switch (dh) {
-    case 16: return by_g<T, 16>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
-    case 32: return by_g<T, 32>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
-    case 64: return by_g<T, 64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
-    case 128: return by_g<T, 128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
+    case 16: return by_g<T, 16>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+    case 32: return by_g<T, 32>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+    case 64: return by_g<T, 64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+    case 128: return by_g<T, 128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -649,11 +658,11 @@ size_t decode_part_floats(int B, int H, int dh, int nchunk_max) {
 
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos, int B,
                         int H, int Hkv, int dh, int T_max, float* part, int nchunk_max, int* work_counter,
-                        void* o, cudaStream_t s) {
+                        int window, void* o, cudaStream_t s) {
   const int G = H / Hkv;
-  if (dtype == TB_F32) return by_dh<float>(dh, G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, o, s);
-  if (dh == 128) return stream_by_g<128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, o, s);
-  if (dh == 64) return stream_by_g<64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, o, s);
+  if (dtype == TB_F32) return by_dh<float>(dh, G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+  if (dh == 128) return stream_by_g<128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
+  if (dh == 64) return stream_by_g<64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
   return cudaErrorInvalidValue;
 }
 

@@ -54,14 +54,20 @@ template <int DH> struct AttnCfg {
   static constexpr uint32_t TMEM_O = 2 * kBN;              // S/P of slot g at g·128, O of slot g at 256 + g·DH
 };
 
-// One work item: two query tiles of one sequence that share a KV head.
+// One work item: two query tiles of one sequence that share a KV head.  Slot
+// g attends key tiles lo_g..hi_g (hi_g = its query block, -1: slot empty);
+// the item streams key tiles j0 .. j0 + nkv - 1, their union.
 struct Item {
-  int b, h0, h1, qb0, qb1, nkv0, nkv1, nkv, kvh;
+  int b, h0, h1, qb0, qb1, kvh;
+  int lo0, lo1, hi0, hi1;
+  int j0, nkv;
 };
 
 // Items are numbered heaviest first: all items of the last query block (or
-// block pair) come first, then the next one down.
-__device__ __forceinline__ Item decode_item(int w, int B, int H, int Hkv, int nq, int head_pairs) {
+// block pair) come first, then the next one down.  With a sliding window W the
+// first key tile of query block qb holds key qb·128 - W + 1, the oldest key
+// its first row sees.
+__device__ __forceinline__ Item decode_item(int w, int B, int H, int Hkv, int nq, int head_pairs, int window) {
   Item it;
   if (head_pairs) {
     const int P = H / 2, per = B * P;
@@ -79,9 +85,13 @@ __device__ __forceinline__ Item decode_item(int w, int B, int H, int Hkv, int nq
     it.qb1 = it.qb0 + 1;
   }
   it.kvh = it.h0 / (H / Hkv);
-  it.nkv0 = it.qb0 + 1;                          // key tiles 0..qb hold every visible key
-  it.nkv1 = it.qb1 < nq ? it.qb1 + 1 : 0;        // 0: slot 1 empty
-  it.nkv = it.nkv0 > it.nkv1 ? it.nkv0 : it.nkv1;
+  auto first_tile = [&](int qb) { return window > 0 && qb * kBM >= window ? (qb * kBM - window + 1) / kBN : 0; };
+  it.hi0 = it.qb0;                                 // key tiles past a query block hold no visible key
+  it.hi1 = it.qb1 < nq ? it.qb1 : -1;              // -1: slot 1 empty
+  it.lo0 = first_tile(it.qb0);
+  it.lo1 = first_tile(it.qb1);
+  it.j0 = it.lo0;                                  // qb0 <= qb1, so lo0 <= lo1
+  it.nkv = (it.hi1 > it.hi0 ? it.hi1 : it.hi0) - it.j0 + 1;
   return it;
 }
 
@@ -96,7 +106,7 @@ template <int DH>
 __global__ void __launch_bounds__(320, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ out, int B, int T, int H, int Hkv,
-              int n_qtiles, int head_pairs, int n_items, float scale_log2, int* err) {
+              int n_qtiles, int head_pairs, int n_items, int window, float scale_log2, int* err) {
   using C = AttnCfg<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -158,10 +168,10 @@ __global__ void __launch_bounds__(320, 1)
       for (int k = 0; ok; ++k) {
         const int w = item_of(k);
         if (w >= n_items) break;
-        const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs);
+        const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs, window);
         // the previous item's last S must be done with the Q tiles
         if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, abort_flag, err)) break;
-        const int nq_slots = it.nkv1 > 0 ? 2 : 1;
+        const int nq_slots = it.hi1 >= 0 ? 2 : 1;
         mbar_arrive_expect_tx(q_full, nq_slots * C::Q_BYTES);
         for (int g = 0; g < nq_slots; ++g)
 #pragma unroll
@@ -179,8 +189,8 @@ __global__ void __launch_bounds__(320, 1)
           mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
 #pragma unroll
           for (int blk = 0; blk < C::NB; ++blk)
-            tma_load_3d(&tmK, smem + C::OFF_K + st * C::KV_BYTES + blk * kBN * 128, &k_full[st], blk * 64, j * kBN,
-                        it.b * Hkv + it.kvh);
+            tma_load_3d(&tmK, smem + C::OFF_K + st * C::KV_BYTES + blk * kBN * 128, &k_full[st], blk * 64,
+                        (it.j0 + j) * kBN, it.b * Hkv + it.kvh);
           ++nk_issued;
           if (!mbar_wait(&v_empty[st], ph ^ 1u, abort_flag, err)) {
             ok = false;
@@ -189,8 +199,8 @@ __global__ void __launch_bounds__(320, 1)
           mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
 #pragma unroll
           for (int blk = 0; blk < C::NB; ++blk)
-            tma_load_3d(&tmV, smem + C::OFF_V + st * C::KV_BYTES + blk * kBN * 128, &v_full[st], blk * 64, j * kBN,
-                        it.b * Hkv + it.kvh);
+            tma_load_3d(&tmV, smem + C::OFF_V + st * C::KV_BYTES + blk * kBN * 128, &v_full[st], blk * 64,
+                        (it.j0 + j) * kBN, it.b * Hkv + it.kvh);
           ++nv_issued;
         }
       }
@@ -236,34 +246,37 @@ __global__ void __launch_bounds__(320, 1)
       for (int k = 0; ok; ++k) {
         const int w = item_of(k);
         if (w >= n_items) break;
-        const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs);
+        const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs, window);
         if (!mbar_wait(q_full, k & 1, abort_flag, err) ||
             !mbar_wait(&k_full[kt & 1], (kt >> 1) & 1, abort_flag, err)) {
           ok = false;
           break;
         }
+        // slot g works on key tile j iff lo_g <= j <= hi_g
+        auto on0 = [&](int j) { return j >= it.lo0 && j <= it.hi0; };
+        auto on1 = [&](int j) { return j >= it.lo1 && j <= it.hi1; };
         tc_fence_after();
-        issue_s(0, kt);
-        if (it.nkv1 > 0) issue_s(1, kt);
+        if (on0(it.j0)) issue_s(0, kt);
+        if (on1(it.j0)) issue_s(1, kt);
         mma_commit(&k_empty[kt & 1]);
         if (it.nkv == 1) mma_commit(q_empty);
-        for (int j = 0; j < it.nkv; ++j) {
-          const int t = kt + j;
-          const bool next = j + 1 < it.nkv;
+        for (int jj = 0; jj < it.nkv; ++jj) {
+          const int t = kt + jj, j = it.j0 + jj;
+          const bool next = jj + 1 < it.nkv;
           if (!mbar_wait(&v_full[t & 1], (t >> 1) & 1, abort_flag, err)) {
             ok = false;
             break;
           }
           // slot 0: P·V of tile j, then S of tile j+1
-          if (j < it.nkv0) {
+          if (on0(j)) {
             if (!mbar_wait(&p_full[0], c0 & 1, abort_flag, err)) {
               ok = false;
               break;
             }
             ++c0;
             tc_fence_after();
-            issue_pv(0, t, j > 0);
-            if (j + 1 == it.nkv0) mma_commit(&o_full[0]);
+            issue_pv(0, t, j > it.lo0);
+            if (j == it.hi0) mma_commit(&o_full[0]);
           }
           if (next) {
             if (!mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, err)) {
@@ -271,23 +284,23 @@ __global__ void __launch_bounds__(320, 1)
               break;
             }
             tc_fence_after();
-            if (j + 1 < it.nkv0) issue_s(0, t + 1);
+            if (on0(j + 1)) issue_s(0, t + 1);
           }
           // slot 1: P·V of tile j, then S of tile j+1
-          if (j < it.nkv1) {
+          if (on1(j)) {
             if (!mbar_wait(&p_full[1], c1 & 1, abort_flag, err)) {
               ok = false;
               break;
             }
             ++c1;
             tc_fence_after();
-            issue_pv(1, t, j > 0);
-            if (j + 1 == it.nkv1) mma_commit(&o_full[1]);
+            issue_pv(1, t, j > it.lo1);
+            if (j == it.hi1) mma_commit(&o_full[1]);
           }
           if (next) {
-            if (j + 1 < it.nkv1) issue_s(1, t + 1);
+            if (on1(j + 1)) issue_s(1, t + 1);
             mma_commit(&k_empty[(t + 1) & 1]);
-            if (j + 2 == it.nkv) mma_commit(q_empty);     // the item's last S is issued
+            if (jj + 2 == it.nkv) mma_commit(q_empty);     // the item's last S is issued
           }
           mma_commit(&v_empty[t & 1]);
         }
@@ -310,13 +323,13 @@ __global__ void __launch_bounds__(320, 1)
     for (int k = 0; ok; ++k) {
       const int w = item_of(k);
       if (w >= n_items) break;
-      const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs);
-      const int nk = g ? it.nkv1 : it.nkv0;
-      if (nk == 0) continue;
+      const Item it = decode_item(w, B, H, Hkv, n_qtiles, head_pairs, window);
+      const int lo = g ? it.lo1 : it.lo0, hi = g ? it.hi1 : it.hi0;
+      if (hi < 0) continue;
       const int qb = g ? it.qb1 : it.qb0;
       const int qi = qb * kBM + r;
       float m_used = -INFINITY, l = 0.f;
-      for (int j = 0; j < nk; ++j, ++c) {
+      for (int j = lo; j <= hi; ++j, ++c) {
         if (!mbar_wait_warp(&s_full[g], c & 1, abort_flag, err)) {
           ok = false;
           break;
@@ -332,12 +345,21 @@ __global__ void __launch_bounds__(320, 1)
         }
         tmem_wait_ld();
         // raw row maximum, four chains of three-input maxima; only the
-        // diagonal tile masks future keys
+        // diagonal tile masks future keys, and with a window only the tiles
+        // that reach back past a row's oldest visible key mask older ones.  A
+        // row whose first tile holds none of its keys gets m = -inf there and
+        // weights 0; its next tile rescales O and l by 2^-inf = 0.
         if (j == qb) {
           const int lim = qi - j * kBN;          // column cc is a future key iff cc > lim
 #pragma unroll
           for (int cc = 0; cc < kBN; ++cc)
             if (cc > lim) s[cc] = -INFINITY;
+        }
+        if (window > 0 && (qb - j + 1) * kBN > window) {
+          const int wlim = qi - window + 1 - j * kBN;   // column cc is too old iff cc < wlim
+#pragma unroll
+          for (int cc = 0; cc < kBN; ++cc)
+            if (cc < wlim) s[cc] = -INFINITY;
         }
         float m4[4];
 #pragma unroll
@@ -350,7 +372,7 @@ __global__ void __launch_bounds__(320, 1)
         const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         const float m_new = fmaxf(m_used, mx * scale_log2);
         bool need = false;
-        if (j == 0) {
+        if (j == lo) {
           m_used = m_new;
         } else {
           need = m_new > m_used + kRescaleLog2;
@@ -444,7 +466,7 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int DH>
 cudaError_t run(const void* q, const void* k, const void* v, void* o, int B, int T, int H, int Hkv, int kv_stride,
-                cudaStream_t s) {
+                int window, cudaStream_t s) {
   using C = AttnCfg<DH>;
   CUtensorMap tq, tk, tv;
   cudaError_t e = make_tmap_3d_bf16(&tq, q, (uint64_t)B * H, T, DH, DH, (uint64_t)T * DH, 64, kBM);
@@ -468,18 +490,18 @@ cudaError_t run(const void* q, const void* k, const void* v, void* o, int B, int
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
   const int n_items = (int)items;
   const int grid = n_items < sm_count() ? n_items : sm_count();
-  k_attn_tc<DH><<<grid, 320, C::SMEM, s>>>(tq, tk, tv, (bf16*)o, B, T, H, Hkv, nq, head_pairs, n_items, scale_log2,
-                                           device_error_word());
+  k_attn_tc<DH><<<grid, 320, C::SMEM, s>>>(tq, tk, tv, (bf16*)o, B, T, H, Hkv, nq, head_pairs, n_items, window,
+                                           scale_log2, device_error_word());
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int T, int H, int Hkv,
-                            int dh, int kv_stride, cudaStream_t s) {
+                            int dh, int kv_stride, int window, cudaStream_t s) {
   if (B <= 0 || T <= 0) return cudaSuccess;
-  if (dh == 128) return run<128>(q, k, v, o, B, T, H, Hkv, kv_stride, s);
-  if (dh == 64) return run<64>(q, k, v, o, B, T, H, Hkv, kv_stride, s);
+  if (dh == 128) return run<128>(q, k, v, o, B, T, H, Hkv, kv_stride, window, s);
+  if (dh == 64) return run<64>(q, k, v, o, B, T, H, Hkv, kv_stride, window, s);
   return cudaErrorInvalidValue;
 }
 

@@ -131,17 +131,18 @@ cudaError_t gemm_skinny_w2(const void* A, const void* B, int M, int N, int K, co
 
 // attn_simt.cu (fp32 path)
 cudaError_t attn_prefill_simt(int dtype, const void* q, const void* k, const void* v, void* o, int B,
-                              int T, int H, int Hkv, int dh, int kv_stride, cudaStream_t s);
+                              int T, int H, int Hkv, int dh, int kv_stride, int window, cudaStream_t s);
 
+// Attention launchers take the sliding-window width (0: full causal).
 // attn_tc.cu (bf16 path, dh 64 or 128)
 cudaError_t attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int T, int H, int Hkv,
-                            int dh, int kv_stride, cudaStream_t s);
+                            int dh, int kv_stride, int window, cudaStream_t s);
 
 // attn_decode.cu
 int decode_chunk_keys();
 size_t decode_part_floats(int B, int H, int dh, int nchunk_max);
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos,
                         int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max,
-                        int* work_counter, void* o, cudaStream_t s);
+                        int* work_counter, int window, void* o, cudaStream_t s);
 
 }  // namespace tb

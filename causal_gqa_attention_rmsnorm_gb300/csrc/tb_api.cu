@@ -70,6 +70,7 @@ tb_status check_cfg(const tb_block_cfg* c) {
   if (!(c->rope_base > 0.f)) return fail(TB_ERR_INVALID_ARG, "rope_base must be positive");
   if (!(c->eps >= 0.f)) return fail(TB_ERR_INVALID_ARG, "eps must be non-negative");
   if (c->dtype != TB_F32 && c->dtype != TB_BF16) return fail(TB_ERR_INVALID_ARG, "unknown dtype %d", c->dtype);
+  if (c->window < 0) return fail(TB_ERR_INVALID_ARG, "window (%d) must be non-negative", c->window);
   if (c->dh != 16 && c->dh != 32 && c->dh != 64 && c->dh != 128)
     return fail(TB_ERR_UNSUPPORTED, "dh %d: attention kernels exist for 16, 32, 64 and 128", c->dh);
   const int G = c->H / c->Hkv;
@@ -330,7 +331,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
     rec.stage("qkv");
     TB_TRY(gemm_simt_qkv(dt, x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
-    TB_TRY(attn_prefill_simt(dt, W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, s));
+    TB_TRY(attn_prefill_simt(dt, W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, cfg->window, s));
     rec.stage("wo");
     TB_TRY(gemm_simt_wo(dt, W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
@@ -341,7 +342,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
     rec.stage("qkv");
     TB_TRY(mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
-    TB_TRY(attn_prefill_tc(W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, s));
+    TB_TRY(attn_prefill_tc(W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, cfg->window, s));
     rec.stage("wo");
     TB_TRY(mm_wo(W, W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
@@ -397,7 +398,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(gemm_simt_qkv(dt, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                       W.nchunk_max, W.counter, W.o, s));
+                       W.nchunk_max, W.counter, cfg->window, W.o, s));
     rec.stage("wo");
     TB_TRY(gemm_simt_wo(dt, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
@@ -409,7 +410,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(mm_qkv(W, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                       W.nchunk_max, W.counter, W.o, s));
+                       W.nchunk_max, W.counter, cfg->window, W.o, s));
     rec.stage("wo");
     TB_TRY(mm_wo(W, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");

@@ -73,13 +73,22 @@ typedef enum { TB_F32 = 0, TB_BF16 = 1 } tb_dtype;
  *  dtype            : tb_dtype of x, the weights, the gains and the KV cache.
  *                     TB_BF16 computes with bf16 tensor-core operands, fp32
  *                     accumulation, fp32 softmax and norms; TB_F32 computes in
- *                     fp32 throughout. */
+ *                     fp32 throughout.
+ *  window           : sliding-window width W.  0: full causal attention (key j
+ *                     visible to query i iff j <= i).  W > 0: key j visible iff
+ *                     i - W < j <= i, the query's W most recent positions, its
+ *                     own included ("09 The Transformer" §5, sliding-window
+ *                     attention: with W = 4096 token 10000 attends to tokens
+ *                     5905..10000).  Negative values are TB_ERR_INVALID_ARG.
+ *                     The cache stays indexed by position; a decode step reads
+ *                     only its W most recent rows. */
 typedef struct {
   int32_t d, H, Hkv, dh, f;
   int32_t max_pos;
   float rope_base;
   float eps;
   int32_t dtype;
+  int32_t window;
 } tb_block_cfg;
 
 /* Unpacked weights, device pointers of cfg.dtype, [in, out] row-major:

@@ -28,7 +28,7 @@ D4096_MAX_ABS_BOUND = 1e-1
 
 
 def oracle_cfg(s: BlockShape) -> oracle.Cfg:
-    return oracle.Cfg(s.d, s.H, s.Hkv, s.dh, s.f, s.rope_base, s.eps)
+    return oracle.Cfg(s.d, s.H, s.Hkv, s.dh, s.f, s.rope_base, s.eps, s.window)
 
 
 def oracle_weights(inp):
@@ -38,7 +38,7 @@ def oracle_weights(inp):
 def block_config(s: BlockShape, max_pos: int):
     import causal_gqa_attention_rmsnorm_gb300 as tb
     return tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, max_pos, s.rope_base, s.eps,
-                          tb.TB_F32 if s.dtype == "f32" else tb.TB_BF16)
+                          tb.TB_F32 if s.dtype == "f32" else tb.TB_BF16, s.window)
 
 
 def to_device(inp, device="cuda"):

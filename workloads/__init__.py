@@ -43,6 +43,7 @@ class BlockShape:
     gains: str         # "ones" or "normal" (N(1, 0.1))
     lens_lo: int = 0   # decode only: cached lengths uniform in [lens_lo, lens_hi]
     lens_hi: int = 0
+    window: int = 0    # sliding-window width W (0: full causal attention)
 
     @property
     def torch_dtype(self) -> torch.dtype:
