@@ -11,8 +11,8 @@ cross-check, brute force on tiny inputs); none is "parity unpinned".
 from .block import (Cfg, rms_norm, rope_angles, rope, silu, softmax_rows, visible_keys,
                     causal_attention,
                     qkv_heads, mlp_branch, block_prefill_seq, block_prefill, block_decode_seq,
-                    block_decode)
+                    gather_paged, block_decode)
 
 __all__ = ["Cfg", "rms_norm", "rope_angles", "rope", "silu", "softmax_rows", "visible_keys", "causal_attention",
            "qkv_heads", "mlp_branch", "block_prefill_seq", "block_prefill", "block_decode_seq",
-           "block_decode"]
+           "gather_paged", "block_decode"]

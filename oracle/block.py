@@ -230,6 +230,25 @@ def block_decode_seq(x: np.ndarray, w, cfg: Cfg, k_cache: np.ndarray, v_cache: n
     return {"y": y[0], "k": k_new[0], "v": v_new[0]}
 
 
+def gather_paged(pool: np.ndarray, block_table: Sequence[int], page_size: int, n: int) -> np.ndarray:
+    """Rows 0..n-1 of one sequence of a paged cache, as a contiguous [Hkv, n, dh].
+
+    A paged cache allocates each sequence's cache in fixed-size blocks
+    ("Transformer block" page, implementation notes: "paged KV cache" instead
+    of one contiguous T_max buffer per request; "The Transformer
+    Architecture", pitfalls, KV-cache OOM: paged attention fragments the cache
+    into pages).  Here the pages sit in one pool [num_pages, Hkv, page_size, dh]
+    and row t of the sequence lives in page block_table[t // page_size] at
+    offset t % page_size.
+    """
+    pool = np.asarray(pool)
+    Hkv, dh = pool.shape[1], pool.shape[3]
+    out = np.empty((Hkv, n, dh), pool.dtype)
+    for t in range(n):
+        out[:, t, :] = pool[int(block_table[t // page_size]), :, t % page_size, :]
+    return out
+
+
 def block_decode(x: np.ndarray, w, cfg: Cfg, k_cache: np.ndarray, v_cache: np.ndarray,
                  lens: Sequence[int], batches: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
     """Decode step for x [B, 1, d] over caches [B, Hkv, T_max, dh] of lengths lens.

@@ -258,6 +258,24 @@ def check_window_decode_matches_prefill():
 
 
 # ----------------------------------------------------------------------------
+# Paged cache layout: "Transformer block" page, implementation notes.
+# ----------------------------------------------------------------------------
+
+def check_paged_gather():
+    # scatter a contiguous cache into a shuffled pool by direct indexing, then
+    # the gather must give it back exactly, including a partial last page
+    Hkv, dh, ps, n, num_pages = 3, 5, 4, 14, 9
+    cache = RNG.standard_normal((Hkv, n, dh))
+    table = RNG.permutation(num_pages)[: (n + ps - 1) // ps]
+    pool = np.full((num_pages, Hkv, ps, dh), np.nan)
+    for t in range(n):
+        pool[table[t // ps], :, t % ps, :] = cache[:, t, :]
+    np.testing.assert_array_equal(ob.gather_paged(pool, table, ps, n), cache)
+    # row 6 sits in the second page of the table at offset 2
+    np.testing.assert_array_equal(ob.gather_paged(pool, table, ps, n)[:, 6], pool[table[1], :, 2])
+
+
+# ----------------------------------------------------------------------------
 # Block-level: residual wiring, GQA sharing, causality, decode vs prefill.
 # ----------------------------------------------------------------------------
 
@@ -346,7 +364,7 @@ CHECKS = [check_rope_closed_form, check_swiglu_closed_form, check_rope_invariant
           check_block_zero_branches, check_block_uniform_attention_closed_form,
           check_gqa_equals_duplicated_mha, check_causality_prefix, check_decode_matches_prefill,
           check_window_worked_example, check_window_reductions, check_window_brute_force,
-          check_window_decode_matches_prefill]
+          check_window_decode_matches_prefill, check_paged_gather]
 
 
 def _run(check):
@@ -510,7 +528,18 @@ def mut_window_decode_ignored(monkeypatch):
     monkeypatch.setattr(ob, "block_decode_seq", dec)
 
 
-MUTANTS = [mut_window_one_more, mut_window_decode_ignored, mut_diagonal, mut_rope_on_v, mut_cache_pre_rope, mut_no_max, mut_rope_halves,
+def mut_paged_offset(monkeypatch):
+    # offset counted from the wrong end of the page
+    def gather(pool, block_table, page_size, n):
+        pool = np.asarray(pool)
+        out = np.empty((pool.shape[1], n, pool.shape[3]), pool.dtype)
+        for t in range(n):
+            out[:, t, :] = pool[int(block_table[t // page_size]), :, page_size - 1 - t % page_size, :]
+        return out
+    monkeypatch.setattr(ob, "gather_paged", gather)
+
+
+MUTANTS = [mut_paged_offset, mut_window_one_more, mut_window_decode_ignored, mut_diagonal, mut_rope_on_v, mut_cache_pre_rope, mut_no_max, mut_rope_halves,
            mut_rope_freq, mut_rope_sign, mut_eps_outside, mut_gqa_modulo, mut_scale_dh,
            mut_no_residual, mut_silu_sign, mut_gate_up_swapped]
 
