@@ -483,6 +483,65 @@ def bench_window(args, world, peaks):
     return {"window": W, "prefill": pre, "decode": dec, "gpu_launches": (6 + decode_launches(s.B)) * n}
 
 
+def bench_paged(args, world, peaks):
+    """A decode step of the decode workload through a paged cache: pages of
+    args.page_size rows, the pool shuffled (sequence b's pages scattered over
+    the pool by a seeded permutation), timed over args.steps eager steps."""
+    import numpy as np
+    import torch
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
+    from causal_gqa_attention_rmsnorm_gb300 import binding
+    import workloads
+
+    ps = args.page_size
+    s = workloads.CONFIGS[args.decode_workload]
+    inp = workloads.make_block_inputs(s, seed=0)
+    dev = {k: t.cuda() for k, t in inp.items()}
+    lens = workloads.make_lens(s, seed=0)
+    kc, vc = workloads.make_decode_cache(s, 0, lens, fill=0.0, device="cuda")
+    per = s.T // ps
+    num_pages = s.B * per
+    perm = torch.tensor(np.random.default_rng(0).permutation(num_pages).reshape(s.B, per), dtype=torch.int32)
+    kv = tb.KVCache.empty_paged(s.B, s.Hkv, s.T, s.dh, ps, num_pages, perm.cuda())
+    for b in range(s.B):                             # the same rows, scattered into the pool
+        kv.k[perm[b].long().cuda()] = kc[b].reshape(s.Hkv, per, ps, s.dh).transpose(0, 1)
+        kv.v[perm[b].long().cuda()] = vc[b].reshape(s.Hkv, per, ps, s.dh).transpose(0, 1)
+    del kc, vc
+    lens0 = lens.cuda()
+    cfg = tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, s.T, s.rope_base, s.eps, tb.TB_BF16)
+    packed = tb.tb_pack_weights(cfg, dev)
+    y = torch.empty((s.B, 1, s.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tb.tb_workspace_bytes(cfg, s.B, s.T, 1), dtype=torch.uint8, device="cuda")
+
+    def step():
+        kv.lens.copy_(lens0, non_blocking=True)
+        tb.tb_block_decode(cfg, packed, dev["x"], kv, y=y, ws=ws)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert tb.tb_get_device_error(clear=True) == 0
+    n = max(args.steps, 20)
+    binding.tbx_trace_enable(n)
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    stages = stage_stats([binding.tbx_trace_read(i) for i in range(n)])
+    binding.tbx_trace_enable(0)
+    assert tb.tb_get_device_error(clear=True) == 0 and torch.isfinite(y).all().item()
+    ms = max_over_ranks(a.elapsed_time(b), world) / n
+    kv_bytes = acc.decode_kv_bytes(lens.tolist(), s.Hkv, s.dh, 2)
+    return {"workload": s.name, "page_size": ps, "num_pages": num_pages, "step_ms": ms,
+            "tok_s": world * s.B / (ms * 1e-3), "attn_ms": stages["attn"], "kv_bytes": kv_bytes,
+            "kv_gbs": kv_bytes / (stages["attn"] * 1e-3) / 1e9,
+            "kv_frac_hbm": kv_bytes / (stages["attn"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "gpu_launches": decode_launches(s.B) * n}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -498,6 +557,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the decode step")
     ap.add_argument("--window", type=int, default=4096, help="sliding-window width of the extra window line (0: skip)")
+    ap.add_argument("--page-size", type=int, default=16, help="page size of the paged-cache decode line (0: skip)")
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
     ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample size for cpu_baseline")
     args = ap.parse_args()
@@ -528,6 +588,7 @@ def main():
     pre = bench_prefill(args, s, world, peaks)
     dec = None if args.no_decode else bench_decode(args, world, peaks)
     win = None if (args.window <= 0 or args.no_decode) else bench_window(args, world, peaks)
+    pag = None if (args.page_size <= 0 or args.no_decode) else bench_paged(args, world, peaks)
 
     from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
     tokens = s.B * s.T
@@ -556,6 +617,7 @@ def main():
         "e2e": pre["e2e"],
         "decode": dec,
         "sliding_window": win,
+        "paged_kv": pag,
         "peaks": {"source": peak_src, "bf16_tflops": peaks["bf16_tflops"],
                   "bf16_tflops_sustained": peaks["bf16_tflops_sustained"], "hbm_gbs": peaks["hbm_gbs"]},
     }

@@ -19,7 +19,7 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtb.so")
 
 TB_F32, TB_BF16 = 0, 1
-TB_DEVERR_CACHE_FULL, TB_DEVERR_TIMEOUT = 1, 2
+TB_DEVERR_CACHE_FULL, TB_DEVERR_TIMEOUT, TB_DEVERR_BAD_PAGE = 1, 2, 4
 STATUS = {0: "TB_OK", 1: "TB_ERR_INVALID_ARG", 2: "TB_ERR_UNSUPPORTED", 3: "TB_ERR_CUDA",
           4: "TB_ERR_CACHE_FULL", 5: "TB_ERR_TIMEOUT"}
 WEIGHT_FIELDS = ("g_attn", "wq", "wk", "wv", "wo", "g_mlp", "w1", "w3", "w2")
@@ -40,7 +40,8 @@ class tb_block_weights(ctypes.Structure):
 
 class tb_kvcache(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("lens", c_void_p), ("B", c_int32), ("Hkv", c_int32),
-                ("T_max", c_int32), ("dh", c_int32), ("dtype", c_int32)]
+                ("T_max", c_int32), ("dh", c_int32), ("dtype", c_int32), ("block_table", c_void_p),
+                ("page_size", c_int32), ("num_pages", c_int32)]
 
 
 class TbError(RuntimeError):
@@ -123,28 +124,56 @@ class BlockConfig:
 
 @dataclass
 class KVCache:
-    """Caller-owned cache tensors: k, v [B, Hkv, T_max, dh]; lens int32 [B]."""
+    """Caller-owned cache tensors.  Contiguous: k, v [B, Hkv, T_max, dh].
+    Paged (block_table given): k, v page pools [num_pages, Hkv, page_size, dh]
+    and block_table int32 [B, T_max / page_size].  lens int32 [B]."""
     k: torch.Tensor
     v: torch.Tensor
     lens: torch.Tensor
+    block_table: Optional[torch.Tensor] = None
 
     def c(self) -> tb_kvcache:
-        B, Hkv, T_max, dh = self.k.shape
         for t in (self.k, self.v):
             if not (t.is_cuda and t.is_contiguous()):
                 raise ValueError("cache tensors must be contiguous CUDA tensors")
         if self.v.shape != self.k.shape or self.v.dtype != self.k.dtype:
             raise ValueError("k and v caches must match")
+        dt = TB_F32 if self.k.dtype == torch.float32 else TB_BF16
+        if self.block_table is None:
+            B, Hkv, T_max, dh = self.k.shape
+            bt, ps, npages = None, 0, 0
+        else:
+            npages, Hkv, ps, dh = self.k.shape
+            bt = self.block_table
+            if not (bt.is_cuda and bt.dtype == torch.int32 and bt.dim() == 2 and bt.is_contiguous()):
+                raise ValueError("block_table must be a contiguous CUDA int32 tensor [B, pages per sequence]")
+            B, T_max = bt.shape[0], bt.shape[1] * ps
         if not (self.lens.is_cuda and self.lens.dtype == torch.int32 and self.lens.numel() == B):
             raise ValueError("lens must be a CUDA int32 tensor of B entries")
-        dt = TB_F32 if self.k.dtype == torch.float32 else TB_BF16
-        return tb_kvcache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(), B, Hkv, T_max, dh, dt)
+        return tb_kvcache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(), B, Hkv, T_max, dh, dt,
+                          None if bt is None else bt.data_ptr(), ps, npages)
+
+    @property
+    def T_max(self) -> int:
+        return self.k.shape[2] if self.block_table is None else self.block_table.shape[1] * self.k.shape[2]
 
     @staticmethod
     def empty(B: int, Hkv: int, T_max: int, dh: int, dtype=torch.bfloat16, device="cuda", fill=None) -> "KVCache":
         mk = (lambda: torch.full((B, Hkv, T_max, dh), fill, dtype=dtype, device=device)) if fill is not None \
             else (lambda: torch.empty((B, Hkv, T_max, dh), dtype=dtype, device=device))
         return KVCache(mk(), mk(), torch.zeros(B, dtype=torch.int32, device=device))
+
+    @staticmethod
+    def empty_paged(B: int, Hkv: int, T_max: int, dh: int, page_size: int, num_pages: int, block_table: torch.Tensor,
+                    dtype=torch.bfloat16, device="cuda", fill=None) -> "KVCache":
+        """Page pools of num_pages pages and the caller's block table [B, T_max / page_size]."""
+        shape = (num_pages, Hkv, page_size, dh)
+        mk = (lambda: torch.full(shape, fill, dtype=dtype, device=device)) if fill is not None \
+            else (lambda: torch.empty(shape, dtype=dtype, device=device))
+        if block_table.shape != (B, T_max // page_size):
+            raise ValueError("block_table must be [B, T_max / page_size]")
+        return KVCache(mk(), mk(), torch.zeros(B, dtype=torch.int32, device=device),
+                       block_table.to(device=device, dtype=torch.int32).contiguous())
 
 
 def _stream(stream) -> int:

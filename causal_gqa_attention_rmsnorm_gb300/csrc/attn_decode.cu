@@ -43,13 +43,18 @@ struct PartLayout {
 // sliding-window attention: the query sees its W most recent positions).
 // Chunk c of a sequence covers keys [first + c·chunk, ...).
 __device__ __forceinline__ int window_first(int n, int window) { return window > 0 && n > window ? n - window : 0; }
+// First key of a sequence's first chunk: the window start rounded down to
+// `align` keys (keys below the window start are masked).
+__device__ __forceinline__ int chunk_base(int n, int window, int align) {
+  return window_first(n, window) / align * align;
+}
 
 template <typename T, int DH, int G>
 __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restrict__ q, const T* __restrict__ kc,
                                                               const T* __restrict__ vc,
                                                               const int32_t* __restrict__ pos_arr, int Hkv,
                                                               int T_max, float* __restrict__ part, int nchunk_max,
-                                                              int window, float scale_log2) {
+                                                              int window, PagedKV pg, float scale_log2) {
   constexpr int VEC = 16 / sizeof(T);
   constexpr int LPK = DH / VEC;   // lanes per key row
   static_assert(LPK >= 1 && LPK <= 32 && (32 % LPK) == 0, "row must split evenly over lanes");
@@ -90,6 +95,10 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restric
   const uint4* kb = reinterpret_cast<const uint4*>(kc + head_off * DH) + li;
   const uint4* vb = reinterpret_cast<const uint4*>(vc + head_off * DH) + li;
   constexpr int ROWV = DH / VEC;  // uint4 per row
+  // row j of this (sequence, KV head): -1 for a bad page id
+  auto row_of = [&](int j) -> long long { return pg.bt ? paged_row(pg, Hkv, b, kvh, j) : (long long)j; };
+  const uint4* kpool = pg.bt ? reinterpret_cast<const uint4*>(pg.k) + li : kb;
+  const uint4* vpool = pg.bt ? reinterpret_cast<const uint4*>(pg.v) + li : vb;
 
   for (int base = j0 + warp * H_STEP; base < j1; base += kWarps * H_STEP) {
     Vec16<T> kr[KB], vr[KB];
@@ -97,10 +106,11 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restric
 #pragma unroll
     for (int u = 0; u < KB; ++u) {
       const int j = base + u * KPW + grp;
-      ok[u] = j < j1;
+      const long long row = j < j1 ? row_of(j) : -1;
+      ok[u] = row >= 0;
       if (ok[u]) {
-        kr[u].raw = __ldcs(kb + (size_t)j * ROWV);
-        vr[u].raw = __ldcs(vb + (size_t)j * ROWV);
+        kr[u].raw = __ldcs(kpool + (size_t)row * ROWV);
+        vr[u].raw = __ldcs(vpool + (size_t)row * ROWV);
       } else {
         kr[u].raw = make_uint4(0, 0, 0, 0);
         vr[u].raw = make_uint4(0, 0, 0, 0);
@@ -210,7 +220,7 @@ constexpr int kCombineMaxChunks = 1024;
 template <typename T, int DH>
 __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict__ part,
                                                         const int32_t* __restrict__ pos_arr, int H, int nchunk_max,
-                                                        int chunk, int window, T* __restrict__ o) {
+                                                        int chunk, int window, int align, T* __restrict__ o) {
   // Thread (e, g) sums output column e over chunks g, g + NG, ... with eight
   // independent loads in flight, so the merge costs a few L2 round trips.
   static_assert(256 % DH == 0, "head width must divide the block");
@@ -226,7 +236,7 @@ __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict_
     for (int e = threadIdx.x; e < DH; e += blockDim.x) orow[e] = from_f<T>(0.f);
     return;
   }
-  const int nkeys = pos + 1 - window_first(pos + 1, window);
+  const int nkeys = pos + 1 - chunk_base(pos + 1, window, align);
   const int nc = min((nkeys + chunk - 1) / chunk, kCombineMaxChunks);
   constexpr int P = PartLayout<DH>::stride;
   const float* pr = part + ((size_t)b * H + h) * nchunk_max * P;
@@ -351,8 +361,8 @@ template <int DH, int G>
 __global__ void __launch_bounds__(kMWarps * 32, 1)
     k_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const bf16* __restrict__ q, const int32_t* __restrict__ pos_arr, int B, int Hkv,
-                 float* __restrict__ part, int nchunk_max, int* __restrict__ counter, int window, float scale_log2,
-                 int* err) {
+                 float* __restrict__ part, int nchunk_max, int* __restrict__ counter, int window, PagedKV pg,
+                 float scale_log2, int* err) {
   using C = MCfg<DH>;
   using namespace ptx;
   static_assert(G <= 8, "at most 8 query heads per KV head");
@@ -368,7 +378,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
     for (int b = 0; b < B; ++b) {
       pre[b] = acc;
       const int p = pos_arr[b];
-      acc += p < 0 ? 0 : Hkv * ((p + 1 - window_first(p + 1, window) + kMChunk - 1) / kMChunk);
+      acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kMKeys) + kMChunk - 1) / kMChunk);
     }
     pre[B] = acc;
     abort_word = 0;
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
   uint8_t* slots = smem + warp * C::WARP_BYTES;
   const uint32_t slots_u32 = smem_u32(slots);
 
-  struct Item { int b, kvh, c, key0, nkeys; };
+  struct Item { int b, kvh, c, key0, nkeys, first; };
   auto decode = [&](int id) {
     int lo = 0, hi = B - 1;                    // last b with pre[b] <= id
     while (lo < hi) {
@@ -393,15 +403,16 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
       if (pre[mid] <= id) lo = mid; else hi = mid - 1;
     }
     const int n = pos_arr[lo] + 1;
-    const int first = window_first(n, window);
-    const int nch = (n - first + kMChunk - 1) / kMChunk;
+    const int base = chunk_base(n, window, kMKeys);     // 16-key stages never straddle a page
+    const int nch = (n - base + kMChunk - 1) / kMChunk;
     const int r = id - pre[lo];
     Item it;
     it.b = lo;
     it.kvh = r / nch;
     it.c = r - it.kvh * nch;
-    it.key0 = first + it.c * kMChunk;
+    it.key0 = base + it.c * kMChunk;
     it.nkeys = min(kMChunk, n - it.key0);
+    it.first = window_first(n, window);
     return it;
   };
 
@@ -429,7 +440,18 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
         uint8_t* base = slots + sl * C::SLOT;
         fence_proxy_async();       // earlier generic writes to the slot, before the TMA overwrite
         mbar_arrive_expect_tx(&full[sl], C::SLOT);
-        const int y = it.key0 + pst * kMKeys, z = it.b * Hkv + it.kvh;
+        const int key = it.key0 + pst * kMKeys;
+        int y = key, z = it.b * Hkv + it.kvh;
+        if (pg.bt) {                 // paged: the stage lies inside one page
+          const int page = pg.bt[(size_t)it.b * pg.max_pages + key / pg.ps];
+          y = key % pg.ps;
+          if (page < 0 || page >= pg.num_pages) {
+            atomicOr(err, TB_DEVERR_BAD_PAGE);
+            z = pg.num_pages * Hkv;   // outside the pool: the copy reads zeros
+          } else {
+            z = page * Hkv + it.kvh;
+          }
+        }
 #pragma unroll
         for (int hb = 0; hb < C::NB; ++hb) {
           tma_load_3d(&tmK, base + hb * C::BOX, &full[sl], hb * 64, y, z);
@@ -505,8 +527,9 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
       }
       // online softmax of head g over the stage's keys (raw scores; scale folded into the exponent)
       const int k0 = 2 * t, k1 = 2 * t + 1, k2 = 8 + 2 * t, k3 = 9 + 2 * t;
-      float r0 = k0 < nvalid ? s0[0] : -INFINITY, r1 = k1 < nvalid ? s0[1] : -INFINITY;
-      float r2 = k2 < nvalid ? s1[0] : -INFINITY, r3 = k3 < nvalid ? s1[1] : -INFINITY;
+      const int lead = it.first - (it.key0 + st * kMKeys);   // keys below lead precede the window
+      float r0 = k0 < nvalid && k0 >= lead ? s0[0] : -INFINITY, r1 = k1 < nvalid && k1 >= lead ? s0[1] : -INFINITY;
+      float r2 = k2 < nvalid && k2 >= lead ? s1[0] : -INFINITY, r3 = k3 < nvalid && k3 >= lead ? s1[1] : -INFINITY;
       float mx = fmaxf(fmaxf(r0, r1), fmaxf(r2, r3));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -573,12 +596,16 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
 
 template <int DH, int G>
 cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
-                       float* part, int nchunk_max, int* counter, int window, void* o, cudaStream_t s) {
+                       float* part, int nchunk_max, int* counter, int window, const PagedKV& pg, void* o,
+                       cudaStream_t s) {
   using C = MCfg<DH>;
   CUtensorMap tk, tv;
-  cudaError_t e = make_tmap_3d_bf16(&tk, kc, (uint64_t)B * Hkv, T_max, DH, DH, (uint64_t)T_max * DH, 64, kMKeys);
+  // planes of rows: (sequence, KV head) planes of T_max rows, or (page, KV head) planes of page_size rows
+  const uint64_t planes = pg.bt ? (uint64_t)pg.num_pages * Hkv : (uint64_t)B * Hkv;
+  const uint64_t rows = pg.bt ? (uint64_t)pg.ps : (uint64_t)T_max;
+  cudaError_t e = make_tmap_3d_bf16(&tk, pg.bt ? pg.k : kc, planes, rows, DH, DH, rows * DH, 64, kMKeys);
   if (e != cudaSuccess) return e;
-  e = make_tmap_3d_bf16(&tv, vc, (uint64_t)B * Hkv, T_max, DH, DH, (uint64_t)T_max * DH, 64, kMKeys);
+  e = make_tmap_3d_bf16(&tv, pg.bt ? pg.v : vc, planes, rows, DH, DH, rows * DH, 64, kMKeys);
   if (e != cudaSuccess) return e;
   const size_t smem = C::OFF_PRE + (size_t)(B + 1) * 4 + 1024;
   if (smem > 232448) return cudaErrorInvalidValue;
@@ -595,55 +622,57 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_mma<DH, G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, (const bf16*)q, pos, B, Hkv, part,
-                                                             nchunk_max, counter, window, scale_log2,
+                                                             nchunk_max, counter, window, pg, scale_log2,
                                                              device_error_word());
   k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kMChunk, window,
-                                                               (bf16*)o);
+                                                               kMKeys, (bf16*)o);
   return cudaGetLastError();
 }
 
 template <int DH>
 cudaError_t stream_by_g(int G, const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv,
-                        int T_max, float* part, int nchunk_max, int* counter, int window, void* o, cudaStream_t s) {
+                        int T_max, float* part, int nchunk_max, int* counter, int window, const PagedKV& pg, void* o,
+                        cudaStream_t s) {
   switch (G) {
-    case 1: return run_stream<DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, o, s);
-    case 2: return run_stream<DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, o, s);
-    case 4: return run_stream<DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, o, s);
-    case 8: return run_stream<DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, o, s);
+    case 1: return run_stream<DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, pg, o, s);
+    case 2: return run_stream<DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, pg, o, s);
+    case 4: return run_stream<DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, pg, o, s);
+    case 8: return run_stream<DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, pg, o, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T, int DH, int G>
 cudaError_t run(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
-                float* part, int nchunk_max, int window, void* o, cudaStream_t s) {
+                float* part, int nchunk_max, int window, const PagedKV& pg, void* o, cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   k_decode_split<T, DH, G><<<dim3(nchunk_max, Hkv, B), kWarps * 32, 0, s>>>(
-      (const T*)q, (const T*)kc, (const T*)vc, pos, Hkv, T_max, part, nchunk_max, window, scale_log2);
-  k_decode_combine<T, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kChunk, window, (T*)o);
+      (const T*)q, (const T*)kc, (const T*)vc, pos, Hkv, T_max, part, nchunk_max, window, pg, scale_log2);
+  k_decode_combine<T, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kChunk, window, 1,
+                                                           (T*)o);
   return cudaGetLastError();
 }
 
 template <typename T, int DH>
 cudaError_t by_g(int G, const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv,
-                 int T_max, float* part, int nchunk_max, int window, void* o, cudaStream_t s) {
+                 int T_max, float* part, int nchunk_max, int window, const PagedKV& pg, void* o, cudaStream_t s) {
   switch (G) {
-    case 1: return run<T, DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
-    case 2: return run<T, DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
-    case 4: return run<T, DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
-    case 8: return run<T, DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+    case 1: return run<T, DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
+    case 2: return run<T, DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
+    case 4: return run<T, DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
+    case 8: return run<T, DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T>
 cudaError_t by_dh(int dh, int G, const void* q, const void* kc, const void* vc, const int32_t* pos, int B,
-                  int Hkv, int T_max, float* part, int nchunk_max, int window, void* o, cudaStream_t s) {
+                  int Hkv, int T_max, float* part, int nchunk_max, int window, const PagedKV& pg, void* o, cudaStream_t s) {
   switch (dh) {
-    case 16: return by_g<T, 16>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
-    case 32: return by_g<T, 32>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
-    case 64: return by_g<T, 64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
-    case 128: return by_g<T, 128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
+    case 16: return by_g<T, 16>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
+    case 32: return by_g<T, 32>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
+    case 64: return by_g<T, 64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
+    case 128: return by_g<T, 128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -658,11 +687,11 @@ size_t decode_part_floats(int B, int H, int dh, int nchunk_max) {
 
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos, int B,
                         int H, int Hkv, int dh, int T_max, float* part, int nchunk_max, int* work_counter,
-                        int window, void* o, cudaStream_t s) {
+                        int window, const PagedKV& pg, void* o, cudaStream_t s) {
   const int G = H / Hkv;
-  if (dtype == TB_F32) return by_dh<float>(dh, G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, o, s);
-  if (dh == 128) return stream_by_g<128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
-  if (dh == 64) return stream_by_g<64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
+  if (dtype == TB_F32) return by_dh<float>(dh, G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
+  if (dh == 128) return stream_by_g<128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, pg, o, s);
+  if (dh == 64) return stream_by_g<64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, pg, o, s);
   return cudaErrorInvalidValue;
 }
 

@@ -79,6 +79,29 @@ cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, 
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new,
                              int n, int* err, cudaStream_t s);
 
+// A paged cache as kernels see it (bt == nullptr: none).  Row t of sequence b
+// lives in page bt[b·max_pages + t/ps] at offset t % ps of pools
+// [num_pages, Hkv, ps, dh]; a page id outside [0, num_pages) is never
+// dereferenced and sets TB_DEVERR_BAD_PAGE.
+struct PagedKV {
+  void* k = nullptr;
+  void* v = nullptr;
+  const int32_t* bt = nullptr;
+  int ps = 0, max_pages = 0, num_pages = 0;
+  int* err = nullptr;
+};
+
+// Row offset (in rows of dh values) of key t of (sequence b, KV head h) in a
+// paged pool, or -1 for a bad page id (flagged in the error word).
+__device__ __forceinline__ long long paged_row(const PagedKV& p, int Hkv, int b, int h, int t) {
+  const int page = p.bt[(size_t)b * p.max_pages + t / p.ps];
+  if (page < 0 || page >= p.num_pages) {
+    atomicOr(p.err, TB_DEVERR_BAD_PAGE);
+    return -1;
+  }
+  return ((long long)page * Hkv + h) * p.ps + t % p.ps;
+}
+
 // GEMM epilogue argument bundles.
 struct QKVArgs {
   const float* r;          // [M] RMSNorm-1 inverse RMS of each token
@@ -89,6 +112,7 @@ struct QKVArgs {
   int T;                   // tokens per sequence (1 for decode)
   int kv_stride;           // rows per (b, kv head) in k/v
   const int32_t* pos;      // decode: position of sequence b (-1: skip); prefill: nullptr
+  PagedKV pg;              // also (or, with k == nullptr, only) store k and v rows into this paged cache
 };
 struct WoArgs {
   const void* x;           // [M, d] residual input (cfg dtype)
@@ -143,6 +167,6 @@ int decode_chunk_keys();
 size_t decode_part_floats(int B, int H, int dh, int nchunk_max);
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos,
                         int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max,
-                        int* work_counter, int window, void* o, cudaStream_t s);
+                        int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s);
 
 }  // namespace tb

@@ -117,7 +117,7 @@ __global__ void k_row_stats(const T* __restrict__ x, int M, int d, float eps, fl
 // flagged by k_append_bump, which reads the same unchanged lens[b].
 __global__ void k_append_copy(uint4* __restrict__ kc, uint4* __restrict__ vc, const int32_t* __restrict__ lens,
                               int Hkv, int T_max, int row_vecs, const uint4* __restrict__ kn,
-                              const uint4* __restrict__ vn, int n) {
+                              const uint4* __restrict__ vn, int n, PagedKV pg) {
   const int b = blockIdx.y;
   const int L = lens[b];
   if (L < 0 || L + n > T_max) return;
@@ -125,7 +125,15 @@ __global__ void k_append_copy(uint4* __restrict__ kc, uint4* __restrict__ vc, co
   const size_t total = (size_t)Hkv * per_head;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const size_t h = i / per_head, rem = i % per_head;
-    const size_t dst = (((size_t)b * Hkv + h) * T_max + L) * row_vecs + rem;
+    const int r = (int)(rem / row_vecs), piece = (int)(rem % row_vecs);
+    size_t dst;
+    if (pg.bt) {                     // paged: the page holding row L + r
+      const long long row = paged_row(pg, Hkv, b, (int)h, L + r);
+      if (row < 0) continue;
+      dst = (size_t)row * row_vecs + piece;
+    } else {
+      dst = (((size_t)b * Hkv + h) * T_max + L) * row_vecs + rem;
+    }
     const size_t src = ((size_t)b * Hkv + h) * per_head + rem;
     kc[dst] = kn[src];
     vc[dst] = vn[src];
@@ -194,8 +202,18 @@ cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new,
   const int row_vecs = kv.dh * esz / 16;
   const size_t per_seq = (size_t)kv.Hkv * n * row_vecs;
   const unsigned gx = (unsigned)std::min<size_t>((per_seq + 255) / 256, 1024);
+  PagedKV pg;
+  if (kv.block_table) {
+    pg.k = kv.k;
+    pg.v = kv.v;
+    pg.bt = kv.block_table;
+    pg.ps = kv.page_size;
+    pg.max_pages = kv.T_max / kv.page_size;
+    pg.num_pages = kv.num_pages;
+    pg.err = err;
+  }
   k_append_copy<<<dim3(gx, kv.B), 256, 0, s>>>((uint4*)kv.k, (uint4*)kv.v, kv.lens, kv.Hkv, kv.T_max,
-                                               row_vecs, (const uint4*)k_new, (const uint4*)v_new, n);
+                                               row_vecs, (const uint4*)k_new, (const uint4*)v_new, n, pg);
   k_append_bump<<<(kv.B + 127) / 128, 128, 0, s>>>(kv.lens, kv.B, kv.T_max, n, err);
   return cudaGetLastError();
 }

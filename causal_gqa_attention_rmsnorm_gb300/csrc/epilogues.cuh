@@ -100,8 +100,14 @@ struct EpiQKV {
     } else if (ra.t >= 0) {
       const bool is_k = col < qn + kn;
       const int h = (col - (is_k ? qn : qn + kn)) / dh;
-      T* base = (T*)(is_k ? a.k : a.v);
-      store4<T>(base + (((size_t)ra.b * Hkv + h) * a.kv_stride + ra.t) * dh + e, v);
+      if (a.k) {
+        T* base = (T*)(is_k ? a.k : a.v);
+        store4<T>(base + (((size_t)ra.b * Hkv + h) * a.kv_stride + ra.t) * dh + e, v);
+      }
+      if (a.pg.bt) {
+        const long long row = paged_row(a.pg, Hkv, ra.b, h, ra.t);
+        if (row >= 0) store4<T>((T*)(is_k ? a.pg.k : a.pg.v) + row * dh + e, v);
+      }
     }
     return 0.f;
   }

@@ -205,7 +205,30 @@ tb_status check_kv(const tb_block_cfg* c, const tb_kvcache* kv, int B) {
   if (kv->T_max <= 0) return fail(TB_ERR_INVALID_ARG, "kv->T_max must be positive");
   if (!aligned16(kv->k) || !aligned16(kv->v) || ((uintptr_t)kv->lens & 3u))
     return fail(TB_ERR_INVALID_ARG, "kv cache pointers must be 16-byte aligned (lens 4-byte)");
+  if (kv->block_table) {
+    if (kv->page_size <= 0 || kv->page_size % 16)
+      return fail(TB_ERR_INVALID_ARG, "page_size (%d) must be a positive multiple of 16", kv->page_size);
+    if (kv->T_max % kv->page_size)
+      return fail(TB_ERR_INVALID_ARG, "page_size (%d) must divide T_max (%d)", kv->page_size, kv->T_max);
+    if (kv->num_pages <= 0) return fail(TB_ERR_INVALID_ARG, "num_pages must be positive");
+    if ((uintptr_t)kv->block_table & 3u) return fail(TB_ERR_INVALID_ARG, "block_table must be 4-byte aligned");
+  }
   return TB_OK;
+}
+
+// The paged view kernels use (bt == nullptr for a contiguous cache).
+PagedKV paged_of(const tb_kvcache* kv, int* err) {
+  PagedKV p;
+  if (kv && kv->block_table) {
+    p.k = kv->k;
+    p.v = kv->v;
+    p.bt = kv->block_table;
+    p.ps = kv->page_size;
+    p.max_pages = kv->T_max / kv->page_size;
+    p.num_pages = kv->num_pages;
+    p.err = err;
+  }
+  return p;
 }
 
 // Per-stage CUDA-event trace (test and benchmark hook).  When enabled, each
@@ -315,15 +338,18 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
   const int M = B * T;
   const int dt = cfg->dtype;
   const int nqkv = (cfg->H + 2 * cfg->Hkv) * cfg->dh;
-  void* kbuf = kv ? kv->k : W.k;
-  void* vbuf = kv ? kv->v : W.v;
-  const int kv_stride = kv ? kv->T_max : T;
+  // attention reads K/V from a contiguous cache in place, else from the
+  // workspace; a paged cache receives the rows as a second store
+  const bool contiguous_cache = kv && !kv->block_table;
+  void* kbuf = contiguous_cache ? kv->k : W.k;
+  void* vbuf = contiguous_cache ? kv->v : W.v;
+  const int kv_stride = contiguous_cache ? kv->T_max : T;
 
   StageRecorder rec(s);
   rec.stage("rms");
   TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, W.ssq, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
                           nullptr, err, s));
-  const QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr};
+  const QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr, paged_of(kv, err)};
   const WoArgs wa{x, W.h, W.hb, W.ssq};
   const W13Args ga{W.ssq, W.a};
   const W2Args ya{W.h, y, y_dtype};
@@ -389,7 +415,8 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
   rec.stage("rms");
   TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, W.ssq, 1, nullptr, kv->lens, W.pos, kv->T_max,
                           W.counter, err, s));
-  const QKVArgs qa{W.r, P.rope, W.q, kv->k, kv->v, 1, kv->T_max, W.pos};
+  const PagedKV pg = paged_of(kv, err);
+  const QKVArgs qa{W.r, P.rope, W.q, pg.bt ? nullptr : kv->k, pg.bt ? nullptr : kv->v, 1, kv->T_max, W.pos, pg};
   const WoArgs wa{x, W.h, W.hb, W.ssq};
   const W13Args ga{W.ssq, W.a};
   const W2Args ya{W.h, y, y_dtype};
@@ -398,7 +425,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(gemm_simt_qkv(dt, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                       W.nchunk_max, W.counter, cfg->window, W.o, s));
+                       W.nchunk_max, W.counter, cfg->window, pg, W.o, s));
     rec.stage("wo");
     TB_TRY(gemm_simt_wo(dt, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
@@ -410,7 +437,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(mm_qkv(W, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                       W.nchunk_max, W.counter, cfg->window, W.o, s));
+                       W.nchunk_max, W.counter, cfg->window, pg, W.o, s));
     rec.stage("wo");
     TB_TRY(mm_wo(W, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
@@ -434,6 +461,10 @@ tb_status tb_kvcache_append(const tb_kvcache* kv, const void* k_new, const void*
     return fail(TB_ERR_INVALID_ARG, "cache and new-row pointers must be non-NULL");
   if (!aligned16(kv->k) || !aligned16(kv->v) || !aligned16(k_new) || !aligned16(v_new))
     return fail(TB_ERR_INVALID_ARG, "cache and new-row pointers must be 16-byte aligned");
+  if (kv->block_table &&
+      (kv->page_size <= 0 || kv->T_max % kv->page_size || kv->num_pages <= 0 || ((uintptr_t)kv->block_table & 3u)))
+    return fail(TB_ERR_INVALID_ARG, "paged cache: page_size must divide T_max, num_pages be positive, "
+                                    "block_table 4-byte aligned");
   int* err = device_error_word();
   if (!err) return fail(TB_ERR_CUDA, "cannot resolve the device error word");
   TB_TRY(launch_kv_append(kv->dtype, *kv, k_new, v_new, n, err, (cudaStream_t)stream));

@@ -61,6 +61,7 @@ typedef enum { TB_F32 = 0, TB_BF16 = 1 } tb_dtype;
 /* Bits of the device error word (tb_get_device_error). */
 #define TB_DEVERR_CACHE_FULL 1  /* a decode/append row found lens[b] + n > T_max; that row was skipped */
 #define TB_DEVERR_TIMEOUT    2  /* a kernel's bounded wait ran out; its output is not valid */
+#define TB_DEVERR_BAD_PAGE   4  /* a paged cache's block table held a page id outside [0, num_pages) */
 
 /* Block hyper-parameters.
  *  d, H, Hkv, dh, f : widths in the pages' notation; H·dh must equal d, H a
@@ -99,8 +100,18 @@ typedef struct {
   const void *g_attn, *wq, *wk, *wv, *wo, *g_mlp, *w1, *w3, *w2;
 } tb_block_weights;
 
-/* KV cache of post-RoPE keys and values.
- *  k, v  : device, cfg.dtype, [B, Hkv, T_max, dh] each, row-major.
+/* KV cache of post-RoPE keys and values, in one of two layouts.
+ *  Contiguous (block_table == NULL):
+ *    k, v  : device, cfg.dtype, [B, Hkv, T_max, dh] each, row-major.
+ *  Paged (block_table != NULL), the cache allocated per sequence in fixed-size
+ *  blocks ("Transformer block" page, implementation notes: paged KV cache):
+ *    k, v        : device, cfg.dtype, page pools [num_pages, Hkv, page_size, dh].
+ *    block_table : device int32 [B, T_max / page_size]; row t of sequence b
+ *                  lives in page block_table[b·(T_max/page_size) + t/page_size]
+ *                  at offset t % page_size.  Entries are caller-owned page ids
+ *                  in [0, num_pages); a kernel that meets one outside that
+ *                  range writes nothing through it and sets TB_DEVERR_BAD_PAGE.
+ *    page_size   : a multiple of 16 that divides T_max.
  *  lens  : device int32 [B], the number of valid rows of each sequence.
  * Rows at or beyond lens[b] are never read. */
 typedef struct {
@@ -108,6 +119,8 @@ typedef struct {
   int32_t *lens;
   int32_t B, Hkv, T_max, dh;
   int32_t dtype;
+  const int32_t *block_table;
+  int32_t page_size, num_pages;
 } tb_kvcache;
 
 /* Bytes the packed weight blob of tb_pack_weights needs. */
