@@ -92,6 +92,23 @@ def weight_bytes(d: int, H: int, Hkv: int, dh: int, f: int, bytes_per_value: int
     return block_matrix_params(d, H, Hkv, dh, f) * bytes_per_value
 
 
+def model_params(L: int, d: int, H: int, Hkv: int, dh: int, f: int, V: int, tied: bool = False) -> int:
+    """Parameters of an L-layer model: the blocks, the embedding table [V, d],
+    the final norm's gain [d] and the LM head [d, V] (none when tied to the
+    embedding)."""
+    return L * block_params(d, H, Hkv, dh, f) + V * d + d + (0 if tied else V * d)
+
+
+def lm_head_flops(tokens: int, d: int, V: int) -> int:
+    """FLOPs of the LM head for ``tokens`` rows: 2·d·V per row."""
+    return 2 * tokens * d * V
+
+
+def logits_bytes(tokens: int, V: int, bytes_per_value: int = 4) -> int:
+    """Bytes of materialised logits [tokens, V] ("The Transformer" §5, step 18)."""
+    return tokens * V * bytes_per_value
+
+
 def forward_flops_per_token(N: int, L: int, T: int, d: int) -> int:
     """The pages' rule 2N + 4·L·T·d forward FLOPs per token (full square)."""
     return 2 * N + 4 * L * T * d

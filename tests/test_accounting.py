@@ -24,8 +24,7 @@ def _rows():
 
 
 def _model(a):
-    per_block = acc.block_params(a["d"], a["H"], a["Hkv"], a["dh"], a["f"])
-    return a["L"] * per_block + 2 * a["V"] * a["d"]
+    return acc.model_params(a["L"], a["d"], a["H"], a["Hkv"], a["dh"], a["f"], a["V"], a.get("tied", False))
 
 
 def _evaluate(qty, a):
@@ -54,6 +53,12 @@ def _evaluate(qty, a):
         return 2 * a["k"] * a["n"]
     if qty == "weight_bytes_one":
         return a["k"] * a["n"] * a["bytes"]
+    if qty == "embed_params":
+        return a["V"] * a["d"]
+    if qty == "logits_bytes":
+        return acc.logits_bytes(a["tokens"], a["V"])
+    if qty == "stack_matrix_params":
+        return a["L"] * acc.block_matrix_params(a["d"], a["H"], a["Hkv"], a["dh"], a["f"])
     if qty == "gpt2_total":
         d = a["d"]
         return a["L"] * acc.block_matrix_params(d, 1, 1, d, 8 * d / 3) + a["V"] * d + a["P"] * d
