@@ -542,6 +542,113 @@ def bench_paged(args, world, peaks):
             "gpu_launches": decode_launches(s.B) * n}
 
 
+def bench_stack(args, world, peaks):
+    """An args.stack_layers-layer model of the prefill workload's block shape:
+    the embedding gather, the stack, and the LM head's chunked per-token loss
+    over every token (vocabulary args.vocab, head tied to the embedding); then
+    one decode step through the same stack for the decode workload."""
+    import torch
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
+    import workloads
+
+    L, V = args.stack_layers, args.vocab
+    s = workloads.CONFIGS[args.workload]
+    if args.batch:
+        s = s.with_(B=args.batch)
+    n = max(min(args.steps, 5), 2)
+    sd = workloads.CONFIGS[args.decode_workload]
+    cfg = tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, max(s.T, sd.T), s.rope_base, s.eps, tb.TB_BF16)
+    packed = []
+    for l in range(L):
+        w = {k: t.cuda() for k, t in workloads.make_block_inputs(s.with_(B=1, T=1), seed=100 + l).items()}
+        packed.append(tb.tb_pack_weights(cfg, w))
+        del w
+    g = torch.Generator().manual_seed(7)
+    table = (0.02 * torch.randn(V, s.d, generator=g)).to(torch.bfloat16).cuda()
+    gain = (1 + 0.1 * torch.randn(s.d, generator=g)).to(torch.bfloat16).cuda()
+    hcfg = tb.HeadConfig(s.d, V, s.eps, tb.TB_BF16)
+    head = tb.tb_pack_lm_head(hcfg, gain, table, tied=True)
+    ids = torch.randint(0, V, (s.B, s.T), generator=g, dtype=torch.int32).cuda()
+    targets = torch.roll(ids, -1, dims=1).reshape(-1).contiguous()
+    x = torch.empty((s.B, s.T, s.d), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((s.B, s.T, s.d), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(tb.binding.lib().tb_stack_workspace_bytes(ctypes_cfg(cfg), s.B, s.T, 0), dtype=torch.uint8,
+                     device="cuda")
+    hws = torch.empty(tb.binding.lib().tb_lm_head_workspace_bytes(ctypes_cfg(hcfg), 4096), dtype=torch.uint8,
+                      device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    def step(record):
+        if record:
+            ev[0].record()
+        tb.tb_embed(table, ids, x=x)
+        y2 = tb.tb_stack_prefill(cfg, packed, x, y_dtype=tb.TB_BF16, ws=ws)
+        if record:
+            ev[1].record()
+        _, nll = tb.tb_lm_head(hcfg, head, y2.reshape(-1, s.d), want_logits=False, targets=targets, row_chunk=4096,
+                               ws=hws)
+        if record:
+            ev[2].record()
+        return nll
+    for _ in range(2):
+        step(False)
+    torch.cuda.synchronize()
+    assert tb.tb_get_device_error(clear=True) == 0
+    t_stack = t_head = 0.0
+    for _ in range(n):
+        nll = step(True)
+        torch.cuda.synchronize()
+        t_stack += ev[0].elapsed_time(ev[1])
+        t_head += ev[1].elapsed_time(ev[2])
+    assert tb.tb_get_device_error(clear=True) == 0 and torch.isfinite(nll).all().item()
+    t_stack, t_head = t_stack / n, t_head / n
+    tokens = s.B * s.T
+    head_fl = acc.lm_head_flops(tokens, s.d, V)
+    pre = {"workload": s.name, "layers": L, "vocab": V, "tokens": tokens, "stack_ms": t_stack,
+           "stack_tok_s": world * tokens / (t_stack * 1e-3), "head_ms": t_head,
+           "head_tflops": head_fl / (t_head * 1e-3) / 1e12, "head_frac_bf16": head_fl / (t_head * 1e-3) / 1e12 / peaks["bf16_tflops"],
+           "model_tok_s": world * tokens / ((t_stack + t_head) * 1e-3), "mean_nll": float(nll.mean())}
+    del x, y, ws, hws
+
+    lens = workloads.make_lens(sd, seed=0)
+    kvs = []
+    for l in range(L):
+        kc, vc = workloads.make_decode_cache(sd, l, lens, fill=0.0, device="cuda")
+        kvs.append(tb.KVCache(kc, vc, lens.cuda()))
+    lens0 = lens.cuda()
+    ids1 = torch.randint(0, V, (sd.B, 1), generator=g, dtype=torch.int32).cuda()
+    x1 = torch.empty((sd.B, 1, sd.d), dtype=torch.bfloat16, device="cuda")
+    dws = torch.empty(tb.binding.lib().tb_stack_workspace_bytes(ctypes_cfg(cfg), sd.B, sd.T, 1), dtype=torch.uint8,
+                      device="cuda")
+
+    def dstep():
+        for kv in kvs:
+            kv.lens.copy_(lens0, non_blocking=True)
+        tb.tb_embed(table, ids1, x=x1)
+        h = tb.tb_stack_decode(cfg, packed, x1, kvs, y_dtype=tb.TB_BF16, ws=dws)
+        return tb.tb_lm_head(hcfg, head, h.reshape(-1, sd.d))[0]
+    for _ in range(3):
+        dstep()
+    torch.cuda.synchronize()
+    m = max(args.steps, 10)
+    ev[0].record()
+    for _ in range(m):
+        lg = dstep()
+    ev[1].record()
+    torch.cuda.synchronize()
+    assert tb.tb_get_device_error(clear=True) == 0 and torch.isfinite(lg).all().item()
+    dms = ev[0].elapsed_time(ev[1]) / m
+    dec = {"workload": sd.name, "layers": L, "step_ms": dms, "tok_s": world * sd.B / (dms * 1e-3)}
+    return {"prefill": pre, "decode": dec,
+            "gpu_launches": n * (1 + 6 * L + 3 * (tokens + 4095) // 4096) + m * (1 + decode_launches(sd.B) * L + 3)}
+
+
+def ctypes_cfg(cfg):
+    import ctypes
+    return ctypes.byref(cfg.c())
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -558,6 +665,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the decode step")
     ap.add_argument("--window", type=int, default=4096, help="sliding-window width of the extra window line (0: skip)")
     ap.add_argument("--page-size", type=int, default=16, help="page size of the paged-cache decode line (0: skip)")
+    ap.add_argument("--stack-layers", type=int, default=4, help="layers of the model line (0: skip)")
+    ap.add_argument("--vocab", type=int, default=128256, help="vocabulary of the model line's LM head")
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
     ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample size for cpu_baseline")
     args = ap.parse_args()
@@ -589,6 +698,7 @@ def main():
     dec = None if args.no_decode else bench_decode(args, world, peaks)
     win = None if (args.window <= 0 or args.no_decode) else bench_window(args, world, peaks)
     pag = None if (args.page_size <= 0 or args.no_decode) else bench_paged(args, world, peaks)
+    stk = None if (args.stack_layers <= 0 or args.no_decode) else bench_stack(args, world, peaks)
 
     from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
     tokens = s.B * s.T
@@ -618,6 +728,7 @@ def main():
         "decode": dec,
         "sliding_window": win,
         "paged_kv": pag,
+        "model": stk,
         "peaks": {"source": peak_src, "bf16_tflops": peaks["bf16_tflops"],
                   "bf16_tflops_sustained": peaks["bf16_tflops_sustained"], "hbm_gbs": peaks["hbm_gbs"]},
     }

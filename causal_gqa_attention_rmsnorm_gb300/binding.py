@@ -19,13 +19,15 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtb.so")
 
 TB_F32, TB_BF16 = 0, 1
-TB_DEVERR_CACHE_FULL, TB_DEVERR_TIMEOUT, TB_DEVERR_BAD_PAGE = 1, 2, 4
+TB_DEVERR_CACHE_FULL, TB_DEVERR_TIMEOUT, TB_DEVERR_BAD_PAGE, TB_DEVERR_BAD_TOKEN = 1, 2, 4, 8
 STATUS = {0: "TB_OK", 1: "TB_ERR_INVALID_ARG", 2: "TB_ERR_UNSUPPORTED", 3: "TB_ERR_CUDA",
           4: "TB_ERR_CACHE_FULL", 5: "TB_ERR_TIMEOUT"}
 WEIGHT_FIELDS = ("g_attn", "wq", "wk", "wv", "wo", "g_mlp", "w1", "w3", "w2")
 EXPORTED = ("tb_packed_weights_bytes", "tb_pack_weights", "tb_workspace_bytes", "tb_block_prefill",
             "tb_block_decode", "tb_block_decode_noalloc", "tb_kvcache_append", "tb_get_device_error", "tb_status_string",
-            "tb_last_error_message")
+            "tb_last_error_message", "tb_embed", "tb_lm_head_packed_bytes", "tb_pack_lm_head",
+            "tb_lm_head_workspace_bytes", "tb_lm_head", "tb_stack_workspace_bytes", "tb_stack_prefill",
+            "tb_stack_decode")
 
 
 class tb_block_cfg(ctypes.Structure):
@@ -42,6 +44,10 @@ class tb_kvcache(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("lens", c_void_p), ("B", c_int32), ("Hkv", c_int32),
                 ("T_max", c_int32), ("dh", c_int32), ("dtype", c_int32), ("block_table", c_void_p),
                 ("page_size", c_int32), ("num_pages", c_int32)]
+
+
+class tb_head_cfg(ctypes.Structure):
+    _fields_ = [("d", c_int32), ("V", c_int32), ("eps", c_float), ("dtype", c_int32)]
 
 
 class TbError(RuntimeError):
@@ -86,9 +92,23 @@ def lib() -> ctypes.CDLL:
         L.tbx_trace_read.restype = c_int32
         L.tbx_trace_stage_name.argtypes = [c_int32]
         L.tbx_trace_stage_name.restype = ctypes.c_char_p
+        L.tb_embed.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, ctypes.c_int64, c_void_p, c_void_p]
+        L.tb_lm_head_packed_bytes.argtypes = [P(tb_head_cfg)]
+        L.tb_lm_head_packed_bytes.restype = c_size_t
+        L.tb_pack_lm_head.argtypes = [P(tb_head_cfg), c_void_p, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]
+        L.tb_lm_head_workspace_bytes.argtypes = [P(tb_head_cfg), c_int32]
+        L.tb_lm_head_workspace_bytes.restype = c_size_t
+        L.tb_lm_head.argtypes = [P(tb_head_cfg), c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_int32,
+                                 c_void_p, c_size_t, c_void_p]
+        L.tb_stack_workspace_bytes.argtypes = [P(tb_block_cfg), c_int32, c_int32, c_int32]
+        L.tb_stack_workspace_bytes.restype = c_size_t
+        L.tb_stack_prefill.argtypes = [P(tb_block_cfg), c_int32, P(c_void_p), c_void_p, c_void_p, c_int32, c_int32,
+                                       c_int32, P(tb_kvcache), c_void_p, c_size_t, c_void_p]
+        L.tb_stack_decode.argtypes = [P(tb_block_cfg), c_int32, P(c_void_p), c_void_p, c_void_p, c_int32,
+                                      P(tb_kvcache), c_void_p, c_size_t, c_void_p]
         for fn in ("tb_pack_weights", "tb_block_prefill", "tb_block_decode", "tb_block_decode_noalloc",
-                   "tb_kvcache_append",
-                   "tb_get_device_error", "tbx_gemm_bf16"):
+                   "tb_kvcache_append", "tb_embed", "tb_pack_lm_head", "tb_lm_head", "tb_stack_prefill",
+                   "tb_stack_decode", "tb_get_device_error", "tbx_gemm_bf16"):
             getattr(L, fn).restype = c_int32
         _lib = L
     return _lib
@@ -330,3 +350,118 @@ def tbx_trace_read(slot: int):
     if n < 0:
         raise RuntimeError("tbx_trace_read: CUDA error")
     return [(lib().tbx_trace_stage_name(i).decode(), float(buf[i])) for i in range(n)]
+
+
+# ---- around the block: embedding, LM head, L-layer stack -------------------
+
+@dataclass
+class HeadConfig:
+    """Python mirror of tb_head_cfg."""
+    d: int
+    V: int
+    eps: float
+    dtype: int = TB_BF16
+
+    def c(self) -> tb_head_cfg:
+        return tb_head_cfg(self.d, self.V, self.eps, self.dtype)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == TB_F32 else torch.bfloat16
+
+
+def tb_embed(table: torch.Tensor, ids: torch.Tensor, x: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """x[t] = table[ids[t]]: table [V, d], ids int32 (any shape) -> x [*ids.shape, d]."""
+    V, d = table.shape
+    _need(table, "table", table.dtype)
+    _need(ids, "ids", torch.int32)
+    if x is None:
+        x = torch.empty((*ids.shape, d), dtype=table.dtype, device=table.device)
+    _need(x, "x", table.dtype, (*ids.shape, d))
+    dt = TB_F32 if table.dtype == torch.float32 else TB_BF16
+    _check("tb_embed", lib().tb_embed(table.data_ptr(), V, d, dt, ids.data_ptr(), ids.numel(), x.data_ptr(),
+                                      _stream(stream)))
+    return x
+
+
+def tb_pack_lm_head(cfg: HeadConfig, g_final: torch.Tensor, w_u: torch.Tensor, tied: bool = False,
+                    stream=None) -> torch.Tensor:
+    """Pack the head: w_u [d, V], or with tied=True the embedding table [V, d]."""
+    _need(g_final, "g_final", cfg.torch_dtype, (cfg.d,))
+    _need(w_u, "w_u", cfg.torch_dtype, (cfg.V, cfg.d) if tied else (cfg.d, cfg.V))
+    n = lib().tb_lm_head_packed_bytes(ctypes.byref(cfg.c()))
+    if n == 0:
+        raise TbError("tb_lm_head_packed_bytes", 1, lib().tb_last_error_message().decode())
+    packed = torch.empty(n, dtype=torch.uint8, device=w_u.device)
+    _check("tb_pack_lm_head", lib().tb_pack_lm_head(ctypes.byref(cfg.c()), g_final.data_ptr(), w_u.data_ptr(),
+                                                    1 if tied else 0, packed.data_ptr(), n, _stream(stream)))
+    return packed
+
+
+def tb_lm_head(cfg: HeadConfig, packed: torch.Tensor, x: torch.Tensor, want_logits: bool = True,
+               targets: Optional[torch.Tensor] = None, row_chunk: int = 0, ws: Optional[torch.Tensor] = None,
+               stream=None):
+    """Head over x [M, d]: returns (logits [M, V] fp32 or None, nll [M] fp32 or None)."""
+    M = x.shape[0]
+    _need(x, "x", cfg.torch_dtype, (M, cfg.d))
+    logits = torch.empty((M, cfg.V), dtype=torch.float32, device=x.device) if want_logits else None
+    nll = None
+    if targets is not None:
+        _need(targets, "targets", torch.int32, (M,))
+        nll = torch.empty(M, dtype=torch.float32, device=x.device)
+    need = lib().tb_lm_head_workspace_bytes(ctypes.byref(cfg.c()), row_chunk)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    _check("tb_lm_head", lib().tb_lm_head(ctypes.byref(cfg.c()), packed.data_ptr(), x.data_ptr(), M,
+                                          None if logits is None else logits.data_ptr(),
+                                          None if targets is None else targets.data_ptr(),
+                                          None if nll is None else nll.data_ptr(), row_chunk, ws.data_ptr(),
+                                          ws.numel(), _stream(stream)))
+    return logits, nll
+
+
+def _packed_array(packed):
+    arr = (c_void_p * len(packed))(*[p.data_ptr() for p in packed])
+    return arr
+
+
+def tb_stack_prefill(cfg: BlockConfig, packed, x: torch.Tensor, kvs=None, y_dtype: int = TB_F32,
+                     ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """An L-layer prefill (L = len(packed)); kvs: None or a list of L KVCache."""
+    B, T, d = x.shape
+    _need(x, "x", cfg.torch_dtype, (B, T, cfg.d))
+    L = len(packed)
+    ydt = torch.float32 if y_dtype == TB_F32 else torch.bfloat16
+    y = torch.empty((B, T, d), dtype=ydt, device=x.device)
+    kv_arr = None
+    if kvs is not None:
+        if len(kvs) != L:
+            raise ValueError("one cache per layer")
+        kv_arr = (tb_kvcache * L)(*[kv.c() for kv in kvs])
+    need = lib().tb_stack_workspace_bytes(ctypes.byref(cfg.c()), B, T, 0)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    _check("tb_stack_prefill", lib().tb_stack_prefill(ctypes.byref(cfg.c()), L, _packed_array(packed), x.data_ptr(),
+                                                      y.data_ptr(), y_dtype, B, T, kv_arr, ws.data_ptr(), ws.numel(),
+                                                      _stream(stream)))
+    return y
+
+
+def tb_stack_decode(cfg: BlockConfig, packed, x: torch.Tensor, kvs, y_dtype: int = TB_F32,
+                    ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step through the L-layer stack: x [B, 1, d]; kvs a list of L KVCache."""
+    L = len(packed)
+    if len(kvs) != L:
+        raise ValueError("one cache per layer")
+    kv_arr = (tb_kvcache * L)(*[kv.c() for kv in kvs])
+    B, T_max = kv_arr[0].B, kv_arr[0].T_max
+    _need(x, "x", cfg.torch_dtype, (B, 1, cfg.d))
+    ydt = torch.float32 if y_dtype == TB_F32 else torch.bfloat16
+    y = torch.empty((B, 1, cfg.d), dtype=ydt, device=x.device)
+    need = lib().tb_stack_workspace_bytes(ctypes.byref(cfg.c()), B, T_max, 1)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    _check("tb_stack_decode", lib().tb_stack_decode(ctypes.byref(cfg.c()), L, _packed_array(packed), x.data_ptr(),
+                                                    y.data_ptr(), y_dtype, kv_arr, ws.data_ptr(), ws.numel(),
+                                                    _stream(stream)))
+    return y

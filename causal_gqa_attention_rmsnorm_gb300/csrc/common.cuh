@@ -124,11 +124,33 @@ struct W13Args {
   const float* ssq;        // [M] Σ h²
   void* a;                 // [M, f] SiLU(gate)·up
 };
+struct LogitsArgs {
+  const float* r;          // [M] final-norm inverse RMS of each row
+  float* out;              // [M, ld] fp32 logits
+  int ld;
+};
 struct W2Args {
   const float* h;          // [M, d]
   void* y;                 // [M, d]
   int y_dtype;
 };
+
+// LM head GEMMs (logits = (x·r)·Wᵀ, W [N, K] packed): tile, few-token and fp32 forms
+cudaError_t gemm_tc_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, cudaStream_t s);
+cudaError_t gemm_skinny_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, float* part,
+                               cudaStream_t s);
+cudaError_t gemm_simt_logits(int dtype, const void* A, const void* B, int M, int N, int K, const LogitsArgs& e,
+                             cudaStream_t s);
+
+// head.cu: embedding gather, LM-head reductions
+cudaError_t launch_embed(int dtype, const void* table, int V, int d, const int32_t* ids, long long n, void* x,
+                         int* err, cudaStream_t s);
+cudaError_t launch_lse_nll(const float* logits, int ld, int M, int V, const int32_t* targets, float* nll, int* err,
+                           cudaStream_t s);
+cudaError_t launch_scale_cols(int dtype, const void* src, const void* gain, int rows, int cols, void* dst,
+                              cudaStream_t s);
+cudaError_t launch_pack_transpose(int dtype, const void* src, int K, int N, const void* gain, void* dst,
+                                  cudaStream_t s);
 
 // gemm_simt.cu (fp32 path)
 cudaError_t gemm_simt_qkv(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,

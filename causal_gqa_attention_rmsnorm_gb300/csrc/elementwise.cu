@@ -196,6 +196,17 @@ cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, 
   return cudaGetLastError();
 }
 
+cudaError_t launch_pack_transpose(int dtype, const void* src, int K, int N, const void* gain, void* dst,
+                                  cudaStream_t s) {
+  const dim3 blk(32, 8), grid((N + 31) / 32, (K + 31) / 32);
+  if (grid.y > 65535) return cudaErrorInvalidValue;
+  if (dtype == TB_F32)
+    k_pack_transpose<float><<<grid, blk, 0, s>>>((const float*)src, K, N, (const float*)gain, (float*)dst, 1, 0);
+  else
+    k_pack_transpose<bf16><<<grid, blk, 0, s>>>((const bf16*)src, K, N, (const bf16*)gain, (bf16*)dst, 1, 0);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new, int n,
                              int* err, cudaStream_t s) {
   const int esz = dtype == TB_F32 ? 4 : 2;

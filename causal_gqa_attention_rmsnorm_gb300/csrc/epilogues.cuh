@@ -183,4 +183,23 @@ struct EpiW2 {
   __device__ __forceinline__ void row_reduce(int, float) const {}
 };
 
+// LM head: logits = (x·r)·W_Uᵀ with the final norm's gain folded into the
+// packed W_U and r the final RMSNorm's row scale ("Transformer block" page,
+// "How it works", step 4); fp32 logits, row stride ld.
+struct EpiLogits {
+  static constexpr bool kRowReduce = false;
+  LogitsArgs a;
+  struct RowAux { float r; };
+  struct Aux {};
+  __device__ __forceinline__ RowAux row_aux(int row) const { return RowAux{a.r[row]}; }
+  __device__ __forceinline__ Aux aux(int, int, const RowAux&) const { return Aux{}; }
+  __device__ __forceinline__ float operator()(int row, int col, float v[4], const RowAux& ra, const Aux&) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] *= ra.r;
+    store4<float>(a.out + (size_t)row * a.ld + col, v);
+    return 0.f;
+  }
+  __device__ __forceinline__ void row_reduce(int, float) const {}
+};
+
 }  // namespace tb

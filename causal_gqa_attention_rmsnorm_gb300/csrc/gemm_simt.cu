@@ -96,4 +96,10 @@ cudaError_t gemm_simt_w2(int dtype, const void* A, const void* B, int M, int N, 
   return run<bf16>(A, B, M, N, K, EpiW2{e, D.d}, s);
 }
 
+cudaError_t gemm_simt_logits(int dtype, const void* A, const void* B, int M, int N, int K, const LogitsArgs& e,
+                             cudaStream_t s) {
+  if (dtype == TB_F32) return run<float>(A, B, M, N, K, EpiLogits{e}, s);
+  return run<bf16>(A, B, M, N, K, EpiLogits{e}, s);
+}
+
 }  // namespace tb

@@ -316,10 +316,12 @@ cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& ep
   const int m_tiles = (M + BM - 1) / BM;
   const int tiles = m_tiles * ((N + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  // Short K with a B panel beyond what L2 keeps: group 32 row blocks (32 MB of
-  // A at K = 4096).  Otherwise n fastest.
+  // Short K with a B panel beyond what L2 keeps: group up to 32 row blocks (32
+  // MB of A at K = 4096), m fastest inside a group, so each B tile is read
+  // from HBM once per group rather than once per row block.  Otherwise n
+  // fastest.
   const size_t b_bytes = (size_t)N * K * 2;
-  const int group_m = (K <= 8192 && b_bytes > (size_t(48) << 20) && m_tiles > 32) ? 32 : 0;
+  const int group_m = (K <= 8192 && b_bytes > (size_t(48) << 20) && m_tiles > 1) ? (m_tiles < 32 ? m_tiles : 32) : 0;
   k_gemm_tc<BN, Epi><<<grid, 192, C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
                                                 device_error_word());
   return cudaGetLastError();
@@ -392,6 +394,9 @@ cudaError_t gemm_tc_w13(const void* A, const void* B, int M, int N, int K, const
 cudaError_t gemm_tc_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
                        cudaStream_t s) {
   return run_auto(A, B, M, N, K, EpiW2{e, D.d}, s);
+}
+cudaError_t gemm_tc_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, cudaStream_t s) {
+  return run_auto(A, B, M, N, K, EpiLogits{e}, s);
 }
 cudaError_t gemm_tc_f32out(const void* A, const void* B, float* Cp, int M, int N, int K, int bn, cudaStream_t s) {
   if (bn == 256) return run<256>(A, B, M, N, K, EpiF32{Cp, N}, s);

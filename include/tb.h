@@ -62,6 +62,7 @@ typedef enum { TB_F32 = 0, TB_BF16 = 1 } tb_dtype;
 #define TB_DEVERR_CACHE_FULL 1  /* a decode/append row found lens[b] + n > T_max; that row was skipped */
 #define TB_DEVERR_TIMEOUT    2  /* a kernel's bounded wait ran out; its output is not valid */
 #define TB_DEVERR_BAD_PAGE   4  /* a paged cache's block table held a page id outside [0, num_pages) */
+#define TB_DEVERR_BAD_TOKEN  8  /* an embedding or loss token id outside [0, V); its row is zero / NaN */
 
 /* Block hyper-parameters.
  *  d, H, Hkv, dh, f : widths in the pages' notation; H·dh must equal d, H a
@@ -209,6 +210,64 @@ TB_API const char *tb_status_string(tb_status s);
 
 /* Detail of the last non-OK status returned on the calling thread. */
 TB_API const char *tb_last_error_message(void);
+
+/* ---- Around the block: embedding, an L-layer stack, final norm and LM head ----
+ * "Transformer block" page (tirogla.com), "How it works": (1) token ids index an
+ * embedding table [V, d]; the blocks run in order; (4) after the last block a
+ * final RMSNorm, then logits = h·W_U with W_U [d, V], possibly tied to the
+ * embedding table.  "The Transformer" (GenerativeAIDocs) §5, "Step 18 is a
+ * memory trap": full [B, T, V] fp32 logits are large, so the head works in row
+ * chunks and can return the per-token loss without materialising them. */
+
+/* x[t] = table[ids[t]] for t < n.  table: device [V, d] of dtype; ids: device
+ * int32 [n]; x: device [n, d] of dtype (16-byte aligned, d·sizeof a multiple of
+ * 16).  An id outside [0, V) gives a zero row and sets TB_DEVERR_BAD_TOKEN. */
+TB_API tb_status tb_embed(const void *table, int32_t V, int32_t d, int32_t dtype, const int32_t *ids, int64_t n,
+                          void *x, void *stream);
+
+/* LM head hyper-parameters: width d, vocabulary V (a multiple of 4), the final
+ * RMSNorm's eps, and dtype (of x, the weights and the gain).  The bf16 path
+ * needs d a multiple of 64. */
+typedef struct {
+  int32_t d, V;
+  float eps;
+  int32_t dtype;
+} tb_head_cfg;
+
+/* Packed head: W_U transposed to [V, d] with the final norm's gain g_final [d]
+ * folded into its columns.  w_u: device [d, V] ([in, out], like the block's
+ * weights), or with tied != 0 the embedding table [V, d] (W_U = tableᵀ). */
+TB_API size_t tb_lm_head_packed_bytes(const tb_head_cfg *cfg);
+TB_API tb_status tb_pack_lm_head(const tb_head_cfg *cfg, const void *g_final, const void *w_u, int32_t tied,
+                                 void *packed, size_t packed_bytes, void *stream);
+
+/* Workspace of tb_lm_head for chunks of row_chunk rows (0: 4096). */
+TB_API size_t tb_lm_head_workspace_bytes(const tb_head_cfg *cfg, int32_t row_chunk);
+
+/* Head over M rows x [M, d] (device, cfg dtype): per row r = RMSNorm scale,
+ * logits = (x·r)·packedᵀ in fp32.  logits (device [M, V], or NULL) receives
+ * them; with targets (device int32 [M]) and nll (device fp32 [M]) non-NULL,
+ * nll[m] = logsumexp(logits[m]) - logits[m, targets[m]].  Rows are processed
+ * row_chunk at a time; with logits NULL only one chunk of logits ever exists
+ * (in ws).  A target outside [0, V) gives NaN and sets TB_DEVERR_BAD_TOKEN. */
+TB_API tb_status tb_lm_head(const tb_head_cfg *cfg, const void *packed, const void *x, int32_t M, float *logits,
+                            const int32_t *targets, float *nll, int32_t row_chunk, void *ws, size_t ws_bytes,
+                            void *stream);
+
+/* An L-layer stack of blocks of one configuration.  packed: host array of L
+ * device pointers (each a tb_pack_weights blob).  Prefill: x [B, T, d] in
+ * cfg.dtype -> y [B, T, d] in y_dtype; kvs: NULL or a host array of L caches
+ * (layer l's cache receives layer l's keys and values).  Decode: x [B, 1, d],
+ * kvs required (all at the same lens).  Between layers the residual stream is
+ * stored in cfg.dtype (each block's input type).  The workspace holds one
+ * block's workspace and two activation buffers. */
+TB_API size_t tb_stack_workspace_bytes(const tb_block_cfg *cfg, int32_t B, int32_t T, int32_t mode);
+TB_API tb_status tb_stack_prefill(const tb_block_cfg *cfg, int32_t L, const void *const *packed, const void *x,
+                                  void *y, int32_t y_dtype, int32_t B, int32_t T, const tb_kvcache *kvs, void *ws,
+                                  size_t ws_bytes, void *stream);
+TB_API tb_status tb_stack_decode(const tb_block_cfg *cfg, int32_t L, const void *const *packed, const void *x,
+                                 void *y, int32_t y_dtype, const tb_kvcache *kvs, void *ws, size_t ws_bytes,
+                                 void *stream);
 
 #ifdef __cplusplus
 }

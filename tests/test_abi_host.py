@@ -141,3 +141,29 @@ def test_workspace_grows_with_tokens(lib):
 def test_status_strings(lib):
     assert tb.tb_status_string(0) == "ok"
     assert tb.tb_status_string(4) == "KV cache full"
+
+
+def test_model_level_entry_points_validate_first(lib):
+    """The embedding, LM head and stack entry points reject bad arguments on the
+    host, before any launch."""
+    P = ctypes.POINTER
+    # embedding: unknown dtype, and d·sizeof not a multiple of 16
+    assert lib.tb_embed(FAKE, 10, 64, 7, FAKE, 5, FAKE, None) == 1
+    assert lib.tb_embed(FAKE, 10, 12, tb.TB_BF16, FAKE, 5, FAKE, None) == 2
+    # head: V not a multiple of 4, bf16 d not a multiple of 64, targets without nll
+    bad_v = binding.tb_head_cfg(256, 1001, 1e-5, tb.TB_BF16)
+    assert lib.tb_lm_head_packed_bytes(ctypes.byref(bad_v)) == 0
+    bad_d = binding.tb_head_cfg(96, 1000, 1e-5, tb.TB_BF16)
+    assert lib.tb_lm_head_workspace_bytes(ctypes.byref(bad_d), 16) == 0
+    good = binding.tb_head_cfg(256, 1000, 1e-5, tb.TB_BF16)
+    assert lib.tb_lm_head_packed_bytes(ctypes.byref(good)) >= 256 * 1000 * 2
+    assert lib.tb_lm_head(ctypes.byref(good), FAKE, FAKE, 4, None, FAKE, None, 0, FAKE, 1 << 30, None) == 1
+    # nothing requested: a no-op
+    assert lib.tb_lm_head(ctypes.byref(good), FAKE, FAKE, 4, None, None, None, 0, FAKE, 1 << 30, None) == 0
+    # stack: L = 0, and a workspace smaller than the stack needs
+    c = cfg()
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    assert lib.tb_stack_prefill(ctypes.byref(c), 0, arr, FAKE, FAKE + 4096, 0, 2, 16, None, FAKE, 1 << 30, None) == 1
+    need = lib.tb_stack_workspace_bytes(ctypes.byref(c), 2, 16, 0)
+    assert need > lib.tb_workspace_bytes(ctypes.byref(c), 2, 16, 0)
+    assert lib.tb_stack_prefill(ctypes.byref(c), 2, arr, FAKE, FAKE + 4096, 0, 2, 16, None, FAKE, need - 1, None) == 1
