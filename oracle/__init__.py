@@ -11,10 +11,10 @@ cross-check, brute force on tiny inputs); none is "parity unpinned".
 from .block import (Cfg, rms_norm, rope_angles, rope, silu, softmax_rows, visible_keys,
                     causal_attention,
                     qkv_heads, mlp_branch, block_prefill_seq, block_prefill, block_decode_seq,
-                    gather_paged, block_decode)
+                    gather_paged, quantize_rows, dequantize_rows, block_decode_seq_int8, block_decode)
 
 from .model import embed, lm_head, token_nll, stack_prefill_seq, stack_decode_seq
 
 __all__ = ["embed", "lm_head", "token_nll", "stack_prefill_seq", "stack_decode_seq", "Cfg", "rms_norm", "rope_angles", "rope", "silu", "softmax_rows", "visible_keys", "causal_attention",
            "qkv_heads", "mlp_branch", "block_prefill_seq", "block_prefill", "block_decode_seq",
-           "gather_paged", "block_decode"]
+           "gather_paged", "quantize_rows", "dequantize_rows", "block_decode_seq_int8", "block_decode"]

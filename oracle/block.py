@@ -230,6 +230,49 @@ def block_decode_seq(x: np.ndarray, w, cfg: Cfg, k_cache: np.ndarray, v_cache: n
     return {"y": y[0], "k": k_new[0], "v": v_new[0]}
 
 
+def quantize_rows(x: np.ndarray):
+    """Symmetric int8 quantisation of each row (last axis) with its own scale.
+
+    "The Transformer Architecture" (thegeniusblogs), pitfalls, KV-cache OOM:
+    the cache itself can be quantised to int8.  Here every cached row (one
+    token of one KV head, dh values) gets the scale s = max|x| / 127 and codes
+    q = round(x / s) in [-127, 127] (ties to even); a zero row has s = 0 and
+    q = 0.  Returns (q int8 [..., dh], s [...]).
+    """
+    x = np.asarray(x, F64)
+    s = np.max(np.abs(x), axis=-1) / 127.0
+    safe = np.where(s > 0, s, 1.0)
+    q = np.clip(np.rint(x / safe[..., None]), -127, 127)
+    q = np.where(s[..., None] > 0, q, 0.0)
+    return q.astype(np.int8), s
+
+
+def dequantize_rows(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """x̂ = q · s, row by row."""
+    return np.asarray(q, F64) * np.asarray(s, F64)[..., None]
+
+
+def block_decode_seq_int8(x: np.ndarray, w, cfg: Cfg, k_q: np.ndarray, k_s: np.ndarray, v_q: np.ndarray,
+                          v_s: np.ndarray, pos: int) -> Dict[str, np.ndarray]:
+    """One decode step over an int8 cache: rows 0..pos-1 of K and V stored as
+    codes [Hkv, >=pos, dh] with scales [Hkv, >=pos].  The new token's k and v
+    are quantised like every cached row before the query attends over all pos+1
+    dequantised rows.  Returns dict(y, k_q, k_s, v_q, v_s) with the new row's
+    codes and scales."""
+    w = _f64_weights(w)
+    x = np.asarray(x, F64)[None, :]
+    xn = rms_norm(x, w["g_attn"], cfg.eps)
+    q, k_new, v_new = qkv_heads(xn, w, cfg, [pos])
+    kq, ks = quantize_rows(k_new[0])
+    vq, vs = quantize_rows(v_new[0])
+    k_all = np.concatenate([dequantize_rows(k_q[:, :pos], k_s[:, :pos]), dequantize_rows(kq, ks)[:, None, :]], axis=1)
+    v_all = np.concatenate([dequantize_rows(v_q[:, :pos], v_s[:, :pos]), dequantize_rows(vq, vs)[:, None, :]], axis=1)
+    o = causal_attention(q, k_all.transpose(1, 0, 2), v_all.transpose(1, 0, 2), [pos], cfg.window)
+    h = x + o.reshape(1, cfg.H * cfg.dh) @ w["wo"]
+    y = mlp_branch(h, w, cfg)
+    return {"y": y[0], "k_q": kq, "k_s": ks, "v_q": vq, "v_s": vs}
+
+
 def gather_paged(pool: np.ndarray, block_table: Sequence[int], page_size: int, n: int) -> np.ndarray:
     """Rows 0..n-1 of one sequence of a paged cache, as a contiguous [Hkv, n, dh].
 

@@ -276,6 +276,46 @@ def check_paged_gather():
 
 
 # ----------------------------------------------------------------------------
+# int8 cache rows: "The Transformer Architecture", pitfalls (quantise the cache).
+# ----------------------------------------------------------------------------
+
+def check_int8_rows():
+    # rows of very different magnitudes, each with its own scale
+    x = RNG.standard_normal((6, 32)) * np.array([1e-3, 0.1, 1, 10, 300, 1])[:, None]
+    x[5] = 0.0
+    q, s = ob.quantize_rows(x)
+    assert q.dtype == np.int8 and s.shape == (6,)
+    np.testing.assert_allclose(s[:5], np.max(np.abs(x[:5]), axis=1) / 127, rtol=1e-15)
+    # the largest element of a row maps to ±127; every element is within s/2
+    for r in range(5):
+        assert abs(int(q[r, np.argmax(np.abs(x[r]))])) == 127
+        assert np.all(np.abs(ob.dequantize_rows(q, s)[r] - x[r]) <= s[r] / 2 * (1 + 1e-12))
+    assert s[5] == 0 and not q[5].any()
+    # rows built from codes and a scale come back exactly
+    codes = RNG.integers(-127, 128, size=(3, 16)); codes[:, 0] = 127
+    q2, s2 = ob.quantize_rows(codes * 0.25)
+    np.testing.assert_array_equal(q2, codes)
+    np.testing.assert_array_equal(s2, 0.25)
+
+
+def check_int8_decode_close_to_exact():
+    cfg = _cfg()
+    w = _weights(cfg, RNG)
+    T = 12
+    x = RNG.standard_normal((T, cfg.d))
+    pre = ob.block_prefill_seq(x, w, cfg)
+    kq, ks = ob.quantize_rows(pre["k"][:, :T - 1])
+    vq, vs = ob.quantize_rows(pre["v"][:, :T - 1])
+    dec = ob.block_decode_seq_int8(x[T - 1], w, cfg, kq, ks, vq, vs, T - 1)
+    exact = pre["y"][T - 1]
+    rel = np.linalg.norm(dec["y"] - exact) / np.linalg.norm(exact)
+    assert 0 < rel < 1e-2, rel
+    # the appended row is the quantised exact k
+    kq_new, ks_new = ob.quantize_rows(pre["k"][:, T - 1])
+    np.testing.assert_array_equal(dec["k_q"], kq_new)
+
+
+# ----------------------------------------------------------------------------
 # Block-level: residual wiring, GQA sharing, causality, decode vs prefill.
 # ----------------------------------------------------------------------------
 
@@ -364,7 +404,8 @@ CHECKS = [check_rope_closed_form, check_swiglu_closed_form, check_rope_invariant
           check_block_zero_branches, check_block_uniform_attention_closed_form,
           check_gqa_equals_duplicated_mha, check_causality_prefix, check_decode_matches_prefill,
           check_window_worked_example, check_window_reductions, check_window_brute_force,
-          check_window_decode_matches_prefill, check_paged_gather]
+          check_window_decode_matches_prefill, check_paged_gather, check_int8_rows,
+          check_int8_decode_close_to_exact]
 
 
 def _run(check):
@@ -539,7 +580,34 @@ def mut_paged_offset(monkeypatch):
     monkeypatch.setattr(ob, "gather_paged", gather)
 
 
-MUTANTS = [mut_paged_offset, mut_window_one_more, mut_window_decode_ignored, mut_diagonal, mut_rope_on_v, mut_cache_pre_rope, mut_no_max, mut_rope_halves,
+def mut_int8_floor(monkeypatch):
+    def quant(x):
+        x = np.asarray(x, float)
+        s = np.max(np.abs(x), axis=-1) / 127.0
+        safe = np.where(s > 0, s, 1.0)
+        return np.clip(np.floor(x / safe[..., None]), -127, 127).astype(np.int8), s
+    monkeypatch.setattr(ob, "quantize_rows", quant)
+
+
+def mut_int8_scale_128(monkeypatch):
+    def quant(x):
+        x = np.asarray(x, float)
+        s = np.max(np.abs(x), axis=-1) / 128.0
+        safe = np.where(s > 0, s, 1.0)
+        return np.clip(np.rint(x / safe[..., None]), -127, 127).astype(np.int8), s
+    monkeypatch.setattr(ob, "quantize_rows", quant)
+
+
+def mut_int8_one_scale(monkeypatch):
+    def quant(x):
+        x = np.asarray(x, float)
+        s = np.full(x.shape[:-1], np.max(np.abs(x)) / 127.0)
+        safe = np.where(s > 0, s, 1.0)
+        return np.clip(np.rint(x / safe[..., None]), -127, 127).astype(np.int8), s
+    monkeypatch.setattr(ob, "quantize_rows", quant)
+
+
+MUTANTS = [mut_int8_floor, mut_int8_scale_128, mut_int8_one_scale, mut_paged_offset, mut_window_one_more, mut_window_decode_ignored, mut_diagonal, mut_rope_on_v, mut_cache_pre_rope, mut_no_max, mut_rope_halves,
            mut_rope_freq, mut_rope_sign, mut_eps_outside, mut_gqa_modulo, mut_scale_dh,
            mut_no_residual, mut_silu_sign, mut_gate_up_swapped]
 
