@@ -237,14 +237,17 @@ def quantize_rows(x: np.ndarray):
     the cache itself can be quantised to int8.  Here every cached row (one
     token of one KV head, dh values) gets the scale s = max|x| / 127 and codes
     q = round(x / s) in [-127, 127] (ties to even); a zero row has s = 0 and
-    q = 0.  Returns (q int8 [..., dh], s [...]).
+    q = 0.  The pages fix no precision for this step, so the scale is an fp32
+    number (the cache stores it as one) and the division and the rounding are
+    done on the fp32 row: the decision of every code is an fp32 one.
+    Returns (q int8 [..., dh], s [...] as float64 holding the fp32 values).
     """
-    x = np.asarray(x, F64)
-    s = np.max(np.abs(x), axis=-1) / 127.0
-    safe = np.where(s > 0, s, 1.0)
-    q = np.clip(np.rint(x / safe[..., None]), -127, 127)
+    x32 = np.asarray(x, F64).astype(np.float32)
+    s = np.max(np.abs(x32), axis=-1) / np.float32(127.0)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    q = np.clip(np.rint(x32 / safe[..., None]), -127, 127)
     q = np.where(s[..., None] > 0, q, 0.0)
-    return q.astype(np.int8), s
+    return q.astype(np.int8), s.astype(F64)
 
 
 def dequantize_rows(q: np.ndarray, s: np.ndarray) -> np.ndarray:

@@ -285,17 +285,22 @@ def check_int8_rows():
     x[5] = 0.0
     q, s = ob.quantize_rows(x)
     assert q.dtype == np.int8 and s.shape == (6,)
-    np.testing.assert_allclose(s[:5], np.max(np.abs(x[:5]), axis=1) / 127, rtol=1e-15)
+    # the scale is the fp32 number max|x|/127 (two fp32 roundings from the exact quotient)
+    np.testing.assert_allclose(s[:5], np.max(np.abs(x[:5]), axis=1) / 127, rtol=2.5e-7)
     # the largest element of a row maps to ±127; every element is within s/2
     for r in range(5):
         assert abs(int(q[r, np.argmax(np.abs(x[r]))])) == 127
-        assert np.all(np.abs(ob.dequantize_rows(q, s)[r] - x[r]) <= s[r] / 2 * (1 + 1e-12))
+        assert np.all(np.abs(ob.dequantize_rows(q, s)[r] - x[r]) <= s[r] / 2 * (1 + 1e-4))
     assert s[5] == 0 and not q[5].any()
     # rows built from codes and a scale come back exactly
     codes = RNG.integers(-127, 128, size=(3, 16)); codes[:, 0] = 127
     q2, s2 = ob.quantize_rows(codes * 0.25)
     np.testing.assert_array_equal(q2, codes)
     np.testing.assert_array_equal(s2, 0.25)
+    # halfway values go to the even code: x/s = 0.5, 1.5, 2.5, -0.5, -1.5 with s = 0.25
+    q3, s3 = ob.quantize_rows(np.array([31.75, 0.125, 0.375, 0.625, -0.125, -0.375]))
+    assert s3 == 0.25
+    np.testing.assert_array_equal(q3, [127, 0, 2, 2, 0, -2])
 
 
 def check_int8_decode_close_to_exact():
@@ -607,7 +612,18 @@ def mut_int8_one_scale(monkeypatch):
     monkeypatch.setattr(ob, "quantize_rows", quant)
 
 
-MUTANTS = [mut_int8_floor, mut_int8_scale_128, mut_int8_one_scale, mut_paged_offset, mut_window_one_more, mut_window_decode_ignored, mut_diagonal, mut_rope_on_v, mut_cache_pre_rope, mut_no_max, mut_rope_halves,
+def mut_int8_half_away(monkeypatch):
+    # round half away from zero instead of to even
+    def quant(x):
+        x = np.asarray(x, np.float64)
+        s = np.max(np.abs(x), axis=-1) / 127.0
+        safe = np.where(s > 0, s, 1.0)
+        y = x / safe[..., None]
+        return np.clip(np.sign(y) * np.floor(np.abs(y) + 0.5), -127, 127).astype(np.int8), s
+    monkeypatch.setattr(ob, "quantize_rows", quant)
+
+
+MUTANTS = [mut_int8_half_away, mut_int8_floor, mut_int8_scale_128, mut_int8_one_scale, mut_paged_offset, mut_window_one_more, mut_window_decode_ignored, mut_diagonal, mut_rope_on_v, mut_cache_pre_rope, mut_no_max, mut_rope_halves,
            mut_rope_freq, mut_rope_sign, mut_eps_outside, mut_gqa_modulo, mut_scale_dh,
            mut_no_residual, mut_silu_sign, mut_gate_up_swapped]
 
