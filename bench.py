@@ -542,6 +542,82 @@ def bench_paged(args, world, peaks):
             "gpu_launches": decode_launches(s.B) * n}
 
 
+def bench_int8(args, world, peaks):
+    """A decode step of the decode workload over an int8 cache: the same rows
+    as the bf16 decode line, quantised into the cache through the C ABI's
+    append, timed over args.steps eager steps and as a replayed CUDA graph."""
+    import torch
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
+    from causal_gqa_attention_rmsnorm_gb300 import binding
+    import workloads
+
+    s = workloads.CONFIGS[args.decode_workload]
+    inp = workloads.make_block_inputs(s, seed=0)
+    dev = {k: t.cuda() for k, t in inp.items()}
+    lens = workloads.make_lens(s, seed=0)
+    kc, vc = workloads.make_decode_cache(s, 0, lens, fill=0.0, device="cuda")
+    kv = tb.KVCache.empty_int8(s.B, s.Hkv, s.T, s.dh)
+    tb.tb_kvcache_append(kv, kc, vc)                 # quantise every row of the bf16 cache
+    del kc, vc
+    lens0 = lens.cuda()
+    cfg = tb.BlockConfig(s.d, s.H, s.Hkv, s.dh, s.f, s.T, s.rope_base, s.eps, tb.TB_BF16)
+    packed = tb.tb_pack_weights(cfg, dev)
+    y = torch.empty((s.B, 1, s.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(tb.tb_workspace_bytes(cfg, s.B, s.T, 1), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kv.lens.copy_(lens0, non_blocking=True)
+        tb.tb_block_decode(cfg, packed, dev["x"], kv, y=y, ws=ws)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert tb.tb_get_device_error(clear=True) == 0
+    n = max(args.steps, 20)
+    binding.tbx_trace_enable(n)
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    stages = stage_stats([binding.tbx_trace_read(i) for i in range(n)])
+    binding.tbx_trace_enable(0)
+    assert tb.tb_get_device_error(clear=True) == 0 and torch.isfinite(y).all().item()
+    ms = max_over_ranks(a.elapsed_time(b), world) / n
+    graph_ms = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        a.record(stream)
+        for _ in range(n):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = max_over_ranks(a.elapsed_time(b), world) / n
+        assert torch.isfinite(y).all().item()
+    kv_bytes = acc.decode_kv_bytes(lens.tolist(), s.Hkv, s.dh, 1, scale_bytes=4)
+    return {"workload": s.name, "step_ms": ms, "tok_s": world * s.B / (ms * 1e-3), "attn_ms": stages["attn"],
+            "quant_ms": stages["quant"], "kv_bytes": kv_bytes, "kv_gbs": kv_bytes / (stages["attn"] * 1e-3) / 1e9,
+            "kv_frac_hbm": kv_bytes / (stages["attn"] * 1e-3) / 1e9 / peaks["hbm_gbs"], "stages_ms": stages,
+            "graph_step_ms": graph_ms,
+            "graph_tok_s": None if graph_ms is None else world * s.B / (graph_ms * 1e-3),
+            "gpu_launches": (decode_launches(s.B) + 1) * n}
+
+
 def bench_stack(args, world, peaks):
     """An args.stack_layers-layer model of the prefill workload's block shape:
     the embedding gather, the stack, and the LM head's chunked per-token loss
@@ -665,6 +741,7 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the decode step")
     ap.add_argument("--window", type=int, default=4096, help="sliding-window width of the extra window line (0: skip)")
     ap.add_argument("--page-size", type=int, default=16, help="page size of the paged-cache decode line (0: skip)")
+    ap.add_argument("--no-int8", action="store_true", help="skip the int8-cache decode line")
     ap.add_argument("--stack-layers", type=int, default=4, help="layers of the model line (0: skip)")
     ap.add_argument("--vocab", type=int, default=128256, help="vocabulary of the model line's LM head")
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
@@ -698,6 +775,7 @@ def main():
     dec = None if args.no_decode else bench_decode(args, world, peaks)
     win = None if (args.window <= 0 or args.no_decode) else bench_window(args, world, peaks)
     pag = None if (args.page_size <= 0 or args.no_decode) else bench_paged(args, world, peaks)
+    i8 = None if (args.no_int8 or args.no_decode) else bench_int8(args, world, peaks)
     stk = None if (args.stack_layers <= 0 or args.no_decode) else bench_stack(args, world, peaks)
 
     from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
@@ -728,6 +806,7 @@ def main():
         "decode": dec,
         "sliding_window": win,
         "paged_kv": pag,
+        "int8_kv": i8,
         "model": stk,
         "peaks": {"source": peak_src, "bf16_tflops": peaks["bf16_tflops"],
                   "bf16_tflops_sustained": peaks["bf16_tflops_sustained"], "hbm_gbs": peaks["hbm_gbs"]},

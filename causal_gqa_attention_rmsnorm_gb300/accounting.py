@@ -82,9 +82,11 @@ def attended_keys(lens: Iterable[int], window: int = 0) -> int:
     return sum(min(int(n) + 1, window) if window > 0 else int(n) + 1 for n in lens)
 
 
-def decode_kv_bytes(lens: Iterable[int], Hkv: int, dh: int, bytes_per_value: int, window: int = 0) -> int:
-    """KV bytes one decode step must read: the attended rows of K and V."""
-    return attended_keys(lens, window) * kv_bytes_per_token(1, Hkv, dh, bytes_per_value)
+def decode_kv_bytes(lens: Iterable[int], Hkv: int, dh: int, bytes_per_value: int, window: int = 0,
+                    scale_bytes: int = 0) -> int:
+    """KV bytes one decode step must read: the attended rows of K and V, and
+    for a quantised cache each row's scale (scale_bytes per row of K and of V)."""
+    return attended_keys(lens, window) * (kv_bytes_per_token(1, Hkv, dh, bytes_per_value) + 2 * Hkv * scale_bytes)
 
 
 def weight_bytes(d: int, H: int, Hkv: int, dh: int, f: int, bytes_per_value: int) -> int:

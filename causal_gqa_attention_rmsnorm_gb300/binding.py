@@ -18,7 +18,7 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtb.so")
 
-TB_F32, TB_BF16 = 0, 1
+TB_F32, TB_BF16, TB_I8 = 0, 1, 2
 TB_DEVERR_CACHE_FULL, TB_DEVERR_TIMEOUT, TB_DEVERR_BAD_PAGE, TB_DEVERR_BAD_TOKEN = 1, 2, 4, 8
 STATUS = {0: "TB_OK", 1: "TB_ERR_INVALID_ARG", 2: "TB_ERR_UNSUPPORTED", 3: "TB_ERR_CUDA",
           4: "TB_ERR_CACHE_FULL", 5: "TB_ERR_TIMEOUT"}
@@ -43,7 +43,7 @@ class tb_block_weights(ctypes.Structure):
 class tb_kvcache(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("lens", c_void_p), ("B", c_int32), ("Hkv", c_int32),
                 ("T_max", c_int32), ("dh", c_int32), ("dtype", c_int32), ("block_table", c_void_p),
-                ("page_size", c_int32), ("num_pages", c_int32)]
+                ("page_size", c_int32), ("num_pages", c_int32), ("k_scale", c_void_p), ("v_scale", c_void_p)]
 
 
 class tb_head_cfg(ctypes.Structure):
@@ -146,11 +146,15 @@ class BlockConfig:
 class KVCache:
     """Caller-owned cache tensors.  Contiguous: k, v [B, Hkv, T_max, dh].
     Paged (block_table given): k, v page pools [num_pages, Hkv, page_size, dh]
-    and block_table int32 [B, T_max / page_size].  lens int32 [B]."""
+    and block_table int32 [B, T_max / page_size].  int8 (k, v of torch.int8):
+    codes [B, Hkv, T_max, dh] with fp32 row scales k_scale, v_scale
+    [B, Hkv, T_max].  lens int32 [B]."""
     k: torch.Tensor
     v: torch.Tensor
     lens: torch.Tensor
     block_table: Optional[torch.Tensor] = None
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
 
     def c(self) -> tb_kvcache:
         for t in (self.k, self.v):
@@ -158,7 +162,9 @@ class KVCache:
                 raise ValueError("cache tensors must be contiguous CUDA tensors")
         if self.v.shape != self.k.shape or self.v.dtype != self.k.dtype:
             raise ValueError("k and v caches must match")
-        dt = TB_F32 if self.k.dtype == torch.float32 else TB_BF16
+        dt = {torch.float32: TB_F32, torch.bfloat16: TB_BF16, torch.int8: TB_I8}.get(self.k.dtype)
+        if dt is None:
+            raise ValueError(f"cache dtype {self.k.dtype} is not float32, bfloat16 or int8")
         if self.block_table is None:
             B, Hkv, T_max, dh = self.k.shape
             bt, ps, npages = None, 0, 0
@@ -170,8 +176,15 @@ class KVCache:
             B, T_max = bt.shape[0], bt.shape[1] * ps
         if not (self.lens.is_cuda and self.lens.dtype == torch.int32 and self.lens.numel() == B):
             raise ValueError("lens must be a CUDA int32 tensor of B entries")
+        ks = vs = None
+        if dt == TB_I8:
+            for name, t in (("k_scale", self.k_scale), ("v_scale", self.v_scale)):
+                if t is None:
+                    raise ValueError(f"an int8 cache needs {name}")
+                _need(t, name, torch.float32, (B, Hkv, T_max))
+            ks, vs = self.k_scale.data_ptr(), self.v_scale.data_ptr()
         return tb_kvcache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(), B, Hkv, T_max, dh, dt,
-                          None if bt is None else bt.data_ptr(), ps, npages)
+                          None if bt is None else bt.data_ptr(), ps, npages, ks, vs)
 
     @property
     def T_max(self) -> int:
@@ -182,6 +195,19 @@ class KVCache:
         mk = (lambda: torch.full((B, Hkv, T_max, dh), fill, dtype=dtype, device=device)) if fill is not None \
             else (lambda: torch.empty((B, Hkv, T_max, dh), dtype=dtype, device=device))
         return KVCache(mk(), mk(), torch.zeros(B, dtype=torch.int32, device=device))
+
+    @staticmethod
+    def empty_int8(B: int, Hkv: int, T_max: int, dh: int = 128, device="cuda") -> "KVCache":
+        """Zeroed int8 codes and scales (every row reads back as 0)."""
+        codes = lambda: torch.zeros((B, Hkv, T_max, dh), dtype=torch.int8, device=device)
+        scales = lambda: torch.zeros((B, Hkv, T_max), dtype=torch.float32, device=device)
+        return KVCache(codes(), codes(), torch.zeros(B, dtype=torch.int32, device=device), None, scales(), scales())
+
+    def dequantized(self):
+        """(k, v) of an int8 cache as fp32 code·scale, [B, Hkv, T_max, dh]."""
+        if self.k.dtype != torch.int8:
+            raise ValueError("not an int8 cache")
+        return (self.k.float() * self.k_scale[..., None], self.v.float() * self.v_scale[..., None])
 
     @staticmethod
     def empty_paged(B: int, Hkv: int, T_max: int, dh: int, page_size: int, num_pages: int, block_table: torch.Tensor,
@@ -307,12 +333,14 @@ def tb_block_decode_noalloc(cfg: BlockConfig, packed: torch.Tensor, x: torch.Ten
 
 
 def tb_kvcache_append(kv: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
-    """Append k_new, v_new [B, Hkv, n, dh] at rows lens[b].. of each sequence."""
+    """Append k_new, v_new [B, Hkv, n, dh] at rows lens[b].. of each sequence
+    (bf16 rows for an int8 cache, quantised as they are stored)."""
     kvs = kv.c()
     n = k_new.shape[2]
     shape = (kvs.B, kvs.Hkv, n, kvs.dh)
-    _need(k_new, "k_new", kv.k.dtype, shape)
-    _need(v_new, "v_new", kv.k.dtype, shape)
+    row_dtype = torch.bfloat16 if kv.k.dtype == torch.int8 else kv.k.dtype
+    _need(k_new, "k_new", row_dtype, shape)
+    _need(v_new, "v_new", row_dtype, shape)
     _check("tb_kvcache_append", lib().tb_kvcache_append(ctypes.byref(kvs), k_new.data_ptr(), v_new.data_ptr(), n,
                                                         _stream(stream)))
 

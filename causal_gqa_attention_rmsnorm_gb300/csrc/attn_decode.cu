@@ -594,6 +594,379 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// int8-cache streaming kernel (dh = 128)
+// ---------------------------------------------------------------------------
+//
+// Same work items, queue and chunk states as k_decode_mma, over a cache of
+// int8 codes with one fp32 scale per row (a row reads back as code·scale).  A
+// 16-key stage is 2 KB of K codes and 2 KB of V codes, half a bf16 stage, so a
+// warp keeps six stages in shared memory where the bf16 kernel keeps three,
+// plus the stage's 32 row scales (two 64-byte bulk copies).
+//
+// Both contractions are fp16 m16n8k16 MMAs with fp32 accumulators.  A code c
+// becomes an exact fp16 integer in registers: after XOR 0x80 its byte is
+// u = c + 128, the fp16 bit pattern 0x6400 | u is 1024 + u, and subtracting
+// 1152 leaves c.  Two codes per PRMT + HSUB2.
+//   S = Q·Kᵀ: ldmatrix gives lane (g, t) four consecutive codes of key g
+//   (dims 16p+4t .. 16p+4t+3); the MMA's k index is mapped onto dims so that
+//   those four are its two k pairs, and Q's fragment is loaded with the same
+//   map (a dot product does not depend on the order of its terms).  Q is
+//   converted to fp16 once per item with a power-of-two scale per head that
+//   puts its largest element in [0.5, 1), so every bf16 query fits.
+//   O += P·V: ldmatrix.trans on 16-bit units gives lane (g, t) the codes of
+//   keys 2t and 2t+1 at dims 2g and 2g+1; a PRMT pairs them per dimension, so
+//   one load feeds the n-tile of even dims and the n-tile of odd dims.
+// The K scales multiply the fp32 scores.  The V scales multiply P before P is
+// rounded to fp16, inside a power-of-two frame vf (the accumulators hold
+// vf·O) chosen so that the stage's largest visible scale times vf lies in
+// [1/16, 16]: P·scale·vf then stays far from fp16's overflow and underflow
+// whatever the magnitude of V.  The frame moves like the softmax maximum,
+// rarely, and both rescale O by exact factors.
+constexpr int kQSlots = 6;
+struct QCfg {
+  static constexpr uint32_t BOX = kMKeys * 128;        // 16 rows x 128 codes
+  static constexpr uint32_t SLOT = 2 * BOX;            // K codes, then V codes
+  static constexpr uint32_t WARP_BYTES = kQSlots * SLOT;
+  static constexpr uint32_t SC = 2 * kMKeys * 4;       // K then V scales of one stage
+  static constexpr uint32_t TX = SLOT + SC;            // bytes one stage brings in
+  static constexpr uint32_t OFF_SC = kMWarps * WARP_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_SC + kMWarps * kQSlots * SC;
+  static constexpr uint32_t OFF_PRE = OFF_BAR + kMWarps * kQSlots * 8;
+};
+
+// D = A·B + D, m16n8k16, fp16 inputs, fp32 accumulators; rows 8..15 of A are zero.
+__device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// The two codes of `w` (already XORed with 0x80808080) that `sel` picks, as an
+// fp16 pair (sel's nibbles 4 insert the byte 0x64).
+__device__ __forceinline__ uint32_t codes_f16x2(uint32_t w, uint32_t sel) {
+  const uint32_t h = __byte_perm(w, 0x64646464u, sel);
+  uint32_t d;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(0x64806480u));
+  return d;
+}
+
+// 2^-e with x·2^-e in [0.5, 1) for a normal x > 0 (read off the exponent
+// field), clamped to normal powers of two; 1 for x <= 0 or NaN.
+__device__ __forceinline__ float pow2_frame(float x) {
+  if (!(x > 0.f)) return 1.f;
+  int e = (int)((__float_as_uint(x) >> 23) & 0xffu) - 126;
+  e = max(-126, min(126, e));
+  return __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
+// 16-byte piece `chunk` of row `row` of a 16-row x 128-byte stage written by
+// TMA with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz128(uint32_t base, int row, int chunk) {
+  return base + row * 128 + (((chunk ^ row) & 7) << 4);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kMWarps * 32, 1)
+    k_decode_mma_i8(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const float* __restrict__ kscale, const float* __restrict__ vscale, const bf16* __restrict__ q,
+                    const int32_t* __restrict__ pos_arr, int B, int Hkv, int T_max, float* __restrict__ part,
+                    int nchunk_max, int* __restrict__ counter, int window, float scale_log2, int* err) {
+  constexpr int DH = 128;
+  using C = QCfg;
+  using namespace ptx;
+  static_assert(G <= 8, "at most 8 query heads per KV head");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
+  __shared__ int abort_word;
+
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+      pre[b] = acc;
+      const int p = pos_arr[b];
+      acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kMKeys) + kMChunk - 1) / kMChunk);
+    }
+    pre[B] = acc;
+    abort_word = 0;
+  }
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * kQSlots;
+  if (lane == 0) {
+    for (int i = 0; i < kQSlots; ++i) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int* abort_flag = &abort_word;
+  const int total = pre[B];
+  const int H = Hkv * G;
+  uint8_t* slots = smem + warp * C::WARP_BYTES;
+  float* scales = reinterpret_cast<float*>(smem + C::OFF_SC + warp * kQSlots * C::SC);
+  const uint32_t slots_u32 = smem_u32(slots);
+
+  struct Item { int b, kvh, c, key0, nkeys, first; };
+  auto decode = [&](int id) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= id) lo = mid; else hi = mid - 1;
+    }
+    const int n = pos_arr[lo] + 1;
+    const int base = chunk_base(n, window, kMKeys);
+    const int nch = (n - base + kMChunk - 1) / kMChunk;
+    const int r = id - pre[lo];
+    Item it;
+    it.b = lo;
+    it.kvh = r / nch;
+    it.c = r - it.kvh * nch;
+    it.key0 = base + it.c * kMChunk;
+    it.nkeys = min(kMChunk, n - it.key0);
+    it.first = window_first(n, window);
+    return it;
+  };
+
+  // ---- lane 0: item queue and stage producer ----
+  int queue[4] = {0, 0, 0, 0};
+  int qn = 0, reserve = 0, pidx = 0, pst = 0;
+  uint32_t issued = 0, consumed = 0;
+  bool stream_done = false;
+  auto push = [&]() {
+    queue[qn++] = reserve;
+    reserve = atomicAdd(counter, 1);
+  };
+  auto issue_one = [&]() {
+    while (!stream_done) {
+      if (pidx >= qn) push();
+      const int id = queue[pidx];
+      if (id >= total) {
+        stream_done = true;
+        return;
+      }
+      const Item it = decode(id);
+      const int nst = (it.nkeys + kMKeys - 1) / kMKeys;
+      if (pst < nst) {
+        const int sl = issued % kQSlots;
+        uint8_t* base = slots + sl * C::SLOT;
+        float* sc = scales + sl * (C::SC / 4);
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&full[sl], C::TX);
+        // key + 16 <= T_max: keys start on 16-row boundaries below n <= T_max, T_max % 16 == 0
+        const int key = it.key0 + pst * kMKeys, plane = it.b * Hkv + it.kvh;
+        tma_load_3d(&tmK, base, &full[sl], 0, key, plane);
+        tma_load_3d(&tmV, base + C::BOX, &full[sl], 0, key, plane);
+        const size_t srow = (size_t)plane * T_max + key;
+        bulk_load(sc, kscale + srow, kMKeys * 4, &full[sl]);
+        bulk_load(sc + kMKeys, vscale + srow, kMKeys * 4, &full[sl]);
+        ++pst;
+        ++issued;
+        return;
+      }
+      ++pidx;
+      pst = 0;
+    }
+  };
+  if (lane == 0) {
+    reserve = atomicAdd(counter, 1);
+    push();
+  }
+
+  bool ok = true;
+  while (ok) {
+    const int cur = __shfl_sync(0xffffffffu, queue[0], 0);
+    if (cur >= total) break;
+    const Item it = decode(cur);
+    const int nst = (it.nkeys + kMKeys - 1) / kMKeys;
+    // Q fragments of head g (rows >= G are zero): dims 16p + 4t .. 16p + 4t + 3 of
+    // 16-dim slice p, in fp16 after the head's power-of-two scale qf
+    uint32_t qa0[DH / 16], qa2[DH / 16];
+    float cq;   // log2(e)/sqrt(dh) / qf: turns a raw score (times the K scale) into log2 units
+    {
+      const bf16* qrow = q + ((size_t)it.b * H + it.kvh * G + (g < G ? g : 0)) * DH + 4 * t;
+      float qv[DH / 16][4];
+      float amax = 0.f;
+#pragma unroll
+      for (int p = 0; p < DH / 16; ++p) {
+        const uint2 raw = g < G ? *reinterpret_cast<const uint2*>(qrow + 16 * p) : make_uint2(0u, 0u);
+        qv[p][0] = __uint_as_float(raw.x << 16);
+        qv[p][1] = __uint_as_float(raw.x & 0xffff0000u);
+        qv[p][2] = __uint_as_float(raw.y << 16);
+        qv[p][3] = __uint_as_float(raw.y & 0xffff0000u);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(qv[p][0]), fabsf(qv[p][1])), fmaxf(fabsf(qv[p][2]), fabsf(qv[p][3]))));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const float qf = pow2_frame(amax);
+      cq = scale_log2 / qf;
+#pragma unroll
+      for (int p = 0; p < DH / 16; ++p) {
+        qa0[p] = pack_f16(qv[p][0] * qf, qv[p][1] * qf);
+        qa2[p] = pack_f16(qv[p][2] * qf, qv[p][3] * qf);
+      }
+    }
+    float o[DH / 8][4];
+#pragma unroll
+    for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_used = -INFINITY, lsum = 0.f, vf = 1.f;
+
+    for (int st = 0; st < nst; ++st) {
+      if (lane == 0)
+        while (!stream_done && issued < consumed + kQSlots) issue_one();
+      const int sl = consumed % kQSlots;
+      if (!mbar_wait_warp(&full[sl], (consumed / kQSlots) & 1, abort_flag, err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t ks_base = slots_u32 + sl * C::SLOT, vs_base = ks_base + C::BOX;
+      const float* sc = scales + sl * (C::SC / 4);
+      const int nvalid = min(kMKeys, it.nkeys - st * kMKeys);
+      const int mi = lane >> 3, lrow = (lane & 7) + 8 * (mi & 1);
+
+      // S = Q·Kᵀ for keys 0-7 (s0) and 8-15 (s1)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int pp = 0; pp < DH / 32; ++pp) {
+        uint32_t kb[4];
+        ldsm_x4(swz128(ks_base, lrow, 2 * pp + (mi >> 1)), kb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) kb[j] ^= 0x80808080u;
+        mma16816_f16(s0, qa0[2 * pp], qa2[2 * pp], codes_f16x2(kb[0], 0x4140), codes_f16x2(kb[0], 0x4342));
+        mma16816_f16(s1, qa0[2 * pp], qa2[2 * pp], codes_f16x2(kb[1], 0x4140), codes_f16x2(kb[1], 0x4342));
+        mma16816_f16(s0, qa0[2 * pp + 1], qa2[2 * pp + 1], codes_f16x2(kb[2], 0x4140), codes_f16x2(kb[2], 0x4342));
+        mma16816_f16(s1, qa0[2 * pp + 1], qa2[2 * pp + 1], codes_f16x2(kb[3], 0x4140), codes_f16x2(kb[3], 0x4342));
+      }
+      // lane (g, t) holds the scores of keys 2t, 2t+1 (s0) and 8+2t, 9+2t (s1) for head g
+      const float2 kA = *reinterpret_cast<const float2*>(sc + 2 * t);
+      const float2 kB = *reinterpret_cast<const float2*>(sc + 8 + 2 * t);
+      const float2 vA = *reinterpret_cast<const float2*>(sc + kMKeys + 2 * t);
+      const float2 vB = *reinterpret_cast<const float2*>(sc + kMKeys + 8 + 2 * t);
+      const int lead = it.first - (it.key0 + st * kMKeys);   // keys below lead precede the window
+      const int k0 = 2 * t, k2 = 8 + 2 * t;
+      const bool ok0 = k0 < nvalid && k0 >= lead, ok1 = k0 + 1 < nvalid && k0 + 1 >= lead;
+      const bool ok2 = k2 < nvalid && k2 >= lead, ok3 = k2 + 1 < nvalid && k2 + 1 >= lead;
+      const float r0 = ok0 ? s0[0] * (kA.x * cq) : -INFINITY, r1 = ok1 ? s0[1] * (kA.y * cq) : -INFINITY;
+      const float r2 = ok2 ? s1[0] * (kB.x * cq) : -INFINITY, r3 = ok3 ? s1[1] * (kB.y * cq) : -INFINITY;
+      float mx = fmax3(r0, r1, fmaxf(r2, r3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_used, mx);      // finite: the stage has a visible key
+      const float w0 = ok0 ? vA.x : 0.f, w1 = ok1 ? vA.y : 0.f, w2 = ok2 ? vB.x : 0.f, w3 = ok3 ? vB.y : 0.f;
+      float vmax = fmaxf(fmaxf(w0, w1), fmaxf(w2, w3));
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+      const float vr = vmax * vf;
+      const bool new_frame = vr > 16.f || (vmax > 0.f && vr < 0.0625f);
+      const bool new_max = m_new > m_used + kRescaleLog2 || m_used == -INFINITY;
+      if (new_frame || new_max) {
+        float f = 1.f;
+        if (new_max) {
+          f = m_used == -INFINITY ? 0.f : ex2_approx(m_used - m_new);
+          lsum *= f;
+          m_used = m_new;
+        }
+        if (new_frame) {
+          const float vf_new = pow2_frame(vmax);
+          if (f != 0.f) f *= vf_new / vf;        // both powers of two: exact
+          vf = vf_new;
+        }
+#pragma unroll
+        for (int i = 0; i < DH / 8; ++i) {
+          o[i][0] *= f;
+          o[i][1] *= f;
+        }
+      }
+      const float p0 = ex2_approx(r0 - m_used), p1 = ex2_approx(r1 - m_used);
+      const float p2 = ex2_approx(r2 - m_used), p3 = ex2_approx(r3 - m_used);
+      lsum += (p0 + p1) + (p2 + p3);
+      const uint32_t pa0 = pack_f16(p0 * (w0 * vf), p1 * (w1 * vf));
+      const uint32_t pa2 = pack_f16(p2 * (w2 * vf), p3 * (w3 * vf));
+      // O += P·V: n-tiles 4pp, 4pp+1 = even, odd dims of slice 2pp; 4pp+2, 4pp+3 of slice 2pp+1
+#pragma unroll
+      for (int pp = 0; pp < DH / 32; ++pp) {
+        uint32_t vb[4];
+        ldsm_x4_t(swz128(vs_base, lrow, 2 * pp + (mi >> 1)), vb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) vb[j] ^= 0x80808080u;
+        mma16816_f16(o[4 * pp], pa0, pa2, codes_f16x2(vb[0], 0x4240), codes_f16x2(vb[1], 0x4240));
+        mma16816_f16(o[4 * pp + 1], pa0, pa2, codes_f16x2(vb[0], 0x4341), codes_f16x2(vb[1], 0x4341));
+        mma16816_f16(o[4 * pp + 2], pa0, pa2, codes_f16x2(vb[2], 0x4240), codes_f16x2(vb[3], 0x4240));
+        mma16816_f16(o[4 * pp + 3], pa0, pa2, codes_f16x2(vb[2], 0x4341), codes_f16x2(vb[3], 0x4341));
+      }
+      __syncwarp();           // the slot may be refilled after this
+      ++consumed;
+    }
+    if (!ok) break;
+    float l = lsum;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (g < G) {
+      // lane (g, t) holds dims 16p + 4t .. 16p + 4t + 3 of slice p: even tile n = 2t, odd 2t, even 2t+1, odd 2t+1
+      float* pr = part + (((size_t)it.b * H + it.kvh * G + g) * nchunk_max + it.c) * PartLayout<DH>::stride;
+      const float inv = 1.0f / vf;   // a power of two: exact
+#pragma unroll
+      for (int p = 0; p < DH / 16; ++p)
+        *reinterpret_cast<float4*>(pr + 4 + 16 * p + 4 * t) =
+            make_float4(o[2 * p][0] * inv, o[2 * p + 1][0] * inv, o[2 * p][1] * inv, o[2 * p + 1][1] * inv);
+      if (t == 0) {
+        pr[0] = m_used;
+        pr[1] = l;
+      }
+    }
+    if (lane == 0) {
+      queue[0] = queue[1];
+      queue[1] = queue[2];
+      queue[2] = queue[3];
+      --qn;
+      --pidx;
+    }
+  }
+  issued = __shfl_sync(0xffffffffu, issued, 0);
+  if (!ok && lane == 0) {
+    volatile int no_abort = 0;
+    for (uint32_t k = consumed; k < issued; ++k)
+      mbar_wait(&full[k % kQSlots], (k / kQSlots) & 1, &no_abort, err);
+  }
+}
+
+template <int G>
+cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
+                          const int32_t* pos, int B, int Hkv, int T_max, float* part, int nchunk_max, int* counter,
+                          int window, void* o, cudaStream_t s) {
+  using C = QCfg;
+  CUtensorMap tk, tv;
+  const uint64_t planes = (uint64_t)B * Hkv;
+  cudaError_t e = make_tmap_3d_u8(&tk, kc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kMKeys);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_3d_u8(&tv, vc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kMKeys);
+  if (e != cudaSuccess) return e;
+  const size_t smem = C::OFF_PRE + (size_t)(B + 1) * 4 + 1024;
+  if (smem > 232448) return cudaErrorInvalidValue;
+  static size_t attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || attr_set[dev] < smem) {
+    e = cudaFuncSetAttribute(k_decode_mma_i8<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = smem;
+  }
+  const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+  k_decode_mma_i8<G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, ks, vs, (const bf16*)q, pos, B, Hkv, T_max, part,
+                                                           nchunk_max, counter, window, scale_log2,
+                                                           device_error_word());
+  k_decode_combine<bf16, 128><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kMChunk, window,
+                                                                kMKeys, (bf16*)o);
+  return cudaGetLastError();
+}
+
 template <int DH, int G>
 cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
                        float* part, int nchunk_max, int* counter, int window, const PagedKV& pg, void* o,
@@ -680,6 +1053,18 @@ cudaError_t by_dh(int dh, int G, const void* q, const void* kc, const void* vc, 
 }  // namespace
 
 int decode_chunk_keys() { return kChunk; }
+
+cudaError_t attn_decode_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
+                           const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max,
+                           int* work_counter, int window, void* o, cudaStream_t s) {
+  switch (H / Hkv) {
+    case 1: return run_stream_i8<1>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
+    case 2: return run_stream_i8<2>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
+    case 4: return run_stream_i8<4>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
+    case 8: return run_stream_i8<8>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 size_t decode_part_floats(int B, int H, int dh, int nchunk_max) {
   return (size_t)B * H * nchunk_max * (dh + 4);

@@ -78,6 +78,11 @@ cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, 
                              int32_t* pos_out, int T_max, int* zero_word, int* err, cudaStream_t s);
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new,
                              int n, int* err, cudaStream_t s);
+// Quantise bf16 rows k_new, v_new [B, Hkv, rows, 128] into the int8 cache kv
+// at rows start[b] + r (start == nullptr: 0).  A sequence whose start is
+// negative or whose rows would pass T_max is skipped.
+cudaError_t launch_quantize_kv(const tb_kvcache& kv, const void* k_new, const void* v_new, int rows,
+                               const int32_t* start, cudaStream_t s);
 
 // A paged cache as kernels see it (bt == nullptr: none).  Row t of sequence b
 // lives in page bt[b·max_pages + t/ps] at offset t % ps of pools
@@ -113,6 +118,7 @@ struct QKVArgs {
   int kv_stride;           // rows per (b, kv head) in k/v
   const int32_t* pos;      // decode: position of sequence b (-1: skip); prefill: nullptr
   PagedKV pg;              // also (or, with k == nullptr, only) store k and v rows into this paged cache
+  bool kv_dense = false;   // k/v take the call's rows densely: row = token index in the call, not its position
 };
 struct WoArgs {
   const void* x;           // [M, d] residual input (cfg dtype)
@@ -190,5 +196,10 @@ size_t decode_part_floats(int B, int H, int dh, int nchunk_max);
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos,
                         int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max,
                         int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s);
+// Decode over an int8 cache (dh 128): codes kc, vc [B, Hkv, T_max, 128], row
+// scales ks, vs [B, Hkv, T_max]; bf16 q and o.
+cudaError_t attn_decode_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
+                           const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max,
+                           int* work_counter, int window, void* o, cudaStream_t s);
 
 }  // namespace tb

@@ -151,6 +151,49 @@ __global__ void k_append_bump(int32_t* __restrict__ lens, int B, int T_max, int 
   lens[b] = L + n;
 }
 
+// int8 cache rows ("The Transformer Architecture", thegeniusblogs, pitfalls:
+// the KV cache itself can be quantised to int8).  Each row of dh = 128 values
+// gets the scale s = max|x| / 127 and codes round-half-even(x / s) clamped to
+// [-127, 127]; s and x / s are fp32 operations (IEEE division), and a zero
+// row keeps s = 0 and zero codes.  One warp per row, four values per lane.
+__device__ __forceinline__ void quantize_row128(const bf16* __restrict__ x, int8_t* __restrict__ q,
+                                                float* __restrict__ s_out, int lane) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(x + lane * 4);
+  const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float s = m / 127.0f;
+  uint32_t packed = 0;
+  if (s > 0.f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = min(127, max(-127, __float2int_rn(v[i] / s)));
+      packed |= (uint32_t)(c & 0xff) << (8 * i);
+    }
+  }
+  *reinterpret_cast<uint32_t*>(q + lane * 4) = packed;
+  if (lane == 0) *s_out = s;
+}
+
+// k and v rows [B, Hkv, rows, 128] -> cache rows start[b] + r of codes
+// [B, Hkv, T_max, 128] and scales [B, Hkv, T_max].  A sequence whose start is
+// negative (a skipped decode row) or whose rows would pass T_max is left alone.
+__global__ void k_quantize_kv(const bf16* __restrict__ kn, const bf16* __restrict__ vn, int rows,
+                              const int32_t* __restrict__ start, int Hkv, int T_max, int8_t* __restrict__ kq,
+                              float* __restrict__ ks, int8_t* __restrict__ vq, float* __restrict__ vs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + warp, h = blockIdx.y, b = blockIdx.z;
+  if (r >= rows) return;
+  const int t0 = start ? start[b] : 0;
+  if (t0 < 0 || t0 + rows > T_max) return;
+  const size_t src = (((size_t)b * Hkv + h) * rows + r) * 128;
+  const size_t row = ((size_t)b * Hkv + h) * T_max + t0 + r;
+  quantize_row128(kn + src, kq + row * 128, ks + row, lane);
+  quantize_row128(vn + src, vq + row * 128, vs + row, lane);
+}
+
 template <typename T>
 void pack_all(const Dims& D, const tb_block_weights& w, const Packed& P, float rope_base, cudaStream_t s) {
   const dim3 blk(32, 8);
@@ -207,8 +250,25 @@ cudaError_t launch_pack_transpose(int dtype, const void* src, int K, int N, cons
   return cudaGetLastError();
 }
 
+cudaError_t launch_quantize_kv(const tb_kvcache& kv, const void* k_new, const void* v_new, int rows,
+                               const int32_t* start, cudaStream_t s) {
+  if (rows <= 0 || kv.B <= 0) return cudaSuccess;
+  if (kv.B > 65535 || kv.Hkv > 65535) return cudaErrorInvalidValue;
+  const int warps = std::min(rows, 8);
+  const dim3 grid((unsigned)((rows + warps - 1) / warps), kv.Hkv, kv.B);
+  k_quantize_kv<<<grid, 32 * warps, 0, s>>>((const bf16*)k_new, (const bf16*)v_new, rows, start, kv.Hkv, kv.T_max,
+                                            (int8_t*)kv.k, kv.k_scale, (int8_t*)kv.v, kv.v_scale);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new, int n,
                              int* err, cudaStream_t s) {
+  if (kv.dtype == TB_I8) {      // quantise the bf16 rows into place, then grow lens
+    const cudaError_t e = launch_quantize_kv(kv, k_new, v_new, n, kv.lens, s);
+    if (e != cudaSuccess) return e;
+    k_append_bump<<<(kv.B + 127) / 128, 128, 0, s>>>(kv.lens, kv.B, kv.T_max, n, err);
+    return cudaGetLastError();
+  }
   const int esz = dtype == TB_F32 ? 4 : 2;
   const int row_vecs = kv.dh * esz / 16;
   const size_t per_seq = (size_t)kv.Hkv * n * row_vecs;

@@ -64,7 +64,7 @@ struct EpiQKV {
   static constexpr bool kRowReduce = false;
   QKVArgs a;
   int H, Hkv, dh;
-  struct RowAux { float r; int b, t, qt; };
+  struct RowAux { float r; int b, t, qt, kt; };
   struct Aux { float2 c0, c1; };
   __device__ __forceinline__ RowAux row_aux(int row) const {
     RowAux ra;
@@ -73,6 +73,7 @@ struct EpiQKV {
     } else {
       ra.b = row / a.T; ra.t = row - ra.b * a.T; ra.qt = ra.t;
     }
+    ra.kt = a.kv_dense ? ra.qt : ra.t;
     ra.r = a.r[row];
     return ra;
   }
@@ -102,7 +103,7 @@ struct EpiQKV {
       const int h = (col - (is_k ? qn : qn + kn)) / dh;
       if (a.k) {
         T* base = (T*)(is_k ? a.k : a.v);
-        store4<T>(base + (((size_t)ra.b * Hkv + h) * a.kv_stride + ra.t) * dh + e, v);
+        store4<T>(base + (((size_t)ra.b * Hkv + h) * a.kv_stride + ra.kt) * dh + e, v);
       }
       if (a.pg.bt) {
         const long long row = paged_row(a.pg, Hkv, ra.b, h, ra.t);

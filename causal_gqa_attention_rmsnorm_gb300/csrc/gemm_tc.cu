@@ -364,19 +364,34 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
-                              uint64_t row_stride_elems, uint64_t plane_stride_elems, uint32_t box_cols,
-                              uint32_t box_rows) {
+namespace {
+cudaError_t make_tmap_3d(CUtensorMap* m, CUtensorMapDataType type, uint32_t esize, const void* base,
+                         uint64_t planes, uint64_t rows, uint64_t cols, uint64_t row_stride_elems,
+                         uint64_t plane_stride_elems, uint32_t box_cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {cols, rows, planes};
-  const cuuint64_t strides[2] = {row_stride_elems * 2, plane_stride_elems * 2};
+  const cuuint64_t strides[2] = {row_stride_elems * esize, plane_stride_elems * esize};
   const cuuint32_t box[3] = {box_cols, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(m, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+}  // namespace
+
+cudaError_t make_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
+                              uint64_t row_stride_elems, uint64_t plane_stride_elems, uint32_t box_cols,
+                              uint32_t box_rows) {
+  return make_tmap_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, planes, rows, cols, row_stride_elems,
+                      plane_stride_elems, box_cols, box_rows);
+}
+
+cudaError_t make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
+                            uint64_t row_stride, uint64_t plane_stride, uint32_t box_cols, uint32_t box_rows) {
+  return make_tmap_3d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, planes, rows, cols, row_stride, plane_stride,
+                      box_cols, box_rows);
 }
 
 cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,

@@ -16,6 +16,9 @@ cudaError_t make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t rows, u
 cudaError_t make_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
                               uint64_t row_stride_elems, uint64_t plane_stride_elems, uint32_t box_cols,
                               uint32_t box_rows);
+// 3-D byte tensor (int8 codes), strides in bytes, same box rules (box_cols must be 128).
+cudaError_t make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
+                            uint64_t row_stride, uint64_t plane_stride, uint32_t box_cols, uint32_t box_rows);
 int sm_count();
 
 cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,

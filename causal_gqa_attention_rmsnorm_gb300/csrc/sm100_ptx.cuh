@@ -108,6 +108,15 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* m, void* dst, uin
       : "memory");
 }
 
+// Untiled bulk copy of `bytes` bytes (a multiple of 16; both addresses 16-byte
+// aligned) from global memory into smem; the bytes complete on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(static_cast<uint64_t>(__cvta_generic_to_global(src))), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 2^x on the special-function unit (flush-to-zero; -inf gives 0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

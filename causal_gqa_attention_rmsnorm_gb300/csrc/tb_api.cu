@@ -154,10 +154,10 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
   w.pos = (int32_t*)take((size_t)B * 4);
   w.counter = (int*)take(4);
   w.q = take(M * hd * es);
-  if (mode == 0) {
-    w.k = take(M * kvd * es);
-    w.v = take(M * kvd * es);
-  }
+  // prefill: K/V of the call when no contiguous cache of the block's type
+  // takes them in place; decode: the new rows on their way into an int8 cache
+  w.k = take(M * kvd * es);
+  w.v = take(M * kvd * es);
   w.o = take(M * hd * es);
   w.h = (float*)take(M * c->d * 4);
   w.hb = c->dtype == TB_F32 ? (void*)w.h : take(M * c->d * es);
@@ -195,14 +195,30 @@ cudaError_t mm_w2(const Work& W, const void* A, const void* Bw, int M, int N, in
   return W.skpart ? gemm_skinny_w2(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_w2(A, Bw, M, N, K, D, e, s);
 }
 
+// The int8 layout's own rules (dh 128, contiguous, 16-row stages, scales).
+tb_status check_i8(const tb_kvcache* kv) {
+  if (kv->dh != 128) return fail(TB_ERR_UNSUPPORTED, "an int8 cache needs dh 128 (dh=%d)", kv->dh);
+  if (kv->block_table) return fail(TB_ERR_UNSUPPORTED, "an int8 cache is contiguous (no block table)");
+  if (kv->T_max % 16) return fail(TB_ERR_UNSUPPORTED, "an int8 cache needs T_max a multiple of 16 (%d)", kv->T_max);
+  if (!kv->k_scale || !kv->v_scale || !aligned16(kv->k_scale) || !aligned16(kv->v_scale))
+    return fail(TB_ERR_INVALID_ARG, "an int8 cache needs 16-byte aligned k_scale and v_scale");
+  return TB_OK;
+}
+
 tb_status check_kv(const tb_block_cfg* c, const tb_kvcache* kv, int B) {
   if (!kv->k || !kv->v || !kv->lens) return fail(TB_ERR_INVALID_ARG, "kv cache pointers must be non-NULL");
   if (kv->B != B) return fail(TB_ERR_INVALID_ARG, "kv->B (%d) differs from B (%d)", kv->B, B);
   if (kv->Hkv != c->Hkv || kv->dh != c->dh)
     return fail(TB_ERR_INVALID_ARG, "kv cache heads/width (%d, %d) differ from cfg (%d, %d)", kv->Hkv, kv->dh,
                 c->Hkv, c->dh);
-  if (kv->dtype != c->dtype) return fail(TB_ERR_INVALID_ARG, "kv cache dtype differs from cfg dtype");
   if (kv->T_max <= 0) return fail(TB_ERR_INVALID_ARG, "kv->T_max must be positive");
+  if (kv->dtype == TB_I8) {
+    const tb_status st = check_i8(kv);
+    if (st != TB_OK) return st;
+    if (c->dtype != TB_BF16) return fail(TB_ERR_UNSUPPORTED, "an int8 cache needs a bf16 block");
+  } else if (kv->dtype != c->dtype) {
+    return fail(TB_ERR_INVALID_ARG, "kv cache dtype differs from cfg dtype");
+  }
   if (!aligned16(kv->k) || !aligned16(kv->v) || ((uintptr_t)kv->lens & 3u))
     return fail(TB_ERR_INVALID_ARG, "kv cache pointers must be 16-byte aligned (lens 4-byte)");
   if (kv->block_table) {
@@ -339,8 +355,10 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
   const int dt = cfg->dtype;
   const int nqkv = (cfg->H + 2 * cfg->Hkv) * cfg->dh;
   // attention reads K/V from a contiguous cache in place, else from the
-  // workspace; a paged cache receives the rows as a second store
-  const bool contiguous_cache = kv && !kv->block_table;
+  // workspace; a paged cache receives the rows as a second store, an int8
+  // cache their codes
+  const bool i8_cache = kv && kv->dtype == TB_I8;
+  const bool contiguous_cache = kv && !kv->block_table && !i8_cache;
   void* kbuf = contiguous_cache ? kv->k : W.k;
   void* vbuf = contiguous_cache ? kv->v : W.v;
   const int kv_stride = contiguous_cache ? kv->T_max : T;
@@ -367,6 +385,10 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
   } else {
     rec.stage("qkv");
     TB_TRY(mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
+    if (i8_cache) {
+      rec.stage("quant");
+      TB_TRY(launch_quantize_kv(*kv, W.k, W.v, T, nullptr, s));
+    }
     rec.stage("attn");
     TB_TRY(attn_prefill_tc(W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, cfg->window, s));
     rec.stage("wo");
@@ -416,7 +438,11 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
   TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, W.ssq, 1, nullptr, kv->lens, W.pos, kv->T_max,
                           W.counter, err, s));
   const PagedKV pg = paged_of(kv, err);
-  const QKVArgs qa{W.r, P.rope, W.q, pg.bt ? nullptr : kv->k, pg.bt ? nullptr : kv->v, 1, kv->T_max, W.pos, pg};
+  // an int8 cache gets the new rows through the workspace and the quantiser
+  const bool i8 = kv->dtype == TB_I8;
+  void* knew = pg.bt ? nullptr : (i8 ? W.k : kv->k);
+  void* vnew = pg.bt ? nullptr : (i8 ? W.v : kv->v);
+  const QKVArgs qa{W.r, P.rope, W.q, knew, vnew, 1, i8 ? 1 : kv->T_max, W.pos, pg, i8};
   const WoArgs wa{x, W.h, W.hb, W.ssq};
   const W13Args ga{W.ssq, W.a};
   const W2Args ya{W.h, y, y_dtype};
@@ -435,9 +461,17 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
   } else {
     rec.stage("qkv");
     TB_TRY(mm_qkv(W, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
-    rec.stage("attn");
-    TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                       W.nchunk_max, W.counter, cfg->window, pg, W.o, s));
+    if (i8) {
+      rec.stage("quant");
+      TB_TRY(launch_quantize_kv(*kv, W.k, W.v, 1, W.pos, s));
+      rec.stage("attn");
+      TB_TRY(attn_decode_i8(W.q, kv->k, kv->v, kv->k_scale, kv->v_scale, W.pos, B, cfg->H, cfg->Hkv, kv->T_max,
+                            W.part, W.nchunk_max, W.counter, cfg->window, W.o, s));
+    } else {
+      rec.stage("attn");
+      TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
+                         W.nchunk_max, W.counter, cfg->window, pg, W.o, s));
+    }
     rec.stage("wo");
     TB_TRY(mm_wo(W, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
@@ -451,10 +485,16 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
 tb_status tb_kvcache_append(const tb_kvcache* kv, const void* k_new, const void* v_new, int32_t n, void* stream) {
   if (!kv) return fail(TB_ERR_INVALID_ARG, "kv is NULL");
   if (n < 0) return fail(TB_ERR_INVALID_ARG, "n must be non-negative");
-  if (kv->dtype != TB_F32 && kv->dtype != TB_BF16) return fail(TB_ERR_INVALID_ARG, "unknown kv dtype");
+  if (kv->dtype != TB_F32 && kv->dtype != TB_BF16 && kv->dtype != TB_I8)
+    return fail(TB_ERR_INVALID_ARG, "unknown kv dtype");
   if (kv->B < 0 || kv->Hkv <= 0 || kv->dh <= 0 || kv->T_max <= 0)
     return fail(TB_ERR_INVALID_ARG, "kv shape must be positive (B may be 0)");
-  if ((kv->dh * (int)esize(kv->dtype)) % 16) return fail(TB_ERR_UNSUPPORTED, "dh·sizeof must be a multiple of 16");
+  if (kv->dtype == TB_I8) {
+    const tb_status st = check_i8(kv);
+    if (st != TB_OK) return st;
+  } else if ((kv->dh * (int)esize(kv->dtype)) % 16) {
+    return fail(TB_ERR_UNSUPPORTED, "dh·sizeof must be a multiple of 16");
+  }
   if (n == 0 || kv->B == 0) return TB_OK;
   if (n > kv->T_max) return fail(TB_ERR_CACHE_FULL, "n (%d) exceeds T_max (%d)", n, kv->T_max);
   if (!kv->k || !kv->v || !kv->lens || !k_new || !v_new)

@@ -56,7 +56,9 @@ typedef enum {
   TB_ERR_TIMEOUT = 5        /* reserved for a host-side wait that ran out */
 } tb_status;
 
-typedef enum { TB_F32 = 0, TB_BF16 = 1 } tb_dtype;
+/* TB_I8 is a KV-cache storage type only (tb_kvcache.dtype): int8 codes with a
+ * per-row fp32 scale. */
+typedef enum { TB_F32 = 0, TB_BF16 = 1, TB_I8 = 2 } tb_dtype;
 
 /* Bits of the device error word (tb_get_device_error). */
 #define TB_DEVERR_CACHE_FULL 1  /* a decode/append row found lens[b] + n > T_max; that row was skipped */
@@ -101,8 +103,8 @@ typedef struct {
   const void *g_attn, *wq, *wk, *wv, *wo, *g_mlp, *w1, *w3, *w2;
 } tb_block_weights;
 
-/* KV cache of post-RoPE keys and values, in one of two layouts.
- *  Contiguous (block_table == NULL):
+/* KV cache of post-RoPE keys and values, in one of three layouts.
+ *  Contiguous (block_table == NULL, dtype == cfg.dtype):
  *    k, v  : device, cfg.dtype, [B, Hkv, T_max, dh] each, row-major.
  *  Paged (block_table != NULL), the cache allocated per sequence in fixed-size
  *  blocks ("Transformer block" page, implementation notes: paged KV cache):
@@ -113,8 +115,20 @@ typedef struct {
  *                  in [0, num_pages); a kernel that meets one outside that
  *                  range writes nothing through it and sets TB_DEVERR_BAD_PAGE.
  *    page_size   : a multiple of 16 that divides T_max.
+ *  int8 (dtype == TB_I8, block_table == NULL), the cache quantised to int8
+ *  ("The Transformer Architecture", thegeniusblogs, pitfalls: KV-cache OOM):
+ *    k, v              : device int8 codes [B, Hkv, T_max, dh], row-major.
+ *    k_scale, v_scale  : device fp32 [B, Hkv, T_max], one scale per row.
+ *    Row x (one token of one KV head) is stored as s = max|x| / 127 and codes
+ *    q = round-half-even(x / s) clamped to [-127, 127], s and x / s evaluated
+ *    in fp32 (a zero row: s = 0, q = 0); it reads back as q·s.  Only a bf16
+ *    block with dh = 128 and T_max a multiple of 16 takes an int8 cache.
+ *    Prefill attends over the unquantised rows and stores their codes; a
+ *    decode step stores the new token's codes first, then attends over the
+ *    dequantised rows, its own included.
  *  lens  : device int32 [B], the number of valid rows of each sequence.
- * Rows at or beyond lens[b] are never read. */
+ * Rows at or beyond lens[b] are never read.  k_scale and v_scale are ignored
+ * unless dtype == TB_I8. */
 typedef struct {
   void *k, *v;
   int32_t *lens;
@@ -122,6 +136,7 @@ typedef struct {
   int32_t dtype;
   const int32_t *block_table;
   int32_t page_size, num_pages;
+  float *k_scale, *v_scale;
 } tb_kvcache;
 
 /* Bytes the packed weight blob of tb_pack_weights needs. */
@@ -195,7 +210,8 @@ TB_API tb_status tb_block_decode_noalloc(const tb_block_cfg *cfg, const void *pa
                                          int32_t y_dtype, const tb_kvcache *kv, void *stream);
 
 /* Append n post-RoPE rows per sequence: k_new, v_new are device
- * [B, Hkv, n, dh] of kv->dtype; rows go to [lens[b], lens[b]+n) and lens[b]
+ * [B, Hkv, n, dh] of kv->dtype (bf16 for an int8 cache, whose rows are
+ * quantised as they are stored); rows go to [lens[b], lens[b]+n) and lens[b]
  * grows by n.  A sequence with lens[b] + n > T_max sets TB_DEVERR_CACHE_FULL
  * and is left unchanged.  n == 0 is a no-op. */
 TB_API tb_status tb_kvcache_append(const tb_kvcache *kv, const void *k_new, const void *v_new, int32_t n,

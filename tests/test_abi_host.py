@@ -130,6 +130,27 @@ def test_append_argument_checks(lib):
     assert lib.tb_kvcache_append(ctypes.byref(kv), None, FAKE, 3, None) == 1
 
 
+def test_int8_cache_checks(lib):
+    """An int8 cache takes a bf16 block with dh 128, a contiguous layout, T_max a
+    multiple of 16 and both scale arrays; anything else is refused before a launch."""
+    c = cfg(d=512, H=4, Hkv=2, dh=128)
+    decode = lambda kv, cc=c: lib.tb_block_decode(ctypes.byref(cc), FAKE, FAKE, FAKE + 4096, 0, ctypes.byref(kv),
+                                                  FAKE, 1 << 30, None)
+    i8 = lambda **k: binding.tb_kvcache(FAKE, FAKE, FAKE, 2, 2, k.get("T_max", 256), k.get("dh", 128), tb.TB_I8,
+                                        k.get("bt", None), k.get("ps", 0), k.get("np", 0), k.get("ks", FAKE),
+                                        k.get("vs", FAKE))
+    assert decode(i8(ks=None)) == 1 and b"k_scale" in lib.tb_last_error_message()
+    assert decode(i8(vs=FAKE + 4)) == 1                       # misaligned scales
+    assert decode(i8(T_max=250)) == 2                         # T_max not a multiple of 16
+    assert decode(i8(bt=FAKE, ps=16, np=8)) == 2              # no paged int8 layout
+    assert decode(i8(), cfg(d=512, H=4, Hkv=2, dh=128, dtype=tb.TB_F32)) == 2   # fp32 block
+    assert decode(i8(dh=64), cfg()) == 2                      # dh 64
+    # append: bf16 rows into the int8 layout, same rules
+    assert lib.tb_kvcache_append(ctypes.byref(i8(T_max=250)), FAKE, FAKE, 3, None) == 2
+    assert lib.tb_kvcache_append(ctypes.byref(i8(ks=None)), FAKE, FAKE, 3, None) == 1
+    assert lib.tb_kvcache_append(ctypes.byref(i8()), FAKE, FAKE, 300, None) == 4    # more rows than T_max
+
+
 def test_workspace_grows_with_tokens(lib):
     c = cfg()
     a = lib.tb_workspace_bytes(ctypes.byref(c), 1, 128, 0)

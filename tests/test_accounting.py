@@ -109,3 +109,11 @@ def test_window_pairs_and_keys():
     lens = [3, 0, 9000, 4095]
     assert acc.decode_kv_bytes(lens, 8, 128, 2, window=4096) == (4 + 1 + 4096 + 4096) * 4096
     assert acc.decode_kv_bytes(lens, 8, 128, 2, window=100000) == acc.decode_kv_bytes(lens, 8, 128, 2)
+
+
+def test_int8_kv_bytes():
+    # an int8 row of dh codes plus its fp32 scale, for K and V of every KV head
+    assert acc.decode_kv_bytes([3, 0], 8, 128, 1, scale_bytes=4) == (4 + 1) * 2 * 8 * (128 + 4)
+    # a little over half the bf16 read
+    r = acc.decode_kv_bytes([9000], 8, 128, 1, scale_bytes=4) / acc.decode_kv_bytes([9000], 8, 128, 2)
+    assert r == (128 + 4) / 256
