@@ -331,6 +331,13 @@ def roofline_entry(stages, work, peaks, peak_src, workload):
     return out
 
 
+def decode_shape(args):
+    """The decode workload, with B overridden by --decode-batch (profiling runs)."""
+    import workloads
+    s = workloads.CONFIGS[args.decode_workload]
+    return s.with_(name=f"{s.name}_b{args.decode_batch}", B=args.decode_batch) if args.decode_batch else s
+
+
 def bench_decode(args, world, peaks):
     import torch
     import causal_gqa_attention_rmsnorm_gb300 as tb
@@ -338,7 +345,7 @@ def bench_decode(args, world, peaks):
     from causal_gqa_attention_rmsnorm_gb300 import binding
     import workloads
 
-    s = workloads.CONFIGS[args.decode_workload]
+    s = decode_shape(args)
     inp = workloads.make_block_inputs(s, seed=0)
     dev = {n: t.cuda() for n, t in inp.items()}
     lens = workloads.make_lens(s, seed=0)
@@ -552,7 +559,7 @@ def bench_int8(args, world, peaks):
     from causal_gqa_attention_rmsnorm_gb300 import binding
     import workloads
 
-    s = workloads.CONFIGS[args.decode_workload]
+    s = decode_shape(args)
     inp = workloads.make_block_inputs(s, seed=0)
     dev = {k: t.cuda() for k, t in inp.items()}
     lens = workloads.make_lens(s, seed=0)
@@ -735,7 +742,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override B of the prefill workload (profiling runs)")
     ap.add_argument("--decode-workload", default="gqa_decode")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling runs); prints the decode object")
+    ap.add_argument("--decode-batch", type=int, default=0, help="override B of the decode lines (profiling runs)")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode lines only (profiling runs); prints the decode and int8 objects")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the decode step")
@@ -768,8 +777,9 @@ def main():
 
     if args.no_prefill:
         dec = bench_decode(args, world, peaks)
+        i8 = None if args.no_int8 else bench_int8(args, world, peaks)
         if rank == 0:
-            print(json.dumps({"decode": dec}))
+            print(json.dumps({"decode": dec, "int8_kv": i8}))
         return
     pre = bench_prefill(args, s, world, peaks)
     dec = None if args.no_decode else bench_decode(args, world, peaks)

@@ -425,6 +425,8 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
     queue[qn++] = reserve;
     reserve = atomicAdd(counter, 1);          // the reply is needed only at the next push
   };
+  Item pit{};                  // the producer's current item, decoded once
+  int pit_id = -1, pit_nst = 0;
   auto issue_one = [&]() {
     while (!stream_done) {
       if (pidx >= qn) push();
@@ -433,9 +435,13 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
         stream_done = true;
         return;
       }
-      const Item it = decode(id);
-      const int nst = (it.nkeys + kMKeys - 1) / kMKeys;
-      if (pst < nst) {
+      if (id != pit_id) {        // ids are unique: a new id is a new item
+        pit = decode(id);
+        pit_id = id;
+        pit_nst = (pit.nkeys + kMKeys - 1) / kMKeys;
+      }
+      const Item& it = pit;
+      if (pst < pit_nst) {
         const int sl = issued % kMSlots;
         uint8_t* base = slots + sl * C::SLOT;
         fence_proxy_async();       // earlier generic writes to the slot, before the TMA overwrite
@@ -744,6 +750,8 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
     queue[qn++] = reserve;
     reserve = atomicAdd(counter, 1);
   };
+  Item pit{};
+  int pit_id = -1, pit_nst = 0;
   auto issue_one = [&]() {
     while (!stream_done) {
       if (pidx >= qn) push();
@@ -752,9 +760,13 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
         stream_done = true;
         return;
       }
-      const Item it = decode(id);
-      const int nst = (it.nkeys + kMKeys - 1) / kMKeys;
-      if (pst < nst) {
+      if (id != pit_id) {
+        pit = decode(id);
+        pit_id = id;
+        pit_nst = (pit.nkeys + kMKeys - 1) / kMKeys;
+      }
+      const Item& it = pit;
+      if (pst < pit_nst) {
         const int sl = issued % kQSlots;
         uint8_t* base = slots + sl * C::SLOT;
         float* sc = scales + sl * (C::SC / 4);
