@@ -604,50 +604,73 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
 // int8-cache streaming kernel (dh = 128)
 // ---------------------------------------------------------------------------
 //
-// Same work items, queue and chunk states as k_decode_mma, over a cache of
-// int8 codes with one fp32 scale per row (a row reads back as code·scale).  A
-// 16-key stage is 2 KB of K codes and 2 KB of V codes, half a bf16 stage, so a
-// warp keeps six stages in shared memory where the bf16 kernel keeps three,
-// plus the stage's 32 row scales (two 64-byte bulk copies).
+// The same work items and chunk states as k_decode_mma, over a cache of int8
+// codes with one fp32 scale per row (a row reads back as code·scale).  A
+// 16-key stage is 2 KB of K codes and 2 KB of V codes, half a bf16 stage, plus
+// the stage's 32 row scales.
 //
-// Both contractions are fp16 m16n8k16 MMAs with fp32 accumulators.  A code c
-// becomes an exact fp16 integer in registers: after XOR 0x80 its byte is
-// u = c + 128, the fp16 bit pattern 0x6400 | u is 1024 + u, and subtracting
-// 1152 leaves c.  Two codes per PRMT + HSUB2.
-//   S = Q·Kᵀ: ldmatrix gives lane (g, t) four consecutive codes of key g
-//   (dims 16p+4t .. 16p+4t+3); the MMA's k index is mapped onto dims so that
-//   those four are its two k pairs, and Q's fragment is loaded with the same
-//   map (a dot product does not depend on the order of its terms).  Q is
-//   converted to fp16 once per item with a power-of-two scale per head that
-//   puts its largest element in [0.5, 1), so every bf16 query fits.
-//   O += P·V: ldmatrix.trans on 16-bit units gives lane (g, t) the codes of
-//   keys 2t and 2t+1 at dims 2g and 2g+1; a PRMT pairs them per dimension, so
-//   one load feeds the n-tile of even dims and the n-tile of odd dims.
-// The K scales multiply the fp32 scores.  The V scales multiply P before P is
+// Sixteen warps per CTA (the transposed layout below keeps a warp at 124
+// registers), each with a ring of three stage slots; as in the bf16 kernel,
+// lane 0 of each warp takes work items from the global counter and issues the
+// warp's own copies (two TMA boxes of codes, two 64-byte bulk copies of
+// scales), writing beside each slot which item and stage it holds so that the
+// warp never decodes an item.  Producers in every warp keep the copies spread
+// over all four schedulers; one producer warp for the whole CTA could not
+// issue them fast enough.
+//
+// Both contractions run transposed, on fp16 m16n8k16 MMAs with fp32
+// accumulators, so that the query heads sit on the MMA's n side (8 columns)
+// instead of padding its 16 rows:
+//   Sᵀ[16 keys × 8 heads] = K·Qᵀ.  ldmatrix gives lane (g, t) four
+//     consecutive codes of key g (dims 16p+4t .. 16p+4t+3); the MMA's k index
+//     is mapped onto dims so that those four are its two k pairs, and Q's
+//     fragment uses the same map (a dot product does not depend on the order
+//     of its terms).
+//   Oᵀ[16 dims × 8 heads] += Vᵀ·Pᵀ.  ldmatrix.trans on 16-bit units gives
+//     lane (g, t) the codes of keys 2t, 2t+1 at dims 2g, 2g+1: one word is the
+//     A fragment of rows g (dim 16p+2g) and g+8 (dim 16p+2g+1).  Pᵀ comes from
+//     Sᵀ's accumulator layout by one movmatrix transpose per 8 keys.
+// A code c enters the MMA as the fp16 number 1152 + c: after XOR 0x80 its
+// byte is u = c + 128, and the fp16 bit pattern 0x6400 | u is 1024 + u.  The
+// bias is removed after the products, exactly in the algebra and to fp32
+// rounding in the arithmetic: Σ_d q_d(c_d + 1152) - 1152·Σ_d q_d for the
+// scores, Σ_j P_j(c_j + 1152) - 1152·Σ_j P_j for the output, with the sums
+// taken over the fp16 values the MMA multiplies.
+// Q is converted to fp16 once per item with a power-of-two scale per head that
+// puts its largest element in [0.5, 1), so every bf16 query fits.  The K
+// scales multiply the fp32 scores.  The V scales multiply P before P is
 // rounded to fp16, inside a power-of-two frame vf (the accumulators hold
 // vf·O) chosen so that the stage's largest visible scale times vf lies in
 // [1/16, 16]: P·scale·vf then stays far from fp16's overflow and underflow
 // whatever the magnitude of V.  The frame moves like the softmax maximum,
 // rarely, and both rescale O by exact factors.
-constexpr int kQSlots = 6;
+constexpr int kQWarps = 16;      // warps per CTA, each its own producer
+constexpr int kQSlots = 3;       // stage slots per warp
+struct QDesc {
+  int4 a;                        // sequence, KV head, chunk, stage
+  int4 b;                        // first key of the chunk, its keys, first visible key, item id (-1: no more)
+};
 struct QCfg {
   static constexpr uint32_t BOX = kMKeys * 128;        // 16 rows x 128 codes
   static constexpr uint32_t SLOT = 2 * BOX;            // K codes, then V codes
   static constexpr uint32_t WARP_BYTES = kQSlots * SLOT;
   static constexpr uint32_t SC = 2 * kMKeys * 4;       // K then V scales of one stage
   static constexpr uint32_t TX = SLOT + SC;            // bytes one stage brings in
-  static constexpr uint32_t OFF_SC = kMWarps * WARP_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_SC + kMWarps * kQSlots * SC;
-  static constexpr uint32_t OFF_PRE = OFF_BAR + kMWarps * kQSlots * 8;
+  static constexpr uint32_t OFF_SC = kQWarps * WARP_BYTES;
+  static constexpr uint32_t OFF_DESC = OFF_SC + kQWarps * kQSlots * SC;
+  static constexpr uint32_t OFF_BAR = OFF_DESC + kQWarps * kQSlots * sizeof(QDesc);
+  static constexpr uint32_t OFF_PRE = OFF_BAR + kQWarps * kQSlots * 8;   // then pre[B + 1], nlen[B]
 };
+static_assert(QCfg::OFF_SC % 1024 == 0 && QCfg::OFF_DESC % 16 == 0 && QCfg::OFF_BAR % 8 == 0, "layout");
 
-// D = A·B + D, m16n8k16, fp16 inputs, fp32 accumulators; rows 8..15 of A are zero.
-__device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+// D = A·B + D, m16n8k16, fp16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -656,13 +679,23 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return d;
 }
 
-// The two codes of `w` (already XORed with 0x80808080) that `sel` picks, as an
-// fp16 pair (sel's nibbles 4 insert the byte 0x64).
-__device__ __forceinline__ uint32_t codes_f16x2(uint32_t w, uint32_t sel) {
-  const uint32_t h = __byte_perm(w, 0x64646464u, sel);
-  uint32_t d;
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(h), "r"(0x64806480u));
-  return d;
+__device__ __forceinline__ float2 unpack_f16(uint32_t h) {
+  float2 r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(h));
+  return r;
+}
+
+// The two codes of `w` (already XORed with 0x80808080) that `sel` picks, as the
+// fp16 pair 1152 + code (sel's nibbles 4 insert the byte 0x64).
+__device__ __forceinline__ uint32_t biased_f16x2(uint32_t w, uint32_t sel) { return __byte_perm(w, 0x64646464u, sel); }
+
+// Transpose of an 8x8 matrix of 16-bit elements held as MMA fragments.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 // 2^-e with x·2^-e in [0.5, 1) for a normal x > 0 (read off the exponent
@@ -681,20 +714,22 @@ __device__ __forceinline__ uint32_t swz128(uint32_t base, int row, int chunk) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kMWarps * 32, 1)
-    k_decode_mma_i8(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const float* __restrict__ kscale, const float* __restrict__ vscale, const bf16* __restrict__ q,
-                    const int32_t* __restrict__ pos_arr, int B, int Hkv, int T_max, float* __restrict__ part,
-                    int nchunk_max, int* __restrict__ counter, int window, float scale_log2, int* err) {
-  constexpr int DH = 128;
+__global__ void __launch_bounds__(kQWarps * 32, 1)
+    k_decode_i8(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const float* __restrict__ kscale, const float* __restrict__ vscale, const bf16* __restrict__ q,
+                const int32_t* __restrict__ pos_arr, int B, int Hkv, int T_max, float* __restrict__ part,
+                int nchunk_max, int* __restrict__ counter, int window, float scale_log2, int* err) {
+  constexpr int DH = 128, S = kQSlots;
   using C = QCfg;
   using namespace ptx;
   static_assert(G <= 8, "at most 8 query heads per KV head");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
   int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
+  int* nlen = pre + B + 1;           // keys of sequence b this step (0: skipped)
+  QDesc* desc = reinterpret_cast<QDesc*>(smem + C::OFF_DESC);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);   // [warp][slot]
   __shared__ int abort_word;
 
   if (threadIdx.x == 0) {
@@ -702,108 +737,108 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
     for (int b = 0; b < B; ++b) {
       pre[b] = acc;
       const int p = pos_arr[b];
+      nlen[b] = p < 0 ? 0 : p + 1;
       acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kMKeys) + kMChunk - 1) / kMChunk);
     }
     pre[B] = acc;
     abort_word = 0;
-  }
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + warp * kQSlots;
-  if (lane == 0) {
-    for (int i = 0; i < kQSlots; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kQWarps * S; ++i) mbar_init(&full[i], 1);
     fence_barrier_init();
   }
   __syncthreads();
   volatile int* abort_flag = &abort_word;
   const int total = pre[B];
   const int H = Hkv * G;
-  uint8_t* slots = smem + warp * C::WARP_BYTES;
-  float* scales = reinterpret_cast<float*>(smem + C::OFF_SC + warp * kQSlots * C::SC);
-  const uint32_t slots_u32 = smem_u32(slots);
 
-  struct Item { int b, kvh, c, key0, nkeys, first; };
-  auto decode = [&](int id) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= id) lo = mid; else hi = mid - 1;
-    }
-    const int n = pos_arr[lo] + 1;
-    const int base = chunk_base(n, window, kMKeys);
-    const int nch = (n - base + kMChunk - 1) / kMChunk;
-    const int r = id - pre[lo];
-    Item it;
-    it.b = lo;
-    it.kvh = r / nch;
-    it.c = r - it.kvh * nch;
-    it.key0 = base + it.c * kMChunk;
-    it.nkeys = min(kMChunk, n - it.key0);
-    it.first = window_first(n, window);
-    return it;
-  };
-
-  // ---- lane 0: item queue and stage producer ----
-  int queue[4] = {0, 0, 0, 0};
-  int qn = 0, reserve = 0, pidx = 0, pst = 0;
-  uint32_t issued = 0, consumed = 0;
-  bool stream_done = false;
-  auto push = [&]() {
-    queue[qn++] = reserve;
-    reserve = atomicAdd(counter, 1);
-  };
-  Item pit{};
-  int pit_id = -1, pit_nst = 0;
-  auto issue_one = [&]() {
-    while (!stream_done) {
-      if (pidx >= qn) push();
-      const int id = queue[pidx];
-      if (id >= total) {
-        stream_done = true;
-        return;
+  // ---------------- lane 0 of each warp fills the warp's own slots ----------------
+  const int pw = warp;
+  int pb = 0, pkvh = 0, pc = 0, pkey0 = 0, pnkeys = 0, pfirst = 0, pst = 0, pnst = 0, pid = 0;
+  uint32_t issued = 0;
+  bool pdone = false;
+  int next = lane == 0 ? atomicAdd(counter, 1) : 0;
+  auto produce = [&](uint32_t consumed) {
+    while (!pdone && issued < consumed + S) {
+      const int sl = issued % S, bi = pw * S + sl;
+      if (pst == pnst) {
+        if (next >= total) {
+          desc[bi].b = make_int4(0, 0, 0, -1);
+          mbar_arrive(&full[bi]);
+          pdone = true;
+          ++issued;
+          return;
+        }
+        pid = next;
+        next = atomicAdd(counter, 1);
+        int lo = pb;
+        if (pre[lo + 1] <= pid) {
+          int l2 = lo + 1, hi = B - 1;
+          while (l2 < hi) {
+            const int mid = (l2 + hi + 1) >> 1;
+            if (pre[mid] <= pid) l2 = mid; else hi = mid - 1;
+          }
+          lo = l2;
+        }
+        const int n = nlen[lo];
+        const int base = chunk_base(n, window, kMKeys);
+        const int nch = (n - base + kMChunk - 1) / kMChunk;
+        const int r = pid - pre[lo];
+        pb = lo;
+        pkvh = r / nch;
+        pc = r - pkvh * nch;
+        pkey0 = base + pc * kMChunk;
+        pnkeys = min(kMChunk, n - pkey0);
+        pfirst = window_first(n, window);
+        pst = 0;
+        pnst = (pnkeys + kMKeys - 1) / kMKeys;
       }
-      if (id != pit_id) {
-        pit = decode(id);
-        pit_id = id;
-        pit_nst = (pit.nkeys + kMKeys - 1) / kMKeys;
-      }
-      const Item& it = pit;
-      if (pst < pit_nst) {
-        const int sl = issued % kQSlots;
-        uint8_t* base = slots + sl * C::SLOT;
-        float* sc = scales + sl * (C::SC / 4);
-        fence_proxy_async();
-        mbar_arrive_expect_tx(&full[sl], C::TX);
-        // key + 16 <= T_max: keys start on 16-row boundaries below n <= T_max, T_max % 16 == 0
-        const int key = it.key0 + pst * kMKeys, plane = it.b * Hkv + it.kvh;
-        tma_load_3d(&tmK, base, &full[sl], 0, key, plane);
-        tma_load_3d(&tmV, base + C::BOX, &full[sl], 0, key, plane);
-        const size_t srow = (size_t)plane * T_max + key;
-        bulk_load(sc, kscale + srow, kMKeys * 4, &full[sl]);
-        bulk_load(sc + kMKeys, vscale + srow, kMKeys * 4, &full[sl]);
-        ++pst;
-        ++issued;
-        return;
-      }
-      ++pidx;
-      pst = 0;
+      desc[bi].a = make_int4(pb, pkvh, pc, pst);
+      desc[bi].b = make_int4(pkey0, pnkeys, pfirst, pid);
+      uint8_t* dst = smem + pw * C::WARP_BYTES + sl * C::SLOT;
+      float* sc = reinterpret_cast<float*>(smem + C::OFF_SC + bi * C::SC);
+      mbar_arrive_expect_tx(&full[bi], C::TX);
+      const int key = pkey0 + pst * kMKeys, plane = pb * Hkv + pkvh;
+      tma_load_3d(&tmK, dst, &full[bi], 0, key, plane);
+      tma_load_3d(&tmV, dst + C::BOX, &full[bi], 0, key, plane);
+      const size_t srow = (size_t)plane * T_max + key;
+      bulk_load(sc, kscale + srow, kMKeys * 4, &full[bi]);
+      bulk_load(sc + kMKeys, vscale + srow, kMKeys * 4, &full[bi]);
+      ++pst;
+      ++issued;
     }
   };
-  if (lane == 0) {
-    reserve = atomicAdd(counter, 1);
-    push();
-  }
 
+  // ---------------- consumers ----------------
+  const int w = warp;
+  const int g = lane >> 2, t = lane & 3;
+  const int mi = lane >> 3, lrow = (lane & 7) + 8 * (mi & 1);
+  const uint32_t slots_u32 = smem_u32(smem + w * C::WARP_BYTES);
+  const float* scw = reinterpret_cast<const float*>(smem + C::OFF_SC + w * S * C::SC);
+  uint32_t qb0[DH / 16], qb1[DH / 16];
+  float A0 = 0.f, A1 = 0.f, Bc0 = 0.f, Bc1 = 0.f;   // per head 2t, 2t+1: score scale and bias term
+  float o[DH / 16][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, lv0 = 0.f, lv1 = 0.f, vf = 1.f;
+  int ib = 0, ikvh = 0, ic = 0, ikey0 = 0, inkeys = 0, ifirst = 0;
   bool ok = true;
-  while (ok) {
-    const int cur = __shfl_sync(0xffffffffu, queue[0], 0);
-    if (cur >= total) break;
-    const Item it = decode(cur);
-    const int nst = (it.nkeys + kMKeys - 1) / kMKeys;
-    // Q fragments of head g (rows >= G are zero): dims 16p + 4t .. 16p + 4t + 3 of
-    // 16-dim slice p, in fp16 after the head's power-of-two scale qf
-    uint32_t qa0[DH / 16], qa2[DH / 16];
-    float cq;   // log2(e)/sqrt(dh) / qf: turns a raw score (times the K scale) into log2 units
-    {
-      const bf16* qrow = q + ((size_t)it.b * H + it.kvh * G + (g < G ? g : 0)) * DH + 4 * t;
+  uint32_t k = 0;
+  for (;; ++k) {
+    if (lane == 0) produce(k);
+    const int sl = k % S, bi = w * S + sl;
+    if (!mbar_wait_warp(&full[bi], (k / S) & 1, abort_flag, err)) {
+      ok = false;
+      break;
+    }
+    const int4 da = desc[bi].a, db = desc[bi].b;
+    if (db.w < 0) break;
+    const int st = da.w;
+    if (st == 0) {
+      // a new item: Q fragments of head g (rows >= G zero), dims 16p + 4t .. 16p + 4t + 3 of slice p
+      ib = da.x;
+      ikvh = da.y;
+      ic = da.z;
+      ikey0 = db.x;
+      inkeys = db.y;
+      ifirst = db.z;
+      const bf16* qrow = q + ((size_t)ib * H + ikvh * G + (g < G ? g : 0)) * DH + 4 * t;
       float qv[DH / 16][4];
       float amax = 0.f;
 #pragma unroll
@@ -818,134 +853,157 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       const float qf = pow2_frame(amax);
-      cq = scale_log2 / qf;
+      float qs = 0.f;                   // Σ of the fp16 query values, for the score bias
 #pragma unroll
       for (int p = 0; p < DH / 16; ++p) {
-        qa0[p] = pack_f16(qv[p][0] * qf, qv[p][1] * qf);
-        qa2[p] = pack_f16(qv[p][2] * qf, qv[p][3] * qf);
+        qb0[p] = pack_f16(qv[p][0] * qf, qv[p][1] * qf);
+        qb1[p] = pack_f16(qv[p][2] * qf, qv[p][3] * qf);
+        const float2 a = unpack_f16(qb0[p]), c = unpack_f16(qb1[p]);
+        qs += (a.x + a.y) + (c.x + c.y);
       }
-    }
-    float o[DH / 8][4];
+      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+      const float cq = scale_log2 / qf, cb = 1152.f * qs * cq;
+      A0 = __shfl_sync(0xffffffffu, cq, 8 * t);         // lane 8t holds head 2t, lane 8t+4 head 2t+1
+      A1 = __shfl_sync(0xffffffffu, cq, 8 * t + 4);
+      Bc0 = __shfl_sync(0xffffffffu, cb, 8 * t);
+      Bc1 = __shfl_sync(0xffffffffu, cb, 8 * t + 4);
 #pragma unroll
-    for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_used = -INFINITY, lsum = 0.f, vf = 1.f;
+      for (int p = 0; p < DH / 16; ++p) o[p][0] = o[p][1] = o[p][2] = o[p][3] = 0.f;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = lv0 = lv1 = 0.f;
+      vf = 1.f;
+    }
+    const uint32_t kbase = slots_u32 + sl * C::SLOT, vbase = kbase + C::BOX;
+    const float* sc = scw + sl * (C::SC / 4);
+    const int nvalid = min(kMKeys, inkeys - st * kMKeys);
+    const int lead = ifirst - (ikey0 + st * kMKeys);   // keys below lead precede the window
 
-    for (int st = 0; st < nst; ++st) {
-      if (lane == 0)
-        while (!stream_done && issued < consumed + kQSlots) issue_one();
-      const int sl = consumed % kQSlots;
-      if (!mbar_wait_warp(&full[sl], (consumed / kQSlots) & 1, abort_flag, err)) {
-        ok = false;
-        break;
-      }
-      const uint32_t ks_base = slots_u32 + sl * C::SLOT, vs_base = ks_base + C::BOX;
-      const float* sc = scales + sl * (C::SC / 4);
-      const int nvalid = min(kMKeys, it.nkeys - st * kMKeys);
-      const int mi = lane >> 3, lrow = (lane & 7) + 8 * (mi & 1);
-
-      // S = Q·Kᵀ for keys 0-7 (s0) and 8-15 (s1)
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    // Sᵀ = K·Qᵀ (biased codes), even and odd slices in two accumulators
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int pp = 0; pp < DH / 32; ++pp) {
-        uint32_t kb[4];
-        ldsm_x4(swz128(ks_base, lrow, 2 * pp + (mi >> 1)), kb);
+    for (int pp = 0; pp < DH / 32; ++pp) {
+      uint32_t kb[4];
+      ldsm_x4(swz128(kbase, lrow, 2 * pp + (mi >> 1)), kb);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) kb[j] ^= 0x80808080u;
-        mma16816_f16(s0, qa0[2 * pp], qa2[2 * pp], codes_f16x2(kb[0], 0x4140), codes_f16x2(kb[0], 0x4342));
-        mma16816_f16(s1, qa0[2 * pp], qa2[2 * pp], codes_f16x2(kb[1], 0x4140), codes_f16x2(kb[1], 0x4342));
-        mma16816_f16(s0, qa0[2 * pp + 1], qa2[2 * pp + 1], codes_f16x2(kb[2], 0x4140), codes_f16x2(kb[2], 0x4342));
-        mma16816_f16(s1, qa0[2 * pp + 1], qa2[2 * pp + 1], codes_f16x2(kb[3], 0x4140), codes_f16x2(kb[3], 0x4342));
-      }
-      // lane (g, t) holds the scores of keys 2t, 2t+1 (s0) and 8+2t, 9+2t (s1) for head g
-      const float2 kA = *reinterpret_cast<const float2*>(sc + 2 * t);
-      const float2 kB = *reinterpret_cast<const float2*>(sc + 8 + 2 * t);
-      const float2 vA = *reinterpret_cast<const float2*>(sc + kMKeys + 2 * t);
-      const float2 vB = *reinterpret_cast<const float2*>(sc + kMKeys + 8 + 2 * t);
-      const int lead = it.first - (it.key0 + st * kMKeys);   // keys below lead precede the window
-      const int k0 = 2 * t, k2 = 8 + 2 * t;
-      const bool ok0 = k0 < nvalid && k0 >= lead, ok1 = k0 + 1 < nvalid && k0 + 1 >= lead;
-      const bool ok2 = k2 < nvalid && k2 >= lead, ok3 = k2 + 1 < nvalid && k2 + 1 >= lead;
-      const float r0 = ok0 ? s0[0] * (kA.x * cq) : -INFINITY, r1 = ok1 ? s0[1] * (kA.y * cq) : -INFINITY;
-      const float r2 = ok2 ? s1[0] * (kB.x * cq) : -INFINITY, r3 = ok3 ? s1[1] * (kB.y * cq) : -INFINITY;
-      float mx = fmax3(r0, r1, fmaxf(r2, r3));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_used, mx);      // finite: the stage has a visible key
-      const float w0 = ok0 ? vA.x : 0.f, w1 = ok1 ? vA.y : 0.f, w2 = ok2 ? vB.x : 0.f, w3 = ok3 ? vB.y : 0.f;
-      float vmax = fmaxf(fmaxf(w0, w1), fmaxf(w2, w3));
-      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
-      const float vr = vmax * vf;
-      const bool new_frame = vr > 16.f || (vmax > 0.f && vr < 0.0625f);
-      const bool new_max = m_new > m_used + kRescaleLog2 || m_used == -INFINITY;
-      if (new_frame || new_max) {
-        float f = 1.f;
-        if (new_max) {
-          f = m_used == -INFINITY ? 0.f : ex2_approx(m_used - m_new);
-          lsum *= f;
-          m_used = m_new;
-        }
-        if (new_frame) {
-          const float vf_new = pow2_frame(vmax);
-          if (f != 0.f) f *= vf_new / vf;        // both powers of two: exact
-          vf = vf_new;
-        }
-#pragma unroll
-        for (int i = 0; i < DH / 8; ++i) {
-          o[i][0] *= f;
-          o[i][1] *= f;
-        }
-      }
-      const float p0 = ex2_approx(r0 - m_used), p1 = ex2_approx(r1 - m_used);
-      const float p2 = ex2_approx(r2 - m_used), p3 = ex2_approx(r3 - m_used);
-      lsum += (p0 + p1) + (p2 + p3);
-      const uint32_t pa0 = pack_f16(p0 * (w0 * vf), p1 * (w1 * vf));
-      const uint32_t pa2 = pack_f16(p2 * (w2 * vf), p3 * (w3 * vf));
-      // O += P·V: n-tiles 4pp, 4pp+1 = even, odd dims of slice 2pp; 4pp+2, 4pp+3 of slice 2pp+1
-#pragma unroll
-      for (int pp = 0; pp < DH / 32; ++pp) {
-        uint32_t vb[4];
-        ldsm_x4_t(swz128(vs_base, lrow, 2 * pp + (mi >> 1)), vb);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) vb[j] ^= 0x80808080u;
-        mma16816_f16(o[4 * pp], pa0, pa2, codes_f16x2(vb[0], 0x4240), codes_f16x2(vb[1], 0x4240));
-        mma16816_f16(o[4 * pp + 1], pa0, pa2, codes_f16x2(vb[0], 0x4341), codes_f16x2(vb[1], 0x4341));
-        mma16816_f16(o[4 * pp + 2], pa0, pa2, codes_f16x2(vb[2], 0x4240), codes_f16x2(vb[3], 0x4240));
-        mma16816_f16(o[4 * pp + 3], pa0, pa2, codes_f16x2(vb[2], 0x4341), codes_f16x2(vb[3], 0x4341));
-      }
-      __syncwarp();           // the slot may be refilled after this
-      ++consumed;
+      for (int j = 0; j < 4; ++j) kb[j] ^= 0x80808080u;
+      mma16816_f16(sa, biased_f16x2(kb[0], 0x4140), biased_f16x2(kb[1], 0x4140), biased_f16x2(kb[0], 0x4342),
+                   biased_f16x2(kb[1], 0x4342), qb0[2 * pp], qb1[2 * pp]);
+      mma16816_f16(sb, biased_f16x2(kb[2], 0x4140), biased_f16x2(kb[3], 0x4140), biased_f16x2(kb[2], 0x4342),
+                   biased_f16x2(kb[3], 0x4342), qb0[2 * pp + 1], qb1[2 * pp + 1]);
     }
-    if (!ok) break;
-    float l = lsum;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (g < G) {
-      // lane (g, t) holds dims 16p + 4t .. 16p + 4t + 3 of slice p: even tile n = 2t, odd 2t, even 2t+1, odd 2t+1
-      float* pr = part + (((size_t)it.b * H + it.kvh * G + g) * nchunk_max + it.c) * PartLayout<DH>::stride;
-      const float inv = 1.0f / vf;   // a power of two: exact
+    // lane (g, t): keys g and g+8, heads 2t and 2t+1
+    const float ks_lo = sc[g], ks_hi = sc[8 + g], vs_lo = sc[16 + g], vs_hi = sc[24 + g];
+    const bool ok_lo = g < nvalid && g >= lead, ok_hi = g + 8 < nvalid && g + 8 >= lead;
+    const float r00 = ok_lo ? ks_lo * fmaf(sa[0] + sb[0], A0, -Bc0) : -INFINITY;
+    const float r01 = ok_lo ? ks_lo * fmaf(sa[1] + sb[1], A1, -Bc1) : -INFINITY;
+    const float r10 = ok_hi ? ks_hi * fmaf(sa[2] + sb[2], A0, -Bc0) : -INFINITY;
+    const float r11 = ok_hi ? ks_hi * fmaf(sa[3] + sb[3], A1, -Bc1) : -INFINITY;
+    const float w_lo = ok_lo ? vs_lo : 0.f, w_hi = ok_hi ? vs_hi : 0.f;
+    float mx0 = fmaxf(r00, r10), mx1 = fmaxf(r01, r11), vmax = fmaxf(w_lo, w_hi);
 #pragma unroll
-      for (int p = 0; p < DH / 16; ++p)
-        *reinterpret_cast<float4*>(pr + 4 + 16 * p + 4 * t) =
-            make_float4(o[2 * p][0] * inv, o[2 * p + 1][0] * inv, o[2 * p][1] * inv, o[2 * p + 1][1] * inv);
-      if (t == 0) {
-        pr[0] = m_used;
-        pr[1] = l;
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: the stage has a visible key
+    const bool nm0 = m0 == -INFINITY || mn0 > m0 + kRescaleLog2;
+    const bool nm1 = m1 == -INFINITY || mn1 > m1 + kRescaleLog2;
+    const float vr = vmax * vf;
+    const bool nf = vr > 16.f || (vmax > 0.f && vr < 0.0625f);
+    if (nm0 || nm1 || nf) {
+      float f0 = 1.f, f1 = 1.f;
+      if (nm0) {
+        f0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mn0);
+        l0 *= f0;
+        m0 = mn0;
+      }
+      if (nm1) {
+        f1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mn1);
+        l1 *= f1;
+        m1 = mn1;
+      }
+      if (nf) {
+        const float vf_new = pow2_frame(vmax);
+        const float rr = vf_new / vf;            // both powers of two: exact
+        vf = vf_new;
+        if (f0 != 0.f) f0 *= rr;
+        if (f1 != 0.f) f1 *= rr;
+      }
+      lv0 *= f0;
+      lv1 *= f1;
+#pragma unroll
+      for (int p = 0; p < DH / 16; ++p) {
+        o[p][0] *= f0;
+        o[p][2] *= f0;
+        o[p][1] *= f1;
+        o[p][3] *= f1;
       }
     }
-    if (lane == 0) {
-      queue[0] = queue[1];
-      queue[1] = queue[2];
-      queue[2] = queue[3];
-      --qn;
-      --pidx;
+    const float p00 = ex2_approx(r00 - m0), p01 = ex2_approx(r01 - m1);
+    const float p10 = ex2_approx(r10 - m0), p11 = ex2_approx(r11 - m1);
+    l0 += p00 + p10;
+    l1 += p01 + p11;
+    const float wl = w_lo * vf, wh = w_hi * vf;
+    const uint32_t pk_lo = pack_f16(p00 * wl, p01 * wl), pk_hi = pack_f16(p10 * wh, p11 * wh);
+    {
+      const float2 a = unpack_f16(pk_lo), c = unpack_f16(pk_hi);
+      lv0 += a.x + c.x;
+      lv1 += a.y + c.y;
+    }
+    const uint32_t pb0 = movmatrix_t(pk_lo), pb1 = movmatrix_t(pk_hi);   // Pᵀ fragments: keys 2t, 2t+1 (+8) of head g
+    // Oᵀ += Vᵀ·Pᵀ: m-tile p = dims 16p + 2g (rows g) and 16p + 2g + 1 (rows g+8)
+#pragma unroll
+    for (int pp = 0; pp < DH / 32; ++pp) {
+      uint32_t vb[4];
+      ldsm_x4_t(swz128(vbase, lrow, 2 * pp + (mi >> 1)), vb);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vb[j] ^= 0x80808080u;
+      mma16816_f16(o[2 * pp], biased_f16x2(vb[0], 0x4240), biased_f16x2(vb[0], 0x4341), biased_f16x2(vb[1], 0x4240),
+                   biased_f16x2(vb[1], 0x4341), pb0, pb1);
+      mma16816_f16(o[2 * pp + 1], biased_f16x2(vb[2], 0x4240), biased_f16x2(vb[2], 0x4341),
+                   biased_f16x2(vb[3], 0x4240), biased_f16x2(vb[3], 0x4341), pb0, pb1);
+    }
+    __syncwarp();             // the slot may be refilled after this
+    if ((st + 1) * kMKeys >= inkeys) {
+      // the item's partial state for heads 2t and 2t+1: sums over the eight key rows g
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        lv0 += __shfl_xor_sync(0xffffffffu, lv0, off);
+        lv1 += __shfl_xor_sync(0xffffffffu, lv1, off);
+      }
+      const float inv = 1.0f / vf, c0 = 1152.f * lv0, c1 = 1152.f * lv1;
+      const int h0 = 2 * t, h1 = 2 * t + 1;
+      constexpr int P = PartLayout<DH>::stride;
+      if (h0 < G) {
+        float* pr = part + (((size_t)ib * H + ikvh * G + h0) * nchunk_max + ic) * P;
+#pragma unroll
+        for (int p = 0; p < DH / 16; ++p)
+          *reinterpret_cast<float2*>(pr + 4 + 16 * p + 2 * g) = make_float2((o[p][0] - c0) * inv, (o[p][2] - c0) * inv);
+        if (g == 0) {
+          pr[0] = m0;
+          pr[1] = l0;
+        }
+      }
+      if (h1 < G) {
+        float* pr = part + (((size_t)ib * H + ikvh * G + h1) * nchunk_max + ic) * P;
+#pragma unroll
+        for (int p = 0; p < DH / 16; ++p)
+          *reinterpret_cast<float2*>(pr + 4 + 16 * p + 2 * g) = make_float2((o[p][1] - c1) * inv, (o[p][3] - c1) * inv);
+        if (g == 0) {
+          pr[0] = m1;
+          pr[1] = l1;
+        }
+      }
     }
   }
   issued = __shfl_sync(0xffffffffu, issued, 0);
-  if (!ok && lane == 0) {
+  if (!ok && lane == 0) {      // copies issued but not consumed must land before the CTA exits
     volatile int no_abort = 0;
-    for (uint32_t k = consumed; k < issued; ++k)
-      mbar_wait(&full[k % kQSlots], (k / kQSlots) & 1, &no_abort, err);
+    for (uint32_t j = k; j < issued; ++j) mbar_wait(&full[pw * S + j % S], (j / S) & 1, &no_abort, err);
   }
 }
 
@@ -960,20 +1018,20 @@ cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const f
   if (e != cudaSuccess) return e;
   e = make_tmap_3d_u8(&tv, vc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kMKeys);
   if (e != cudaSuccess) return e;
-  const size_t smem = C::OFF_PRE + (size_t)(B + 1) * 4 + 1024;
+  const size_t smem = C::OFF_PRE + (size_t)(2 * B + 1) * 4 + 1024;
   if (smem > 232448) return cudaErrorInvalidValue;
   static size_t attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || attr_set[dev] < smem) {
-    e = cudaFuncSetAttribute(k_decode_mma_i8<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(k_decode_i8<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = smem;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
-  k_decode_mma_i8<G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, ks, vs, (const bf16*)q, pos, B, Hkv, T_max, part,
-                                                           nchunk_max, counter, window, scale_log2,
-                                                           device_error_word());
+  k_decode_i8<G><<<sm_count(), kQWarps * 32, smem, s>>>(tk, tv, ks, vs, (const bf16*)q, pos, B, Hkv, T_max,
+                                                               part, nchunk_max, counter, window, scale_log2,
+                                                               device_error_word());
   k_decode_combine<bf16, 128><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kMChunk, window,
                                                                 kMKeys, (bf16*)o);
   return cudaGetLastError();
