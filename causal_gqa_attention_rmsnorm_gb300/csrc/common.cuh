@@ -74,7 +74,7 @@ tb_status report(tb_status st, const char* fmt, ...);
 cudaError_t launch_pack(int dtype, const Dims& D, const tb_block_weights& w, void* packed,
                         const Packed& P, float rope_base, cudaStream_t s);
 cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, float* r,
-                             float* ssq_zero, int T, int32_t* lens_set, int32_t* lens_bump,
+                             int* cnt_zero, int T, int32_t* lens_set, int32_t* lens_bump,
                              int32_t* pos_out, int T_max, int* zero_word, int* err, cudaStream_t s);
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new,
                              int n, int* err, cudaStream_t s);
@@ -107,6 +107,18 @@ __device__ __forceinline__ long long paged_row(const PagedKV& p, int Hkv, int b,
   return ((long long)page * Hkv + h) * p.ps + t % p.ps;
 }
 
+// Row sums in a fixed order, so that a run is reproducible bit for bit: each
+// of a row's producers (one per column tile or column range of the GEMM that
+// forms the row) stores its partial at part[row·stride + p]; the producer that
+// arrives last at a group of rows (counted in cnt[group], zeroed before the
+// GEMM) adds the partials in the order p = 0, 1, ... and writes out[row].
+struct RowSum {
+  float* part;             // [M, stride]
+  float* out;              // [M]
+  int* cnt;                // one arrival counter per row group
+  int stride;              // partials per row the buffer holds
+};
+
 // GEMM epilogue argument bundles.
 struct QKVArgs {
   const float* r;          // [M] RMSNorm-1 inverse RMS of each token
@@ -124,7 +136,7 @@ struct WoArgs {
   const void* x;           // [M, d] residual input (cfg dtype)
   float* h;                // [M, d] fp32 residual stream after attention
   void* hb;                // [M, d] cfg dtype copy of h (A operand of W1/W3), may be == h for f32
-  float* ssq;              // [M] Σ h² (accumulated)
+  RowSum ssq;              // Σ h² of each row: out [M]
 };
 struct W13Args {
   const float* ssq;        // [M] Σ h²

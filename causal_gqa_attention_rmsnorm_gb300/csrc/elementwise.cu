@@ -46,13 +46,14 @@ __global__ void k_rope_table(float2* __restrict__ tab, int max_pos, int half, in
 }
 
 // One warp per token row: r = 1/sqrt(mean(x²) + eps).  Side duties, done by
-// lane 0 of the row: clear the Σh² accumulator of the second norm, set the
+// lane 0 of the row: clear the row's arrival counter of the second norm's
+// ordered row sums (cnt_zero), set the
 // cache length after a prefill (lens_set), or take the decode position and
 // advance the cache length (lens_bump -> pos_out, -1 when the cache is full),
 // and zero a counter a later kernel of the step uses (zero_word).
 template <typename T>
 __global__ void k_row_stats(const T* __restrict__ x, int M, int d, float eps, float* __restrict__ r,
-                            float* __restrict__ ssq_zero, int Tseq, int32_t* __restrict__ lens_set,
+                            int* __restrict__ cnt_zero, int Tseq, int32_t* __restrict__ lens_set,
                             int32_t* __restrict__ lens_bump, int32_t* __restrict__ pos_out, int T_max,
                             int* __restrict__ zero_word, int* __restrict__ err) {
   const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
@@ -96,7 +97,7 @@ __global__ void k_row_stats(const T* __restrict__ x, int M, int d, float eps, fl
   s = warp_sum(s);
   if (lane == 0) {
     r[row] = 1.0f / sqrtf(s / (float)d + eps);
-    if (ssq_zero) ssq_zero[row] = 0.f;
+    if (cnt_zero) cnt_zero[row] = 0;
     if (zero_word && row == 0) *zero_word = 0;
     if (lens_set && (row % Tseq) == 0) lens_set[row / Tseq] = Tseq;
     if (lens_bump) {
@@ -225,16 +226,16 @@ cudaError_t launch_pack(int dtype, const Dims& D, const tb_block_weights& w, voi
   return cudaGetLastError();
 }
 
-cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, float* r, float* ssq_zero,
+cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, float* r, int* cnt_zero,
                              int T, int32_t* lens_set, int32_t* lens_bump, int32_t* pos_out, int T_max,
                              int* zero_word, int* err, cudaStream_t s) {
   const int threads = 256;
   const unsigned blocks = (unsigned)(((size_t)M * 32 + threads - 1) / threads);
   if (dtype == TB_F32)
-    k_row_stats<float><<<blocks, threads, 0, s>>>((const float*)x, M, d, eps, r, ssq_zero, T, lens_set,
+    k_row_stats<float><<<blocks, threads, 0, s>>>((const float*)x, M, d, eps, r, cnt_zero, T, lens_set,
                                                   lens_bump, pos_out, T_max, zero_word, err);
   else
-    k_row_stats<bf16><<<blocks, threads, 0, s>>>((const bf16*)x, M, d, eps, r, ssq_zero, T, lens_set,
+    k_row_stats<bf16><<<blocks, threads, 0, s>>>((const bf16*)x, M, d, eps, r, cnt_zero, T, lens_set,
                                                  lens_bump, pos_out, T_max, zero_word, err);
   return cudaGetLastError();
 }

@@ -1,7 +1,8 @@
 // GEMM epilogues of the block, shared by the fp32 SIMT GEMM and the bf16
 // tcgen05 GEMM.  Each functor receives 4 consecutive output columns
 // [col, col+4) of one row with col % 4 == 0, in fp32, and returns a value the
-// caller sums over the row's columns when kRowReduce is set.
+// caller sums over the row's columns when kRowReduce is set (into the RowSum
+// that row_sums() names).
 //
 // Steps ("Transformer block" page, tirogla.com, "How it works" step 2-3):
 //   QKV  : × r (RMSNorm-1 row scale), RoPE on q and k, scatter q / k / v
@@ -112,7 +113,6 @@ struct EpiQKV {
     }
     return 0.f;
   }
-  __device__ __forceinline__ void row_reduce(int, float) const {}
 };
 
 template <typename T>
@@ -135,7 +135,7 @@ struct EpiWo {
     if ((void*)a.hb != (void*)a.h) store4<T>((T*)a.hb + (size_t)row * d + col, v);
     return v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
   }
-  __device__ __forceinline__ void row_reduce(int row, float s) const { atomicAdd(a.ssq + row, s); }
+  __device__ __forceinline__ const RowSum& row_sums() const { return a.ssq; }
 };
 
 template <typename T>
@@ -157,7 +157,6 @@ struct EpiW13 {
     store2<T>((T*)a.a + (size_t)row * f + (col >> 1), o0, o1);
     return 0.f;
   }
-  __device__ __forceinline__ void row_reduce(int, float) const {}
 };
 
 struct EpiW2 {
@@ -181,7 +180,6 @@ struct EpiW2 {
       store4<bf16>((bf16*)a.y + (size_t)row * d + col, v);
     return 0.f;
   }
-  __device__ __forceinline__ void row_reduce(int, float) const {}
 };
 
 // LM head: logits = (x·r)·W_Uᵀ with the final norm's gain folded into the
@@ -200,7 +198,6 @@ struct EpiLogits {
     store4<float>(a.out + (size_t)row * a.ld + col, v);
     return 0.f;
   }
-  __device__ __forceinline__ void row_reduce(int, float) const {}
 };
 
 }  // namespace tb

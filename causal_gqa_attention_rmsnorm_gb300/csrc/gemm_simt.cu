@@ -58,10 +58,26 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const T* __restrict__ A, cons
       part = epi(row, col, acc[i], ra, epi.aux(row, col, ra));
     }
     if constexpr (Epi::kRowReduce) {
-      // the 16 threads of a half-warp share this row
+      // the 16 threads of a half-warp share this row: its partial blockIdx.x
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-      if (tx == 0 && row < M) epi.row_reduce(row, part);
+      if (tx == 0 && row < M) epi.row_sums().part[(size_t)row * epi.row_sums().stride + blockIdx.x] = part;
+    }
+  }
+  if constexpr (Epi::kRowReduce) {
+    // the CTA that completes a 64-row block sums each row's partials in order
+    const RowSum& rs = epi.row_sums();
+    __threadfence();
+    __syncthreads();
+    __shared__ int last;
+    if (threadIdx.x == 0) last = atomicAdd(rs.cnt + blockIdx.y, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (last && threadIdx.x < BM && m0 + (int)threadIdx.x < M) {
+      __threadfence();
+      const int row = m0 + threadIdx.x;
+      float sum = 0.f;
+      for (int p = 0; p < (int)gridDim.x; ++p) sum += __ldcg(rs.part + (size_t)row * rs.stride + p);
+      rs.out[row] = sum;
     }
   }
 }

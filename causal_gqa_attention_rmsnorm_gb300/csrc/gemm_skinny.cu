@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(192)
 
 // Sum of the K-range partials of 4 consecutive outputs of one token, then the
 // fused epilogue.  Rows (tokens) are blockIdx.y, so a row reduction (Σh² of
-// the Wo epilogue) is a warp sum and one atomic per warp.
+// the Wo epilogue) is a warp sum per warp and one ordered sum per row.
 template <class Epi>
 __global__ void __launch_bounds__(256)
     k_splitk_epilogue(const float* __restrict__ part, int splits, int M, int N, Epi epi) {
@@ -229,8 +229,25 @@ __global__ void __launch_bounds__(256)
     r = epi(m, col, v, ra, ax);
   }
   if constexpr (Epi::kRowReduce) {
+    // each warp's share of row m is one partial; the CTA that completes the
+    // row sums them in a fixed order
+    const RowSum& rs = epi.row_sums();
+    constexpr int kWarpsPerCta = 256 / 32;
+    const int nparts = gridDim.x * kWarpsPerCta;
     r = warp_sum(r);
-    if ((threadIdx.x & 31) == 0) epi.row_reduce(m, r);
+    if ((threadIdx.x & 31) == 0) rs.part[(size_t)m * rs.stride + blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)] = r;
+    __threadfence();
+    __syncthreads();
+    __shared__ int last;
+    if (threadIdx.x == 0) last = atomicAdd(rs.cnt + m, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (last && threadIdx.x < 32) {
+      __threadfence();
+      float sum = 0.f;
+      for (int p = threadIdx.x; p < nparts; p += 32) sum += __ldcg(rs.part + (size_t)m * rs.stride + p);
+      sum = warp_sum(sum);
+      if (threadIdx.x == 0) rs.out[m] = sum;
+    }
   }
 }
 

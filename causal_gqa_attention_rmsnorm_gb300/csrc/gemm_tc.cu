@@ -55,7 +55,6 @@ struct EpiF32 {
     *reinterpret_cast<float4*>(C + (size_t)row * N + col) = make_float4(v[0], v[1], v[2], v[3]);
     return 0.f;
   }
-  __device__ __forceinline__ void row_reduce(int, float) const {}
 };
 
 // Tile index -> (m, n) tile.  group_m == 0 walks n fastest (CTAs running
@@ -200,12 +199,39 @@ __global__ void __launch_bounds__(192, 1)
     const int quad = warp & 3;
     float* stage = reinterpret_cast<float*>(smem + C::OFF_EPI) + (warp - 2) * 32 * C::EPI_STRIDE;
     const int sub_row = lane >> 3, sub_col = 4 * (lane & 7);
+    // Ordered row sums (RowSum): after a tile's partials are stored, the warp
+    // counts its arrival at the 32-row group, and the warp that completes the
+    // group adds the group's n_tiles partials in order.  The count is taken at
+    // the next tile, once its accumulator is ready, so that the fence before
+    // it finds this tile's stores long finished instead of waiting for them.
+    int pend_row0 = -1;
+    auto row_arrive = [&]() {
+      if constexpr (Epi::kRowReduce) {
+        if (pend_row0 < 0) return;
+        const RowSum& rs = epi.row_sums();
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(rs.cnt + pend_row0 / 32, 1) == n_tiles - 1;
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence();
+          const int row = pend_row0 + lane;
+          if (row < M) {
+            float sum = 0.f;
+            for (int p = 0; p < n_tiles; ++p) sum += __ldcg(rs.part + (size_t)row * rs.stride + p);
+            rs.out[row] = sum;
+          }
+        }
+        pend_row0 = -1;
+      }
+    };
     int local = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, err)) break;
       tc_fence_after();
+      row_arrive();
       int mt, nt;
       tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
       const int row0 = mt * BM + quad * 32;
@@ -258,6 +284,8 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();            // before the next chunk overwrites the stage
       }
       if constexpr (Epi::kRowReduce) {
+        // this tile's share of each of the warp's 32 rows is partial nt; its
+        // arrival is counted at the next tile (see row_arrive)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           float t = rsum[i];
@@ -265,10 +293,12 @@ __global__ void __launch_bounds__(192, 1)
           t += __shfl_xor_sync(0xffffffffu, t, 2);
           t += __shfl_xor_sync(0xffffffffu, t, 4);
           const int row = row0 + sub_row + 4 * i;
-          if ((lane & 7) == 0 && row < M) epi.row_reduce(row, t);
+          if ((lane & 7) == 0 && row < M) epi.row_sums().part[(size_t)row * epi.row_sums().stride + nt] = t;
         }
+        pend_row0 = row0;
       }
     }
+    row_arrive();
   }
 
   tc_fence_before();

@@ -121,7 +121,10 @@ Packed packed_views(const tb_block_cfg* c, const void* blob) {
 // Workspace carving.  Prefill keeps K/V in the workspace when no cache is given.
 struct Work {
   float* r;
-  float* ssq;
+  float* ssq;                // [M] Σ h² of each row (the second norm)
+  float* ssq_part;           // [M, ssq_stride] its ordered partials
+  int* ssq_cnt;              // [M] arrival counters, zeroed by the row statistics
+  int ssq_stride;
   int32_t* pos;
   int* counter;
   void* q;
@@ -151,6 +154,12 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
   const size_t hd = (size_t)c->H * c->dh, kvd = (size_t)c->Hkv * c->dh;
   w.r = (float*)take(M * 4);
   w.ssq = (float*)take(M * 4);
+  // partials per row: one per column tile (tile GEMM, ≥ 128 columns), per
+  // 1024-column CTA warp (few-token epilogue: 8 per 1024 columns) or per 64
+  // columns (fp32 GEMM)
+  w.ssq_stride = (c->d + 63) / 64 + 8;
+  w.ssq_part = (float*)take(M * w.ssq_stride * 4);
+  w.ssq_cnt = (int*)take(M * 4);
   w.pos = (int32_t*)take((size_t)B * 4);
   w.counter = (int*)take(4);
   w.q = take(M * hd * es);
@@ -365,10 +374,10 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
 
   StageRecorder rec(s);
   rec.stage("rms");
-  TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, W.ssq, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
+  TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, W.ssq_cnt, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
                           nullptr, err, s));
   const QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr, paged_of(kv, err)};
-  const WoArgs wa{x, W.h, W.hb, W.ssq};
+  const WoArgs wa{x, W.h, W.hb, RowSum{W.ssq_part, W.ssq, W.ssq_cnt, W.ssq_stride}};
   const W13Args ga{W.ssq, W.a};
   const W2Args ya{W.h, y, y_dtype};
   if (dt == TB_F32) {
@@ -435,7 +444,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
 
   StageRecorder rec(s);
   rec.stage("rms");
-  TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, W.ssq, 1, nullptr, kv->lens, W.pos, kv->T_max,
+  TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, W.ssq_cnt, 1, nullptr, kv->lens, W.pos, kv->T_max,
                           W.counter, err, s));
   const PagedKV pg = paged_of(kv, err);
   // an int8 cache gets the new rows through the workspace and the quantiser
@@ -443,7 +452,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
   void* knew = pg.bt ? nullptr : (i8 ? W.k : kv->k);
   void* vnew = pg.bt ? nullptr : (i8 ? W.v : kv->v);
   const QKVArgs qa{W.r, P.rope, W.q, knew, vnew, 1, i8 ? 1 : kv->T_max, W.pos, pg, i8};
-  const WoArgs wa{x, W.h, W.hb, W.ssq};
+  const WoArgs wa{x, W.h, W.hb, RowSum{W.ssq_part, W.ssq, W.ssq_cnt, W.ssq_stride}};
   const W13Args ga{W.ssq, W.a};
   const W2Args ya{W.h, y, y_dtype};
   if (dt == TB_F32) {
