@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restric
                                                               const int32_t* __restrict__ pos_arr, int Hkv,
                                                               int T_max, float* __restrict__ part, int nchunk_max,
                                                               int window, PagedKV pg, float scale_log2) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int VEC = 16 / sizeof(T);
   constexpr int LPK = DH / VEC;   // lanes per key row
   static_assert(LPK >= 1 && LPK <= 32 && (32 % LPK) == 0, "row must split evenly over lanes");
@@ -221,6 +223,8 @@ template <typename T, int DH>
 __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict__ part,
                                                         const int32_t* __restrict__ pos_arr, int H, int nchunk_max,
                                                         int chunk, int window, int align, T* __restrict__ o) {
+  pdl_trigger();
+  pdl_wait();
   // Thread (e, g) sums output column e over chunks g, g + NG, ... with eight
   // independent loads in flight, so the merge costs a few L2 round trips.
   static_assert(256 % DH == 0, "head width must divide the block");
@@ -363,6 +367,8 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
                  const bf16* __restrict__ q, const int32_t* __restrict__ pos_arr, int B, int Hkv,
                  float* __restrict__ part, int nchunk_max, int* __restrict__ counter, int window, PagedKV pg,
                  float scale_log2, int* err) {
+  pdl_trigger();
+  pdl_wait();
   using C = MCfg<DH>;
   using namespace ptx;
   static_assert(G <= 8, "at most 8 query heads per KV head");
@@ -719,6 +725,8 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
                 const float* __restrict__ kscale, const float* __restrict__ vscale, const bf16* __restrict__ q,
                 const int32_t* __restrict__ pos_arr, int B, int Hkv, int T_max, float* __restrict__ part,
                 int nchunk_max, int* __restrict__ counter, int window, float scale_log2, int* err) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int DH = 128, S = kQSlots;
   using C = QCfg;
   using namespace ptx;
@@ -1029,12 +1037,11 @@ cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const f
     if (dev >= 0 && dev < 64) attr_set[dev] = smem;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
-  k_decode_i8<G><<<sm_count(), kQWarps * 32, smem, s>>>(tk, tv, ks, vs, (const bf16*)q, pos, B, Hkv, T_max,
-                                                               part, nchunk_max, counter, window, scale_log2,
-                                                               device_error_word());
-  k_decode_combine<bf16, 128><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kMChunk, window,
-                                                                kMKeys, (bf16*)o);
-  return cudaGetLastError();
+  e = launch_pdl(k_decode_i8<G>, dim3(sm_count()), dim3(kQWarps * 32), smem, s, tk, tv, ks, vs, (const bf16*)q, pos, B,
+                 Hkv, T_max, part, nchunk_max, counter, window, scale_log2, device_error_word());
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_decode_combine<bf16, 128>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
+                    nchunk_max, kMChunk, window, kMKeys, (bf16*)o);
 }
 
 template <int DH, int G>
@@ -1064,12 +1071,11 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
     if (dev >= 0 && dev < 64) attr_set[dev] = smem;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
-  k_decode_mma<DH, G><<<sm_count(), kMWarps * 32, smem, s>>>(tk, tv, (const bf16*)q, pos, B, Hkv, part,
-                                                             nchunk_max, counter, window, pg, scale_log2,
-                                                             device_error_word());
-  k_decode_combine<bf16, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kMChunk, window,
-                                                               kMKeys, (bf16*)o);
-  return cudaGetLastError();
+  e = launch_pdl(k_decode_mma<DH, G>, dim3(sm_count()), dim3(kMWarps * 32), smem, s, tk, tv, (const bf16*)q, pos, B,
+                 Hkv, part, nchunk_max, counter, window, pg, scale_log2, device_error_word());
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_decode_combine<bf16, DH>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
+                    nchunk_max, kMChunk, window, kMKeys, (bf16*)o);
 }
 
 template <int DH>
@@ -1089,11 +1095,12 @@ template <typename T, int DH, int G>
 cudaError_t run(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
                 float* part, int nchunk_max, int window, const PagedKV& pg, void* o, cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
-  k_decode_split<T, DH, G><<<dim3(nchunk_max, Hkv, B), kWarps * 32, 0, s>>>(
-      (const T*)q, (const T*)kc, (const T*)vc, pos, Hkv, T_max, part, nchunk_max, window, pg, scale_log2);
-  k_decode_combine<T, DH><<<dim3(Hkv * G, B), 256, 0, s>>>(part, pos, Hkv * G, nchunk_max, kChunk, window, 1,
-                                                           (T*)o);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(k_decode_split<T, DH, G>, dim3(nchunk_max, Hkv, B), dim3(kWarps * 32), 0, s,
+                                   (const T*)q, (const T*)kc, (const T*)vc, pos, Hkv, T_max, part, nchunk_max, window,
+                                   pg, scale_log2);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_decode_combine<T, DH>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
+                    nchunk_max, kChunk, window, 1, (T*)o);
 }
 
 template <typename T, int DH>

@@ -19,6 +19,33 @@ template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
 
+// Programmatic dependent launch.  The kernels of a decode step are launched
+// (launch_pdl) so that each may be scheduled while the one before it drains:
+// a kernel calls pdl_trigger() at its start, which lets the next launch as
+// soon as every CTA of this one has started, and pdl_wait() before it touches
+// any global memory an earlier kernel of the stream writes or reads — the wait
+// returns once the previous grid has completed and its writes are visible.
+// Every CTA passes pdl_wait() before it exits, so completion is ordered along
+// the whole chain.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // 16-byte vector of T: 4 floats or 8 bf16.
 template <typename T> struct Vec16 {
   static constexpr int N = 16 / sizeof(T);

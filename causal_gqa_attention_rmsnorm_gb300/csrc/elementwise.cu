@@ -56,6 +56,8 @@ __global__ void k_row_stats(const T* __restrict__ x, int M, int d, float eps, fl
                             int* __restrict__ cnt_zero, int Tseq, int32_t* __restrict__ lens_set,
                             int32_t* __restrict__ lens_bump, int32_t* __restrict__ pos_out, int T_max,
                             int* __restrict__ zero_word, int* __restrict__ err) {
+  pdl_trigger();
+  pdl_wait();
   const int row = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -184,6 +186,8 @@ __device__ __forceinline__ void quantize_row128(const bf16* __restrict__ x, int8
 __global__ void k_quantize_kv(const bf16* __restrict__ kn, const bf16* __restrict__ vn, int rows,
                               const int32_t* __restrict__ start, int Hkv, int T_max, int8_t* __restrict__ kq,
                               float* __restrict__ ks, int8_t* __restrict__ vq, float* __restrict__ vs) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + warp, h = blockIdx.y, b = blockIdx.z;
   if (r >= rows) return;
@@ -232,12 +236,10 @@ cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, 
   const int threads = 256;
   const unsigned blocks = (unsigned)(((size_t)M * 32 + threads - 1) / threads);
   if (dtype == TB_F32)
-    k_row_stats<float><<<blocks, threads, 0, s>>>((const float*)x, M, d, eps, r, cnt_zero, T, lens_set,
-                                                  lens_bump, pos_out, T_max, zero_word, err);
-  else
-    k_row_stats<bf16><<<blocks, threads, 0, s>>>((const bf16*)x, M, d, eps, r, cnt_zero, T, lens_set,
-                                                 lens_bump, pos_out, T_max, zero_word, err);
-  return cudaGetLastError();
+    return launch_pdl(k_row_stats<float>, dim3(blocks), dim3(threads), 0, s, (const float*)x, M, d, eps, r,
+                      cnt_zero, T, lens_set, lens_bump, pos_out, T_max, zero_word, err);
+  return launch_pdl(k_row_stats<bf16>, dim3(blocks), dim3(threads), 0, s, (const bf16*)x, M, d, eps, r, cnt_zero,
+                    T, lens_set, lens_bump, pos_out, T_max, zero_word, err);
 }
 
 cudaError_t launch_pack_transpose(int dtype, const void* src, int K, int N, const void* gain, void* dst,
@@ -257,9 +259,8 @@ cudaError_t launch_quantize_kv(const tb_kvcache& kv, const void* k_new, const vo
   if (kv.B > 65535 || kv.Hkv > 65535) return cudaErrorInvalidValue;
   const int warps = std::min(rows, 8);
   const dim3 grid((unsigned)((rows + warps - 1) / warps), kv.Hkv, kv.B);
-  k_quantize_kv<<<grid, 32 * warps, 0, s>>>((const bf16*)k_new, (const bf16*)v_new, rows, start, kv.Hkv, kv.T_max,
-                                            (int8_t*)kv.k, kv.k_scale, (int8_t*)kv.v, kv.v_scale);
-  return cudaGetLastError();
+  return launch_pdl(k_quantize_kv, grid, dim3(32 * warps), 0, s, (const bf16*)k_new, (const bf16*)v_new, rows,
+                    start, kv.Hkv, kv.T_max, (int8_t*)kv.k, kv.k_scale, (int8_t*)kv.v, kv.v_scale);
 }
 
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new, int n,

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(192)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int items = tiles * splits;
   auto krange = [&](int sp, int& kb0, int& nkb) {
@@ -96,6 +97,18 @@ __global__ void __launch_bounds__(192)
 
   if (warp == 0) {
     if (lane == 0) {
+      // The weights do not depend on earlier kernels: the first STAGES weight
+      // tiles are requested before the wait for the previous kernel, so they
+      // stream while it drains; their token tiles follow the wait.
+      int held_kb[STAGES];
+      int held = 0;
+      bool dep = false;
+      auto release = [&]() {
+        pdl_wait();
+        dep = true;
+        for (int h = 0; h < held; ++h)       // stage h holds the h-th K block issued
+          tma_load_2d(&tmX, smem + h * C::STAGE_BYTES + C::W_BYTES, &full[h], held_kb[h] * kBK, 0);
+      };
       int i = 0;                                  // running K-block count: stage i % STAGES
       bool ok = true;
       for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
@@ -111,9 +124,15 @@ __global__ void __launch_bounds__(192)
           uint8_t* sw = smem + st * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
           tma_load_2d(&tmW, sw, &full[st], (kb0 + j) * kBK, tile * kRows);
-          tma_load_2d(&tmX, sw + C::W_BYTES, &full[st], (kb0 + j) * kBK, 0);
+          if (dep) {
+            tma_load_2d(&tmX, sw + C::W_BYTES, &full[st], (kb0 + j) * kBK, 0);
+          } else {
+            held_kb[held++] = kb0 + j;
+            if (held == STAGES) release();
+          }
         }
       }
+      if (!dep) release();
       // every copy issued must land before the CTA may exit (earlier copies
       // into the same stages were consumed, hence complete)
       volatile int no_abort = 0;
@@ -193,6 +212,8 @@ __global__ void __launch_bounds__(192)
 template <class Epi>
 __global__ void __launch_bounds__(256)
     k_splitk_epilogue(const float* __restrict__ part, int splits, int M, int N, Epi epi) {
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.y;
   const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   float r = 0.f;
@@ -289,12 +310,11 @@ cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi&
   const int tiles = (N + kRows - 1) / kRows, kblocks = K / kBK;
   const int splits = split_count(tiles, kblocks);
   const int items = tiles * splits, slots = 2 * sm_count();
-  k_gemm_skinny<NT><<<items < slots ? items : slots, 192, C::SMEM, s>>>(tw, tx, M, N, tiles, kblocks, splits, part,
-                                                                       device_error_word());
-  e = cudaGetLastError();
+  e = launch_pdl(k_gemm_skinny<NT>, dim3(items < slots ? items : slots), dim3(192), C::SMEM, s, tw, tx, M, N, tiles,
+                 kblocks, splits, part, device_error_word());
   if (e != cudaSuccess) return e;
-  k_splitk_epilogue<Epi><<<dim3((N / 4 + 255) / 256, M), 256, 0, s>>>(part, splits, M, N, epi);
-  return cudaGetLastError();
+  return launch_pdl(k_splitk_epilogue<Epi>, dim3((N / 4 + 255) / 256, M), dim3(256), 0, s, (const float*)part, splits,
+                    M, N, epi);
 }
 
 template <class Epi>
