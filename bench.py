@@ -784,7 +784,7 @@ def main():
     ap.add_argument("--stack-layers", type=int, default=4, help="layers of the model line (0: skip)")
     ap.add_argument("--vocab", type=int, default=128256, help="vocabulary of the model line's LM head")
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
-    ap.add_argument("--cpu-tokens", type=int, default=2048, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=4096, help="oracle sample size for cpu_baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -834,6 +834,7 @@ def main():
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(1,0.1) gains)",
         "config": workload_config(s),
         "attn_tflops": attn_tflops, "attn_frac_bf16": attn_tflops / peaks["bf16_tflops"],
+        "attn_tflops_tile_count": acc.causal_attn_flops_tiles(s.B, s.H, s.dh, s.T) / (stages["attn"] * 1e-3) / 1e12,
         "attn_frac_bf16_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
         "gemm_tflops": gemm_tflops, "gemm_frac_bf16": gemm_tflops / peaks["bf16_tflops"],
         "gemm_frac_bf16_sustained": gemm_tflops / peaks["bf16_tflops_sustained"],

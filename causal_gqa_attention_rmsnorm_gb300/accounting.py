@@ -60,6 +60,14 @@ def causal_attn_flops(B: int, H: int, dh: int, T: int, window: int = 0) -> int:
     return 4 * B * H * dh * visible_pairs(T, window)
 
 
+def causal_attn_flops_tiles(B: int, H: int, dh: int, T: int, tile: int = 128) -> int:
+    """Causal attention FLOPs counted per tile: every (query tile, key tile)
+    pair on or below the diagonal counted in full, tile x tile pairs (a
+    kernel's work with the diagonal tiles unmasked)."""
+    nt = (T + tile - 1) // tile
+    return 4 * B * H * dh * tile * tile * nt * (nt + 1) // 2
+
+
 def full_attn_flops(B: int, H: int, dh: int, T: int) -> int:
     """Attention FLOPs counting the whole T×T square (the pages' 4·T·d per token)."""
     return 4 * B * H * dh * T * T

@@ -91,6 +91,16 @@ def test_causal_attention_is_about_half_the_square():
     assert abs(causal / full - 0.5) < 1e-3
 
 
+def test_tile_granular_attention_count():
+    # one tile: the whole tile square; T a multiple of the tile: nt(nt+1)/2 squares,
+    # just above the exact pair count by the upper halves of the diagonal tiles
+    assert acc.causal_attn_flops_tiles(1, 1, 1, 128) == 4 * 128 * 128
+    T, nt = 8192, 64
+    tiles = acc.causal_attn_flops_tiles(4, 32, 128, T)
+    exact = acc.causal_attn_flops(4, 32, 128, T)
+    assert tiles - exact == 4 * 4 * 32 * 128 * nt * (128 * 127 // 2)
+
+
 def test_decode_kv_bytes():
     # GQA decode reads lens+1 rows of K and V per KV head
     assert acc.decode_kv_bytes([3, 0], Hkv=8, dh=128, bytes_per_value=2) == (4 + 1) * 2 * 8 * 128 * 2
