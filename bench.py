@@ -784,7 +784,7 @@ def main():
     ap.add_argument("--stack-layers", type=int, default=4, help="layers of the model line (0: skip)")
     ap.add_argument("--vocab", type=int, default=128256, help="vocabulary of the model line's LM head")
     ap.add_argument("--ref-tokens", type=int, default=512, help="oracle sample size per reference step")
-    ap.add_argument("--cpu-tokens", type=int, default=4096, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=6144, help="oracle sample size for cpu_baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
