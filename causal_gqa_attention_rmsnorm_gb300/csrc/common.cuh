@@ -146,6 +146,22 @@ struct RowSum {
   int stride;              // partials per row the buffer holds
 };
 
+// Σ_{p < n} part[p] added in the order p = 0, 1, ..., with the loads issued
+// eight at a time (L2 reads of partials other CTAs wrote).
+__device__ __forceinline__ float ordered_sum(const float* part, int n) {
+  float sum = 0.f;
+  int p = 0;
+  for (; p + 8 <= n; p += 8) {
+    float t[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) t[u] = __ldcg(part + p + u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) sum += t[u];
+  }
+  for (; p < n; ++p) sum += __ldcg(part + p);
+  return sum;
+}
+
 // GEMM epilogue argument bundles.
 struct QKVArgs {
   const float* r;          // [M] RMSNorm-1 inverse RMS of each token

@@ -75,9 +75,7 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const T* __restrict__ A, cons
     if (last && threadIdx.x < BM && m0 + (int)threadIdx.x < M) {
       __threadfence();
       const int row = m0 + threadIdx.x;
-      float sum = 0.f;
-      for (int p = 0; p < (int)gridDim.x; ++p) sum += __ldcg(rs.part + (size_t)row * rs.stride + p);
-      rs.out[row] = sum;
+      rs.out[row] = ordered_sum(rs.part + (size_t)row * rs.stride, (int)gridDim.x);
     }
   }
 }

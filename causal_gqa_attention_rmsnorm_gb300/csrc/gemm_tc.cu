@@ -217,9 +217,7 @@ __global__ void __launch_bounds__(192, 1)
           __threadfence();
           const int row = pend_row0 + lane;
           if (row < M) {
-            float sum = 0.f;
-            for (int p = 0; p < n_tiles; ++p) sum += __ldcg(rs.part + (size_t)row * rs.stride + p);
-            rs.out[row] = sum;
+            rs.out[row] = ordered_sum(rs.part + (size_t)row * rs.stride, n_tiles);
           }
         }
         pend_row0 = -1;

@@ -138,6 +138,30 @@ def test_int8_decode_matches_oracle(Hkv, W):
         np.testing.assert_array_equal(np.delete(kq[b], pos, axis=1), np.delete(host[0][b], pos, axis=1))
 
 
+def test_int8_decode_full_cache_sets_error_and_skips_row():
+    """A sequence whose cache is full is skipped (error bit set, its rows and
+    length untouched); the others step normally."""
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    T_max = 64
+    lens = [10, T_max, 63]
+    s = BASE.with_(B=3, T=T_max)
+    inp = workloads.make_block_inputs(s, seed=5)
+    kv, host = _int8_cache(s, 5, lens[:1] + [T_max - 1] + lens[2:], T_max)
+    kv.lens.copy_(torch.tensor(lens, dtype=torch.int32))
+    cfg = block_config(s, max_pos=T_max)
+    dev = to_device(inp)
+    packed = tb.tb_pack_weights(cfg, dev)
+    y = tb.tb_block_decode(cfg, packed, dev["x"], kv)
+    assert tb.tb_get_device_error(clear=True) & tb.TB_DEVERR_CACHE_FULL
+    assert kv.lens.cpu().tolist() == [11, T_max, 64]
+    np.testing.assert_array_equal(kv.k[1].cpu().numpy(), host[0][1])
+    np.testing.assert_array_equal(kv.k_scale[1].cpu().numpy(), host[1][1])
+    for b in (0, 2):
+        ref = _oracle_i8(s, inp, host, b, lens[b])
+        assert_close(y[b, 0].cpu().double().numpy(), ref["y"], "bf16", f"y b={b}")
+        _check_new_row(kv, b, lens[b], ref, f"b={b}")
+
+
 def test_int8_decode_noalloc_equals_decode():
     import causal_gqa_attention_rmsnorm_gb300 as tb
     lens = [3, 300, 700]
