@@ -40,6 +40,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FEW_TOKENS = 64
 
 
+# The headline metric, the same string on both arms.
+METRIC = "prefill tokens/s per block (attention TFLOP/s, GEMM TFLOP/s; decode KV GB/s)"
+
+
 def decode_launches(B: int) -> int:
     """Kernels one decode step launches: row statistics, the two attention
     kernels, and the four GEMMs."""
@@ -185,7 +189,7 @@ def run_reference(args, world, rank):
     value = tokens * len(times) / total
     sample = f"fp64 oracle prefill of the first {tokens} tokens of one sequence of {s.name}, per step"
     line = {
-        "impl": "reference", "metric": "prefill tokens/s per block", "value": value, "unit": "tok/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(s),
@@ -828,7 +832,7 @@ def main():
     gemm_ms = sum(stages[k] for k in ("qkv", "wo", "w13", "w2"))
     gemm_tflops = sum(work[k][1] for k in ("qkv", "wo", "w13", "w2")) / (gemm_ms * 1e-3) / 1e12
     line = {
-        "metric": "prefill tokens/s per block (attention TFLOP/s, GEMM TFLOP/s; decode KV GB/s)",
+        "metric": METRIC,
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(1,0.1) gains)",
