@@ -612,26 +612,27 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
 //
 // The same work items and chunk states as k_decode_mma, over a cache of int8
 // codes with one fp32 scale per row (a row reads back as code·scale).  A
-// 16-key stage is 2 KB of K codes and 2 KB of V codes, half a bf16 stage, plus
-// the stage's 32 row scales.
+// 32-key stage is 4 KB of K codes and 4 KB of V codes, as much as a 16-key
+// bf16 stage, plus the stage's 64 row scales.
 //
-// Sixteen warps per CTA (the transposed layout below keeps a warp at 124
-// registers), each with a ring of three stage slots; as in the bf16 kernel,
+// Twelve warps per CTA (the transposed layout below keeps a warp at 155
+// registers), each with a ring of two stage slots; as in the bf16 kernel,
 // lane 0 of each warp takes work items from the global counter and issues the
-// warp's own copies (two TMA boxes of codes, two 64-byte bulk copies of
+// warp's own copies (two TMA boxes of codes, two 128-byte bulk copies of
 // scales), writing beside each slot which item and stage it holds so that the
 // warp never decodes an item.  Producers in every warp keep the copies spread
 // over all four schedulers; one producer warp for the whole CTA could not
-// issue them fast enough.
+// issue them fast enough.  (Sixteen warps with three 16-key slots each ran
+// 2.5% slower.)
 //
 // Both contractions run transposed, on fp16 m16n8k16 MMAs with fp32
 // accumulators, so that the query heads sit on the MMA's n side (8 columns)
 // instead of padding its 16 rows:
-//   Sᵀ[16 keys × 8 heads] = K·Qᵀ.  ldmatrix gives lane (g, t) four
-//     consecutive codes of key g (dims 16p+4t .. 16p+4t+3); the MMA's k index
-//     is mapped onto dims so that those four are its two k pairs, and Q's
-//     fragment uses the same map (a dot product does not depend on the order
-//     of its terms).
+//   Sᵀ[16 keys × 8 heads] = K·Qᵀ for each 16-key half of a stage.  ldmatrix
+//     gives lane (g, t) four consecutive codes of key g (dims 16p+4t ..
+//     16p+4t+3); the MMA's k index is mapped onto dims so that those four are
+//     its two k pairs, and Q's fragment uses the same map (a dot product does
+//     not depend on the order of its terms).
 //   Oᵀ[16 dims × 8 heads] += Vᵀ·Pᵀ.  ldmatrix.trans on 16-bit units gives
 //     lane (g, t) the codes of keys 2t, 2t+1 at dims 2g, 2g+1: one word is the
 //     A fragment of rows g (dim 16p+2g) and g+8 (dim 16p+2g+1).  Pᵀ comes from
@@ -650,17 +651,18 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
 // [1/16, 16]: P·scale·vf then stays far from fp16's overflow and underflow
 // whatever the magnitude of V.  The frame moves like the softmax maximum,
 // rarely, and both rescale O by exact factors.
-constexpr int kQWarps = 16;      // warps per CTA, each its own producer
-constexpr int kQSlots = 3;       // stage slots per warp
+constexpr int kQKeys = 32;       // keys per stage
+constexpr int kQWarps = 12;      // warps per CTA, each its own producer
+constexpr int kQSlots = 2;       // stage slots per warp
 struct QDesc {
   int4 a;                        // sequence, KV head, chunk, stage
   int4 b;                        // first key of the chunk, its keys, first visible key, item id (-1: no more)
 };
 struct QCfg {
-  static constexpr uint32_t BOX = kMKeys * 128;        // 16 rows x 128 codes
+  static constexpr uint32_t BOX = kQKeys * 128;        // 32 rows x 128 codes
   static constexpr uint32_t SLOT = 2 * BOX;            // K codes, then V codes
   static constexpr uint32_t WARP_BYTES = kQSlots * SLOT;
-  static constexpr uint32_t SC = 2 * kMKeys * 4;       // K then V scales of one stage
+  static constexpr uint32_t SC = 2 * kQKeys * 4;       // K then V scales of one stage
   static constexpr uint32_t TX = SLOT + SC;            // bytes one stage brings in
   static constexpr uint32_t OFF_SC = kQWarps * WARP_BYTES;
   static constexpr uint32_t OFF_DESC = OFF_SC + kQWarps * kQSlots * SC;
@@ -746,7 +748,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
       pre[b] = acc;
       const int p = pos_arr[b];
       nlen[b] = p < 0 ? 0 : p + 1;
-      acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kMKeys) + kMChunk - 1) / kMChunk);
+      acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kQKeys) + kMChunk - 1) / kMChunk);
     }
     pre[B] = acc;
     abort_word = 0;
@@ -787,7 +789,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
           lo = l2;
         }
         const int n = nlen[lo];
-        const int base = chunk_base(n, window, kMKeys);
+        const int base = chunk_base(n, window, kQKeys);
         const int nch = (n - base + kMChunk - 1) / kMChunk;
         const int r = pid - pre[lo];
         pb = lo;
@@ -797,19 +799,19 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
         pnkeys = min(kMChunk, n - pkey0);
         pfirst = window_first(n, window);
         pst = 0;
-        pnst = (pnkeys + kMKeys - 1) / kMKeys;
+        pnst = (pnkeys + kQKeys - 1) / kQKeys;
       }
       desc[bi].a = make_int4(pb, pkvh, pc, pst);
       desc[bi].b = make_int4(pkey0, pnkeys, pfirst, pid);
       uint8_t* dst = smem + pw * C::WARP_BYTES + sl * C::SLOT;
       float* sc = reinterpret_cast<float*>(smem + C::OFF_SC + bi * C::SC);
       mbar_arrive_expect_tx(&full[bi], C::TX);
-      const int key = pkey0 + pst * kMKeys, plane = pb * Hkv + pkvh;
+      const int key = pkey0 + pst * kQKeys, plane = pb * Hkv + pkvh;
       tma_load_3d(&tmK, dst, &full[bi], 0, key, plane);
       tma_load_3d(&tmV, dst + C::BOX, &full[bi], 0, key, plane);
       const size_t srow = (size_t)plane * T_max + key;
-      bulk_load(sc, kscale + srow, kMKeys * 4, &full[bi]);
-      bulk_load(sc + kMKeys, vscale + srow, kMKeys * 4, &full[bi]);
+      bulk_load(sc, kscale + srow, kQKeys * 4, &full[bi]);
+      bulk_load(sc + kQKeys, vscale + srow, kQKeys * 4, &full[bi]);
       ++pst;
       ++issued;
     }
@@ -884,31 +886,46 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
     }
     const uint32_t kbase = slots_u32 + sl * C::SLOT, vbase = kbase + C::BOX;
     const float* sc = scw + sl * (C::SC / 4);
-    const int nvalid = min(kMKeys, inkeys - st * kMKeys);
-    const int lead = ifirst - (ikey0 + st * kMKeys);   // keys below lead precede the window
+    const int nvalid = min(kQKeys, inkeys - st * kQKeys);
+    const int lead = ifirst - (ikey0 + st * kQKeys);   // keys below lead precede the window
 
-    // Sᵀ = K·Qᵀ (biased codes), even and odd slices in two accumulators
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    // Sᵀ = K·Qᵀ (biased codes) for keys 16h .. 16h+15, h = 0, 1; even and odd
+    // slices in separate accumulators
+    float sa[2][4], sb[2][4];
 #pragma unroll
-    for (int pp = 0; pp < DH / 32; ++pp) {
-      uint32_t kb[4];
-      ldsm_x4(swz128(kbase, lrow, 2 * pp + (mi >> 1)), kb);
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) kb[j] ^= 0x80808080u;
-      mma16816_f16(sa, biased_f16x2(kb[0], 0x4140), biased_f16x2(kb[1], 0x4140), biased_f16x2(kb[0], 0x4342),
-                   biased_f16x2(kb[1], 0x4342), qb0[2 * pp], qb1[2 * pp]);
-      mma16816_f16(sb, biased_f16x2(kb[2], 0x4140), biased_f16x2(kb[3], 0x4140), biased_f16x2(kb[2], 0x4342),
-                   biased_f16x2(kb[3], 0x4342), qb0[2 * pp + 1], qb1[2 * pp + 1]);
-    }
-    // lane (g, t): keys g and g+8, heads 2t and 2t+1
-    const float ks_lo = sc[g], ks_hi = sc[8 + g], vs_lo = sc[16 + g], vs_hi = sc[24 + g];
-    const bool ok_lo = g < nvalid && g >= lead, ok_hi = g + 8 < nvalid && g + 8 >= lead;
-    const float r00 = ok_lo ? ks_lo * fmaf(sa[0] + sb[0], A0, -Bc0) : -INFINITY;
-    const float r01 = ok_lo ? ks_lo * fmaf(sa[1] + sb[1], A1, -Bc1) : -INFINITY;
-    const float r10 = ok_hi ? ks_hi * fmaf(sa[2] + sb[2], A0, -Bc0) : -INFINITY;
-    const float r11 = ok_hi ? ks_hi * fmaf(sa[3] + sb[3], A1, -Bc1) : -INFINITY;
-    const float w_lo = ok_lo ? vs_lo : 0.f, w_hi = ok_hi ? vs_hi : 0.f;
-    float mx0 = fmaxf(r00, r10), mx1 = fmaxf(r01, r11), vmax = fmaxf(w_lo, w_hi);
+      for (int j = 0; j < 4; ++j) sa[h][j] = sb[h][j] = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < DH / 32; ++pp)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t kb[4];
+        ldsm_x4(swz128(kbase, lrow + 16 * h, 2 * pp + (mi >> 1)), kb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) kb[j] ^= 0x80808080u;
+        mma16816_f16(sa[h], biased_f16x2(kb[0], 0x4140), biased_f16x2(kb[1], 0x4140), biased_f16x2(kb[0], 0x4342),
+                     biased_f16x2(kb[1], 0x4342), qb0[2 * pp], qb1[2 * pp]);
+        mma16816_f16(sb[h], biased_f16x2(kb[2], 0x4140), biased_f16x2(kb[3], 0x4140), biased_f16x2(kb[2], 0x4342),
+                     biased_f16x2(kb[3], 0x4342), qb0[2 * pp + 1], qb1[2 * pp + 1]);
+      }
+    // lane (g, t): keys 16h + 8s + g (h, s = 0, 1), heads 2t and 2t+1
+    float r[2][2][2], wv[2][2];
+    float mx0 = -INFINITY, mx1 = -INFINITY, vmax = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int sk = 0; sk < 2; ++sk) {
+        const int key = 16 * h + 8 * sk + g;
+        const bool ok = key < nvalid && key >= lead;
+        const float ks = sc[key], vs = sc[kQKeys + key];
+        r[h][sk][0] = ok ? ks * fmaf(sa[h][2 * sk] + sb[h][2 * sk], A0, -Bc0) : -INFINITY;
+        r[h][sk][1] = ok ? ks * fmaf(sa[h][2 * sk + 1] + sb[h][2 * sk + 1], A1, -Bc1) : -INFINITY;
+        wv[h][sk] = ok ? vs : 0.f;
+        mx0 = fmaxf(mx0, r[h][sk][0]);
+        mx1 = fmaxf(mx1, r[h][sk][1]);
+        vmax = fmaxf(vmax, wv[h][sk]);
+      }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -949,32 +966,38 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
         o[p][3] *= f1;
       }
     }
-    const float p00 = ex2_approx(r00 - m0), p01 = ex2_approx(r01 - m1);
-    const float p10 = ex2_approx(r10 - m0), p11 = ex2_approx(r11 - m1);
-    l0 += p00 + p10;
-    l1 += p01 + p11;
-    const float wl = w_lo * vf, wh = w_hi * vf;
-    const uint32_t pk_lo = pack_f16(p00 * wl, p01 * wl), pk_hi = pack_f16(p10 * wh, p11 * wh);
-    {
+    // P·scale·vf in fp16, then the Pᵀ fragments of each 16-key half by movmatrix
+    uint32_t pb0[2], pb1[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float p00 = ex2_approx(r[h][0][0] - m0), p01 = ex2_approx(r[h][0][1] - m1);
+      const float p10 = ex2_approx(r[h][1][0] - m0), p11 = ex2_approx(r[h][1][1] - m1);
+      l0 += p00 + p10;
+      l1 += p01 + p11;
+      const float wl = wv[h][0] * vf, wh = wv[h][1] * vf;
+      const uint32_t pk_lo = pack_f16(p00 * wl, p01 * wl), pk_hi = pack_f16(p10 * wh, p11 * wh);
       const float2 a = unpack_f16(pk_lo), c = unpack_f16(pk_hi);
       lv0 += a.x + c.x;
       lv1 += a.y + c.y;
+      pb0[h] = movmatrix_t(pk_lo);
+      pb1[h] = movmatrix_t(pk_hi);
     }
-    const uint32_t pb0 = movmatrix_t(pk_lo), pb1 = movmatrix_t(pk_hi);   // Pᵀ fragments: keys 2t, 2t+1 (+8) of head g
-    // Oᵀ += Vᵀ·Pᵀ: m-tile p = dims 16p + 2g (rows g) and 16p + 2g + 1 (rows g+8)
+    // Oᵀ += Vᵀ·Pᵀ: m-tile p = dims 16p + 2g (rows g) and 16p + 2g + 1 (rows g+8), k = the two key halves
 #pragma unroll
-    for (int pp = 0; pp < DH / 32; ++pp) {
-      uint32_t vb[4];
-      ldsm_x4_t(swz128(vbase, lrow, 2 * pp + (mi >> 1)), vb);
+    for (int pp = 0; pp < DH / 32; ++pp)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) vb[j] ^= 0x80808080u;
-      mma16816_f16(o[2 * pp], biased_f16x2(vb[0], 0x4240), biased_f16x2(vb[0], 0x4341), biased_f16x2(vb[1], 0x4240),
-                   biased_f16x2(vb[1], 0x4341), pb0, pb1);
-      mma16816_f16(o[2 * pp + 1], biased_f16x2(vb[2], 0x4240), biased_f16x2(vb[2], 0x4341),
-                   biased_f16x2(vb[3], 0x4240), biased_f16x2(vb[3], 0x4341), pb0, pb1);
-    }
+      for (int h = 0; h < 2; ++h) {
+        uint32_t vb[4];
+        ldsm_x4_t(swz128(vbase, lrow + 16 * h, 2 * pp + (mi >> 1)), vb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) vb[j] ^= 0x80808080u;
+        mma16816_f16(o[2 * pp], biased_f16x2(vb[0], 0x4240), biased_f16x2(vb[0], 0x4341),
+                     biased_f16x2(vb[1], 0x4240), biased_f16x2(vb[1], 0x4341), pb0[h], pb1[h]);
+        mma16816_f16(o[2 * pp + 1], biased_f16x2(vb[2], 0x4240), biased_f16x2(vb[2], 0x4341),
+                     biased_f16x2(vb[3], 0x4240), biased_f16x2(vb[3], 0x4341), pb0[h], pb1[h]);
+      }
     __syncwarp();             // the slot may be refilled after this
-    if ((st + 1) * kMKeys >= inkeys) {
+    if ((st + 1) * kQKeys >= inkeys) {
       // the item's partial state for heads 2t and 2t+1: sums over the eight key rows g
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
@@ -1022,9 +1045,9 @@ cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const f
   using C = QCfg;
   CUtensorMap tk, tv;
   const uint64_t planes = (uint64_t)B * Hkv;
-  cudaError_t e = make_tmap_3d_u8(&tk, kc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kMKeys);
+  cudaError_t e = make_tmap_3d_u8(&tk, kc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kQKeys);
   if (e != cudaSuccess) return e;
-  e = make_tmap_3d_u8(&tv, vc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kMKeys);
+  e = make_tmap_3d_u8(&tv, vc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kQKeys);
   if (e != cudaSuccess) return e;
   const size_t smem = C::OFF_PRE + (size_t)(2 * B + 1) * 4 + 1024;
   if (smem > 232448) return cudaErrorInvalidValue;
@@ -1041,7 +1064,7 @@ cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const f
                  Hkv, T_max, part, nchunk_max, counter, window, scale_log2, device_error_word());
   if (e != cudaSuccess) return e;
   return launch_pdl(k_decode_combine<bf16, 128>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
-                    nchunk_max, kMChunk, window, kMKeys, (bf16*)o);
+                    nchunk_max, kMChunk, window, kQKeys, (bf16*)o);
 }
 
 template <int DH, int G>

@@ -204,11 +204,11 @@ cudaError_t mm_w2(const Work& W, const void* A, const void* Bw, int M, int N, in
   return W.skpart ? gemm_skinny_w2(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_w2(A, Bw, M, N, K, D, e, s);
 }
 
-// The int8 layout's own rules (dh 128, contiguous, 16-row stages, scales).
+// The int8 layout's own rules (dh 128, contiguous, 32-row stages, scales).
 tb_status check_i8(const tb_kvcache* kv) {
   if (kv->dh != 128) return fail(TB_ERR_UNSUPPORTED, "an int8 cache needs dh 128 (dh=%d)", kv->dh);
   if (kv->block_table) return fail(TB_ERR_UNSUPPORTED, "an int8 cache is contiguous (no block table)");
-  if (kv->T_max % 16) return fail(TB_ERR_UNSUPPORTED, "an int8 cache needs T_max a multiple of 16 (%d)", kv->T_max);
+  if (kv->T_max % 32) return fail(TB_ERR_UNSUPPORTED, "an int8 cache needs T_max a multiple of 32 (%d)", kv->T_max);
   if (!kv->k_scale || !kv->v_scale || !aligned16(kv->k_scale) || !aligned16(kv->v_scale))
     return fail(TB_ERR_INVALID_ARG, "an int8 cache needs 16-byte aligned k_scale and v_scale");
   return TB_OK;

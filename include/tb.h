@@ -122,7 +122,7 @@ typedef struct {
  *    Row x (one token of one KV head) is stored as s = max|x| / 127 and codes
  *    q = round-half-even(x / s) clamped to [-127, 127], s and x / s evaluated
  *    in fp32 (a zero row: s = 0, q = 0); it reads back as q·s.  Only a bf16
- *    block with dh = 128 and T_max a multiple of 16 takes an int8 cache.
+ *    block with dh = 128 and T_max a multiple of 32 takes an int8 cache.
  *    Prefill attends over the unquantised rows and stores their codes; a
  *    decode step stores the new token's codes first, then attends over the
  *    dequantised rows, its own included.

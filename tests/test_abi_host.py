@@ -141,12 +141,12 @@ def test_int8_cache_checks(lib):
                                         k.get("vs", FAKE))
     assert decode(i8(ks=None)) == 1 and b"k_scale" in lib.tb_last_error_message()
     assert decode(i8(vs=FAKE + 4)) == 1                       # misaligned scales
-    assert decode(i8(T_max=250)) == 2                         # T_max not a multiple of 16
+    assert decode(i8(T_max=240)) == 2                         # T_max not a multiple of 32
     assert decode(i8(bt=FAKE, ps=16, np=8)) == 2              # no paged int8 layout
     assert decode(i8(), cfg(d=512, H=4, Hkv=2, dh=128, dtype=tb.TB_F32)) == 2   # fp32 block
     assert decode(i8(dh=64), cfg()) == 2                      # dh 64
     # append: bf16 rows into the int8 layout, same rules
-    assert lib.tb_kvcache_append(ctypes.byref(i8(T_max=250)), FAKE, FAKE, 3, None) == 2
+    assert lib.tb_kvcache_append(ctypes.byref(i8(T_max=240)), FAKE, FAKE, 3, None) == 2
     assert lib.tb_kvcache_append(ctypes.byref(i8(ks=None)), FAKE, FAKE, 3, None) == 1
     assert lib.tb_kvcache_append(ctypes.byref(i8()), FAKE, FAKE, 300, None) == 4    # more rows than T_max
 
