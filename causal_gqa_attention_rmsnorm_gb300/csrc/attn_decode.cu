@@ -214,10 +214,14 @@ __global__ void __launch_bounds__(kWarps * 32) k_decode_split(const T* __restric
 }
 
 // o[b, h·DH + e] = Σ_c acc_c[e]·2^(m_c - M) / Σ_c l_c·2^(m_c - M), M = max_c m_c.
-// One CTA per (head, sequence): the chunk maxima and sums are read in
-// parallel into shared memory, every thread forms the weights from there, and
-// each output dimension sums its chunks with independent loads.
+// One CTA per (head, sequence).  Every global load is issued first: each
+// thread reads the (m, l) pair of a chunk and, for output column e, the values
+// of up to kCombineRegs of its chunks into registers; after one block
+// reduction of the maxima and one of the sums, the weighted sums need no
+// further global round trip (chunks beyond what the registers hold are read in
+// a second pass).  All sums run in a fixed order.
 constexpr int kCombineMaxChunks = 1024;
+constexpr int kCombineRegs = 32;
 
 template <typename T, int DH>
 __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict__ part,
@@ -225,12 +229,9 @@ __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict_
                                                         int chunk, int window, int align, T* __restrict__ o) {
   pdl_trigger();
   pdl_wait();
-  // Thread (e, g) sums output column e over chunks g, g + NG, ... with eight
-  // independent loads in flight, so the merge costs a few L2 round trips.
   static_assert(256 % DH == 0, "head width must divide the block");
-  constexpr int NG = 256 / DH;
-  constexpr int U = 8;
-  __shared__ float w_s[kCombineMaxChunks];
+  constexpr int NG = 256 / DH;      // thread groups, each covering the DH columns
+  __shared__ float w_s[kCombineMaxChunks], l_s[kCombineMaxChunks];
   __shared__ float red[256 / 32];
   __shared__ float acc_s[NG][DH];
   const int h = blockIdx.x, b = blockIdx.y;
@@ -245,12 +246,20 @@ __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict_
   constexpr int P = PartLayout<DH>::stride;
   const float* pr = part + ((size_t)b * H + h) * nchunk_max * P;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // M = max_c m_c
+  const int e = threadIdx.x % DH, g = threadIdx.x / DH;
+  // thread (e, g) holds column e of chunks g, g + NG, ...
+  float v[kCombineRegs];
+#pragma unroll
+  for (int u = 0; u < kCombineRegs; ++u) {
+    const int c = g + NG * u;
+    v[u] = c < nc ? pr[(size_t)c * P + 4 + e] : 0.f;
+  }
   float mx = -INFINITY;
   for (int c = threadIdx.x; c < nc; c += blockDim.x) {
-    const float m = pr[(size_t)c * P];
-    w_s[c] = m;
-    mx = fmaxf(mx, m);
+    const float2 ml = *reinterpret_cast<const float2*>(pr + (size_t)c * P);
+    w_s[c] = ml.x;
+    l_s[c] = ml.y;
+    mx = fmaxf(mx, ml.x);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict_
   for (int c = threadIdx.x; c < nc; c += blockDim.x) {
     const float w = exp2f(w_s[c] - M);
     w_s[c] = w;
-    Lp += pr[(size_t)c * P + 1] * w;
+    Lp += l_s[c] * w;
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, off);
@@ -274,23 +283,14 @@ __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict_
   float L = 0.f;
 #pragma unroll
   for (int i = 0; i < 256 / 32; ++i) L += red[i];
-  const int e = threadIdx.x % DH, g = threadIdx.x / DH;
-  float a[U];
+  float a = 0.f;
 #pragma unroll
-  for (int u = 0; u < U; ++u) a[u] = 0.f;
-  int c = g;
-  for (; c + (U - 1) * NG < nc; c += U * NG) {
-    float v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) v[u] = pr[(size_t)(c + u * NG) * P + 4 + e];
-#pragma unroll
-    for (int u = 0; u < U; ++u) a[u] = fmaf(v[u], w_s[c + u * NG], a[u]);
+  for (int u = 0; u < kCombineRegs; ++u) {
+    const int c = g + NG * u;
+    if (c < nc) a = fmaf(v[u], w_s[c], a);
   }
-  for (; c < nc; c += NG) a[0] = fmaf(pr[(size_t)c * P + 4 + e], w_s[c], a[0]);
-  float t = 0.f;
-#pragma unroll
-  for (int u = 0; u < U; ++u) t += a[u];
-  acc_s[g][e] = t;
+  for (int c = g + NG * kCombineRegs; c < nc; c += NG) a = fmaf(pr[(size_t)c * P + 4 + e], w_s[c], a);
+  acc_s[g][e] = a;
   __syncthreads();
   if (g == 0) {
     float sum = 0.f;
