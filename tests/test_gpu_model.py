@@ -137,3 +137,30 @@ def test_stack_of_one_is_the_block():
     y_block = tb.tb_block_prefill(cfg, packed[0], x)
     # the same kernels on the same inputs: the same bytes
     assert torch.equal(y_stack, y_block)
+
+
+def test_stack_over_int8_caches_is_the_blocks_layer_by_layer():
+    """The stack entry points with an int8 cache per layer run the same kernels
+    as the block calls one layer after another: the same bytes in the outputs
+    and in every layer's codes and scales."""
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    s = STACK.with_(name="stack_i8", d=512, dh=128)
+    L = 2
+    cfg, packed, layers, table, gain, hcfg, head, ids = _stack_model(s, L, 64)
+    x = tb.tb_embed(table.cuda(), ids[:, :s.T - 1].contiguous().cuda())
+    x1 = tb.tb_embed(table.cuda(), ids[:, s.T - 1:].contiguous().cuda())
+    kv_s = [tb.KVCache.empty_int8(s.B, s.Hkv, 128, s.dh) for _ in range(L)]
+    h = tb.tb_stack_prefill(cfg, packed, x, kvs=kv_s, y_dtype=tb.TB_BF16)
+    h1 = tb.tb_stack_decode(cfg, packed, x1, kv_s, y_dtype=tb.TB_BF16)
+    kv_b = [tb.KVCache.empty_int8(s.B, s.Hkv, 128, s.dh) for _ in range(L)]
+    g, g1 = x, x1
+    for l in range(L):
+        g = tb.tb_block_prefill(cfg, packed[l], g, kv=kv_b[l], y_dtype=tb.TB_BF16)
+    for l in range(L):
+        g1 = tb.tb_block_decode(cfg, packed[l], g1, kv_b[l], y_dtype=tb.TB_BF16)
+    assert tb.tb_get_device_error(clear=True) == 0
+    assert torch.equal(h, g) and torch.equal(h1, g1)
+    for l in range(L):
+        for a, b in ((kv_s[l].k, kv_b[l].k), (kv_s[l].v, kv_b[l].v), (kv_s[l].k_scale, kv_b[l].k_scale),
+                     (kv_s[l].v_scale, kv_b[l].v_scale), (kv_s[l].lens, kv_b[l].lens)):
+            assert torch.equal(a, b), l
