@@ -377,6 +377,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;     // MMA fragment row (query head) and column pair
   int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
+  int* nlen = pre + B + 1;           // keys of sequence b this step (0: skipped)
   __shared__ int abort_word;
 
   if (threadIdx.x == 0) {
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
     for (int b = 0; b < B; ++b) {
       pre[b] = acc;
       const int p = pos_arr[b];
+      nlen[b] = p < 0 ? 0 : p + 1;
       acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kMKeys) + kMChunk - 1) / kMChunk);
     }
     pre[B] = acc;
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
       const int mid = (lo + hi + 1) >> 1;
       if (pre[mid] <= id) lo = mid; else hi = mid - 1;
     }
-    const int n = pos_arr[lo] + 1;
+    const int n = nlen[lo];
     const int base = chunk_base(n, window, kMKeys);     // 16-key stages never straddle a page
     const int nch = (n - base + kMChunk - 1) / kMChunk;
     const int r = id - pre[lo];
@@ -1080,7 +1082,7 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
   if (e != cudaSuccess) return e;
   e = make_tmap_3d_bf16(&tv, pg.bt ? pg.v : vc, planes, rows, DH, DH, rows * DH, 64, kMKeys);
   if (e != cudaSuccess) return e;
-  const size_t smem = C::OFF_PRE + (size_t)(B + 1) * 4 + 1024;
+  const size_t smem = C::OFF_PRE + (size_t)(2 * B + 1) * 4 + 1024;
   if (smem > 232448) return cudaErrorInvalidValue;
   // raise the kernel's dynamic shared-memory limit only when a launch needs
   // more than this device has been given so far (no attribute call in the
