@@ -140,12 +140,13 @@ def test_prefill_mha_768_all_rows():
 
 
 def _gqa_rows(b, T):
-    rng = np.random.default_rng(100 + b)
+    """gqa_8k rows checked against the oracle: every row of sequence 0; of the
+    others the first 64, the last 64 and 256 seeded-random rows (each computed
+    over the sequence's full K/V; the emitted cache is compared whole)."""
     if b == 0:
-        return np.r_[np.arange(64), np.arange(T - 64, T), rng.choice(T, 128, replace=False)]
-    if b == 3:
-        return np.r_[np.arange(16), np.arange(T - 16, T), rng.choice(T, 32, replace=False)]
-    return []
+        return None
+    rng = np.random.default_rng(100 + b)
+    return np.unique(np.r_[np.arange(64), np.arange(T - 64, T), rng.choice(T, 256, replace=False)])
 
 
 _D4096 = {}
@@ -157,6 +158,8 @@ def _d4096_report(name):
         sample = _gqa_rows if name == "gqa_8k" else None
         s, y, rep = _full_rows_case(name, sample=sample)
         assert torch.isfinite(y).all()
+        for b, e in enumerate(rep):
+            print(f"{name} b={b}: rel_l2 {e['rel_l2']:.2e} max_abs {e['max_abs']:.2e}")
         _D4096[name] = rep
     return _D4096[name]
 
