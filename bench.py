@@ -334,10 +334,10 @@ def bench_prefill(args, s, world, peaks):
 
 # DRAM bytes (read + write) per launch of a kernel at the benchmark workload,
 # from one ncu capture of the current kernel (see profiles/): the W13 GEMM was
-# captured at B = 1 (541.8 MB read + 222.9 MB write) and every term (A once,
+# captured at B = 1 (543.6 MB read + 222.6 MB write) and every term (A once,
 # the weight panel once per 32-row-block group, the output once) grows with the
 # row count, so a B = 4 launch moves 4x that.
-NCU_TRAFFIC = {("gqa_8k", "w13"): 4 * (541.8e6 + 222.9e6)}
+NCU_TRAFFIC = {("gqa_8k", "w13"): 4 * (543.6e6 + 222.6e6)}
 
 
 def roofline_entry(stages, work, peaks, peak_src, workload):
