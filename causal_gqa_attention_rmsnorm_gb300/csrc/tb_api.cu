@@ -58,6 +58,10 @@ size_t esize(int dtype) { return dtype == TB_F32 ? 4 : 2; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// The bf16 and int8 decode attention kernels keep two ints per sequence in
+// shared memory beside their stage rings.
+constexpr int kDecodeMaxBatch = 2048;
+
 tb_status check_cfg(const tb_block_cfg* c) {
   if (!c) return fail(TB_ERR_INVALID_ARG, "cfg is NULL");
   if (c->d <= 0 || c->H <= 0 || c->Hkv <= 0 || c->dh <= 0 || c->f <= 0)
@@ -427,6 +431,9 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
                 1024 * decode_chunk_keys());
   const int B = kv->B;
   if (B == 0) return TB_OK;
+  if (cfg->dtype == TB_BF16 && B > kDecodeMaxBatch)
+    return fail(TB_ERR_UNSUPPORTED, "decode of %d sequences: the bf16 decode attention takes at most %d per call", B,
+                kDecodeMaxBatch);
   if (!packed || !x || !y || !ws) return fail(TB_ERR_INVALID_ARG, "packed, x, y and ws must be non-NULL");
   if (!aligned16(x) || !aligned16(y) || ((uintptr_t)packed & 255u) || ((uintptr_t)ws & 255u))
     return fail(TB_ERR_INVALID_ARG, "x, y must be 16-byte aligned; packed, ws 256-byte aligned");

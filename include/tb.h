@@ -182,7 +182,8 @@ TB_API tb_status tb_block_prefill(const tb_block_cfg *cfg, const void *packed, c
  *  kv : required; kv->T_max ≤ cfg->max_pos.
  *  ws : device workspace of ws_bytes ≥ tb_workspace_bytes(cfg, B, kv->T_max, 1).
  * A sequence with lens[b] ≥ T_max sets TB_DEVERR_CACHE_FULL, keeps its cache
- * and length unchanged, and gets an unspecified y row. */
+ * and length unchanged, and gets an unspecified y row.  A bf16 block decodes
+ * at most 2048 sequences per call (TB_ERR_UNSUPPORTED above that). */
 TB_API tb_status tb_block_decode(const tb_block_cfg *cfg, const void *packed, const void *x, void *y,
                           int32_t y_dtype, const tb_kvcache *kv, void *ws, size_t ws_bytes,
                           void *stream);

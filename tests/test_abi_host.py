@@ -105,6 +105,9 @@ def test_decode_argument_checks(lib):
     kv = binding.tb_kvcache(FAKE, FAKE, FAKE, 2, 2, 4096, 64, 1)     # T_max > max_pos
     assert lib.tb_block_decode(ctypes.byref(c), FAKE, FAKE, FAKE + 4096, 0, ctypes.byref(kv), FAKE, 1 << 30,
                                None) == 1
+    kv = binding.tb_kvcache(FAKE, FAKE, FAKE, 2049, 2, 512, 64, 1)    # above the decode batch limit
+    assert lib.tb_block_decode(ctypes.byref(c), FAKE, FAKE, FAKE + 4096, 0, ctypes.byref(kv), FAKE, 1 << 40,
+                               None) == 2
     kv = binding.tb_kvcache(FAKE, FAKE, FAKE, 0, 2, 512, 64, 1)       # no sequences: no-op
     assert lib.tb_block_decode(ctypes.byref(c), FAKE, FAKE, FAKE + 4096, 0, ctypes.byref(kv), FAKE, 0, None) == 0
 

@@ -181,3 +181,46 @@ def test_decode_gqa_full_workload_sampled_sequences():
 def test_decode_gqa_full_workload_max_abs_bar():
     for b, (ey, _) in _full_decode_report().items():
         assert ey["max_abs"] <= BF16_MAX_ABS_TOL, (b, ey)
+
+
+@pytest.mark.parametrize("cache", ["bf16", "int8"])
+def test_decode_at_the_batch_limit(cache):
+    """2048 sequences, the most one decode call takes: sampled sequences match
+    the oracle (the kernels' per-sequence tables still fit in shared memory)."""
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    s = workloads.BlockShape("max_b", "decode", "bf16", B=2048, T=0, d=256, H=2, Hkv=1, dh=128, f=256,
+                             rope_base=1e4, eps=1e-6, gains="normal")
+    T_max = 64
+    lens = np.random.default_rng(3).integers(0, T_max - 1, size=s.B).tolist()
+    sampled = [0, 1, 777, 2047]
+    if cache == "bf16":
+        s, inp, kv, y, err = _decode_case(s, 13, lens, T_max, batches_with_data=sampled)
+        assert err == 0
+        for b in sampled:
+            ref = _oracle_step(s, inp, kv, b, lens[b])
+            assert_close(y[b, 0].cpu().double().numpy(), ref["y"], "bf16", f"y b={b}")
+    else:
+        s = s.with_(T=T_max)
+        inp = workloads.make_block_inputs(s, seed=13)
+        # the sampled sequences hold the oracle's codes of N(0, 1) rows, the others zero codes and scales
+        shape = (s.B, s.Hkv, T_max, s.dh)
+        kq, vq = np.zeros(shape, np.int8), np.zeros(shape, np.int8)
+        ks, vs = np.zeros(shape[:3], np.float32), np.zeros(shape[:3], np.float32)
+        for b in sampled:
+            kb, vb = workloads.make_cache_rows(s, 13, b, lens[b])
+            kq[b, :, :lens[b]], ks[b, :, :lens[b]] = oracle.quantize_rows(workloads.to_f64(kb))
+            vq[b, :, :lens[b]], vs[b, :, :lens[b]] = oracle.quantize_rows(workloads.to_f64(vb))
+        kv = tb.KVCache(torch.from_numpy(kq).cuda(), torch.from_numpy(vq).cuda(),
+                        torch.tensor(lens, dtype=torch.int32).cuda(), None, torch.from_numpy(ks).cuda(),
+                        torch.from_numpy(vs).cuda())
+        cfg = block_config(s, max_pos=T_max)
+        dev = to_device(inp)
+        packed = tb.tb_pack_weights(cfg, dev)
+        y = tb.tb_block_decode(cfg, packed, dev["x"], kv)
+        assert tb.tb_get_device_error(clear=True) == 0
+        for b in sampled:
+            ref = oracle.block_decode_seq_int8(workloads.to_f64(inp["x"][b, 0]), oracle_weights(inp), oracle_cfg(s),
+                                               kq[b], ks[b].astype(np.float64), vq[b], vs[b].astype(np.float64),
+                                               lens[b])
+            assert_close(y[b, 0].cpu().double().numpy(), ref["y"], "bf16", f"y b={b}")
+    assert kv.lens.cpu().tolist() == [n + 1 for n in lens]
