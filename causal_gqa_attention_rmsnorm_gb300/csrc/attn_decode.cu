@@ -365,8 +365,8 @@ template <int DH, int G>
 __global__ void __launch_bounds__(kMWarps * 32, 1)
     k_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const bf16* __restrict__ q, const int32_t* __restrict__ pos_arr, int B, int Hkv,
-                 float* __restrict__ part, int nchunk_max, int* __restrict__ counter, int window, PagedKV pg,
-                 float scale_log2, int* err) {
+                 float* __restrict__ part, int nchunk_max, int chunk, int* __restrict__ counter, int window,
+                 PagedKV pg, float scale_log2, int* err) {
   pdl_trigger();
   pdl_wait();
   using C = MCfg<DH>;
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
       pre[b] = acc;
       const int p = pos_arr[b];
       nlen[b] = p < 0 ? 0 : p + 1;
-      acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kMKeys) + kMChunk - 1) / kMChunk);
+      acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kMKeys) + chunk - 1) / chunk);
     }
     pre[B] = acc;
     abort_word = 0;
@@ -412,14 +412,14 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
     }
     const int n = nlen[lo];
     const int base = chunk_base(n, window, kMKeys);     // 16-key stages never straddle a page
-    const int nch = (n - base + kMChunk - 1) / kMChunk;
+    const int nch = (n - base + chunk - 1) / chunk;
     const int r = id - pre[lo];
     Item it;
     it.b = lo;
     it.kvh = r / nch;
     it.c = r - it.kvh * nch;
-    it.key0 = base + it.c * kMChunk;
-    it.nkeys = min(kMChunk, n - it.key0);
+    it.key0 = base + it.c * chunk;
+    it.nkeys = min(chunk, n - it.key0);
     it.first = window_first(n, window);
     return it;
   };
@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
     k_decode_i8(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const float* __restrict__ kscale, const float* __restrict__ vscale, const bf16* __restrict__ q,
                 const int32_t* __restrict__ pos_arr, int B, int Hkv, int T_max, float* __restrict__ part,
-                int nchunk_max, int* __restrict__ counter, int window, float scale_log2, int* err) {
+                int nchunk_max, int chunk, int* __restrict__ counter, int window, float scale_log2, int* err) {
   pdl_trigger();
   pdl_wait();
   constexpr int DH = 128, S = kQSlots;
@@ -750,7 +750,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
       pre[b] = acc;
       const int p = pos_arr[b];
       nlen[b] = p < 0 ? 0 : p + 1;
-      acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kQKeys) + kMChunk - 1) / kMChunk);
+      acc += p < 0 ? 0 : Hkv * ((p + 1 - chunk_base(p + 1, window, kQKeys) + chunk - 1) / chunk);
     }
     pre[B] = acc;
     abort_word = 0;
@@ -792,13 +792,13 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
         }
         const int n = nlen[lo];
         const int base = chunk_base(n, window, kQKeys);
-        const int nch = (n - base + kMChunk - 1) / kMChunk;
+        const int nch = (n - base + chunk - 1) / chunk;
         const int r = pid - pre[lo];
         pb = lo;
         pkvh = r / nch;
         pc = r - pkvh * nch;
-        pkey0 = base + pc * kMChunk;
-        pnkeys = min(kMChunk, n - pkey0);
+        pkey0 = base + pc * chunk;
+        pnkeys = min(chunk, n - pkey0);
         pfirst = window_first(n, window);
         pst = 0;
         pnst = (pnkeys + kQKeys - 1) / kQKeys;
@@ -1042,8 +1042,8 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
 
 template <int G>
 cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
-                          const int32_t* pos, int B, int Hkv, int T_max, float* part, int nchunk_max, int* counter,
-                          int window, void* o, cudaStream_t s) {
+                          const int32_t* pos, int B, int Hkv, int T_max, float* part, int nchunk_max, int chunk,
+                          int* counter, int window, void* o, cudaStream_t s) {
   using C = QCfg;
   CUtensorMap tk, tv;
   const uint64_t planes = (uint64_t)B * Hkv;
@@ -1063,15 +1063,15 @@ cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const f
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
   e = launch_pdl(k_decode_i8<G>, dim3(sm_count()), dim3(kQWarps * 32), smem, s, tk, tv, ks, vs, (const bf16*)q, pos, B,
-                 Hkv, T_max, part, nchunk_max, counter, window, scale_log2, device_error_word());
+                 Hkv, T_max, part, nchunk_max, chunk, counter, window, scale_log2, device_error_word());
   if (e != cudaSuccess) return e;
   return launch_pdl(k_decode_combine<bf16, 128>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
-                    nchunk_max, kMChunk, window, kQKeys, (bf16*)o);
+                    nchunk_max, chunk, window, kQKeys, (bf16*)o);
 }
 
 template <int DH, int G>
 cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
-                       float* part, int nchunk_max, int* counter, int window, const PagedKV& pg, void* o,
+                       float* part, int nchunk_max, int chunk, int* counter, int window, const PagedKV& pg, void* o,
                        cudaStream_t s) {
   using C = MCfg<DH>;
   CUtensorMap tk, tv;
@@ -1097,21 +1097,25 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   e = launch_pdl(k_decode_mma<DH, G>, dim3(sm_count()), dim3(kMWarps * 32), smem, s, tk, tv, (const bf16*)q, pos, B,
-                 Hkv, part, nchunk_max, counter, window, pg, scale_log2, device_error_word());
+                 Hkv, part, nchunk_max, chunk, counter, window, pg, scale_log2, device_error_word());
   if (e != cudaSuccess) return e;
   return launch_pdl(k_decode_combine<bf16, DH>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
-                    nchunk_max, kMChunk, window, kMKeys, (bf16*)o);
+                    nchunk_max, chunk, window, kMKeys, (bf16*)o);
 }
 
 template <int DH>
 cudaError_t stream_by_g(int G, const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv,
-                        int T_max, float* part, int nchunk_max, int* counter, int window, const PagedKV& pg, void* o,
-                        cudaStream_t s) {
+                        int T_max, float* part, int nchunk_max, int chunk, int* counter, int window, const PagedKV& pg,
+                        void* o, cudaStream_t s) {
   switch (G) {
-    case 1: return run_stream<DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, pg, o, s);
-    case 2: return run_stream<DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, pg, o, s);
-    case 4: return run_stream<DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, pg, o, s);
-    case 8: return run_stream<DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, counter, window, pg, o, s);
+    case 1: return run_stream<DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, o,
+                                         s);
+    case 2: return run_stream<DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, o,
+                                         s);
+    case 4: return run_stream<DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, o,
+                                         s);
+    case 8: return run_stream<DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, o,
+                                         s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1154,16 +1158,36 @@ cudaError_t by_dh(int dh, int G, const void* q, const void* kc, const void* vc, 
 
 }  // namespace
 
-int decode_chunk_keys() { return kChunk; }
+// Keys per work item.  The fp32 kernel takes 256 per CTA.  The streaming
+// kernels take 256 unless a full cache would give fewer items than there are
+// warps on the GPU; then 128 or 64 (small batches: more, shorter items, so
+// that every SM streams), while a sequence of T_max rows stays within the
+// merge's 1024 chunks.  Shorter items cost more per key (each carries its own
+// query setup and partial state), so the chunk is halved only that far.  The
+// workspace and the launch both use this value.
+int decode_chunk_keys(int dtype, int B, int Hkv, int T_max) {
+  if (dtype == TB_F32) return kChunk;
+  const long long target = (long long)sm_count() * kMWarps;
+  int c = kMChunk;
+  while (c > 64 && (long long)B * Hkv * ((T_max + c - 1) / c) < target &&
+         (T_max + c / 2 - 1) / (c / 2) <= kCombineMaxChunks)
+    c /= 2;
+  return c;
+}
 
 cudaError_t attn_decode_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
-                           const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max,
+                           const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max, int chunk,
                            int* work_counter, int window, void* o, cudaStream_t s) {
+  if (chunk % kQKeys) return cudaErrorInvalidValue;
   switch (H / Hkv) {
-    case 1: return run_stream_i8<1>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
-    case 2: return run_stream_i8<2>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
-    case 4: return run_stream_i8<4>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
-    case 8: return run_stream_i8<8>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, o, s);
+    case 1: return run_stream_i8<1>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
+                                         window, o, s);
+    case 2: return run_stream_i8<2>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
+                                         window, o, s);
+    case 4: return run_stream_i8<4>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
+                                         window, o, s);
+    case 8: return run_stream_i8<8>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
+                                         window, o, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1173,12 +1197,15 @@ size_t decode_part_floats(int B, int H, int dh, int nchunk_max) {
 }
 
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos, int B,
-                        int H, int Hkv, int dh, int T_max, float* part, int nchunk_max, int* work_counter,
+                        int H, int Hkv, int dh, int T_max, float* part, int nchunk_max, int chunk, int* work_counter,
                         int window, const PagedKV& pg, void* o, cudaStream_t s) {
   const int G = H / Hkv;
   if (dtype == TB_F32) return by_dh<float>(dh, G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
-  if (dh == 128) return stream_by_g<128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, pg, o, s);
-  if (dh == 64) return stream_by_g<64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, work_counter, window, pg, o, s);
+  if (chunk % kMKeys) return cudaErrorInvalidValue;
+  if (dh == 128)
+    return stream_by_g<128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter, window, pg, o, s);
+  if (dh == 64)
+    return stream_by_g<64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter, window, pg, o, s);
   return cudaErrorInvalidValue;
 }
 

@@ -246,15 +246,17 @@ cudaError_t attn_prefill_tc(const void* q, const void* k, const void* v, void* o
                             int dh, int kv_stride, int window, cudaStream_t s);
 
 // attn_decode.cu
-int decode_chunk_keys();
+// Keys per decode work item (chunk) for a step of B sequences over a T_max-row
+// cache; the workspace holds ceil(T_max / chunk) partial states per head.
+int decode_chunk_keys(int dtype, int B, int Hkv, int T_max);
 size_t decode_part_floats(int B, int H, int dh, int nchunk_max);
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos,
-                        int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max,
+                        int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max, int chunk,
                         int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s);
 // Decode over an int8 cache (dh 128): codes kc, vc [B, Hkv, T_max, 128], row
 // scales ks, vs [B, Hkv, T_max]; bf16 q and o.
 cudaError_t attn_decode_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
                            const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max,
-                           int* work_counter, int window, void* o, cudaStream_t s);
+                           int chunk, int* work_counter, int window, void* o, cudaStream_t s);
 
 }  // namespace tb

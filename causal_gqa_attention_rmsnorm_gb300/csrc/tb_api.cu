@@ -61,6 +61,8 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // The bf16 and int8 decode attention kernels keep two ints per sequence in
 // shared memory beside their stage rings.
 constexpr int kDecodeMaxBatch = 2048;
+// The decode merge takes at most 1024 chunks of at most 256 keys.
+constexpr int kDecodeMaxRows = 1024 * 256;
 
 tb_status check_cfg(const tb_block_cfg* c) {
   if (!c) return fail(TB_ERR_INVALID_ARG, "cfg is NULL");
@@ -140,6 +142,7 @@ struct Work {
   void* a;
   float* part;
   int nchunk_max;
+  int chunk;                 // keys per decode work item
   float* skpart;             // K-split partial sums of the few-token GEMMs (bf16, M ≤ 64)
   size_t total;
 };
@@ -176,7 +179,8 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
   w.hb = c->dtype == TB_F32 ? (void*)w.h : take(M * c->d * es);
   w.a = take(M * c->f * es);
   if (mode == 1) {
-    w.nchunk_max = (T + decode_chunk_keys() - 1) / decode_chunk_keys();
+    w.chunk = decode_chunk_keys(c->dtype, B, c->Hkv, T);
+    w.nchunk_max = (T + w.chunk - 1) / w.chunk;
     w.part = (float*)take(decode_part_floats(B, c->H, c->dh, w.nchunk_max) * 4);
   }
   if (c->dtype == TB_BF16 && M <= (size_t)skinny_max_tokens()) {
@@ -426,9 +430,9 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     return fail(TB_ERR_INVALID_ARG, "y_dtype must be TB_F32, or TB_BF16 for a bf16 block");
   if (kv->T_max > cfg->max_pos)
     return fail(TB_ERR_INVALID_ARG, "kv->T_max (%d) exceeds cfg->max_pos (%d)", kv->T_max, cfg->max_pos);
-  if (kv->T_max > 1024 * decode_chunk_keys())
+  if (kv->T_max > kDecodeMaxRows)
     return fail(TB_ERR_UNSUPPORTED, "kv->T_max (%d) above the %d rows the decode merge supports", kv->T_max,
-                1024 * decode_chunk_keys());
+                kDecodeMaxRows);
   const int B = kv->B;
   if (B == 0) return TB_OK;
   if (cfg->dtype == TB_BF16 && B > kDecodeMaxBatch)
@@ -467,7 +471,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(gemm_simt_qkv(dt, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
     rec.stage("attn");
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                       W.nchunk_max, W.counter, cfg->window, pg, W.o, s));
+                       W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s));
     rec.stage("wo");
     TB_TRY(gemm_simt_wo(dt, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
     rec.stage("w13");
@@ -482,11 +486,11 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
       TB_TRY(launch_quantize_kv(*kv, W.k, W.v, 1, W.pos, s));
       rec.stage("attn");
       TB_TRY(attn_decode_i8(W.q, kv->k, kv->v, kv->k_scale, kv->v_scale, W.pos, B, cfg->H, cfg->Hkv, kv->T_max,
-                            W.part, W.nchunk_max, W.counter, cfg->window, W.o, s));
+                            W.part, W.nchunk_max, W.chunk, W.counter, cfg->window, W.o, s));
     } else {
       rec.stage("attn");
       TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                         W.nchunk_max, W.counter, cfg->window, pg, W.o, s));
+                         W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s));
     }
     rec.stage("wo");
     TB_TRY(mm_wo(W, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
