@@ -190,6 +190,13 @@ struct LogitsArgs {
   float* out;              // [M, ld] fp32 logits
   int ld;
 };
+struct LseArgs {
+  const float* r;          // [M] final-norm inverse RMS of each row
+  const int32_t* targets;  // [M] target token of each row
+  float2* part;            // [M, n_parts] running (max, Σ exp(v - max)) of each column tile
+  float* tgt;              // [M] the target's logit
+  int n_parts;
+};
 struct W2Args {
   const float* h;          // [M, d]
   void* y;                 // [M, d]
@@ -198,6 +205,10 @@ struct W2Args {
 
 // LM head GEMMs (logits = (x·r)·Wᵀ, W [N, K] packed): tile, few-token and fp32 forms
 cudaError_t gemm_tc_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, cudaStream_t s);
+// The per-token loss without logits in memory: per row and 256-column tile a
+// (max, Σ exp) pair and the target's logit (ceil(N / 256) pairs per row).
+cudaError_t gemm_tc_lse(const void* A, const void* B, int M, int N, int K, const LseArgs& e, cudaStream_t s);
+int lse_tile_cols();
 cudaError_t gemm_skinny_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, float* part,
                                cudaStream_t s);
 cudaError_t gemm_simt_logits(int dtype, const void* A, const void* B, int M, int N, int K, const LogitsArgs& e,
@@ -206,6 +217,9 @@ cudaError_t gemm_simt_logits(int dtype, const void* A, const void* B, int M, int
 // head.cu: embedding gather, LM-head reductions
 cudaError_t launch_embed(int dtype, const void* table, int V, int d, const int32_t* ids, long long n, void* x,
                          int* err, cudaStream_t s);
+// nll[m] = logsumexp - target logit from the (max, Σ exp) pairs of gemm_tc_lse
+cudaError_t launch_lse_merge(const float2* part, int n_parts, const float* tgt, const int32_t* targets, int V, int M,
+                             float* nll, int* err, cudaStream_t s);
 cudaError_t launch_lse_nll(const float* logits, int ld, int M, int V, const int32_t* targets, float* nll, int* err,
                            cudaStream_t s);
 cudaError_t launch_scale_cols(int dtype, const void* src, const void* gain, int rows, int cols, void* dst,

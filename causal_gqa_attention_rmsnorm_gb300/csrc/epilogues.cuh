@@ -63,6 +63,7 @@ __device__ __forceinline__ void rope_pair(float& a, float& b, float2 cs) {
 template <typename T>
 struct EpiQKV {
   static constexpr bool kRowReduce = false;
+  static constexpr bool kRowLse = false;
   QKVArgs a;
   int H, Hkv, dh;
   struct RowAux { float r; int b, t, qt, kt; };
@@ -118,6 +119,7 @@ struct EpiQKV {
 template <typename T>
 struct EpiWo {
   static constexpr bool kRowReduce = true;
+  static constexpr bool kRowLse = false;
   WoArgs a;
   int d;
   struct RowAux {};
@@ -141,6 +143,7 @@ struct EpiWo {
 template <typename T>
 struct EpiW13 {
   static constexpr bool kRowReduce = false;
+  static constexpr bool kRowLse = false;
   W13Args a;
   int d, f;
   float eps;
@@ -161,6 +164,7 @@ struct EpiW13 {
 
 struct EpiW2 {
   static constexpr bool kRowReduce = false;
+  static constexpr bool kRowLse = false;
   W2Args a;
   int d;
   struct RowAux {};
@@ -187,6 +191,7 @@ struct EpiW2 {
 // "How it works", step 4); fp32 logits, row stride ld.
 struct EpiLogits {
   static constexpr bool kRowReduce = false;
+  static constexpr bool kRowLse = false;
   LogitsArgs a;
   struct RowAux { float r; };
   struct Aux {};
@@ -197,6 +202,42 @@ struct EpiLogits {
     for (int i = 0; i < 4; ++i) v[i] *= ra.r;
     store4<float>(a.out + (size_t)row * a.ld + col, v);
     return 0.f;
+  }
+};
+
+// The LM head's loss with no logits in memory ("The Transformer" page,
+// GenerativeAIDocs, §5, step 18: the full fp32 logits are a memory trap).  A
+// row's columns of one tile are folded into a running (max, Σ exp(v - max))
+// pair, the max subtracted before each exponential; the column that is the
+// row's target keeps its logit.  The pairs of a row's tiles are merged by
+// launch_lse_merge.
+struct EpiLse {
+  static constexpr bool kRowReduce = false;
+  static constexpr bool kRowLse = true;
+  LseArgs a;
+  struct RowAux { float r; int t; };
+  struct Aux {};
+  __device__ __forceinline__ RowAux row_aux(int row) const { return RowAux{a.r[row], a.targets[row]}; }
+  __device__ __forceinline__ Aux aux(int, int, const RowAux&) const { return Aux{}; }
+  __device__ __forceinline__ float operator()(int, int, float*, const RowAux&, const Aux&) const { return 0.f; }
+  __device__ __forceinline__ void lse(int row, int col, float v[4], const RowAux& ra, float& m, float& s) const {
+    float mx = m;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] *= ra.r;
+      mx = fmaxf(mx, v[i]);
+    }
+    if (mx > m) {
+      s *= expf(m - mx);
+      m = mx;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s += expf(v[i] - m);
+    const int dt = ra.t - col;
+    if (dt >= 0 && dt < 4) a.tgt[row] = dt == 0 ? v[0] : dt == 1 ? v[1] : dt == 2 ? v[2] : v[3];
+  }
+  __device__ __forceinline__ void lse_part(int row, int nt, float m, float s) const {
+    a.part[(size_t)row * a.n_parts + nt] = make_float2(m, s);
   }
 };
 

@@ -45,6 +45,7 @@ template <int BN> struct TcCfg {
 #pragma nv_diag_suppress 177
 struct EpiF32 {
   static constexpr bool kRowReduce = false;
+  static constexpr bool kRowLse = false;
   float* C;
   int N;
   struct RowAux {};
@@ -235,10 +236,13 @@ __global__ void __launch_bounds__(192, 1)
       const int row0 = mt * BM + quad * 32;
       const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
       float rsum[8];
+      float lm[8], ls[8];        // running (max, Σ exp) of each row (kRowLse)
       typename Epi::RowAux ra[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         rsum[i] = 0.f;
+        lm[i] = -INFINITY;
+        ls[i] = 0.f;
         const int row = row0 + sub_row + 4 * i;
         if (row < M) ra[i] = epi.row_aux(row);
       }
@@ -277,9 +281,30 @@ __global__ void __launch_bounds__(192, 1)
           const float4 t = *reinterpret_cast<const float4*>(stage + rl * C::EPI_STRIDE + sub_col);
           float v[4] = {t.x, t.y, t.z, t.w};
           const int row = row0 + rl;
-          if (row < M && col < N) rsum[i] += epi(row, col, v, ra[i], ax[i]);
+          if (row < M && col < N) {
+            if constexpr (Epi::kRowLse)
+              epi.lse(row, col, v, ra[i], lm[i], ls[i]);
+            else
+              rsum[i] += epi(row, col, v, ra[i], ax[i]);
+          }
         }
         __syncwarp();            // before the next chunk overwrites the stage
+      }
+      if constexpr (Epi::kRowLse) {
+        // the 8 lanes of a row merge their pairs in a fixed tree
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float m = lm[i], sv = ls[i];
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sv, o);
+            const float mn = fmaxf(m, m2);
+            sv = mn == -INFINITY ? 0.f : sv * expf(m - mn) + s2 * expf(m2 - mn);
+            m = mn;
+          }
+          const int row = row0 + sub_row + 4 * i;
+          if ((lane & 7) == 0 && row < M) epi.lse_part(row, nt, m, sv);
+        }
       }
       if constexpr (Epi::kRowReduce) {
         // this tile's share of each of the warp's 32 rows is partial nt; its
@@ -440,6 +465,10 @@ cudaError_t gemm_tc_w2(const void* A, const void* B, int M, int N, int K, const 
 }
 cudaError_t gemm_tc_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, cudaStream_t s) {
   return run_auto(A, B, M, N, K, EpiLogits{e}, s);
+}
+int lse_tile_cols() { return 256; }
+cudaError_t gemm_tc_lse(const void* A, const void* B, int M, int N, int K, const LseArgs& e, cudaStream_t s) {
+  return run<256>(A, B, M, N, K, EpiLse{e}, s);
 }
 cudaError_t gemm_tc_f32out(const void* A, const void* B, float* Cp, int M, int N, int K, int bn, cudaStream_t s) {
   if (bn == 256) return run<256>(A, B, M, N, K, EpiF32{Cp, N}, s);

@@ -60,6 +60,42 @@ __global__ void __launch_bounds__(256) k_lse_nll(const float* __restrict__ logit
   }
 }
 
+// nll[r] = M + log S - logit[r, targets[r]] from a row's (max, Σ exp) pairs,
+// one per 256-column tile of the fused head GEMM: lane l merges pairs l, l+32,
+// ... in order, then the lanes merge in a fixed tree.  One warp per row.
+__device__ __forceinline__ void lse_fold(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  s = mn == -INFINITY ? 0.f : s * expf(m - mn) + s2 * expf(m2 - mn);
+  m = mn;
+}
+
+__global__ void __launch_bounds__(256) k_lse_merge(const float2* __restrict__ part, int n_parts,
+                                                   const float* __restrict__ tgt, const int32_t* __restrict__ targets,
+                                                   int V, int M, float* __restrict__ nll, int* __restrict__ err) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= M) return;
+  float m = -INFINITY, s = 0.f;
+  for (int p = lane; p < n_parts; p += 32) {
+    const float2 q = part[(size_t)r * n_parts + p];
+    lse_fold(m, s, q.x, q.y);
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_fold(m, s, m2, s2);
+  }
+  if (lane == 0) {
+    const int t = targets[r];
+    if (t < 0 || t >= V) {
+      atomicOr(err, TB_DEVERR_BAD_TOKEN);
+      nll[r] = NAN;
+    } else {
+      nll[r] = m + logf(s) - tgt[r];
+    }
+  }
+}
+
 // dst[r][c] = src[r][c] · gain[c]: a tied LM head packs the embedding table
 // [V, d] with the final norm's gain folded into its columns.
 template <typename T>
@@ -85,6 +121,13 @@ cudaError_t launch_lse_nll(const float* logits, int ld, int M, int V, const int3
                            cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   k_lse_nll<<<M, 256, 0, s>>>(logits, ld, V, targets, nll, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const float2* part, int n_parts, const float* tgt, const int32_t* targets, int V, int M,
+                             float* nll, int* err, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  k_lse_merge<<<(M + 7) / 8, 256, 0, s>>>(part, n_parts, tgt, targets, V, M, nll, err);
   return cudaGetLastError();
 }
 

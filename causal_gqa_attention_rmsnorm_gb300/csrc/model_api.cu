@@ -28,11 +28,16 @@ tb_status check_head(const tb_head_cfg* c) {
   return TB_OK;
 }
 
-// Workspace of the head: row scales, one chunk of logits, few-row GEMM partials.
+// Workspace of the head: row scales, one chunk of logits, few-row GEMM
+// partials, and for the fused loss the (max, Σ exp) pairs and target logits
+// of one chunk.
 struct HeadWork {
   float* r;
   float* chunk;
   float* part;
+  float2* lse;
+  float* tgt;
+  int n_parts;
   size_t total;
 };
 HeadWork carve_head(const tb_head_cfg* c, int rc, void* base) {
@@ -48,6 +53,11 @@ HeadWork carve_head(const tb_head_cfg* c, int rc, void* base) {
   w.chunk = (float*)take((size_t)rc * c->V * 4);
   w.part = c->dtype == TB_BF16 ? (float*)take(skinny_part_floats(std::min(rc, skinny_max_tokens()), c->V) * 4)
                                : nullptr;
+  w.n_parts = (c->V + lse_tile_cols() - 1) / lse_tile_cols();
+  if (c->dtype == TB_BF16) {
+    w.lse = (float2*)take((size_t)rc * w.n_parts * sizeof(float2));
+    w.tgt = (float*)take((size_t)rc * 4);
+  }
   w.total = off;
   return w;
 }
@@ -124,6 +134,14 @@ tb_status tb_lm_head(const tb_head_cfg* cfg, const void* packed, const void* x, 
     float* out = logits ? logits + (size_t)r0 * cfg->V : W.chunk;
     cudaError_t e = launch_row_stats(cfg->dtype, xa, rows, cfg->d, cfg->eps, W.r, nullptr, 1, nullptr, nullptr,
                                      nullptr, 0, nullptr, err, s);
+    // the loss alone, on the tile GEMM: folded into the GEMM's epilogue, no logits in memory
+    if (e == cudaSuccess && !logits && cfg->dtype == TB_BF16 && rows > skinny_max_tokens()) {
+      e = gemm_tc_lse(xa, packed, rows, cfg->V, cfg->d, LseArgs{W.r, targets + r0, W.lse, W.tgt, W.n_parts}, s);
+      if (e == cudaSuccess)
+        e = launch_lse_merge(W.lse, W.n_parts, W.tgt, targets + r0, cfg->V, rows, nll + r0, err, s);
+      if (e != cudaSuccess) return report(TB_ERR_CUDA, "tb_lm_head: %s", cudaGetErrorString(e));
+      continue;
+    }
     const LogitsArgs la{W.r, out, cfg->V};
     if (e == cudaSuccess) {
       if (cfg->dtype == TB_F32)

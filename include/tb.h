@@ -265,8 +265,11 @@ TB_API size_t tb_lm_head_workspace_bytes(const tb_head_cfg *cfg, int32_t row_chu
  * logits = (x·r)·packedᵀ in fp32.  logits (device [M, V], or NULL) receives
  * them; with targets (device int32 [M]) and nll (device fp32 [M]) non-NULL,
  * nll[m] = logsumexp(logits[m]) - logits[m, targets[m]].  Rows are processed
- * row_chunk at a time; with logits NULL only one chunk of logits ever exists
- * (in ws).  A target outside [0, V) gives NaN and sets TB_DEVERR_BAD_TOKEN. */
+ * row_chunk at a time.  With logits NULL a bf16 head folds the loss into its
+ * GEMM's epilogue (a running max and Σ exp per row and 256-column tile, merged
+ * per row) and never forms the logits; chunks of at most 64 rows and the fp32
+ * head form one chunk of logits in ws.  A target outside [0, V) gives NaN and
+ * sets TB_DEVERR_BAD_TOKEN. */
 TB_API tb_status tb_lm_head(const tb_head_cfg *cfg, const void *packed, const void *x, int32_t M, float *logits,
                             const int32_t *targets, float *nll, int32_t row_chunk, void *ws, size_t ws_bytes,
                             void *stream);

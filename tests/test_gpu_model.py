@@ -85,6 +85,38 @@ def test_lm_head_chunked_loss_without_logits():
     assert torch.isnan(nll_bad[7]) and torch.isfinite(nll_bad[:7]).all()
 
 
+@pytest.mark.parametrize("V,row_chunk", [(4096, 0), (1000, 100), (520, 130)])
+def test_lm_head_loss_inside_the_gemm(V, row_chunk):
+    """No logits buffer and row chunks above 64 rows: the bf16 head folds the
+    loss into its GEMM's epilogue (a running max and Σ exp per row and tile)
+    and never forms the logits.  Same losses as the materialised logits, and
+    the oracle's; a bad target gives NaN and the error bit; chunk ends that
+    fall to few rows (the last chunk) take the logits path."""
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    M = 333
+    cfg, packed, x, targets, ref = _head_case("bf16", M, V=V, tied=V == 1000)
+    t = targets.cuda()
+    logits, nll_full = tb.tb_lm_head(cfg, packed, x, targets=t, row_chunk=512)
+    none, nll_fused = tb.tb_lm_head(cfg, packed, x, want_logits=False, targets=t, row_chunk=row_chunk)
+    assert none is None and tb.tb_get_device_error(clear=True) == 0
+    torch.testing.assert_close(nll_fused, nll_full, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(nll_fused.cpu().double().numpy(), oracle.token_nll(ref, targets.numpy()), atol=3e-2)
+    # the target that sits in the last, partial column tile, and out-of-range targets
+    t2 = t.clone()
+    t2[0] = V - 1
+    t2[5] = V
+    t2[9] = -1
+    _, nll_bad = tb.tb_lm_head(cfg, packed, x, want_logits=False, targets=t2, row_chunk=row_chunk)
+    assert tb.tb_get_device_error(clear=True) & tb.TB_DEVERR_BAD_TOKEN
+    assert torch.isnan(nll_bad[5]) and torch.isnan(nll_bad[9])
+    z = logits[0].double()
+    want0 = (torch.logsumexp(z, 0) - z[V - 1]).item()
+    assert abs(nll_bad[0].item() - want0) < 1e-3
+    keep = torch.ones(M, dtype=torch.bool)
+    keep[[0, 5, 9]] = False
+    torch.testing.assert_close(nll_bad[keep.cuda()], nll_full[keep.cuda()], rtol=1e-5, atol=1e-5)
+
+
 STACK = workloads.BlockShape("stack", "prefill", "bf16", B=2, T=90, d=256, H=4, Hkv=2, dh=64, f=512,
                              rope_base=1e4, eps=1e-6, gains="normal")
 
