@@ -19,6 +19,13 @@ template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __float2bfloat16_rn(v); }
 
+// log2 of a head width (a power of two: 16, 32, 64 or 128).
+inline int log2_dh(int dh) {
+  int s = 0;
+  while ((1 << s) < dh) ++s;
+  return s;
+}
+
 // Programmatic dependent launch.  The kernels of a decode step are launched
 // (launch_pdl) so that each may be scheduled while the one before it drains:
 // a kernel calls pdl_trigger() at its start, which lets the next launch as

@@ -65,7 +65,7 @@ struct EpiQKV {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
   QKVArgs a;
-  int H, Hkv, dh;
+  int H, Hkv, dh, dh_shift;             // dh = 1 << dh_shift
   struct RowAux { float r; int b, t, qt, kt; };
   struct Aux { float2 c0, c1; };
   __device__ __forceinline__ RowAux row_aux(int row) const {
@@ -82,7 +82,7 @@ struct EpiQKV {
   __device__ __forceinline__ Aux aux(int, int col, const RowAux& ra) const {
     Aux x;
     if (col < (H + Hkv) * dh && ra.t >= 0) {
-      const float2* cs = a.rope + (size_t)ra.t * (dh >> 1) + ((col % dh) >> 1);
+      const float2* cs = a.rope + (size_t)ra.t * (dh >> 1) + ((col & (dh - 1)) >> 1);
       x.c0 = cs[0];
       x.c1 = cs[1];
     } else {
@@ -94,15 +94,15 @@ struct EpiQKV {
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] *= ra.r;
     const int qn = H * dh, kn = Hkv * dh;
-    const int e = col % dh;
+    const int e = col & (dh - 1);       // dh is a power of two
     rope_pair(v[0], v[1], x.c0);        // identity rotation for v columns
     rope_pair(v[2], v[3], x.c1);
     if (col < qn) {
-      const int h = col / dh;
+      const int h = col >> dh_shift;
       store4<T>((T*)a.q + (((size_t)ra.b * H + h) * a.T + ra.qt) * dh + e, v);
     } else if (ra.t >= 0) {
       const bool is_k = col < qn + kn;
-      const int h = (col - (is_k ? qn : qn + kn)) / dh;
+      const int h = (col - (is_k ? qn : qn + kn)) >> dh_shift;
       if (a.k) {
         T* base = (T*)(is_k ? a.k : a.v);
         store4<T>(base + (((size_t)ra.b * Hkv + h) * a.kv_stride + ra.kt) * dh + e, v);

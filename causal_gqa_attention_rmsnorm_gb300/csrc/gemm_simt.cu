@@ -91,8 +91,8 @@ cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& e,
 
 cudaError_t gemm_simt_qkv(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
                           const QKVArgs& e, cudaStream_t s) {
-  if (dtype == TB_F32) return run<float>(A, B, M, N, K, EpiQKV<float>{e, D.H, D.Hkv, D.dh}, s);
-  return run<bf16>(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh}, s);
+  if (dtype == TB_F32) return run<float>(A, B, M, N, K, EpiQKV<float>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
+  return run<bf16>(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
 }
 cudaError_t gemm_simt_wo(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
                          const WoArgs& e, cudaStream_t s) {

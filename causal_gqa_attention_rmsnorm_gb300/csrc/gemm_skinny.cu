@@ -338,7 +338,7 @@ size_t skinny_part_floats(int M, int max_n) {
 
 cudaError_t gemm_skinny_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
                             float* part, cudaStream_t s) {
-  return run(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh}, part, s);
+  return run(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, part, s);
 }
 cudaError_t gemm_skinny_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
                            float* part, cudaStream_t s) {

@@ -449,7 +449,7 @@ cudaError_t make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t planes, u
 
 cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
                         cudaStream_t s) {
-  return run_auto(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh}, s);
+  return run_auto(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
 }
 cudaError_t gemm_tc_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
                        cudaStream_t s) {
