@@ -9,14 +9,16 @@
 // chunks whose partial softmax states (running max m, sum l, unnormalised o)
 // a second kernel merges by log-sum-exp.
 //
-// bf16 (k_decode_mma): persistent warps take 256-key chunks from a global
-// counter, so the grid has no idle CTAs and the tail is one chunk.  Each warp
+// bf16 (k_decode_mma): persistent warps take chunks (256 keys, or 128 / 64
+// for small batches, see decode_chunk_keys) from a global counter, so the
+// grid has no idle CTAs and the tail is one chunk.  Each warp
 // streams its chunks in 16-key stages through three shared-memory slots with
 // TMA (128-byte swizzle), two stages always in flight while one is computed.
 // The two small contractions (G query heads against 16 keys) run as
 // warp-level m16n8k16 MMAs on fragments read with ldmatrix, which keeps the
 // instruction count per key far below the SIMT form so the kernel can run at
 // the rate the cache streams in; the softmax stays in fp32 registers.
+// int8 caches (k_decode_i8): the same scheme over int8 codes, see below.
 // fp32 (k_decode_split): one CTA per 256-key chunk, lanes read 16-byte pieces
 // of consecutive rows straight from global memory.
 // Rows at or beyond lens[b]+1 never reach the result.
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(256) k_decode_combine(const float* __restrict_
 // bf16 streaming kernel
 // ---------------------------------------------------------------------------
 
-constexpr int kMChunk = 256;   // keys per work item (one partial state per head)
+constexpr int kMChunk = 256;   // keys per work item at most (one partial state per head)
 constexpr int kMKeys = 16;     // keys per stage
 constexpr int kMSlots = 3;     // stages in shared memory per warp: the current one + 2 in flight
 constexpr int kMWarps = 8;
