@@ -218,16 +218,18 @@ __global__ void __launch_bounds__(256)
   const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   float r = 0.f;
   if (col < N) {
-    // the epilogue's own inputs first, then the partials eight at a time
-    const auto ra = epi.row_aux(m);
-    const auto ax = epi.aux(m, col, ra);
+    // the first eight partials are requested before the epilogue's own inputs
+    // (which may depend on one another), so all of them are in flight together
     constexpr int U = 8;
     float4 a[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* p = part + (size_t)m * N + col;
     const size_t stride = (size_t)M * N;
-    int sp = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      a[u] = u < splits ? *reinterpret_cast<const float4*>(p + (size_t)u * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const auto ra = epi.row_aux(m);
+    const auto ax = epi.aux(m, col, ra);
+    int sp = U;
     for (; sp + U <= splits; sp += U) {
       float4 t[U];
 #pragma unroll
