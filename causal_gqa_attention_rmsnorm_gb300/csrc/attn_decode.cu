@@ -437,6 +437,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
   };
   Item pit{};                  // the producer's current item, decoded once
   int pit_id = -1, pit_nst = 0;
+  const uint64_t pol = policy_evict_first();   // the cache is read once per step
   auto issue_one = [&]() {
     while (!stream_done) {
       if (pidx >= qn) push();
@@ -470,8 +471,8 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
         }
 #pragma unroll
         for (int hb = 0; hb < C::NB; ++hb) {
-          tma_load_3d(&tmK, base + hb * C::BOX, &full[sl], hb * 64, y, z);
-          tma_load_3d(&tmV, base + C::KV_BYTES + hb * C::BOX, &full[sl], hb * 64, y, z);
+          tma_load_3d_hint(&tmK, base + hb * C::BOX, &full[sl], hb * 64, y, z, pol);
+          tma_load_3d_hint(&tmV, base + C::KV_BYTES + hb * C::BOX, &full[sl], hb * 64, y, z, pol);
         }
         ++pst;
         ++issued;
@@ -770,6 +771,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
   uint32_t issued = 0;
   bool pdone = false;
   int next = lane == 0 ? atomicAdd(counter, 1) : 0;
+  const uint64_t pol = policy_evict_first();   // the cache is read once per step
   auto produce = [&](uint32_t consumed) {
     while (!pdone && issued < consumed + S) {
       const int sl = issued % S, bi = pw * S + sl;
@@ -811,11 +813,11 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
       float* sc = reinterpret_cast<float*>(smem + C::OFF_SC + bi * C::SC);
       mbar_arrive_expect_tx(&full[bi], C::TX);
       const int key = pkey0 + pst * kQKeys, plane = pb * Hkv + pkvh;
-      tma_load_3d(&tmK, dst, &full[bi], 0, key, plane);
-      tma_load_3d(&tmV, dst + C::BOX, &full[bi], 0, key, plane);
+      tma_load_3d_hint(&tmK, dst, &full[bi], 0, key, plane, pol);
+      tma_load_3d_hint(&tmV, dst + C::BOX, &full[bi], 0, key, plane, pol);
       const size_t srow = (size_t)plane * T_max + key;
-      bulk_load(sc, kscale + srow, kQKeys * 4, &full[bi]);
-      bulk_load(sc + kQKeys, vscale + srow, kQKeys * 4, &full[bi]);
+      bulk_load_hint(sc, kscale + srow, kQKeys * 4, &full[bi], pol);
+      bulk_load_hint(sc + kQKeys, vscale + srow, kQKeys * 4, &full[bi], pol);
       ++pst;
       ++issued;
     }

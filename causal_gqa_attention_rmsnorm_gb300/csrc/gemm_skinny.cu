@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(192)
       // The weights do not depend on earlier kernels: the first STAGES weight
       // tiles are requested before the wait for the previous kernel, so they
       // stream while it drains; their token tiles follow the wait.
+      const uint64_t pol = policy_evict_first();   // weights are read once per call
       int held_kb[STAGES];
       int held = 0;
       bool dep = false;
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(192)
           }
           uint8_t* sw = smem + st * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
-          tma_load_2d(&tmW, sw, &full[st], (kb0 + j) * kBK, tile * kRows);
+          tma_load_2d_hint(&tmW, sw, &full[st], (kb0 + j) * kBK, tile * kRows, pol);
           if (dep) {
             tma_load_2d(&tmX, sw + C::W_BYTES, &full[st], (kb0 + j) * kBK, 0);
           } else {
