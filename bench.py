@@ -343,7 +343,9 @@ NCU_TRAFFIC = {("gqa_8k", "w13"): 4 * (543.6e6 + 222.6e6)}
 def roofline_entry(stages, work, peaks, peak_src, workload):
     """The longest stage of the step against its roofline: algorithmic FLOPs
     (or bytes) per launch over the live mean launch time, against the measured
-    burst bf16 peak (the timed region is ~0.1 s) or the HBM copy bandwidth."""
+    burst bf16 peak or the HBM copy bandwidth.  The default 50-step run lasts
+    about half a second and reaches the power cap, so a tensor-bound stage also
+    carries its fraction of the measured sustained peak."""
     name = max(stages, key=lambda k: stages[k])
     bound, amount = work[name]
     ms = stages[name]
