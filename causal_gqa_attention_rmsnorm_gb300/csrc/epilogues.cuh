@@ -45,6 +45,51 @@ template <> __device__ __forceinline__ void store2<bf16>(bf16* p, float a, float
   *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
 }
 
+// Streaming forms (ld/st.global.cs: evict-first in L2) for the outputs and
+// residual inputs of a prefill-sized GEMM, which pass through once and are
+// larger than L2; they would otherwise push the GEMM's operand tiles out.
+// Chosen at compile time (kStream): a run-time choice in the epilogue's inner
+// loop measured slower than either form.
+template <typename T> __device__ __forceinline__ void store4cs(T* p, const float v[4]);
+template <> __device__ __forceinline__ void store4cs<float>(float* p, const float v[4]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+}
+template <> __device__ __forceinline__ void store4cs<bf16>(bf16* p, const float v[4]) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  __stcs(reinterpret_cast<uint2*>(p), u);
+}
+template <typename T> __device__ __forceinline__ void load4cs(const T* p, float v[4]);
+template <> __device__ __forceinline__ void load4cs<float>(const float* p, float v[4]) {
+  const float4 f = __ldcs(reinterpret_cast<const float4*>(p));
+  v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+}
+template <> __device__ __forceinline__ void load4cs<bf16>(const bf16* p, float v[4]) {
+  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
+  v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+  v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+template <typename T> __device__ __forceinline__ void store2cs(T* p, float a, float b);
+template <> __device__ __forceinline__ void store2cs<float>(float* p, float a, float b) {
+  __stcs(reinterpret_cast<float2*>(p), make_float2(a, b));
+}
+template <> __device__ __forceinline__ void store2cs<bf16>(bf16* p, float a, float b) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+  __stcs(reinterpret_cast<unsigned int*>(p), *reinterpret_cast<unsigned int*>(&t));
+}
+template <bool CS, typename T> __device__ __forceinline__ void st4(T* p, const float v[4]) {
+  if constexpr (CS) store4cs<T>(p, v); else store4<T>(p, v);
+}
+template <bool CS, typename T> __device__ __forceinline__ void ld4(const T* p, float v[4]) {
+  if constexpr (CS) load4cs<T>(p, v); else load4<T>(p, v);
+}
+template <bool CS, typename T> __device__ __forceinline__ void st2(T* p, float a, float b) {
+  if constexpr (CS) store2cs<T>(p, a, b); else store2<T>(p, a, b);
+}
+
 // RoPE rotation of one adjacent pair by the angle whose (cos, sin) is cs.
 __device__ __forceinline__ void rope_pair(float& a, float& b, float2 cs) {
   const float x = a, y = b;
@@ -54,13 +99,14 @@ __device__ __forceinline__ void rope_pair(float& a, float& b, float2 cs) {
 
 // Every epilogue reads its global inputs in two steps ahead of any store, so a
 // caller processing several (row, 4-column) items can issue all their loads
-// before the first store:
+// before the first store.  kStream (the prefill tile GEMM's instances) turns
+// the once-through traffic into streaming loads and stores:
 //   RowAux row_aux(row)            inputs that depend on the row only (once per tile)
 //   Aux    aux(row, col, RowAux)   inputs of the 4 columns
 //   float  operator()(row, col, v, RowAux, Aux)   compute and store; returns the
 //                                  item's share of a row reduction (kRowReduce)
 
-template <typename T>
+template <typename T, bool kStream = false>
 struct EpiQKV {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
@@ -99,7 +145,7 @@ struct EpiQKV {
     rope_pair(v[2], v[3], x.c1);
     if (col < qn) {
       const int h = col >> dh_shift;
-      store4<T>((T*)a.q + (((size_t)ra.b * H + h) * a.T + ra.qt) * dh + e, v);
+      st4<kStream, T>((T*)a.q + (((size_t)ra.b * H + h) * a.T + ra.qt) * dh + e, v);   // K/V: re-read
     } else if (ra.t >= 0) {
       const bool is_k = col < qn + kn;
       const int h = (col - (is_k ? qn : qn + kn)) >> dh_shift;
@@ -116,7 +162,7 @@ struct EpiQKV {
   }
 };
 
-template <typename T>
+template <typename T, bool kStream = false>
 struct EpiWo {
   static constexpr bool kRowReduce = true;
   static constexpr bool kRowLse = false;
@@ -127,20 +173,20 @@ struct EpiWo {
   __device__ __forceinline__ RowAux row_aux(int) const { return RowAux{}; }
   __device__ __forceinline__ Aux aux(int row, int col, const RowAux&) const {
     Aux x;
-    load4<T>((const T*)a.x + (size_t)row * d + col, x.x);
+    ld4<kStream, T>((const T*)a.x + (size_t)row * d + col, x.x);
     return x;
   }
   __device__ __forceinline__ float operator()(int row, int col, float v[4], const RowAux&, const Aux& x) const {
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] += x.x[i];
-    store4<float>(a.h + (size_t)row * d + col, v);
-    if ((void*)a.hb != (void*)a.h) store4<T>((T*)a.hb + (size_t)row * d + col, v);
+    st4<kStream, float>(a.h + (size_t)row * d + col, v);
+    if ((void*)a.hb != (void*)a.h) st4<kStream, T>((T*)a.hb + (size_t)row * d + col, v);
     return v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
   }
   __device__ __forceinline__ const RowSum& row_sums() const { return a.ssq; }
 };
 
-template <typename T>
+template <typename T, bool kStream = false>
 struct EpiW13 {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
@@ -157,11 +203,12 @@ struct EpiW13 {
     const float r2 = ra.r2;
     const float o0 = silu_f(v[0] * r2) * (v[1] * r2);
     const float o1 = silu_f(v[2] * r2) * (v[3] * r2);
-    store2<T>((T*)a.a + (size_t)row * f + (col >> 1), o0, o1);
+    st2<kStream, T>((T*)a.a + (size_t)row * f + (col >> 1), o0, o1);
     return 0.f;
   }
 };
 
+template <bool kStream = false>
 struct EpiW2 {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
@@ -172,16 +219,16 @@ struct EpiW2 {
   __device__ __forceinline__ RowAux row_aux(int) const { return RowAux{}; }
   __device__ __forceinline__ Aux aux(int row, int col, const RowAux&) const {
     Aux x;
-    load4<float>(a.h + (size_t)row * d + col, x.h);
+    ld4<kStream, float>(a.h + (size_t)row * d + col, x.h);
     return x;
   }
   __device__ __forceinline__ float operator()(int row, int col, float v[4], const RowAux&, const Aux& x) const {
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] += x.h[i];
     if (a.y_dtype == TB_F32)
-      store4<float>((float*)a.y + (size_t)row * d + col, v);
+      st4<kStream, float>((float*)a.y + (size_t)row * d + col, v);
     else
-      store4<bf16>((bf16*)a.y + (size_t)row * d + col, v);
+      st4<kStream, bf16>((bf16*)a.y + (size_t)row * d + col, v);
     return 0.f;
   }
 };

@@ -106,8 +106,8 @@ cudaError_t gemm_simt_w13(int dtype, const void* A, const void* B, int M, int N,
 }
 cudaError_t gemm_simt_w2(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
                          const W2Args& e, cudaStream_t s) {
-  if (dtype == TB_F32) return run<float>(A, B, M, N, K, EpiW2{e, D.d}, s);
-  return run<bf16>(A, B, M, N, K, EpiW2{e, D.d}, s);
+  if (dtype == TB_F32) return run<float>(A, B, M, N, K, EpiW2<>{e, D.d}, s);
+  return run<bf16>(A, B, M, N, K, EpiW2<>{e, D.d}, s);
 }
 
 cudaError_t gemm_simt_logits(int dtype, const void* A, const void* B, int M, int N, int K, const LogitsArgs& e,

@@ -353,7 +353,7 @@ cudaError_t gemm_skinny_w13(const void* A, const void* B, int M, int N, int K, c
 }
 cudaError_t gemm_skinny_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
                            float* part, cudaStream_t s) {
-  return run(A, B, M, N, K, EpiW2{e, D.d}, part, s);
+  return run(A, B, M, N, K, EpiW2<>{e, D.d}, part, s);
 }
 
 cudaError_t gemm_skinny_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, float* part,

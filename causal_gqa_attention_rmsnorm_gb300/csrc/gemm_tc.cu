@@ -449,19 +449,19 @@ cudaError_t make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t planes, u
 
 cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
                         cudaStream_t s) {
-  return run_auto(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
+  return run_auto(A, B, M, N, K, EpiQKV<bf16, true>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
 }
 cudaError_t gemm_tc_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
                        cudaStream_t s) {
-  return run_auto(A, B, M, N, K, EpiWo<bf16>{e, D.d}, s);
+  return run_auto(A, B, M, N, K, EpiWo<bf16, true>{e, D.d}, s);
 }
 cudaError_t gemm_tc_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
                         cudaStream_t s) {
-  return run_auto(A, B, M, N, K, EpiW13<bf16>{e, D.d, D.f, D.eps}, s);
+  return run_auto(A, B, M, N, K, EpiW13<bf16, true>{e, D.d, D.f, D.eps}, s);
 }
 cudaError_t gemm_tc_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
                        cudaStream_t s) {
-  return run_auto(A, B, M, N, K, EpiW2{e, D.d}, s);
+  return run_auto(A, B, M, N, K, EpiW2<true>{e, D.d}, s);
 }
 cudaError_t gemm_tc_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, cudaStream_t s) {
   return run_auto(A, B, M, N, K, EpiLogits{e}, s);
