@@ -50,7 +50,7 @@ extern "C" {
 typedef enum {
   TB_OK = 0,
   TB_ERR_INVALID_ARG = 1,   /* a null/misaligned pointer, inconsistent shape, too small a buffer */
-  TB_ERR_UNSUPPORTED = 2,   /* a valid shape this build has no kernel for */
+  TB_ERR_UNSUPPORTED = 2,   /* a valid shape the library has no kernel for */
   TB_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
   TB_ERR_CACHE_FULL = 4,    /* host-visible cache overflow (append of n rows past T_max) */
   TB_ERR_TIMEOUT = 5        /* reserved for a host-side wait that ran out */
