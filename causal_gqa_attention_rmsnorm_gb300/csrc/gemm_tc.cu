@@ -9,11 +9,14 @@
 //               K = 16) into one of two TMEM accumulators, and commits each
 //               stage back to the producer when the tensor core is done with it;
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (each warp
-//               owns its 32-lane quarter of TMEM, i.e. 32 rows), the fused
-//               epilogue, global stores; then the accumulator is released, so
-//               the next tile's MMAs overlap this tile's epilogue.
+//               owns its 32-lane quarter of TMEM, i.e. 32 rows), released as
+//               soon as its last columns are in registers, so the next tile's
+//               MMAs overlap this tile's fused epilogue and global stores (the
+//               prefill instances stream their once-through loads and stores,
+//               see epilogues.cuh).
 // Tiles are visited n-fastest so that the CTAs running together share the A
-// row block and the weight panel stays resident in L2.
+// row block and the weight panel stays resident in L2, or, when the weight
+// panel is larger than L2 and K short, in groups of row blocks (see run).
 #include <cudaTypedefs.h>
 
 #include <mutex>
