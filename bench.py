@@ -199,10 +199,18 @@ def run_reference(args, world, rank):
     print(json.dumps(line))
 
 
+L2_BYTES = 129 << 20     # GB300 L2
+
+
 def workload_config(s):
+    from causal_gqa_attention_rmsnorm_gb300 import accounting as acc
+    esz = 4 if s.dtype == "f32" else 2
+    step_bytes = s.B * s.T * s.d * esz + acc.weight_bytes(s.d, s.H, s.Hkv, s.dh, s.f, esz)
+    l2 = ("inputs larger than L2 (no flush)" if step_bytes > L2_BYTES
+          else "inputs smaller than L2, not flushed: a parity workload, not a bench line")
     return {"workload": s.name, "B": s.B, "T": s.T, "d": s.d, "H": s.H, "Hkv": s.Hkv, "dh": s.dh, "f": s.f,
             "rope_base": s.rope_base, "eps": s.eps, "storage": s.dtype, "accumulate": "f32",
-            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+            "l2": l2, "parallelism": "replicas"}
 
 
 # ---------------------------------------------------------------------------
