@@ -27,3 +27,13 @@ def test_product_sources_do_not_reference_the_oracle():
                 if "import oracle" in text or "from oracle" in text:
                     hits.append(str(p.relative_to(ROOT)))
     assert hits == []
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import pytest
+    from causal_gqa_attention_rmsnorm_gb300 import binding
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "libtb.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    cfg = binding.BlockConfig(64, 4, 2, 16, 176, 16, 1e4, 1e-6, binding.TB_F32)
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.tb_workspace_bytes(cfg, 1, 16, 0)
