@@ -32,9 +32,14 @@ using namespace ptx;
 
 constexpr int BM = 128, BK = 64;
 
-template <int BN> struct TcCfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;
+// MT row blocks per CTA tile: 1, or 2 for a long-K GEMM, where the pair of
+// 128-row A blocks shares each staged B tile (a third less operand traffic
+// per FLOP; the two accumulators then fill TMEM, so the epilogue no longer
+// overlaps the next tile's MMAs, a small cost when K is long).
+template <int BN, int MT = 1> struct TcCfg {
+  static constexpr int STAGES = MT == 2 ? 3 : (BN == 256 ? 4 : 6);
+  static constexpr uint32_t A_BLOCK = BM * BK * 2;
+  static constexpr uint32_t A_BYTES = MT * A_BLOCK;
   static constexpr uint32_t B_BYTES = BN * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -82,11 +87,13 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
   nt = local / gm;
 }
 
-template <int BN, class Epi>
+template <int BN, class Epi, int MT = 1>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
               uint32_t a_box_bytes, int group_m, Epi epi, int* err) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, MT>;
+  static_assert(MT == 1 || (MT == 2 && BN * MT <= 512 && !Epi::kRowReduce && !Epi::kRowLse),
+                "row pairs: TMEM holds both accumulators; no row reductions");
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -100,7 +107,8 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
-  const int tiles = m_tiles * n_tiles;
+  const int m_units = (m_tiles + MT - 1) / MT;     // CTA tiles along M
+  const int tiles = m_units * n_tiles;
   const int kblocks = K / BK;
 
   if (threadIdx.x == 0) {
@@ -136,8 +144,8 @@ __global__ void __launch_bounds__(192, 1)
       for (int s = 0; s < STAGES; ++s) issued[s] = 0, last_phase[s] = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
-        int mt, nt;
-        tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
+        int mu, nt;
+        tile_coords(tile, m_units, n_tiles, group_m, mu, nt);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) {
             ok = false;
@@ -145,8 +153,10 @@ __global__ void __launch_bounds__(192, 1)
           }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           // the A box is shorter than the tile when M < 128; rows past it are never stored
-          mbar_arrive_expect_tx(&full[stage], a_box_bytes + C::B_BYTES);
-          tma_load_2d(&tmA, sa, &full[stage], kb * BK, mt * BM);
+          mbar_arrive_expect_tx(&full[stage], MT * a_box_bytes + C::B_BYTES);
+#pragma unroll
+          for (int r = 0; r < MT; ++r)     // a block past M reads zeros
+            tma_load_2d(&tmA, sa + r * C::A_BLOCK, &full[stage], kb * BK, (mu * MT + r) * BM);
           tma_load_2d(&tmB, sa + C::A_BYTES, &full[stage], kb * BK, nt * BN);
           issued[stage] = 1;
           last_phase[stage] = phase;
@@ -168,11 +178,12 @@ __global__ void __launch_bounds__(192, 1)
       int local = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++local) {
-        const int acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
+        // MT == 1: two accumulators in turn; MT == 2: one pair of accumulators
+        const int acc = MT == 2 ? 0 : (local & 1);
+        const uint32_t acc_phase = (MT == 2 ? local : (local >> 1)) & 1;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        const uint32_t d_tmem = tmem_base + acc * BN;   // row block r of the tile at + r·BN
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
             ok = false;
@@ -183,8 +194,10 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b0 = a0 + C::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_ss(d_tmem, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), idesc,
-                        (kb | k) != 0);
+#pragma unroll
+            for (int r = 0; r < MT; ++r)
+              mma_bf16_ss(d_tmem + r * BN, desc_kmajor_sw128(a0 + r * C::A_BLOCK + k * 32),
+                          desc_kmajor_sw128(b0 + k * 32), idesc, (kb | k) != 0);
           mma_commit(&empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1u;
         }
@@ -229,99 +242,103 @@ __global__ void __launch_bounds__(192, 1)
     };
     int local = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
+      const int acc = MT == 2 ? 0 : (local & 1);
+      const uint32_t acc_phase = (MT == 2 ? local : (local >> 1)) & 1;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, err)) break;
       tc_fence_after();
       row_arrive();
-      int mt, nt;
-      tile_coords(tile, m_tiles, n_tiles, group_m, mt, nt);
-      const int row0 = mt * BM + quad * 32;
-      const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
-      float rsum[8];
-      float lm[8], ls[8];        // running (max, Σ exp) of each row (kRowLse)
-      typename Epi::RowAux ra[8];
+      int mu, nt;
+      tile_coords(tile, m_units, n_tiles, group_m, mu, nt);
+      for (int r = 0; r < MT; ++r) {
+        const int mt = mu * MT + r;
+        const int row0 = mt * BM + quad * 32;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (acc + r) * BN;
+        float rsum[8];
+        float lm[8], ls[8];        // running (max, Σ exp) of each row (kRowLse)
+        typename Epi::RowAux ra[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        rsum[i] = 0.f;
-        lm[i] = -INFINITY;
-        ls[i] = 0.f;
-        const int row = row0 + sub_row + 4 * i;
-        if (row < M) ra[i] = epi.row_aux(row);
-      }
+        for (int i = 0; i < 8; ++i) {
+          rsum[i] = 0.f;
+          lm[i] = -INFINITY;
+          ls[i] = 0.f;
+          const int row = row0 + sub_row + 4 * i;
+          if (row < M) ra[i] = epi.row_aux(row);
+        }
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(taddr + c0, r0);
-        tmem_ld16(taddr + c0 + 16, r1);
-        tmem_wait_ld();
-        if (c0 + 32 == BN) {     // the accumulator is free once its last columns are in registers
-          tc_fence_before();
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(taddr + c0, r0);
+          tmem_ld16(taddr + c0 + 16, r1);
+          tmem_wait_ld();
+          if (c0 + 32 == BN && r == MT - 1) {   // the accumulator(s) free once the last columns are in registers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          float* my = stage + lane * C::EPI_STRIDE;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            *reinterpret_cast<float4*>(my + 4 * i) =
+                make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]), __uint_as_float(r0[4 * i + 2]),
+                            __uint_as_float(r0[4 * i + 3]));
+            *reinterpret_cast<float4*>(my + 16 + 4 * i) =
+                make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
+                            __uint_as_float(r1[4 * i + 3]));
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[acc]);
-        }
-        float* my = stage + lane * C::EPI_STRIDE;
+          const int col = nt * BN + c0 + sub_col;
+          // all global inputs of the chunk first, then compute and store
+          typename Epi::Aux ax[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          *reinterpret_cast<float4*>(my + 4 * i) = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
-                                                               __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
-          *reinterpret_cast<float4*>(my + 16 + 4 * i) =
-              make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
-                          __uint_as_float(r1[4 * i + 3]));
-        }
-        __syncwarp();
-        const int col = nt * BN + c0 + sub_col;
-        // all global inputs of the chunk first, then compute and store
-        typename Epi::Aux ax[8];
+          for (int i = 0; i < 8; ++i) {
+            const int row = row0 + sub_row + 4 * i;
+            if (row < M && col < N) ax[i] = epi.aux(row, col, ra[i]);
+          }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = row0 + sub_row + 4 * i;
-          if (row < M && col < N) ax[i] = epi.aux(row, col, ra[i]);
+          for (int i = 0; i < 8; ++i) {
+            const int rl = sub_row + 4 * i;
+            const float4 t = *reinterpret_cast<const float4*>(stage + rl * C::EPI_STRIDE + sub_col);
+            float v[4] = {t.x, t.y, t.z, t.w};
+            const int row = row0 + rl;
+            if (row < M && col < N) {
+              if constexpr (Epi::kRowLse)
+                epi.lse(row, col, v, ra[i], lm[i], ls[i]);
+              else
+                rsum[i] += epi(row, col, v, ra[i], ax[i]);
+            }
+          }
+          __syncwarp();            // before the next chunk overwrites the stage
         }
+        if constexpr (Epi::kRowLse) {
+          // the 8 lanes of a row merge their pairs in a fixed tree
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rl = sub_row + 4 * i;
-          const float4 t = *reinterpret_cast<const float4*>(stage + rl * C::EPI_STRIDE + sub_col);
-          float v[4] = {t.x, t.y, t.z, t.w};
-          const int row = row0 + rl;
-          if (row < M && col < N) {
-            if constexpr (Epi::kRowLse)
-              epi.lse(row, col, v, ra[i], lm[i], ls[i]);
-            else
-              rsum[i] += epi(row, col, v, ra[i], ax[i]);
+          for (int i = 0; i < 8; ++i) {
+            float m = lm[i], sv = ls[i];
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+              const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sv, o);
+              const float mn = fmaxf(m, m2);
+              sv = mn == -INFINITY ? 0.f : sv * expf(m - mn) + s2 * expf(m2 - mn);
+              m = mn;
+            }
+            const int row = row0 + sub_row + 4 * i;
+            if ((lane & 7) == 0 && row < M) epi.lse_part(row, nt, m, sv);
           }
         }
-        __syncwarp();            // before the next chunk overwrites the stage
-      }
-      if constexpr (Epi::kRowLse) {
-        // the 8 lanes of a row merge their pairs in a fixed tree
+        if constexpr (Epi::kRowReduce) {
+          // this tile's share of each of the warp's 32 rows is partial nt; its
+          // arrival is counted at the next tile (see row_arrive)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float m = lm[i], sv = ls[i];
-#pragma unroll
-          for (int o = 1; o < 8; o <<= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sv, o);
-            const float mn = fmaxf(m, m2);
-            sv = mn == -INFINITY ? 0.f : sv * expf(m - mn) + s2 * expf(m2 - mn);
-            m = mn;
+          for (int i = 0; i < 8; ++i) {
+            float t = rsum[i];
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            t += __shfl_xor_sync(0xffffffffu, t, 4);
+            const int row = row0 + sub_row + 4 * i;
+            if ((lane & 7) == 0 && row < M) epi.row_sums().part[(size_t)row * epi.row_sums().stride + nt] = t;
           }
-          const int row = row0 + sub_row + 4 * i;
-          if ((lane & 7) == 0 && row < M) epi.lse_part(row, nt, m, sv);
+          pend_row0 = row0;
         }
-      }
-      if constexpr (Epi::kRowReduce) {
-        // this tile's share of each of the warp's 32 rows is partial nt; its
-        // arrival is counted at the next tile (see row_arrive)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float t = rsum[i];
-          t += __shfl_xor_sync(0xffffffffu, t, 1);
-          t += __shfl_xor_sync(0xffffffffu, t, 2);
-          t += __shfl_xor_sync(0xffffffffu, t, 4);
-          const int row = row0 + sub_row + 4 * i;
-          if ((lane & 7) == 0 && row < M) epi.row_sums().part[(size_t)row * epi.row_sums().stride + nt] = t;
-        }
-        pend_row0 = row0;
       }
     }
     row_arrive();
@@ -351,9 +368,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BN, class Epi>
+template <int BN, class Epi, int MT = 1>
 cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& epi, cudaStream_t s) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, MT>;
   if (M <= 0 || N <= 0) return cudaSuccess;
   CUtensorMap ta, tbm;
   const uint32_t a_rows = M >= BM ? BM : (uint32_t)((M + 7) / 8 * 8);
@@ -365,21 +382,23 @@ cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& ep
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(k_gemm_tc<BN, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    e = cudaFuncSetAttribute(k_gemm_tc<BN, Epi, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int m_tiles = (M + BM - 1) / BM;
-  const int tiles = m_tiles * ((N + BN - 1) / BN);
+  const int m_units = ((M + BM - 1) / BM + MT - 1) / MT;
+  const int tiles = m_units * ((N + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
   // Short K with a B panel beyond what L2 keeps: group up to 32 row blocks (32
   // MB of A at K = 4096), m fastest inside a group, so each B tile is read
   // from HBM once per group rather than once per row block.  Otherwise n
   // fastest.
   const size_t b_bytes = (size_t)N * K * 2;
-  const int group_m = (K <= 8192 && b_bytes > (size_t(48) << 20) && m_tiles > 1) ? (m_tiles < 32 ? m_tiles : 32) : 0;
-  k_gemm_tc<BN, Epi><<<grid, 192, C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
-                                                device_error_word());
+  const int gmax = 32 / MT;                        // CTA tiles along M per group
+  const int group_m =
+      (K <= 8192 && b_bytes > (size_t(48) << 20) && m_units > 1) ? (m_units < gmax ? m_units : gmax) : 0;
+  k_gemm_tc<BN, Epi, MT><<<grid, 192, C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
+                                                    device_error_word());
   return cudaGetLastError();
 }
 
@@ -464,6 +483,12 @@ cudaError_t gemm_tc_w13(const void* A, const void* B, int M, int N, int K, const
 }
 cudaError_t gemm_tc_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
                        cudaStream_t s) {
+  // long K: pairs of row blocks share each weight tile, when the row blocks
+  // pair up exactly and the pairs still fill several waves
+  const int m_tiles = (M + BM - 1) / BM;
+  const long pairs = (long)(m_tiles / 2) * ((N + 255) / 256);
+  if (K >= 8192 && m_tiles % 2 == 0 && pairs >= 4L * sm_count())
+    return run<256, EpiW2<true>, 2>(A, B, M, N, K, EpiW2<true>{e, D.d}, s);
   return run_auto(A, B, M, N, K, EpiW2<true>{e, D.d}, s);
 }
 cudaError_t gemm_tc_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, cudaStream_t s) {
