@@ -345,7 +345,7 @@ def bench_prefill(args, s, world, peaks):
 # captured at B = 1 (543.6 MB read + 222.6 MB write) and every term (A once,
 # the weight panel once per 32-row-block group, the output once) grows with the
 # row count, so a B = 4 launch moves 4x that.
-NCU_TRAFFIC = {("gqa_8k", "w13"): 4 * (541.2e6 + 222.6e6)}
+NCU_TRAFFIC = {("gqa_8k", "w13"): 4 * (540.8e6 + 221.8e6)}
 
 
 def roofline_entry(stages, work, peaks, peak_src, workload):
