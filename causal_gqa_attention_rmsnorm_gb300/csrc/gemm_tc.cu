@@ -16,7 +16,9 @@
 //               see epilogues.cuh).
 // Tiles are visited n-fastest so that the CTAs running together share the A
 // row block and the weight panel stays resident in L2, or, when the weight
-// panel is larger than L2 and K short, in groups of row blocks (see run).
+// panel is larger than L2 and K short, in groups of row blocks (see run).  A
+// long-K GEMM may take two row blocks per CTA tile against one weight tile
+// (MT = 2, see TcCfg).
 #include <cudaTypedefs.h>
 
 #include <mutex>
