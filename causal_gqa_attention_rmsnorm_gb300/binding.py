@@ -92,6 +92,10 @@ def lib() -> ctypes.CDLL:
         L.tbx_trace_read.restype = c_int32
         L.tbx_trace_stage_name.argtypes = [c_int32]
         L.tbx_trace_stage_name.restype = ctypes.c_char_p
+        L.tbx_skinny_split_count.argtypes = [c_int32, c_int32, c_int32]
+        L.tbx_skinny_split_count.restype = c_int32
+        L.tbx_decode_chunk_keys.argtypes = [c_int32, c_int32, c_int32, c_int32, c_int32]
+        L.tbx_decode_chunk_keys.restype = c_int32
         L.tb_embed.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, ctypes.c_int64, c_void_p, c_void_p]
         L.tb_lm_head_packed_bytes.argtypes = [P(tb_head_cfg)]
         L.tb_lm_head_packed_bytes.restype = c_size_t

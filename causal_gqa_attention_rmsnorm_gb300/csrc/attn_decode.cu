@@ -1170,8 +1170,12 @@ cudaError_t by_dh(int dh, int G, const void* q, const void* kc, const void* vc, 
 // query setup and partial state), so the chunk is halved only that far.  The
 // workspace and the launch both use this value.
 int decode_chunk_keys(int dtype, int B, int Hkv, int T_max) {
+  return decode_chunk_keys_sms(dtype, B, Hkv, T_max, sm_count());
+}
+
+int decode_chunk_keys_sms(int dtype, int B, int Hkv, int T_max, int sms) {
   if (dtype == TB_F32) return kChunk;
-  const long long target = (long long)sm_count() * kMWarps;
+  const long long target = (long long)sms * kMWarps;
   int c = kMChunk;
   while (c > 64 && (long long)B * Hkv * ((T_max + c - 1) / c) < target &&
          (T_max + c / 2 - 1) / (c / 2) <= kCombineMaxChunks)

@@ -248,6 +248,9 @@ cudaError_t gemm_simt_w2(int dtype, const void* A, const void* B, int M, int N, 
 // partial-sum epilogue kernel; `part` holds skinny_part_floats(M, N) floats)
 int skinny_max_tokens();
 size_t skinny_part_floats(int M, int max_n);
+// K ranges per weight tile for `tiles` 128-row weight tiles of `kblocks` K
+// blocks over `slots` resident CTAs (-1 for a non-positive argument)
+int skinny_split_count(int tiles, int kblocks, int slots);
 cudaError_t gemm_skinny_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
                             float* part, cudaStream_t s);
 cudaError_t gemm_skinny_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
@@ -270,6 +273,7 @@ cudaError_t attn_prefill_tc(const void* q, const void* k, const void* v, void* o
 // Keys per decode work item (chunk) for a step of B sequences over a T_max-row
 // cache; the workspace holds ceil(T_max / chunk) partial states per head.
 int decode_chunk_keys(int dtype, int B, int Hkv, int T_max);
+int decode_chunk_keys_sms(int dtype, int B, int Hkv, int T_max, int sms);   // the same rule for `sms` SMs
 size_t decode_part_floats(int B, int H, int dh, int nchunk_max);
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos,
                         int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max, int chunk,

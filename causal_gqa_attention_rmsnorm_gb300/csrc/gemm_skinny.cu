@@ -275,24 +275,7 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// K ranges per weight tile.  Items are equal in size, so the time is the
-// number of item waves over the resident CTAs (two per SM): take the split
-// count whose item count fills its last wave best (fewest splits on a tie),
-// with at least 4 K blocks (64 KB of weights) per item.  The partials
-// (items × 128 × M floats) stay in L2 between the two kernels.
-int split_count(int tiles, int kblocks) {
-  const long long slots = 2LL * sm_count();
-  int spmax = kblocks / 4;
-  if (spmax > kMaxItems / tiles) spmax = kMaxItems / tiles;
-  int best = 1;
-  double best_fill = 0.0;
-  for (int sp = 1; sp <= spmax; ++sp) {
-    const long long items = (long long)tiles * sp, waves = (items + slots - 1) / slots;
-    const double fill = (double)items / (double)(waves * slots);
-    if (fill > best_fill + 1e-3) best = sp, best_fill = fill;
-  }
-  return best;
-}
+int split_count(int tiles, int kblocks) { return skinny_split_count(tiles, kblocks, 2 * sm_count()); }
 
 template <int NT, class Epi>
 cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi& epi, float* part, cudaStream_t s) {
@@ -331,6 +314,26 @@ cudaError_t run(const void* X, const void* W, int M, int N, int K, const Epi& ep
 }
 
 }  // namespace
+
+// K ranges per weight tile.  Items are equal in size, so the time is the
+// number of item waves over the resident CTAs (two per SM): take the split
+// count whose item count fills its last wave best (fewest splits on a tie),
+// with at least 4 K blocks (64 KB of weights) per item and at most kMaxItems
+// items.  The partials (items × 128 × M floats) stay in L2 between the two
+// kernels.
+int skinny_split_count(int tiles, int kblocks, int slots) {
+  if (tiles <= 0 || kblocks <= 0 || slots <= 0) return -1;
+  int spmax = kblocks / 4;
+  if (spmax > kMaxItems / tiles) spmax = kMaxItems / tiles;
+  int best = 1;
+  double best_fill = 0.0;
+  for (int sp = 1; sp <= spmax; ++sp) {
+    const long long items = (long long)tiles * sp, waves = (items + slots - 1) / slots;
+    const double fill = (double)items / (double)(waves * slots);
+    if (fill > best_fill + 1e-3) best = sp, best_fill = fill;
+  }
+  return best;
+}
 
 int skinny_max_tokens() { return kMaxTok; }
 

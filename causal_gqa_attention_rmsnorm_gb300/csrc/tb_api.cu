@@ -590,6 +590,18 @@ TB_API const char* tbx_trace_stage_name(int32_t i) {
   return (i >= 0 && i < (int)g_trace.names.size()) ? g_trace.names[i] : "";
 }
 
+// Host-side selection rules (not part of the public header), for tests that
+// need no GPU: the few-token GEMM's K-range count for `tiles` weight tiles of
+// `kblocks` 64-wide K blocks over `slots` resident CTAs, and the decode work
+// item's key count for a GPU of `sms` SMs.
+TB_API int32_t tbx_skinny_split_count(int32_t tiles, int32_t kblocks, int32_t slots) {
+  return skinny_split_count(tiles, kblocks, slots);
+}
+TB_API int32_t tbx_decode_chunk_keys(int32_t dtype, int32_t B, int32_t Hkv, int32_t T_max, int32_t sms) {
+  if (B <= 0 || Hkv <= 0 || T_max <= 0 || sms <= 0) return -1;
+  return decode_chunk_keys_sms(dtype, B, Hkv, T_max, sms);
+}
+
 // Test hook (not part of the public header): C[M, N] = A[M, K]·B[N, K]ᵀ in
 // fp32 through the bf16 tcgen05 main loop, N-tile width bn (128 or 256).
 TB_API tb_status tbx_gemm_bf16(const void* A, const void* B, float* Cp, int32_t M, int32_t N, int32_t K, int32_t bn,
