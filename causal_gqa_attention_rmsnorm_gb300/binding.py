@@ -85,7 +85,8 @@ def lib() -> ctypes.CDLL:
         L.tb_status_string.restype = ctypes.c_char_p
         L.tb_last_error_message.argtypes = []
         L.tb_last_error_message.restype = ctypes.c_char_p
-        L.tbx_gemm_bf16.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p]
+        L.tbx_gemm_bf16.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
+                                    c_void_p]
         L.tbx_trace_enable.argtypes = [c_int32]
         L.tbx_trace_enable.restype = c_int32
         L.tbx_trace_read.argtypes = [c_int32, ctypes.POINTER(c_float), c_int32]
@@ -206,12 +207,6 @@ class KVCache:
         codes = lambda: torch.zeros((B, Hkv, T_max, dh), dtype=torch.int8, device=device)
         scales = lambda: torch.zeros((B, Hkv, T_max), dtype=torch.float32, device=device)
         return KVCache(codes(), codes(), torch.zeros(B, dtype=torch.int32, device=device), None, scales(), scales())
-
-    def dequantized(self):
-        """(k, v) of an int8 cache as fp32 code·scale, [B, Hkv, T_max, dh]."""
-        if self.k.dtype != torch.int8:
-            raise ValueError("not an int8 cache")
-        return (self.k.float() * self.k_scale[..., None], self.v.float() * self.v_scale[..., None])
 
     @staticmethod
     def empty_paged(B: int, Hkv: int, T_max: int, dh: int, page_size: int, num_pages: int, block_table: torch.Tensor,
@@ -356,14 +351,15 @@ def tb_get_device_error(stream=None, clear: bool = False) -> int:
     return out.value
 
 
-def tbx_gemm_bf16(A: torch.Tensor, B: torch.Tensor, bn: int = 256, stream=None) -> torch.Tensor:
-    """Test hook: A [M, K] · B [N, K]ᵀ in fp32 through the tcgen05 main loop."""
+def tbx_gemm_bf16(A: torch.Tensor, B: torch.Tensor, bn: int = 256, mt: int = 1, stream=None) -> torch.Tensor:
+    """Test hook: A [M, K] · B [N, K]ᵀ in fp32 through the tcgen05 main loop
+    (mt = 2: two 128-row A blocks per 256-column weight tile)."""
     _need(A, "A", torch.bfloat16)
     _need(B, "B", torch.bfloat16)
     M, K = A.shape
     N = B.shape[0]
     C = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    _check("tbx_gemm_bf16", lib().tbx_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, bn,
+    _check("tbx_gemm_bf16", lib().tbx_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, bn, mt,
                                                 _stream(stream)))
     return C
 

@@ -25,7 +25,10 @@ constexpr size_t kStaticScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 // Device address of g_decode_scratch on the current device, looked up once per
-// device (host code cannot use the symbol itself as a device pointer).
+// device (host code cannot use the symbol itself as a device pointer) and kept
+// for the life of the process; a cudaDeviceReset after the first call on a
+// device would reload the module and could move the array, so it is not
+// supported.
 void* scratch_on_current_device(cudaError_t* why) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};

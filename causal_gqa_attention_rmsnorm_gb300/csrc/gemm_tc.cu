@@ -500,7 +500,9 @@ int lse_tile_cols() { return 256; }
 cudaError_t gemm_tc_lse(const void* A, const void* B, int M, int N, int K, const LseArgs& e, cudaStream_t s) {
   return run<256>(A, B, M, N, K, EpiLse{e}, s);
 }
-cudaError_t gemm_tc_f32out(const void* A, const void* B, float* Cp, int M, int N, int K, int bn, cudaStream_t s) {
+cudaError_t gemm_tc_f32out(const void* A, const void* B, float* Cp, int M, int N, int K, int bn, int mt,
+                           cudaStream_t s) {
+  if (mt == 2) return run<256, EpiF32, 2>(A, B, M, N, K, EpiF32{Cp, N}, s);
   if (bn == 256) return run<256>(A, B, M, N, K, EpiF32{Cp, N}, s);
   return run<128>(A, B, M, N, K, EpiF32{Cp, N}, s);
 }

@@ -202,7 +202,9 @@ TB_API tb_status tb_block_decode(const tb_block_cfg *cfg, const void *packed, co
  *  returns TB_ERR_INVALID_ARG and launches nothing.
  *  The first call on each device looks up the array's device address
  *  (cudaGetSymbolAddress) with that device current; make that first call
- *  before any stream capture.
+ *  before any stream capture.  The address is kept for the life of the
+ *  process, so a device reset (cudaDeviceReset) after the first call on that
+ *  device is not supported: the module is reloaded and the array may move.
  *  All calls share the one array and its contents persist between calls (the
  *  step zeroes what it accumulates into), so calls that may overlap on the
  *  GPU — on different streams, or from different threads — race; serialise

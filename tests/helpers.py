@@ -19,12 +19,10 @@ from workloads import BlockShape
 F32_NORMWISE_TOL = 1e-4
 BF16_REL_L2_TOL = 1e-2
 BF16_MAX_ABS_TOL = 3e-2
-# Max-abs bound used for d = 4096 workloads.  A CPU fp32 model of the bf16
-# path's rounding points (tests/rounding_model.py) reaches 7.2e-2 against the
-# oracle on a 1024-token slice of gqa_8k (4.2M outputs); the full workload has
-# ~32x more outputs, whose Gaussian-tail maximum is sqrt(ln(1.3e8)/ln(4.2e6))
-# ≈ 1.1x larger, so 1e-1 leaves ~25% headroom over pure rounding noise.
-D4096_MAX_ABS_BOUND = 1e-1
+# At d = 4096 bf16 operand rounding alone exceeds the 3e-2 max-abs bar; those
+# workloads are held to the relative-L2 bar plus a max-abs bound measured in
+# the same run from the rounding model (tests/rounding_model.py): 1.25x the
+# model's own max-abs error on the same rows.
 
 
 def oracle_cfg(s: BlockShape) -> oracle.Cfg:
@@ -65,3 +63,12 @@ def assert_close(got, ref, dtype: str, what: str = "y", max_abs_tol: float = BF1
         assert e["rel_l2"] <= BF16_REL_L2_TOL, f"{what}: {e}"
         assert e["max_abs"] <= max_abs_tol, f"{what}: {e}"
     return e
+
+
+def dequantized(kv):
+    """(k, v) of an int8 cache as fp32 code·scale, [B, Hkv, T_max, dh] (test
+    inspection of what the cache stores; the library never dequantises on the
+    host)."""
+    if kv.k.dtype != torch.int8:
+        raise ValueError("not an int8 cache")
+    return (kv.k.float() * kv.k_scale[..., None], kv.v.float() * kv.v_scale[..., None])

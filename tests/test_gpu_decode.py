@@ -7,8 +7,9 @@ import torch
 
 import oracle
 import workloads
-from helpers import (BF16_MAX_ABS_TOL, D4096_MAX_ABS_BOUND, assert_close, block_config, errors, oracle_cfg,
+from helpers import (BF16_MAX_ABS_TOL, BF16_REL_L2_TOL, assert_close, block_config, errors, oracle_cfg,
                      oracle_weights, to_device)
+from rounding_model import ERROR_FACTOR, emulate_decode_seq, rounding_consistency
 
 pytestmark = pytest.mark.gpu
 
@@ -148,6 +149,7 @@ def test_kvcache_append():
 
 
 _FULL = {}
+FULL_SAMPLED = [0, 3, 7, 12, 18, 21, 26, 31]
 
 
 def _full_decode_report():
@@ -155,32 +157,61 @@ def _full_decode_report():
     the benchmark's launch configuration, run once per session.  Only the
     sampled sequences hold cache data; every other cache row is NaN, so a read
     past a sequence's own rows or across sequences shows up as NaN in a
-    checked row."""
+    checked row.  Keeps, per sampled sequence, the GPU's y, the oracle's y and
+    the rounding model's y in orders "a" and "b" (over the same seeded cache
+    rows), and the error reports of y and of the appended k row."""
     if not _FULL:
         s = workloads.CONFIGS["gqa_decode"]
         lens = workloads.make_lens(s, seed=0)
-        sampled = [0, 7, 21, 31]
-        s, inp, kv, y, err = _decode_case(s, 0, lens.tolist(), s.T, batches_with_data=sampled)
+        s, inp, kv, y, err = _decode_case(s, 0, lens.tolist(), s.T, batches_with_data=FULL_SAMPLED)
         assert err == 0
         assert kv.lens.cpu().tolist() == [int(n) + 1 for n in lens]
-        for b in sampled:
-            ref = _oracle_step(s, inp, kv, b, int(lens[b]))
-            _FULL[b] = (errors(y[b, 0].cpu().double().numpy(), ref["y"]),
-                        errors(kv.k[b, :, int(lens[b])].cpu().double().numpy(), ref["k"]))
+        for b in FULL_SAMPLED:
+            pos = int(lens[b])
+            ref = _oracle_step(s, inp, kv, b, pos)
+            kc, vc = workloads.make_cache_rows(s, 0, b, pos)
+            got = y[b, 0].cpu().double().numpy()
+            _FULL[b] = dict(got=got, ref=ref["y"],
+                            emu_a=emulate_decode_seq(inp, s, b, kc, vc, order="a").double().numpy(),
+                            emu_b=emulate_decode_seq(inp, s, b, kc, vc, order="b").double().numpy(),
+                            ey=errors(got, ref["y"]),
+                            ek=errors(kv.k[b, :, pos].cpu().double().numpy(), ref["k"]))
     return _FULL
 
 
+def _stack(rep, key):
+    return np.stack([r[key] for r in rep.values()])
+
+
+def test_decode_gqa_full_workload_error_is_bf16_rounding():
+    """On the sampled sequences of the full decode workload the GPU is as close
+    to the rounding model (tests/rounding_model.py, order "a") as the model's
+    second order is, within 1.5x, and its error against the oracle is within
+    1.25x of the model's (max-abs and relative L2 over all sampled rows)."""
+    rep = _full_decode_report()
+    c = rounding_consistency(_stack(rep, "got"), _stack(rep, "emu_a"), _stack(rep, "emu_b"), _stack(rep, "ref"))
+    print(f"gqa_decode sampled rows: order noise {c['noise']}, GPU to model {c['dev']}, "
+          f"model error {c['model']}, GPU error {c['err']}")
+    assert c["ok"], c
+
+
 def test_decode_gqa_full_workload_sampled_sequences():
-    for b, (ey, ek) in _full_decode_report().items():
-        assert ey["finite"] and ey["rel_l2"] <= 1e-2 and ey["max_abs"] <= D4096_MAX_ABS_BOUND, (b, ey)
-        assert ek["finite"] and ek["rel_l2"] <= 1e-2 and ek["max_abs"] <= BF16_MAX_ABS_TOL, (b, ek)
+    """Relative-L2 bar 1e-2 per sampled sequence, max-abs within 1.25x the
+    rounding model's max-abs error over the sampled rows (measured in the same
+    run); the appended k rows meet both bf16 bars."""
+    rep = _full_decode_report()
+    bound = ERROR_FACTOR * errors(_stack(rep, "emu_a"), _stack(rep, "ref"))["max_abs"]
+    for b, r in rep.items():
+        ey, ek = r["ey"], r["ek"]
+        assert ey["finite"] and ey["rel_l2"] <= BF16_REL_L2_TOL and ey["max_abs"] <= bound, (b, ey, bound)
+        assert ek["finite"] and ek["rel_l2"] <= BF16_REL_L2_TOL and ek["max_abs"] <= BF16_MAX_ABS_TOL, (b, ek)
 
 
 @pytest.mark.xfail(strict=True, reason="bf16 operand rounding alone exceeds 3e-2 max-abs at d = 4096 "
                                        "(see test_rounding_floor.py)")
 def test_decode_gqa_full_workload_max_abs_bar():
-    for b, (ey, _) in _full_decode_report().items():
-        assert ey["max_abs"] <= BF16_MAX_ABS_TOL, (b, ey)
+    for b, r in _full_decode_report().items():
+        assert r["ey"]["max_abs"] <= BF16_MAX_ABS_TOL, (b, r["ey"])
 
 
 @pytest.mark.parametrize("cache", ["bf16", "int8"])

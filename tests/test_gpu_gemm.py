@@ -6,20 +6,25 @@ import torch
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("M,N,K,bn", [
-    (128, 256, 64, 256),        # one tile, one k-block
-    (256, 512, 1024, 256),      # several tiles and stages
-    (300, 260, 192, 128),       # ragged M and N
-    (32, 6144, 4096, 128),      # decode-shaped (M = 32)
-    (1000, 768, 768, 256),      # ragged M, N multiple of 256 with K 768
-    (4096, 2304, 768, 256),     # many tiles per CTA (persistent loop, accumulator ping-pong)
+@pytest.mark.parametrize("M,N,K,bn,mt", [
+    (128, 256, 64, 256, 1),        # one tile, one k-block
+    (256, 512, 1024, 256, 1),      # several tiles and stages
+    (300, 260, 192, 128, 1),       # ragged M and N
+    (32, 6144, 4096, 128, 1),      # decode-shaped (M = 32)
+    (1000, 768, 768, 256, 1),      # ragged M, N multiple of 256 with K 768
+    (4096, 2304, 768, 256, 1),     # many tiles per CTA (persistent loop, accumulator ping-pong)
+    # row pairs (the long-K W2 tiles): two 128-row A blocks share each weight tile
+    (256, 256, 64, 256, 2),        # one pair, one k-block
+    (1000, 512, 8192, 256, 2),     # 8 row blocks, the last one ragged (104 rows): the last pair part zero-filled
+    (300, 768, 8192, 256, 2),      # 3 row blocks: the second pair's second block lies wholly past M
+    (4096, 1280, 14336, 256, 2),   # 16 pairs x 5 column tiles over 152 CTAs, K of the W2 shape
 ])
-def test_gemm_bf16_matches_fp32_product(M, N, K, bn):
+def test_gemm_bf16_matches_fp32_product(M, N, K, bn, mt):
     from causal_gqa_attention_rmsnorm_gb300 import binding
     g = torch.Generator(device="cpu").manual_seed(M * 7 + N * 3 + K)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16).cuda()
     B = (0.05 * torch.randn(N, K, generator=g)).to(torch.bfloat16).cuda()
-    C = binding.tbx_gemm_bf16(A, B, bn=bn)
+    C = binding.tbx_gemm_bf16(A, B, bn=bn, mt=mt)
     torch.cuda.synchronize()
     ref = A.double() @ B.double().T
     err = (C.double() - ref).abs().max().item()

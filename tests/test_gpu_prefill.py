@@ -11,8 +11,9 @@ import torch
 
 import oracle
 import workloads
-from helpers import (BF16_MAX_ABS_TOL, BF16_REL_L2_TOL, D4096_MAX_ABS_BOUND, assert_close, block_config, errors,
-                     oracle_cfg, oracle_weights, to_device)
+from helpers import (BF16_MAX_ABS_TOL, BF16_REL_L2_TOL, assert_close, block_config, errors, oracle_cfg,
+                     oracle_weights, to_device)
+from rounding_model import ERROR_FACTOR, emulate_prefill_seq, rounding_consistency
 
 pytestmark = pytest.mark.gpu
 
@@ -113,13 +114,17 @@ def test_empty_prefill_is_a_noop():
 
 
 def _full_rows_case(name, sample=None, seed=0):
+    """Prefill of a whole workload on the GPU and the oracle's rows of every
+    sequence (all rows, or ``sample(b, T)``); returns the shape, the inputs,
+    y, one error report per checked sequence, and sequence 0's GPU and oracle
+    rows as fp64 arrays."""
     s = workloads.CONFIGS[name]
     inp = workloads.make_block_inputs(s, seed=seed)
     y, kv = run_prefill(s, inp, with_cache=True)
     w = oracle_weights(inp)
     cfg = oracle_cfg(s)
     x64 = workloads.to_f64(inp["x"])
-    report = []
+    report, seq0 = [], None
     for b in range(s.B):
         rows = None if sample is None else sample(b, s.T)
         if rows is not None and len(rows) == 0:
@@ -127,14 +132,16 @@ def _full_rows_case(name, sample=None, seed=0):
         ref = oracle.block_prefill_seq(x64[b], w, cfg, rows=rows)
         got = y[b].cpu().double().numpy()[ref["rows"]]
         report.append(errors(got, ref["y"]))
+        if b == 0:
+            seq0 = (got, ref["y"])
         S = ref["k"].shape[1]
         assert_close(kv.k[b, :, :S].cpu().double().numpy(), ref["k"], s.dtype, f"k cache b={b}")
         assert_close(kv.v[b, :, :S].cpu().double().numpy(), ref["v"], s.dtype, f"v cache b={b}")
-    return s, y, report
+    return s, inp, y, report, seq0
 
 
 def test_prefill_mha_768_all_rows():
-    s, y, rep = _full_rows_case("mha_768")
+    s, inp, y, rep, _ = _full_rows_case("mha_768")
     for e in rep:
         assert e["finite"] and e["rel_l2"] <= BF16_REL_L2_TOL and e["max_abs"] <= BF16_MAX_ABS_TOL, e
 
@@ -150,32 +157,64 @@ def _gqa_rows(b, T):
 
 
 _D4096 = {}
+ANCHOR_ROWS = 1024
 
 
-def _d4096_report(name):
-    """Run a d = 4096 workload once per session and keep its error report."""
+def _d4096_run(name):
+    """Run a d = 4096 workload once per session: its error reports, sequence
+    0's GPU rows and oracle rows (all T), and the rounding model of sequence 0
+    in order "a" (all T rows)."""
     if name not in _D4096:
         sample = _gqa_rows if name == "gqa_8k" else None
-        s, y, rep = _full_rows_case(name, sample=sample)
+        s, inp, y, rep, (got0, ref0) = _full_rows_case(name, sample=sample)
         assert torch.isfinite(y).all()
+        del y
+        emu0 = emulate_prefill_seq(inp, s, b=0, order="a").double().numpy()
+        model = errors(emu0, ref0)
         for b, e in enumerate(rep):
-            print(f"{name} b={b}: rel_l2 {e['rel_l2']:.2e} max_abs {e['max_abs']:.2e}")
-        _D4096[name] = rep
+            print(f"{name} seq {b}: rel_l2 {e['rel_l2']:.2e} max_abs {e['max_abs']:.2e}")
+        print(f"{name} rounding model, seq 0: rel_l2 {model['rel_l2']:.2e} max_abs {model['max_abs']:.2e}")
+        _D4096[name] = dict(s=s, inp=inp, rep=rep, got0=got0, ref0=ref0, emu0=emu0, model=model)
     return _D4096[name]
 
 
 @pytest.mark.parametrize("name", ["llama2_7b", "gqa_8k"])
+def test_prefill_d4096_error_is_bf16_rounding(name):
+    """The GPU's deviation at d = 4096 is the bf16 rounding the path is built
+    with, and nothing else.  On the first 1024 rows of sequence 0 the GPU is as
+    close to the rounding model (tests/rounding_model.py, order "a") as the
+    model's second summation order is (within 1.5x, max-abs and relative L2);
+    over all rows of sequence 0 its error against the oracle is within 1.25x of
+    the model's."""
+    r = _d4096_run(name)
+    R = ANCHOR_ROWS
+    pre = dict(r["inp"], x=r["inp"]["x"][:1, :R])
+    emu_b = emulate_prefill_seq(pre, r["s"], b=0, order="b").double().numpy()
+    c = rounding_consistency(r["got0"][:R], r["emu0"][:R], emu_b, r["ref0"][:R])
+    print(f"{name} first {R} rows: order noise {c['noise']}, GPU to model {c['dev']}, "
+          f"model error {c['model']}, GPU error {c['err']}")
+    assert c["ok_noise"], c
+    gpu, model = errors(r["got0"], r["ref0"]), r["model"]
+    assert gpu["max_abs"] <= ERROR_FACTOR * model["max_abs"], (gpu, model)
+    assert gpu["rel_l2"] <= ERROR_FACTOR * model["rel_l2"], (gpu, model)
+
+
+@pytest.mark.parametrize("name", ["llama2_7b", "gqa_8k"])
 def test_prefill_d4096_rel_l2_and_rounding_bound(name):
-    """Relative-L2 bar 1e-2, and max-abs within the bound the bf16 rounding
-    model derives (tests/rounding_model.py)."""
-    for e in _d4096_report(name):
+    """Relative-L2 bar 1e-2 on every checked sequence, and max-abs within
+    1.25x the rounding model's max-abs error on all rows of sequence 0 (a
+    bound measured in the same run, over at least as many outputs as any
+    other checked sequence has)."""
+    r = _d4096_run(name)
+    bound = ERROR_FACTOR * r["model"]["max_abs"]
+    for e in r["rep"]:
         assert e["finite"] and e["rel_l2"] <= BF16_REL_L2_TOL, e
-        assert e["max_abs"] <= D4096_MAX_ABS_BOUND, e
+        assert e["max_abs"] <= bound, (e, bound)
 
 
 @pytest.mark.xfail(strict=True, reason="bf16 operand rounding alone exceeds 3e-2 max-abs at d = 4096 "
                                        "(see test_rounding_floor.py)")
 @pytest.mark.parametrize("name", ["llama2_7b", "gqa_8k"])
 def test_prefill_d4096_max_abs_bar(name):
-    for e in _d4096_report(name):
+    for e in _d4096_run(name)["rep"]:
         assert e["max_abs"] <= BF16_MAX_ABS_TOL, e

@@ -4,14 +4,15 @@ A CPU fp32 model of the bf16 path's rounding points (tests/rounding_model.py,
 no CUDA) is compared with the fp64 oracle on a slice of the gqa_8k workload.
 The rounding alone already exceeds 3e-2 max-abs while staying far inside the
 1e-2 relative-L2 bar; the GPU parity tests therefore hold d = 4096 workloads
-to the relative-L2 bar plus a max-abs bound derived from this model, and keep
+to the relative-L2 bar plus a max-abs bound measured from this model in the
+same run (after showing that the GPU's deviation is the model's), and keep
 the 3e-2 bar as a strict expected failure.
 """
 import numpy as np
 
 import oracle
 import workloads
-from helpers import D4096_MAX_ABS_BOUND, errors, oracle_cfg, oracle_weights
+from helpers import errors, oracle_cfg, oracle_weights
 from rounding_model import emulate_prefill_seq
 
 
@@ -23,4 +24,3 @@ def test_bf16_rounding_floor_at_d4096():
     e = errors(emulate_prefill_seq(inp, s).double().numpy(), ref)
     assert e["rel_l2"] < 1e-2                      # the relative bar holds with margin
     assert e["max_abs"] > 3e-2                     # rounding alone misses the max-abs bar
-    assert e["max_abs"] < D4096_MAX_ABS_BOUND / 1.25  # and the derived bound leaves headroom
