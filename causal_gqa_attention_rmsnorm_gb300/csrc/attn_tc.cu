@@ -500,6 +500,9 @@ cudaError_t run(const void* q, const void* k, const void* v, void* o, int B, int
 cudaError_t attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int T, int H, int Hkv,
                             int dh, int kv_stride, int window, cudaStream_t s) {
   if (B <= 0 || T <= 0) return cudaSuccess;
+  // four query heads per KV group and dh 128: one CTA pair per head quad
+  if (dh == 128 && Hkv > 0 && H % Hkv == 0 && (H / Hkv) % 4 == 0)
+    return attn_prefill_pair(q, k, v, o, B, T, H, Hkv, dh, kv_stride, window, s);
   if (dh == 128) return run<128>(q, k, v, o, B, T, H, Hkv, kv_stride, window, s);
   if (dh == 64) return run<64>(q, k, v, o, B, T, H, Hkv, kv_stride, window, s);
   return cudaErrorInvalidValue;

@@ -265,9 +265,13 @@ cudaError_t attn_prefill_simt(int dtype, const void* q, const void* k, const voi
                               int T, int H, int Hkv, int dh, int kv_stride, int window, cudaStream_t s);
 
 // Attention launchers take the sliding-window width (0: full causal).
-// attn_tc.cu (bf16 path, dh 64 or 128)
+// attn_tc.cu (bf16 path, dh 64 or 128): CTA pairs (attn_pair.cu) where H/Hkv
+// is a multiple of 4 and dh = 128, single CTAs otherwise.
 cudaError_t attn_prefill_tc(const void* q, const void* k, const void* v, void* o, int B, int T, int H, int Hkv,
                             int dh, int kv_stride, int window, cudaStream_t s);
+// attn_pair.cu: cudaErrorNotSupported for shapes it does not take.
+cudaError_t attn_prefill_pair(const void* q, const void* k, const void* v, void* o, int B, int T, int H, int Hkv,
+                              int dh, int kv_stride, int window, cudaStream_t s);
 
 // attn_decode.cu
 // Keys per decode work item (chunk) for a step of B sequences over a T_max-row

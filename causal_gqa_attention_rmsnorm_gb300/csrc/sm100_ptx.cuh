@@ -321,5 +321,151 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn = fals
          | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// ---- CTA pairs (cta_group::2) --------------------------------------------
+//
+// Two CTAs of a cluster share each tensor-core operation: an M = 256 MMA
+// issued by the even CTA (the leader) takes A rows 0..127 from the leader's
+// shared memory or tensor memory and rows 128..255 from its peer's, B columns
+// 0..N/2-1 from the leader and N/2..N-1 from the peer, and writes D rows
+// 0..127 into the leader's tensor memory and 128..255 into the peer's, all at
+// the same addresses in both CTAs.  Tensor memory is allocated by one warp in
+// each CTA of the pair together.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the object at shared::cta address `a` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+// Every thread of both CTAs: release this CTA's prior writes, wait for the peer.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on an mbarrier of either CTA, given its shared::cluster address.
+// What the arrival publishes is tensor-memory data, ordered by the tcgen05
+// fences around the barrier, so the default (CTA-scope) release suffices.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for barriers that threads of the peer CTA arrive on (acquire at
+// cluster scope); same time limit and abort protocol.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicOr(err, TB_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+  const bool ok = mbar_wait_cluster(bar, parity, abort, err);
+  return __all_sync(0xffffffffu, ok);
+}
+// 3-D tiled TMA load into this CTA's shared memory whose bytes complete on the
+// mbarrier at shared::cluster address `bar_cluster`, which may be the peer's.
+__device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* m, void* dst, uint32_t bar_cluster, int x, int y,
+                                                 int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Arrive once on the mbarrier at the same shared::cta address in both CTAs of
+// the pair when every pair MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+// Pair S += Q·Kᵀ over dh = 128: A (Q, 128 rows per CTA) K-major, 64-column
+// blocks 16 KB apart; B (K, 64 key rows per CTA) K-major, blocks 8 KB apart.
+#define TB_MMA2_SS_STEP(OA, OB, PRED)                                          \
+  "add.u32 la, %1, " #OA ";\n\t"                                             \
+  "add.u32 lb, %3, " #OB ";\n\t"                                             \
+  "mov.b64 da, {la, %2};\n\t"                                                 \
+  "mov.b64 db, {lb, %4};\n\t"                                                 \
+  "tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %5, " #PRED ";\n\t"
+__device__ __forceinline__ void mma2_tile_ss128(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  const uint32_t alo = (uint32_t)adesc, ahi = (uint32_t)(adesc >> 32);
+  const uint32_t blo = (uint32_t)bdesc, bhi = (uint32_t)(bdesc >> 32);
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      TB_MMA2_SS_STEP(0, 0, pf) TB_MMA2_SS_STEP(2, 2, pt) TB_MMA2_SS_STEP(4, 4, pt) TB_MMA2_SS_STEP(6, 6, pt)
+      TB_MMA2_SS_STEP(1024, 512, pt) TB_MMA2_SS_STEP(1026, 514, pt) TB_MMA2_SS_STEP(1028, 516, pt)
+      TB_MMA2_SS_STEP(1030, 518, pt) "}" ::"r"(d_tmem),
+      "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc)
+      : "memory");
+}
+#undef TB_MMA2_SS_STEP
+
+// Pair O (+)= P·V over 128 keys: P (bf16 pairs) in tensor memory, 8 columns
+// per 16 keys; V (64 value columns per CTA) MN-major, 16-key slices 2 KB apart.
+#define TB_MMA2_TS_STEP(K, PRED)                                               \
+  "add.u32 ta, %1, " #K "*8;\n\t"                                             \
+  "add.u32 lb, %2, " #K "*128;\n\t"                                           \
+  "mov.b64 db, {lb, %3};\n\t"                                                 \
+  "tcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, " #PRED ";\n\t"
+__device__ __forceinline__ void mma2_tile_ts128(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t acc) {
+  const uint32_t blo = (uint32_t)bdesc, bhi = (uint32_t)(bdesc >> 32);
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b32 ta, lb;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 pf, %5, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      TB_MMA2_TS_STEP(0, pf) TB_MMA2_TS_STEP(1, pt) TB_MMA2_TS_STEP(2, pt) TB_MMA2_TS_STEP(3, pt)
+      TB_MMA2_TS_STEP(4, pt) TB_MMA2_TS_STEP(5, pt) TB_MMA2_TS_STEP(6, pt) TB_MMA2_TS_STEP(7, pt) "}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+#undef TB_MMA2_TS_STEP
+
 }  // namespace ptx
 }  // namespace tb
