@@ -45,9 +45,11 @@ METRIC = "prefill tokens/s per block (attention TFLOP/s, GEMM TFLOP/s; decode KV
 
 
 def decode_launches(B: int) -> int:
-    """Kernels one decode step launches: row statistics, the two attention
-    kernels, and the four GEMMs."""
-    return 3 + 4 * (2 if B <= FEW_TOKENS else 1)
+    """Kernels one bf16 decode step launches: the two attention kernels and
+    the four GEMMs, each with its partial-sum epilogue when the batch takes the
+    few-token GEMM (whose QKV epilogue also forms the row statistics); above
+    that, the tile GEMMs and the row-statistics kernel."""
+    return 2 + 4 * 2 if B <= FEW_TOKENS else 3 + 4
 
 
 def load_peaks():

@@ -108,7 +108,7 @@ tb_status report(tb_status st, const char* fmt, ...);
 cudaError_t launch_pack(int dtype, const Dims& D, const tb_block_weights& w, void* packed,
                         const Packed& P, float rope_base, cudaStream_t s);
 cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, float* r,
-                             int* cnt_zero, int T, int32_t* lens_set, int32_t* lens_bump,
+                             int T, int32_t* lens_set, int32_t* lens_bump,
                              int32_t* pos_out, int T_max, int* zero_word, int* err, cudaStream_t s);
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new,
                              int n, int* err, cudaStream_t s);
@@ -143,33 +143,64 @@ __device__ __forceinline__ long long paged_row(const PagedKV& p, int Hkv, int b,
 
 // Row sums in a fixed order, so that a run is reproducible bit for bit: each
 // of a row's producers (one per column tile or column range of the GEMM that
-// forms the row) stores its partial at part[row·stride + p]; the producer that
-// arrives last at a group of rows (counted in cnt[group], zeroed before the
-// GEMM) adds the partials in the order p = 0, 1, ... and writes out[row].
+// forms the row) stores its partial at part[row·stride + p], p < n; the
+// consumer, a later kernel that sees every partial, adds them in the order
+// p = 0, 1, ..., n-1.  No fence, counter or atomic sits on the producer's
+// path.
 struct RowSum {
   float* part;             // [M, stride]
-  float* out;              // [M]
-  int* cnt;                // one arrival counter per row group
   int stride;              // partials per row the buffer holds
+  int n;                   // partials per row the producing GEMM writes (set by its launcher)
 };
 
 // Σ_{p < n} part[p] added in the order p = 0, 1, ..., with the loads issued
-// eight at a time (L2 reads of partials other CTAs wrote).
+// eight at a time (read-only: the partials come from an earlier kernel).
 __device__ __forceinline__ float ordered_sum(const float* part, int n) {
   float sum = 0.f;
   int p = 0;
   for (; p + 8 <= n; p += 8) {
     float t[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) t[u] = __ldcg(part + p + u);
+    for (int u = 0; u < 8; ++u) t[u] = __ldg(part + p + u);
 #pragma unroll
     for (int u = 0; u < 8; ++u) sum += t[u];
   }
-  for (; p < n; ++p) sum += __ldcg(part + p);
+  for (; p < n; ++p) sum += __ldg(part + p);
   return sum;
 }
 
 // GEMM epilogue argument bundles.
+
+// RMSNorm-1 statistics and the decode step's bookkeeping taken by the QKV
+// GEMM's partial-sum epilogue (few-token decode): every CTA of a token row
+// forms the row's Σx² and reads its position from lens.  x == nullptr: r and
+// the positions come from the row-statistics kernel instead.
+struct QKVStats {
+  const void* x = nullptr;   // [M, d] block input (the block's dtype)
+  int d = 0;
+  float eps = 0.f;
+  const int32_t* lens = nullptr;   // token m sits at lens[m] (advanced later, by the Wo epilogue)
+  int32_t* pos_out = nullptr;      // [M] the positions, -1 for a full cache, for the step's later kernels
+  int T_max = 0;
+  int* zero_word = nullptr;        // zeroed for a later kernel of the step
+  int* err = nullptr;
+};
+// RMSNorm-1 statistics formed inside the tile QKV GEMM (prefill): one extra
+// warp per CTA computes r for its share of each group of kStatRows rows, in
+// group order, and counts the finished group in done[group] (zeroed before the
+// launch); a tile's epilogue waits, bounded, until its group's count reaches
+// the grid size.  The launch is cooperative, so every CTA it waits on runs.
+// x == nullptr: r comes from the row-statistics kernel.
+constexpr int kStatRows = 2048;
+struct TileStats {
+  const void* x = nullptr;   // [M, d] block input (the block's dtype)
+  int d = 0;
+  float eps = 0.f;
+  float* r = nullptr;        // [M] the row scales (the epilogue reads them as QKVArgs::r)
+  int* done = nullptr;       // [ceil(M / kStatRows)] arrival counts
+  int32_t* lens_set = nullptr;   // prefill with a cache: lens[b] = T
+  int T = 0;
+};
 struct QKVArgs {
   const float* r;          // [M] RMSNorm-1 inverse RMS of each token
   const float2* rope;      // [max_pos, dh/2]
@@ -181,15 +212,19 @@ struct QKVArgs {
   const int32_t* pos;      // decode: position of sequence b (-1: skip); prefill: nullptr
   PagedKV pg;              // also (or, with k == nullptr, only) store k and v rows into this paged cache
   bool kv_dense = false;   // k/v take the call's rows densely: row = token index in the call, not its position
+  QKVStats st;             // few-token decode: statistics and positions formed in the epilogue
+  TileStats ts;            // tile GEMM (prefill): statistics formed by the GEMM's statistics warp
 };
 struct WoArgs {
   const void* x;           // [M, d] residual input (cfg dtype)
   float* h;                // [M, d] fp32 residual stream after attention
   void* hb;                // [M, d] cfg dtype copy of h (A operand of W1/W3), may be == h for f32
-  RowSum ssq;              // Σ h² of each row: out [M]
+  RowSum ssq;              // Σ h² of each row, as partials
+  const int32_t* pos = nullptr;   // few-token decode: lens[m] = pos[m] + 1 for pos[m] ≥ 0, here
+  int32_t* lens = nullptr;
 };
 struct W13Args {
-  const float* ssq;        // [M] Σ h²
+  RowSum ssq;              // Σ h² of each row: the Wo GEMM's partials, summed here in order
   void* a;                 // [M, f] SiLU(gate)·up
 };
 struct LogitsArgs {
@@ -238,7 +273,7 @@ cudaError_t launch_pack_transpose(int dtype, const void* src, int K, int N, cons
 cudaError_t gemm_simt_qkv(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
                           const QKVArgs& e, cudaStream_t s);
 cudaError_t gemm_simt_wo(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
-                         const WoArgs& e, cudaStream_t s);
+                         const WoArgs& e, cudaStream_t s, int* row_parts);
 cudaError_t gemm_simt_w13(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
                           const W13Args& e, cudaStream_t s);
 cudaError_t gemm_simt_w2(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
@@ -254,7 +289,7 @@ int skinny_split_count(int tiles, int kblocks, int slots);
 cudaError_t gemm_skinny_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
                             float* part, cudaStream_t s);
 cudaError_t gemm_skinny_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
-                           float* part, cudaStream_t s);
+                           float* part, cudaStream_t s, int* row_parts);
 cudaError_t gemm_skinny_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
                             float* part, cudaStream_t s);
 cudaError_t gemm_skinny_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,

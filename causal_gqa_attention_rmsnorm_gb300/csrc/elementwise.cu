@@ -46,14 +46,13 @@ __global__ void k_rope_table(float2* __restrict__ tab, int max_pos, int half, in
 }
 
 // One warp per token row: r = 1/sqrt(mean(x²) + eps).  Side duties, done by
-// lane 0 of the row: clear the row's arrival counter of the second norm's
-// ordered row sums (cnt_zero), set the
-// cache length after a prefill (lens_set), or take the decode position and
-// advance the cache length (lens_bump -> pos_out, -1 when the cache is full),
-// and zero a counter a later kernel of the step uses (zero_word).
+// lane 0 of the row: set the cache length after a prefill (lens_set), or take
+// the decode position and advance the cache length (lens_bump -> pos_out, -1
+// when the cache is full), and zero a counter a later kernel of the step uses
+// (zero_word).
 template <typename T>
-__global__ void k_row_stats(const T* __restrict__ x, int M, int d, float eps, float* __restrict__ r,
-                            int* __restrict__ cnt_zero, int Tseq, int32_t* __restrict__ lens_set,
+__global__ void k_row_stats(const T* __restrict__ x, int M, int d, float eps, float* __restrict__ r, int Tseq,
+                            int32_t* __restrict__ lens_set,
                             int32_t* __restrict__ lens_bump, int32_t* __restrict__ pos_out, int T_max,
                             int* __restrict__ zero_word, int* __restrict__ err) {
   pdl_trigger();
@@ -99,7 +98,6 @@ __global__ void k_row_stats(const T* __restrict__ x, int M, int d, float eps, fl
   s = warp_sum(s);
   if (lane == 0) {
     r[row] = 1.0f / sqrtf(s / (float)d + eps);
-    if (cnt_zero) cnt_zero[row] = 0;
     if (zero_word && row == 0) *zero_word = 0;
     if (lens_set && (row % Tseq) == 0) lens_set[row / Tseq] = Tseq;
     if (lens_bump) {
@@ -230,16 +228,16 @@ cudaError_t launch_pack(int dtype, const Dims& D, const tb_block_weights& w, voi
   return cudaGetLastError();
 }
 
-cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, float* r, int* cnt_zero,
-                             int T, int32_t* lens_set, int32_t* lens_bump, int32_t* pos_out, int T_max,
-                             int* zero_word, int* err, cudaStream_t s) {
+cudaError_t launch_row_stats(int dtype, const void* x, int M, int d, float eps, float* r, int T, int32_t* lens_set,
+                             int32_t* lens_bump, int32_t* pos_out, int T_max, int* zero_word, int* err,
+                             cudaStream_t s) {
   const int threads = 256;
   const unsigned blocks = (unsigned)(((size_t)M * 32 + threads - 1) / threads);
   if (dtype == TB_F32)
-    return launch_pdl(k_row_stats<float>, dim3(blocks), dim3(threads), 0, s, (const float*)x, M, d, eps, r,
-                      cnt_zero, T, lens_set, lens_bump, pos_out, T_max, zero_word, err);
-  return launch_pdl(k_row_stats<bf16>, dim3(blocks), dim3(threads), 0, s, (const bf16*)x, M, d, eps, r, cnt_zero,
-                    T, lens_set, lens_bump, pos_out, T_max, zero_word, err);
+    return launch_pdl(k_row_stats<float>, dim3(blocks), dim3(threads), 0, s, (const float*)x, M, d, eps, r, T,
+                      lens_set, lens_bump, pos_out, T_max, zero_word, err);
+  return launch_pdl(k_row_stats<bf16>, dim3(blocks), dim3(threads), 0, s, (const bf16*)x, M, d, eps, r, T, lens_set,
+                    lens_bump, pos_out, T_max, zero_word, err);
 }
 
 cudaError_t launch_pack_transpose(int dtype, const void* src, int K, int N, const void* gain, void* dst,

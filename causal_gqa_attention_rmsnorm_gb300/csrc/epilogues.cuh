@@ -1,8 +1,10 @@
 // GEMM epilogues of the block, shared by the fp32 SIMT GEMM and the bf16
 // tcgen05 GEMM.  Each functor receives 4 consecutive output columns
 // [col, col+4) of one row with col % 4 == 0, in fp32, and returns a value the
-// caller sums over the row's columns when kRowReduce is set (into the RowSum
-// that row_sums() names).
+// caller sums over its share of the row's columns when kRowReduce is set, as
+// one partial of the RowSum that row_sums() names.  kRowSumIn marks an
+// epilogue whose row inputs start from such a RowSum (row_sum_in), so that the
+// tile GEMM can form each row's sum once per warp.
 //
 // Steps ("Transformer block" page, tirogla.com, "How it works" step 2-3):
 //   QKV  : × r (RMSNorm-1 row scale), RoPE on q and k, scatter q / k / v
@@ -110,6 +112,10 @@ template <typename T, bool kStream = false>
 struct EpiQKV {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
+  static constexpr bool kRowSumIn = false;
+  static constexpr bool kRowStats = true;           // can form RMSNorm-1 statistics (a.st.x != nullptr)
+  static constexpr bool kRowDone = false;
+  static constexpr bool kTileStats = true;          // the tile GEMM may form them (a.ts.x != nullptr)
   QKVArgs a;
   int H, Hkv, dh, dh_shift;             // dh = 1 << dh_shift
   struct RowAux { float r; int b, t, qt, kt; };
@@ -122,7 +128,95 @@ struct EpiQKV {
       ra.b = row / a.T; ra.t = row - ra.b * a.T; ra.qt = ra.t;
     }
     ra.kt = a.kv_dense ? ra.qt : ra.t;
-    ra.r = a.r[row];
+    ra.r = __ldcg(a.r + row);       // L2: with a.ts.x set, another CTA of this kernel wrote it
+    return ra;
+  }
+  // The tile GEMM's statistics warp: Σx² of token row m over its 32 lanes
+  // (16-byte vectors lane, lane + 32, ...), added across the warp in a fixed
+  // order ("Transformer block" page, RMSNorm: eps inside the root).  Sixteen
+  // loads per lane are in flight at once (a whole 8 KB row at d = 4096), so
+  // that one warp per CTA keeps ahead of the tiles that wait for its rows.
+  __device__ __forceinline__ float tile_row_scale(int m, int lane) const {
+    const int d = a.ts.d;
+    const T* xr = (const T*)a.ts.x + (size_t)m * d;
+    constexpr int V = 16 / sizeof(T), U = 16;
+    float s = 0.f;
+    if (d % V == 0) {
+      const uint4* p = reinterpret_cast<const uint4*>(xr);
+      const int nv = d / V;
+      int i = lane;
+      for (; i + 32 * (U - 1) < nv; i += 32 * U) {
+        Vec16<T> v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u].raw = __ldcs(p + i + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int j = 0; j < V; ++j) {
+            const float f = v[u].get(j);
+            s = fmaf(f, f, s);
+          }
+      }
+      for (; i < nv; i += 32) {
+        Vec16<T> v;
+        v.raw = __ldg(p + i);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+          const float f = v.get(j);
+          s = fmaf(f, f, s);
+        }
+      }
+    } else {
+      for (int i = lane; i < d; i += 32) {
+        const float f = to_f(xr[i]);
+        s = fmaf(f, f, s);
+      }
+    }
+    s = warp_sum(s);
+    return 1.0f / sqrtf(s / (float)d + a.ts.eps);
+  }
+  // Few-token decode with a.st.x set: this thread's share (16-byte vectors
+  // tid, tid + nthreads, ...) of Σx² over token row m ("Transformer block"
+  // page, RMSNorm: mean of squares, eps inside the root).
+  __device__ __forceinline__ float row_stats_partial(int m, int tid, int nthreads) const {
+    const int d = a.st.d;
+    const T* xr = (const T*)a.st.x + (size_t)m * d;
+    constexpr int V = 16 / sizeof(T);
+    float s = 0.f;
+    if (d % V == 0) {
+      const uint4* p = reinterpret_cast<const uint4*>(xr);
+      for (int i = tid; i < d / V; i += nthreads) {
+        Vec16<T> v;
+        v.raw = __ldg(p + i);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+          const float f = v.get(j);
+          s = fmaf(f, f, s);
+        }
+      }
+    } else {
+      for (int i = tid; i < d; i += nthreads) {
+        const float f = to_f(xr[i]);
+        s = fmaf(f, f, s);
+      }
+    }
+    return s;
+  }
+  // The row inputs from Σx² and lens; the row's first CTA (first) publishes
+  // the position, flags a full cache, and zeroes the step's work counter.
+  __device__ __forceinline__ RowAux row_aux_stats(int m, float ssq, bool first) const {
+    RowAux ra;
+    const int p = a.st.lens[m];
+    ra.b = m;
+    ra.t = (p >= 0 && p < a.st.T_max) ? p : -1;
+    ra.qt = 0;
+    ra.kt = a.kv_dense ? ra.qt : ra.t;
+    ra.r = 1.0f / sqrtf(ssq / (float)a.st.d + a.st.eps);
+    if (first) {
+      a.st.pos_out[m] = ra.t;
+      if (ra.t < 0) atomicOr(a.st.err, TB_DEVERR_CACHE_FULL);
+      if (m == 0 && a.st.zero_word) *a.st.zero_word = 0;
+    }
     return ra;
   }
   __device__ __forceinline__ Aux aux(int, int col, const RowAux& ra) const {
@@ -166,6 +260,10 @@ template <typename T, bool kStream = false>
 struct EpiWo {
   static constexpr bool kRowReduce = true;
   static constexpr bool kRowLse = false;
+  static constexpr bool kRowSumIn = false;
+  static constexpr bool kRowStats = false;
+  static constexpr bool kRowDone = true;            // few-token decode: advances the cache length
+  static constexpr bool kTileStats = false;
   WoArgs a;
   int d;
   struct RowAux {};
@@ -184,20 +282,33 @@ struct EpiWo {
     return v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
   }
   __device__ __forceinline__ const RowSum& row_sums() const { return a.ssq; }
+  // once per token row, after every reader of the old cache length
+  __device__ __forceinline__ void row_done(int m) const {
+    if (a.lens && a.pos[m] >= 0) a.lens[m] = a.pos[m] + 1;
+  }
 };
 
 template <typename T, bool kStream = false>
 struct EpiW13 {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
+  static constexpr bool kRowSumIn = true;
+  static constexpr bool kRowStats = false;
+  static constexpr bool kRowDone = false;
+  static constexpr bool kTileStats = false;
   W13Args a;
   int d, f;
   float eps;
   struct RowAux { float r2; };
   struct Aux {};
-  __device__ __forceinline__ RowAux row_aux(int row) const {
-    return RowAux{1.0f / sqrtf(a.ssq[row] / (float)d + eps)};
+  // Σ h² of a row: the Wo GEMM's partials in order
+  __device__ __forceinline__ float row_sum_in(int row) const {
+    return ordered_sum(a.ssq.part + (size_t)row * a.ssq.stride, a.ssq.n);
   }
+  __device__ __forceinline__ RowAux row_aux_with(float ssq) const {
+    return RowAux{1.0f / sqrtf(ssq / (float)d + eps)};
+  }
+  __device__ __forceinline__ RowAux row_aux(int row) const { return row_aux_with(row_sum_in(row)); }
   __device__ __forceinline__ Aux aux(int, int, const RowAux&) const { return Aux{}; }
   __device__ __forceinline__ float operator()(int row, int col, float v[4], const RowAux& ra, const Aux&) const {
     const float r2 = ra.r2;
@@ -212,6 +323,10 @@ template <bool kStream = false>
 struct EpiW2 {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
+  static constexpr bool kRowSumIn = false;
+  static constexpr bool kRowStats = false;
+  static constexpr bool kRowDone = false;
+  static constexpr bool kTileStats = false;
   W2Args a;
   int d;
   struct RowAux {};
@@ -239,6 +354,10 @@ struct EpiW2 {
 struct EpiLogits {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
+  static constexpr bool kRowSumIn = false;
+  static constexpr bool kRowStats = false;
+  static constexpr bool kRowDone = false;
+  static constexpr bool kTileStats = false;
   LogitsArgs a;
   struct RowAux { float r; };
   struct Aux {};
@@ -261,6 +380,10 @@ struct EpiLogits {
 struct EpiLse {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = true;
+  static constexpr bool kRowSumIn = false;
+  static constexpr bool kRowStats = false;
+  static constexpr bool kRowDone = false;
+  static constexpr bool kTileStats = false;
   LseArgs a;
   struct RowAux { float r; int t; };
   struct Aux {};

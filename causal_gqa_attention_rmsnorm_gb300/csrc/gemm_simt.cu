@@ -64,20 +64,6 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const T* __restrict__ A, cons
       if (tx == 0 && row < M) epi.row_sums().part[(size_t)row * epi.row_sums().stride + blockIdx.x] = part;
     }
   }
-  if constexpr (Epi::kRowReduce) {
-    // the CTA that completes a 64-row block sums each row's partials in order
-    const RowSum& rs = epi.row_sums();
-    __threadfence();
-    __syncthreads();
-    __shared__ int last;
-    if (threadIdx.x == 0) last = atomicAdd(rs.cnt + blockIdx.y, 1) == (int)gridDim.x - 1;
-    __syncthreads();
-    if (last && threadIdx.x < BM && m0 + (int)threadIdx.x < M) {
-      __threadfence();
-      const int row = m0 + threadIdx.x;
-      rs.out[row] = ordered_sum(rs.part + (size_t)row * rs.stride, (int)gridDim.x);
-    }
-  }
 }
 
 template <typename T, class Epi>
@@ -95,7 +81,8 @@ cudaError_t gemm_simt_qkv(int dtype, const void* A, const void* B, int M, int N,
   return run<bf16>(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
 }
 cudaError_t gemm_simt_wo(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
-                         const WoArgs& e, cudaStream_t s) {
+                         const WoArgs& e, cudaStream_t s, int* row_parts) {
+  if (row_parts) *row_parts = (N + BN - 1) / BN;     // one Σh² partial per row and column block
   if (dtype == TB_F32) return run<float>(A, B, M, N, K, EpiWo<float>{e, D.d}, s);
   return run<bf16>(A, B, M, N, K, EpiWo<bf16>{e, D.d}, s);
 }

@@ -209,7 +209,12 @@ __global__ void __launch_bounds__(192)
 
 // Sum of the K-range partials of 4 consecutive outputs of one token, then the
 // fused epilogue.  Rows (tokens) are blockIdx.y, so a row reduction (Σh² of
-// the Wo epilogue) is a warp sum per warp and one ordered sum per row.
+// the Wo epilogue) is one partial per warp.  With RMSNorm-1 statistics in the
+// QKV epilogue (kRowStats, a.st.x set) every CTA of row m first forms the
+// row's Σx² itself (the row is a few KB, read from L2 by each of the row's
+// CTAs) in a fixed order: per thread, per warp, then warps in order.
+constexpr int kEpiWarps = 8;                 // warps per CTA of the partial-sum epilogue (256 threads)
+
 template <class Epi>
 __global__ void __launch_bounds__(256)
     k_splitk_epilogue(const float* __restrict__ part, int splits, int M, int N, Epi epi) {
@@ -218,6 +223,28 @@ __global__ void __launch_bounds__(256)
   const int m = blockIdx.y;
   const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   float r = 0.f;
+  typename Epi::RowAux ra_stats{};
+  bool have_stats = false;
+  if constexpr (Epi::kRowStats) {
+    if (epi.a.st.x) {
+      __shared__ float s_part[kEpiWarps];
+      __shared__ typename Epi::RowAux s_ra;
+      const float ss = warp_sum(epi.row_stats_partial(m, threadIdx.x, blockDim.x));
+      if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int w = 0; w < kEpiWarps; ++w) t += s_part[w];
+        s_ra = epi.row_aux_stats(m, t, blockIdx.x == 0);
+      }
+      __syncthreads();
+      ra_stats = s_ra;
+      have_stats = true;
+    }
+  }
+  if constexpr (Epi::kRowDone) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) epi.row_done(m);
+  }
   if (col < N) {
     // the first eight partials are requested before the epilogue's own inputs
     // (which may depend on one another), so all of them are in flight together
@@ -228,7 +255,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int u = 0; u < U; ++u)
       a[u] = u < splits ? *reinterpret_cast<const float4*>(p + (size_t)u * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const auto ra = epi.row_aux(m);
+    const auto ra = have_stats ? ra_stats : epi.row_aux(m);
     const auto ax = epi.aux(m, col, ra);
     int sp = U;
     for (; sp + U <= splits; sp += U) {
@@ -253,25 +280,10 @@ __global__ void __launch_bounds__(256)
     r = epi(m, col, v, ra, ax);
   }
   if constexpr (Epi::kRowReduce) {
-    // each warp's share of row m is one partial; the CTA that completes the
-    // row sums them in a fixed order
+    // each warp's share of row m is one partial
     const RowSum& rs = epi.row_sums();
-    constexpr int kWarpsPerCta = 256 / 32;
-    const int nparts = gridDim.x * kWarpsPerCta;
     r = warp_sum(r);
-    if ((threadIdx.x & 31) == 0) rs.part[(size_t)m * rs.stride + blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5)] = r;
-    __threadfence();
-    __syncthreads();
-    __shared__ int last;
-    if (threadIdx.x == 0) last = atomicAdd(rs.cnt + m, 1) == (int)gridDim.x - 1;
-    __syncthreads();
-    if (last && threadIdx.x < 32) {
-      __threadfence();
-      float sum = 0.f;
-      for (int p = threadIdx.x; p < nparts; p += 32) sum += __ldcg(rs.part + (size_t)m * rs.stride + p);
-      sum = warp_sum(sum);
-      if (threadIdx.x == 0) rs.out[m] = sum;
-    }
+    if ((threadIdx.x & 31) == 0) rs.part[(size_t)m * rs.stride + blockIdx.x * kEpiWarps + (threadIdx.x >> 5)] = r;
   }
 }
 
@@ -299,8 +311,8 @@ cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi&
   e = launch_pdl(k_gemm_skinny<NT>, dim3(items < slots ? items : slots), dim3(192), C::SMEM, s, tw, tx, M, N, tiles,
                  kblocks, splits, part, device_error_word());
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_splitk_epilogue<Epi>, dim3((N / 4 + 255) / 256, M), dim3(256), 0, s, (const float*)part, splits,
-                    M, N, epi);
+  return launch_pdl(k_splitk_epilogue<Epi>, dim3((N / 4 + 255) / 256, M), dim3(32 * kEpiWarps), 0, s,
+                    (const float*)part, splits, M, N, epi);
 }
 
 template <class Epi>
@@ -347,7 +359,9 @@ cudaError_t gemm_skinny_qkv(const void* A, const void* B, int M, int N, int K, c
   return run(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, part, s);
 }
 cudaError_t gemm_skinny_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
-                           float* part, cudaStream_t s) {
+                           float* part, cudaStream_t s, int* row_parts) {
+  // one Σh² partial per row and epilogue warp (128 columns)
+  if (row_parts) *row_parts = (N / 4 + 255) / 256 * kEpiWarps;
   return run(A, B, M, N, K, EpiWo<bf16>{e, D.d}, part, s);
 }
 cudaError_t gemm_skinny_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,

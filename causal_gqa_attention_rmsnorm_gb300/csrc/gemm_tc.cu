@@ -56,6 +56,10 @@ template <int BN, int MT = 1> struct TcCfg {
 struct EpiF32 {
   static constexpr bool kRowReduce = false;
   static constexpr bool kRowLse = false;
+  static constexpr bool kRowSumIn = false;
+  static constexpr bool kRowStats = false;
+  static constexpr bool kRowDone = false;
+  static constexpr bool kTileStats = false;
   float* C;
   int N;
   struct RowAux {};
@@ -89,8 +93,12 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
   nt = local / gm;
 }
 
+// Threads per CTA: producer, MMA issuer, four epilogue warps, and for an
+// epilogue that can take RMSNorm-1 statistics (kTileStats) a statistics warp.
+template <class Epi> constexpr int tc_threads() { return Epi::kTileStats ? 224 : 192; }
+
 template <int BN, class Epi, int MT = 1>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
               uint32_t a_box_bytes, int group_m, Epi epi, int* err) {
   using C = TcCfg<BN, MT>;
@@ -210,47 +218,60 @@ __global__ void __launch_bounds__(192, 1)
       volatile int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, err);
     }
+  } else if (warp == 6) {
+    // Statistics warp (kTileStats with a.ts.x set): r = 1/sqrt(mean(x²) + eps)
+    // for rows g·kStatRows + blockIdx.x + k·gridDim.x of every group g in
+    // order, each group counted in done[g] once this CTA's rows are written.
+    if constexpr (Epi::kTileStats) {
+      const TileStats& ts = epi.a.ts;
+      if (ts.x) {
+        const int ngroups = (M + kStatRows - 1) / kStatRows;
+        for (int g = 0; g < ngroups; ++g) {
+          const int end = min(M, (g + 1) * kStatRows);
+          for (int row = g * kStatRows + (int)blockIdx.x; row < end; row += (int)gridDim.x) {
+            const float r = epi.tile_row_scale(row, lane);
+            if (lane == 0) {
+              ts.r[row] = r;
+              if (ts.lens_set && row % ts.T == 0) ts.lens_set[row / ts.T] = ts.T;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            atomicAdd(ts.done + g, 1);
+          }
+        }
+      }
+    }
   } else {
     // Epilogue: each warp reads its 32 TMEM lanes (32 rows) 32 columns at a
     // time, turns the chunk around in shared memory, and then lets lane l
     // handle columns [4·(l%8), +4) of rows (l/8) + 4·i, so every global access
     // of a warp instruction covers four contiguous row segments.
     const int quad = warp & 3;
+    int stats_ready = -1;          // groups ≤ this one have their row scales (kTileStats)
     float* stage = reinterpret_cast<float*>(smem + C::OFF_EPI) + (warp - 2) * 32 * C::EPI_STRIDE;
     const int sub_row = lane >> 3, sub_col = 4 * (lane & 7);
-    // Ordered row sums (RowSum): after a tile's partials are stored, the warp
-    // counts its arrival at the 32-row group, and the warp that completes the
-    // group adds the group's n_tiles partials in order.  The count is taken at
-    // the next tile, once its accumulator is ready, so that the fence before
-    // it finds this tile's stores long finished instead of waiting for them.
-    int pend_row0 = -1;
-    auto row_arrive = [&]() {
-      if constexpr (Epi::kRowReduce) {
-        if (pend_row0 < 0) return;
-        const RowSum& rs = epi.row_sums();
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(rs.cnt + pend_row0 / 32, 1) == n_tiles - 1;
-        if (__shfl_sync(0xffffffffu, last, 0)) {
-          __threadfence();
-          const int row = pend_row0 + lane;
-          if (row < M) {
-            rs.out[row] = ordered_sum(rs.part + (size_t)row * rs.stride, n_tiles);
-          }
-        }
-        pend_row0 = -1;
-      }
-    };
     int local = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
       const int acc = MT == 2 ? 0 : (local & 1);
       const uint32_t acc_phase = (MT == 2 ? local : (local >> 1)) & 1;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, err)) break;
       tc_fence_after();
-      row_arrive();
       int mu, nt;
       tile_coords(tile, m_units, n_tiles, group_m, mu, nt);
+      if constexpr (Epi::kTileStats) {
+        // the row scales of this tile's group, from every CTA's statistics warp
+        if (epi.a.ts.x) {
+          const int g = mu * MT * BM / kStatRows;
+          if (g > stats_ready) {
+            bool ok = true;
+            if (lane == 0) ok = wait_count(epi.a.ts.done + g, (int)gridDim.x, abort_flag, err);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            stats_ready = g;
+          }
+        }
+      }
       for (int r = 0; r < MT; ++r) {
         const int mt = mu * MT + r;
         const int row0 = mt * BM + quad * 32;
@@ -258,13 +279,24 @@ __global__ void __launch_bounds__(192, 1)
         float rsum[8];
         float lm[8], ls[8];        // running (max, Σ exp) of each row (kRowLse)
         typename Epi::RowAux ra[8];
+        // kRowSumIn: lane l forms the input row sum of row row0 + l, and each
+        // lane takes those of its rows from the lane that owns them
+        float rs_in = 0.f;
+        if constexpr (Epi::kRowSumIn) {
+          if (row0 + lane < M) rs_in = epi.row_sum_in(row0 + lane);
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           rsum[i] = 0.f;
           lm[i] = -INFINITY;
           ls[i] = 0.f;
           const int row = row0 + sub_row + 4 * i;
-          if (row < M) ra[i] = epi.row_aux(row);
+          if constexpr (Epi::kRowSumIn) {
+            const float ss = __shfl_sync(0xffffffffu, rs_in, sub_row + 4 * i);
+            if (row < M) ra[i] = epi.row_aux_with(ss);
+          } else {
+            if (row < M) ra[i] = epi.row_aux(row);
+          }
         }
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -328,8 +360,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         if constexpr (Epi::kRowReduce) {
-          // this tile's share of each of the warp's 32 rows is partial nt; its
-          // arrival is counted at the next tile (see row_arrive)
+          // this tile's share of each of the warp's 32 rows is partial nt
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float t = rsum[i];
@@ -339,11 +370,9 @@ __global__ void __launch_bounds__(192, 1)
             const int row = row0 + sub_row + 4 * i;
             if ((lane & 7) == 0 && row < M) epi.row_sums().part[(size_t)row * epi.row_sums().stride + nt] = t;
           }
-          pend_row0 = row0;
         }
       }
     }
-    row_arrive();
   }
 
   tc_fence_before();
@@ -371,8 +400,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int BN, class Epi, int MT = 1>
-cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& epi, cudaStream_t s) {
+cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& epi, cudaStream_t s,
+                int* n_tiles_out = nullptr) {
   using C = TcCfg<BN, MT>;
+  if (n_tiles_out) *n_tiles_out = (N + BN - 1) / BN;
   if (M <= 0 || N <= 0) return cudaSuccess;
   CUtensorMap ta, tbm;
   const uint32_t a_rows = M >= BM ? BM : (uint32_t)((M + 7) / 8 * 8);
@@ -391,25 +422,44 @@ cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& ep
   const int m_units = ((M + BM - 1) / BM + MT - 1) / MT;
   const int tiles = m_units * ((N + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  // Short K with a B panel beyond what L2 keeps: group up to 32 row blocks (32
+  // Short K with a B panel beyond what L2 keeps: group up to 48 row blocks (48
   // MB of A at K = 4096), m fastest inside a group, so each B tile is read
   // from HBM once per group rather than once per row block.  Otherwise n
-  // fastest.
+  // fastest.  (Measured on the W1/W3 GEMM of 32768 tokens: groups of 32, 48
+  // and 64 row blocks ran at 1775-1790, 1835 and 1622 TFLOP/s.)
   const size_t b_bytes = (size_t)N * K * 2;
-  const int gmax = 32 / MT;                        // CTA tiles along M per group
+  const int gmax = 48 / MT;                        // CTA tiles along M per group
   const int group_m =
       (K <= 8192 && b_bytes > (size_t(48) << 20) && m_units > 1) ? (m_units < gmax ? m_units : gmax) : 0;
-  k_gemm_tc<BN, Epi, MT><<<grid, 192, C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
-                                                    device_error_word());
+  if constexpr (Epi::kTileStats) {
+    if (epi.a.ts.x) {
+      // cooperative: every epilogue waits on the statistics warps of all CTAs
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(grid);
+      cfg.blockDim = dim3(tc_threads<Epi>());
+      cfg.dynamicSmemBytes = C::SMEM;
+      cfg.stream = s;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, Epi, MT>, ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
+                                device_error_word());
+    }
+  }
+  k_gemm_tc<BN, Epi, MT><<<grid, tc_threads<Epi>(), C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
+                                                                   device_error_word());
   return cudaGetLastError();
 }
 
 // Narrow N tiles when the grid would not fill the GPU.
 template <class Epi>
-cudaError_t run_auto(const void* A, const void* B, int M, int N, int K, const Epi& epi, cudaStream_t s) {
+cudaError_t run_auto(const void* A, const void* B, int M, int N, int K, const Epi& epi, cudaStream_t s,
+                     int* n_tiles_out = nullptr) {
   const long tiles256 = (long)((M + BM - 1) / BM) * ((N + 255) / 256);
-  if (tiles256 >= 2L * sm_count()) return run<256, Epi>(A, B, M, N, K, epi, s);
-  return run<128, Epi>(A, B, M, N, K, epi, s);
+  if (tiles256 >= 2L * sm_count()) return run<256, Epi>(A, B, M, N, K, epi, s, n_tiles_out);
+  return run<128, Epi>(A, B, M, N, K, epi, s, n_tiles_out);
 }
 
 }  // namespace
@@ -476,8 +526,9 @@ cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const
   return run_auto(A, B, M, N, K, EpiQKV<bf16, true>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
 }
 cudaError_t gemm_tc_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
-                       cudaStream_t s) {
-  return run_auto(A, B, M, N, K, EpiWo<bf16, true>{e, D.d}, s);
+                       cudaStream_t s, int* row_parts) {
+  // one Σh² partial per row and column tile
+  return run_auto(A, B, M, N, K, EpiWo<bf16, true>{e, D.d}, s, row_parts);
 }
 cudaError_t gemm_tc_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
                         cudaStream_t s) {

@@ -23,8 +23,9 @@ int sm_count();
 
 cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
                         cudaStream_t s);
+// row_parts: Σh² partials per row the launch writes (one per column tile)
 cudaError_t gemm_tc_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
-                       cudaStream_t s);
+                       cudaStream_t s, int* row_parts);
 cudaError_t gemm_tc_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
                         cudaStream_t s);
 cudaError_t gemm_tc_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,

@@ -132,8 +132,8 @@ tb_status tb_lm_head(const tb_head_cfg* cfg, const void* packed, const void* x, 
     const int rows = std::min(rc, M - r0);
     const void* xa = (const char*)x + (size_t)r0 * row_bytes;
     float* out = logits ? logits + (size_t)r0 * cfg->V : W.chunk;
-    cudaError_t e = launch_row_stats(cfg->dtype, xa, rows, cfg->d, cfg->eps, W.r, nullptr, 1, nullptr, nullptr,
-                                     nullptr, 0, nullptr, err, s);
+    cudaError_t e = launch_row_stats(cfg->dtype, xa, rows, cfg->d, cfg->eps, W.r, 1, nullptr, nullptr, nullptr, 0,
+                                     nullptr, err, s);
     // the loss alone, on the tile GEMM: folded into the GEMM's epilogue, no logits in memory
     if (e == cudaSuccess && !logits && cfg->dtype == TB_BF16 && rows > skinny_max_tokens()) {
       e = gemm_tc_lse(xa, packed, rows, cfg->V, cfg->d, LseArgs{W.r, targets + r0, W.lse, W.tgt, W.n_parts}, s);

@@ -77,6 +77,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Wait until the counter at p (in global memory, written by other CTAs of the
+// grid) reaches target, reading it with acquire semantics; same limit and
+// abort protocol as mbar_wait.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort, int* err) {
+  auto load = [p]() {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+  };
+  if (load() >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(128);
+    if (load() >= target) return true;
+    if ((it & 15u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicOr(err, TB_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // mbar_wait for roles where the whole warp proceeds together (warp-collective
 // tcgen05.ld/st and votes follow): every lane waits, and the warp continues only
 // if all lanes saw the phase complete, so a time-out never splits the warp.

@@ -127,12 +127,11 @@ Packed packed_views(const tb_block_cfg* c, const void* blob) {
 // Workspace carving.  Prefill keeps K/V in the workspace when no cache is given.
 struct Work {
   float* r;
-  float* ssq;                // [M] Σ h² of each row (the second norm)
-  float* ssq_part;           // [M, ssq_stride] its ordered partials
-  int* ssq_cnt;              // [M] arrival counters, zeroed by the row statistics
+  float* ssq_part;           // [M, ssq_stride] ordered partials of Σ h² (the second norm) of each row
   int ssq_stride;
   int32_t* pos;
   int* counter;
+  int* stat_done;            // [ceil(M / kStatRows)] group counts of the tile QKV GEMM's statistics warps
   void* q;
   void* k;
   void* v;
@@ -160,15 +159,14 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
   const size_t M = (size_t)B * (mode == 0 ? T : 1);
   const size_t hd = (size_t)c->H * c->dh, kvd = (size_t)c->Hkv * c->dh;
   w.r = (float*)take(M * 4);
-  w.ssq = (float*)take(M * 4);
   // partials per row: one per column tile (tile GEMM, ≥ 128 columns), per
-  // 1024-column CTA warp (few-token epilogue: 8 per 1024 columns) or per 64
-  // columns (fp32 GEMM)
+  // 128-column epilogue warp (few-token epilogue: 8 per 1024 columns) or per
+  // 64 columns (fp32 GEMM)
   w.ssq_stride = (c->d + 63) / 64 + 8;
   w.ssq_part = (float*)take(M * w.ssq_stride * 4);
-  w.ssq_cnt = (int*)take(M * 4);
   w.pos = (int32_t*)take((size_t)B * 4);
   w.counter = (int*)take(4);
+  w.stat_done = (int*)take((M + kStatRows - 1) / kStatRows * 4);
   w.q = take(M * hd * es);
   // prefill: K/V of the call when no contiguous cache of the block's type
   // takes them in place; decode: the new rows on their way into an int8 cache
@@ -200,8 +198,9 @@ cudaError_t mm_qkv(const Work& W, const void* A, const void* Bw, int M, int N, i
   return W.skpart ? gemm_skinny_qkv(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_qkv(A, Bw, M, N, K, D, e, s);
 }
 cudaError_t mm_wo(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D, const WoArgs& e,
-                  cudaStream_t s) {
-  return W.skpart ? gemm_skinny_wo(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_wo(A, Bw, M, N, K, D, e, s);
+                  cudaStream_t s, int* row_parts) {
+  return W.skpart ? gemm_skinny_wo(A, Bw, M, N, K, D, e, W.skpart, s, row_parts)
+                  : gemm_tc_wo(A, Bw, M, N, K, D, e, s, row_parts);
 }
 cudaError_t mm_w13(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D,
                    const W13Args& e, cudaStream_t s) {
@@ -381,12 +380,21 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
   const int kv_stride = contiguous_cache ? kv->T_max : T;
 
   StageRecorder rec(s);
-  rec.stage("rms");
-  TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, W.ssq_cnt, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
-                          nullptr, err, s));
-  const QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr, paged_of(kv, err)};
-  const WoArgs wa{x, W.h, W.hb, RowSum{W.ssq_part, W.ssq, W.ssq_cnt, W.ssq_stride}};
-  const W13Args ga{W.ssq, W.a};
+  // The tile GEMM path (bf16, more tokens than the few-token GEMM takes) forms
+  // RMSNorm-1's statistics inside the QKV GEMM; the other paths run the
+  // row-statistics kernel first.
+  const bool tile_stats = dt == TB_BF16 && !W.skpart;
+  QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr, paged_of(kv, err)};
+  if (tile_stats) {
+    TB_TRY(cudaMemsetAsync(W.stat_done, 0, (size_t)(M + kStatRows - 1) / kStatRows * sizeof(int), s));
+    qa.ts = TileStats{x, cfg->d, cfg->eps, W.r, W.stat_done, kv ? kv->lens : nullptr, T};
+  } else {
+    rec.stage("rms");
+    TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
+                            nullptr, err, s));
+  }
+  const WoArgs wa{x, W.h, W.hb, RowSum{W.ssq_part, W.ssq_stride, 0}};
+  W13Args ga{RowSum{W.ssq_part, W.ssq_stride, 0}, W.a};       // ssq.n: set by the Wo launch
   const W2Args ya{W.h, y, y_dtype};
   if (dt == TB_F32) {
     rec.stage("qkv");
@@ -394,7 +402,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
     rec.stage("attn");
     TB_TRY(attn_prefill_simt(dt, W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, cfg->window, s));
     rec.stage("wo");
-    TB_TRY(gemm_simt_wo(dt, W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    TB_TRY(gemm_simt_wo(dt, W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s, &ga.ssq.n));
     rec.stage("w13");
     TB_TRY(gemm_simt_w13(dt, W.hb, P.w13, M, 2 * cfg->f, cfg->d, D, ga, s));
     rec.stage("w2");
@@ -409,7 +417,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
     rec.stage("attn");
     TB_TRY(attn_prefill_tc(W.q, kbuf, vbuf, W.o, B, T, cfg->H, cfg->Hkv, cfg->dh, kv_stride, cfg->window, s));
     rec.stage("wo");
-    TB_TRY(mm_wo(W, W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    TB_TRY(mm_wo(W, W.o, P.wo, M, cfg->d, cfg->H * cfg->dh, D, wa, s, &ga.ssq.n));
     rec.stage("w13");
     TB_TRY(mm_w13(W, W.hb, P.w13, M, 2 * cfg->f, cfg->d, D, ga, s));
     rec.stage("w2");
@@ -454,17 +462,29 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
   const int nqkv = (cfg->H + 2 * cfg->Hkv) * cfg->dh;
 
   StageRecorder rec(s);
-  rec.stage("rms");
-  TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, W.ssq_cnt, 1, nullptr, kv->lens, W.pos, kv->T_max,
-                          W.counter, err, s));
+  // Few tokens on the bf16 path: RMSNorm-1's statistics, the positions and
+  // the step's counters are formed in the QKV GEMM's partial-sum epilogue,
+  // and the cache lengths advance in the Wo one; otherwise the row-statistics
+  // kernel does all of it first.
+  const bool fused_stats = dt == TB_BF16 && W.skpart;
+  if (!fused_stats) {
+    rec.stage("rms");
+    TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, 1, nullptr, kv->lens, W.pos, kv->T_max, W.counter,
+                            err, s));
+  }
   const PagedKV pg = paged_of(kv, err);
   // an int8 cache gets the new rows through the workspace and the quantiser
   const bool i8 = kv->dtype == TB_I8;
   void* knew = pg.bt ? nullptr : (i8 ? W.k : kv->k);
   void* vnew = pg.bt ? nullptr : (i8 ? W.v : kv->v);
-  const QKVArgs qa{W.r, P.rope, W.q, knew, vnew, 1, i8 ? 1 : kv->T_max, W.pos, pg, i8};
-  const WoArgs wa{x, W.h, W.hb, RowSum{W.ssq_part, W.ssq, W.ssq_cnt, W.ssq_stride}};
-  const W13Args ga{W.ssq, W.a};
+  QKVArgs qa{W.r, P.rope, W.q, knew, vnew, 1, i8 ? 1 : kv->T_max, W.pos, pg, i8};
+  WoArgs wa{x, W.h, W.hb, RowSum{W.ssq_part, W.ssq_stride, 0}};
+  if (fused_stats) {
+    qa.st = QKVStats{x, cfg->d, cfg->eps, kv->lens, W.pos, kv->T_max, W.counter, err};
+    wa.pos = W.pos;
+    wa.lens = kv->lens;
+  }
+  W13Args ga{RowSum{W.ssq_part, W.ssq_stride, 0}, W.a};       // ssq.n: set by the Wo launch
   const W2Args ya{W.h, y, y_dtype};
   if (dt == TB_F32) {
     rec.stage("qkv");
@@ -473,7 +493,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
     TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
                        W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s));
     rec.stage("wo");
-    TB_TRY(gemm_simt_wo(dt, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    TB_TRY(gemm_simt_wo(dt, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s, &ga.ssq.n));
     rec.stage("w13");
     TB_TRY(gemm_simt_w13(dt, W.hb, P.w13, B, 2 * cfg->f, cfg->d, D, ga, s));
     rec.stage("w2");
@@ -493,7 +513,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
                          W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s));
     }
     rec.stage("wo");
-    TB_TRY(mm_wo(W, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s));
+    TB_TRY(mm_wo(W, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s, &ga.ssq.n));
     rec.stage("w13");
     TB_TRY(mm_w13(W, W.hb, P.w13, B, 2 * cfg->f, cfg->d, D, ga, s));
     rec.stage("w2");

@@ -148,10 +148,11 @@ def _attend_chunks(q, k, v, dh, chunk):
 
 
 def _block_rows(inp, s: workloads.BlockShape, x: torch.Tensor, pos: torch.Tensor, kv_rows, order: str,
-                plant: Optional[str], decode: bool = False):
+                plant: Optional[str], decode: bool = False, with_kv: bool = False):
     """The block for tokens x [n, d] at positions pos.  kv_rows(k_new, v_new)
     returns the keys and values [S, Hkv, dh] they attend over and each query's
-    key-position limit; returns y [n, d] (fp32)."""
+    key-position limit; returns y [n, d] (fp32), and with with_kv also the
+    new rows' k and v [n, Hkv, dh] as stored (bf16 values)."""
     if plant is not None and plant not in PLANTS:
         raise ValueError(plant)
     w = {nm: inp[nm].float() for nm in workloads.WEIGHT_NAMES}
@@ -190,7 +191,8 @@ def _block_rows(inp, s: workloads.BlockShape, x: torch.Tensor, pos: torch.Tensor
     u = r2 * _mm(hb, _bf(w["g_mlp"][:, None] * w["w3"]), order)
     a = _bf(g / (1.0 + torch.exp(-g)) * u)
     drop = s.f // 64 // 2 if plant == "w2_block_dropped" else None
-    return hh + _mm(a, w["w2"], order, drop_block=drop)
+    y = hh + _mm(a, w["w2"], order, drop_block=drop)
+    return (y, k_new, v_new) if with_kv else y
 
 
 def emulate_prefill_seq(inp, s: workloads.BlockShape, b: int = 0, order: str = "a",
@@ -218,6 +220,51 @@ def emulate_decode_seq(inp, s: workloads.BlockShape, b: int, k_cache: torch.Tens
         return torch.cat([kc, kn]), torch.cat([vc, vn]), torch.tensor([P])
 
     return _block_rows(inp, s, x, torch.tensor([P]), kv_rows, order, plant, decode=True)[0]
+
+
+def emulate_stack_prefill_seq(ids, table: torch.Tensor, layers, s: workloads.BlockShape, g_final: torch.Tensor,
+                              order: str = "a"):
+    """One sequence through an L-layer stack with the bf16 path's rounding
+    points, and the tied LM head: each block's input stored in bf16, the
+    head's input (the last block's output) in bf16, the final norm's gain
+    folded into the bf16 head weights, the logits (x·W_U')·r in fp32.
+    ids [T]; table [V, d] (the embedding, also W_Uᵀ); layers: per-layer dicts
+    of weights.  Returns dict(logits [T, V], k, v: per layer [Hkv, T, dh])."""
+    x = table[torch.as_tensor(ids, dtype=torch.long)].float()
+    pos = torch.arange(x.shape[0])
+    ks, vs = [], []
+    for lw in layers:
+        x = _bf(x)
+        y, k, v = _block_rows(lw, s, x, pos, lambda kn, vn: (kn, vn, pos), order, None, with_kv=True)
+        ks.append(k.permute(1, 0, 2))
+        vs.append(v.permute(1, 0, 2))
+        x = y
+    h = _bf(x)
+    r = 1.0 / torch.sqrt((h * h).mean(-1, keepdim=True) + s.eps)
+    wu = _bf(table.float() * g_final.float()[None, :])          # [V, d]
+    return {"logits": r * _mm(h, wu.T.contiguous(), order), "k": ks, "v": vs}
+
+
+def emulate_stack_decode_seq(token: int, table: torch.Tensor, layers, s: workloads.BlockShape,
+                             g_final: torch.Tensor, k_caches, v_caches, order: str = "a"):
+    """One decode step of one sequence through the stack (the token at
+    position pos = k_caches[l].shape[1]), each layer over its cached rows
+    [Hkv, pos, dh]; the head as in emulate_stack_prefill_seq.  Returns
+    dict(logits [V], k: per layer the appended row [Hkv, dh])."""
+    x = table[token].float()[None, :]
+    P = k_caches[0].shape[1]
+    ks = []
+    for lw, kc, vc in zip(layers, k_caches, v_caches):
+        x = _bf(x)
+        kcp, vcp = kc.float().permute(1, 0, 2), vc.float().permute(1, 0, 2)
+        x, k, _ = _block_rows(lw, s, x, torch.tensor([P]),
+                              lambda kn, vn: (torch.cat([kcp, kn]), torch.cat([vcp, vn]), torch.tensor([P])), order,
+                              None, decode=True, with_kv=True)
+        ks.append(k[0])
+    h = _bf(x)
+    r = 1.0 / torch.sqrt((h * h).mean(-1, keepdim=True) + s.eps)
+    wu = _bf(table.float() * g_final.float()[None, :])
+    return {"logits": (r * _mm(h, wu.T.contiguous(), order))[0], "k": ks}
 
 
 def _err(got, ref):

@@ -48,7 +48,8 @@ def test_roofline_entry_for_a_bandwidth_stage():
 
 
 def test_decode_launch_counts():
-    # row statistics, the decode attention and its merge, and four GEMMs, each
-    # followed by its partial-sum epilogue when the batch takes the few-token GEMM
-    assert bench.decode_launches(32) == 3 + 4 * 2
+    # the decode attention and its merge, and four GEMMs each followed by its
+    # partial-sum epilogue (the QKV one forms the row statistics) when the batch
+    # takes the few-token GEMM; above that, row statistics and four tile GEMMs
+    assert bench.decode_launches(32) == 2 + 4 * 2
     assert bench.decode_launches(bench.FEW_TOKENS + 1) == 3 + 4

@@ -9,6 +9,7 @@ import torch
 import oracle
 import workloads
 from helpers import block_config, errors, oracle_cfg, oracle_weights, to_device
+from rounding_model import ERROR_FACTOR, emulate_stack_decode_seq, emulate_stack_prefill_seq
 
 pytestmark = pytest.mark.gpu
 
@@ -135,7 +136,24 @@ def _stack_model(s, L, V, seed=5):
     return cfg, packed, layers, table, gain, hcfg, head, ids
 
 
+def _within_model(got, model, ref, what):
+    """The GPU's error against the oracle is at most 1.25x the error of the
+    bf16 rounding model (tests/rounding_model.py) on the same outputs, in the
+    normwise and relative-L2 measures: the stack adds no error of its own to
+    the rounding its path is built with (the block's d = 4096 tests hold the
+    same ratio)."""
+    e, em = errors(got, ref), errors(model, ref)
+    assert e["finite"], what
+    for k in ("normwise", "rel_l2"):
+        assert e[k] <= ERROR_FACTOR * em[k], (what, k, e[k], em[k])
+
+
 def test_stack_prefill_and_decode_against_the_oracle():
+    """Three blocks with the residual stream stored in bf16 between them, and
+    the tied LM head on the last block's bf16 output.  The oracle takes the
+    same bf16 rounding of each block's input; the bound is 1.25x the rounding
+    model's own error on the same outputs (about 6e-4 normwise and 2e-3
+    relative L2 for the logits, 3e-3 normwise for the caches at this shape)."""
     import causal_gqa_attention_rmsnorm_gb300 as tb
     s, L, V = STACK, 3, 520
     cfg, packed, layers, table, gain, hcfg, head, ids = _stack_model(s, L, V)
@@ -154,10 +172,16 @@ def test_stack_prefill_and_decode_against_the_oracle():
     logits = logits.reshape(s.B, s.T - 1, V)
     for b in range(s.B):
         ref = oracle.stack_prefill_seq(ids[b].tolist(), tab64, ow, ocfg, g64, tab64.T, round_between=_bf16_round)
-        _close_normwise(logits[b].cpu().double().numpy(), ref["logits"][:s.T - 1], 2e-2, f"prefill logits b={b}")
-        _close_normwise(logits1[b].cpu().double().numpy(), ref["logits"][s.T - 1], 2e-2, f"decode logits b={b}")
+        pre = ids[b, :s.T - 1].tolist()
+        model = emulate_stack_prefill_seq(pre, table, layers, s, gain)
+        model1 = emulate_stack_decode_seq(int(ids[b, s.T - 1]), table, layers, s, gain, model["k"], model["v"])
+        _within_model(logits[b].cpu().double().numpy(), model["logits"].double().numpy(), ref["logits"][:s.T - 1],
+                      f"prefill logits b={b}")
+        _within_model(logits1[b].cpu().double().numpy(), model1["logits"].double().numpy(), ref["logits"][s.T - 1],
+                      f"decode logits b={b}")
         for l in range(L):
-            _close_normwise(kvs[l].k[b, :, :s.T].cpu().double().numpy(), ref["k"][l], 2e-2, f"k cache l={l} b={b}")
+            mk = torch.cat([model["k"][l], model1["k"][l][:, None]], 1).double().numpy()
+            _within_model(kvs[l].k[b, :, :s.T].cpu().double().numpy(), mk, ref["k"][l], f"k cache l={l} b={b}")
 
 
 def test_stack_of_one_is_the_block():
