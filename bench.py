@@ -347,7 +347,10 @@ def bench_prefill(args, s, world, peaks):
 # captured at B = 1 (543.6 MB read + 222.6 MB write) and every term (A once,
 # the weight panel once per 32-row-block group, the output once) grows with the
 # row count, so a B = 4 launch moves 4x that.
-NCU_TRAFFIC = {("gqa_8k", "w13"): 4 * (540.8e6 + 221.8e6)}
+# DRAM read + write of one launch of the stage's kernel, from a one-pass ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the benchmark's own
+# launch (profiles/gemm_w13_gqa_8k.md).
+NCU_TRAFFIC = {("gqa_8k", "w13"): 2.88e9 + 926.99e6}
 
 
 def roofline_entry(stages, work, peaks, peak_src, workload):
