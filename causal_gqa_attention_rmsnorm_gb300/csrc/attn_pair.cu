@@ -313,28 +313,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           for (int cc = 0; cc < kBN; ++cc)
             if (cc < wlim) s[cc] = -INFINITY;
         }
-        float m4[4];
+        // P = 2^(s·scale − m) in pairs, written as bf16 over the first 64 S
+        // columns; returns Σ P (fp32, before the rounding).  With take_max the
+        // tile's raw row maximum is formed in the same pass (four chains of
+        // three-input maxima) into mx.
+        auto p_pass = [&](float msub, bool take_max, float& mx) -> float {
+          const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-msub, -msub);
+          float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float m = fmaxf(s[2 * i], s[2 * i + 1]);
+          for (int cc = 0; cc < kBN; cc += 16) {
+            uint32_t u[8];
+            if (take_max) {
 #pragma unroll
-          for (int cc = 8 + 2 * i; cc < kBN; cc += 8) m = fmax3(m, s[cc], s[cc + 1]);
-          m4[i] = m;
-        }
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        const float m_new = fmaxf(m_used, mx * scale_log2);
-        bool need = false;
-        if (j == it.lo) {
-          m_used = m_new;
-        } else {
-          need = m_new > m_used + kRescaleLog2;
-        }
-        if (__any_sync(0xffffffffu, need)) {
-          // the previous P·V of this slot must be finished before O is rewritten
-          if (!mbar_wait_warp(&pv_done[g], (c - 1) & 1, abort_flag, err)) {
-            ok = false;
-            break;
+              for (int i = 0; i < 4; ++i)
+                m4[i] = fmax3(fmax3(m4[i], s[cc + 2 * i], s[cc + 2 * i + 1]), s[cc + 8 + 2 * i], s[cc + 9 + 2 * i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float2 arg = __ffma2_rn(make_float2(s[cc + 2 * i], s[cc + 2 * i + 1]), sc2, nm2);
+              const float2 p = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+              sum2[i & 1] = __fadd2_rn(sum2[i & 1], p);
+              __nv_bfloat162 t = __floats2bfloat162_rn(p.x, p.y);
+              u[i] = *reinterpret_cast<uint32_t*>(&t);
+            }
+            tmem_st8(s_col + cc / 2, u);
           }
+          if (take_max) mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          const float2 s01 = __fadd2_rn(sum2[0], sum2[1]);
+          return s01.x + s01.y;
+        };
+        // O ← O · 2^(m_used − m_new) on the lanes that need it, once the
+        // previous P·V of this slot has finished with O.
+        auto rescale_o = [&](bool need, float m_new) -> bool {
+          if (!mbar_wait_warp(&pv_done[g], (c - 1) & 1, abort_flag, err)) return false;
           tc_fence_after();
           const float factor = need ? ex2_approx(m_used - m_new) : 1.f;
 #pragma unroll 1
@@ -351,25 +363,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             l *= factor;
             m_used = m_new;
           }
-        }
-        const float msub = m_used == -INFINITY ? 0.f : m_used;
-        const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-msub, -msub);
-        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int cc = 0; cc < kBN; cc += 16) {
-          uint32_t u[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float2 arg = __ffma2_rn(make_float2(s[cc + 2 * i], s[cc + 2 * i + 1]), sc2, nm2);
-            const float2 p = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
-            sum2[i & 1] = __fadd2_rn(sum2[i & 1], p);
-            __nv_bfloat162 t = __floats2bfloat162_rn(p.x, p.y);
-            u[i] = *reinterpret_cast<uint32_t*>(&t);
+          return true;
+        };
+        // A row's first tile takes its maximum first.  After that P is formed
+        // against the maximum in use, with the tile's maximum alongside, so the
+        // maximum is off the path from S to P; only a tile that raises a row's
+        // maximum by more than 2^kRescaleLog2 (rare once the row has seen keys)
+        // makes the warp rescale O and form P again from the scores it holds.
+        float mx = -INFINITY;
+        if (j != it.lo && !__any_sync(0xffffffffu, m_used == -INFINITY)) {
+          const float sum = p_pass(m_used, true, mx);
+          const float m_new = fmaxf(m_used, mx * scale_log2);
+          const bool need = m_new > m_used + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            tmem_wait_st();
+            if (!rescale_o(need, m_new)) {
+              ok = false;
+              break;
+            }
+            l += p_pass(m_used, false, mx);
+          } else {
+            l += sum;
           }
-          tmem_st8(s_col + cc / 2, u);
+        } else {
+          float m4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float m = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+            for (int cc = 8 + 2 * i; cc < kBN; cc += 8) m = fmax3(m, s[cc], s[cc + 1]);
+            m4[i] = m;
+          }
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          const float m_new = fmaxf(m_used, mx * scale_log2);
+          bool need = false;
+          if (j == it.lo) {
+            m_used = m_new;
+          } else {
+            need = m_new > m_used + kRescaleLog2;
+          }
+          if (__any_sync(0xffffffffu, need) && !rescale_o(need, m_new)) {
+            ok = false;
+            break;
+          }
+          l += p_pass(m_used == -INFINITY ? 0.f : m_used, false, mx);
         }
-        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]);
-        l += s01.x + s01.y;
         tmem_wait_st();
         tc_fence_before();      // P (and any O rescale) before the next MMA
         __syncwarp();
