@@ -44,6 +44,7 @@ using namespace ptx;
 constexpr int kBM = 128, kBN = 128, kDH = 128;
 constexpr int NS = 4;                                      // K/V ring stages
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleBound = 256.0f;                    // 2^kRescaleLog2
 constexpr uint32_t Q_BYTES = kBM * kDH * 2;                // one slot's Q rows in this CTA
 constexpr uint32_t KH_BYTES = (kBN / 2) * kDH * 2;         // 64 keys x 128 dims
 constexpr uint32_t VH_BYTES = kBN * (kDH / 2) * 2;         // 128 keys x 64 dims
@@ -314,21 +315,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             if (cc < wlim) s[cc] = -INFINITY;
         }
         // P = 2^(s·scale − m) in pairs, written as bf16 over the first 64 S
-        // columns; returns Σ P (fp32, before the rounding).  With take_max the
-        // tile's raw row maximum is formed in the same pass (four chains of
-        // three-input maxima) into mx.
-        auto p_pass = [&](float msub, bool take_max, float& mx) -> float {
+        // columns; returns Σ P (fp32, before the rounding).
+        auto p_pass = [&](float msub) -> float {
           const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-msub, -msub);
           float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int cc = 0; cc < kBN; cc += 16) {
             uint32_t u[8];
-            if (take_max) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                m4[i] = fmax3(fmax3(m4[i], s[cc + 2 * i], s[cc + 2 * i + 1]), s[cc + 8 + 2 * i], s[cc + 9 + 2 * i]);
-            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float2 arg = __ffma2_rn(make_float2(s[cc + 2 * i], s[cc + 2 * i + 1]), sc2, nm2);
@@ -339,9 +332,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             }
             tmem_st8(s_col + cc / 2, u);
           }
-          if (take_max) mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           const float2 s01 = __fadd2_rn(sum2[0], sum2[1]);
           return s01.x + s01.y;
+        };
+        // The tile's raw row maximum: four chains of three-input maxima.
+        auto row_max = [&]() -> float {
+          float m4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float m = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+            for (int cc = 8 + 2 * i; cc < kBN; cc += 8) m = fmax3(m, s[cc], s[cc + 1]);
+            m4[i] = m;
+          }
+          return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         };
         // O ← O · 2^(m_used − m_new) on the lanes that need it, once the
         // previous P·V of this slot has finished with O.
@@ -366,14 +370,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
           return true;
         };
         // A row's first tile takes its maximum first.  After that P is formed
-        // against the maximum in use, with the tile's maximum alongside, so the
-        // maximum is off the path from S to P; only a tile that raises a row's
-        // maximum by more than 2^kRescaleLog2 (rare once the row has seen keys)
-        // makes the warp rescale O and form P again from the scores it holds.
-        float mx = -INFINITY;
+        // against the maximum in use, so the maximum is off the path from S
+        // to P.  Every weight is at most Σ P, so Σ P ≤ 2^kRescaleLog2 proves
+        // that no weight exceeds 2^kRescaleLog2, i.e. that the tile does not
+        // raise the row's maximum by more than that, and P stands; otherwise
+        // the tile's exact maximum decides, and a row it raises by more makes
+        // the warp rescale O and form P again from the scores it holds.
         if (j != it.lo && !__any_sync(0xffffffffu, m_used == -INFINITY)) {
-          const float sum = p_pass(m_used, true, mx);
-          const float m_new = fmaxf(m_used, mx * scale_log2);
+          const float sum = p_pass(m_used);
+          float m_new = m_used;
+          if (!(sum <= kRescaleBound)) m_new = fmaxf(m_used, row_max() * scale_log2);
           const bool need = m_new > m_used + kRescaleLog2;
           if (__any_sync(0xffffffffu, need)) {
             tmem_wait_st();
@@ -381,21 +387,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
               ok = false;
               break;
             }
-            l += p_pass(m_used, false, mx);
+            l += p_pass(m_used);
           } else {
             l += sum;
           }
         } else {
-          float m4[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float m = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-            for (int cc = 8 + 2 * i; cc < kBN; cc += 8) m = fmax3(m, s[cc], s[cc + 1]);
-            m4[i] = m;
-          }
-          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          const float m_new = fmaxf(m_used, mx * scale_log2);
+          const float m_new = fmaxf(m_used, row_max() * scale_log2);
           bool need = false;
           if (j == it.lo) {
             m_used = m_new;
@@ -406,7 +403,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
             ok = false;
             break;
           }
-          l += p_pass(m_used == -INFINITY ? 0.f : m_used, false, mx);
+          l += p_pass(m_used == -INFINITY ? 0.f : m_used);
         }
         tmem_wait_st();
         tc_fence_before();      // P (and any O rescale) before the next MMA
