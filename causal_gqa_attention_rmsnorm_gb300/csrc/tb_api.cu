@@ -409,7 +409,17 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
     TB_TRY(gemm_simt_w2(dt, W.a, P.w2, M, cfg->d, cfg->f, D, ya, s));
   } else {
     rec.stage("qkv");
-    TB_TRY(mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
+    cudaError_t e = mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s);
+    if (e == cudaErrorCooperativeLaunchTooLarge && tile_stats) {
+      // fewer SMs than the cooperative grid needs (e.g. a limited share of
+      // the GPU): the row-statistics kernel first, then the plain launch
+      (void)cudaGetLastError();
+      qa.ts = TileStats();
+      TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
+                              nullptr, err, s));
+      e = mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s);
+    }
+    TB_TRY(e);
     if (i8_cache) {
       rec.stage("quant");
       TB_TRY(launch_quantize_kv(*kv, W.k, W.v, T, nullptr, s));

@@ -41,6 +41,14 @@ SMALL = {
     # bf16, GQA 8/1 (largest group), one token per sequence
     "bf16_t1": workloads.BlockShape("bf16_t1", "prefill", "bf16", B=3, T=1, d=1024, H=8, Hkv=1, dh=128,
                                     f=1536, rope_base=1e4, eps=1e-6, gains="normal"),
+    # bf16, 67 tokens in all: the smallest tile-GEMM prefill; the QKV GEMM's
+    # statistics warps cover one partial row group, most CTAs own no row
+    "bf16_tile_min": workloads.BlockShape("bf16_tile_min", "prefill", "bf16", B=1, T=67, d=512, H=8, Hkv=2,
+                                          dh=64, f=1024, rope_base=1e4, eps=1e-6, gains="normal"),
+    # bf16, 2 × 1100 tokens: row groups of 2048 rows, the second one partial,
+    # sequence boundaries inside a group
+    "bf16_two_groups": workloads.BlockShape("bf16_two_groups", "prefill", "bf16", B=2, T=1100, d=256, H=4,
+                                            Hkv=1, dh=64, f=512, rope_base=1e4, eps=1e-6, gains="normal"),
 }
 
 
