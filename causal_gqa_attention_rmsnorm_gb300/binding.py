@@ -353,7 +353,7 @@ def tb_get_device_error(stream=None, clear: bool = False) -> int:
 
 def tbx_gemm_bf16(A: torch.Tensor, B: torch.Tensor, bn: int = 256, mt: int = 1, stream=None) -> torch.Tensor:
     """Test hook: A [M, K] · B [N, K]ᵀ in fp32 through the tcgen05 main loop
-    (mt = 2: two 128-row A blocks per 256-column weight tile)."""
+    (mt = 2: 256-row tiles on CTA pairs, M = 256 MMAs)."""
     _need(A, "A", torch.bfloat16)
     _need(B, "B", torch.bfloat16)
     M, K = A.shape

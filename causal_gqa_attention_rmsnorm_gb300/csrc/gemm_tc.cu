@@ -16,9 +16,10 @@
 //               see epilogues.cuh).
 // Tiles are visited n-fastest so that the CTAs running together share the A
 // row block and the weight panel stays resident in L2, or, when the weight
-// panel is larger than L2 and K short, in groups of row blocks (see run).  A
-// long-K GEMM may take two row blocks per CTA tile against one weight tile
-// (MT = 2, see TcCfg).
+// panel is larger than L2 and K short, in groups of row blocks (see run).
+// The Wo, W1/W3 and W2 GEMMs of a prefill with enough 256-row tiles run on
+// CTA pairs (PAIR, see TcCfg): M = 256 MMAs issued by the even CTA of a
+// cluster, each CTA staging its own A block and half of the weight tile.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -34,15 +35,19 @@ using namespace ptx;
 
 constexpr int BM = 128, BK = 64;
 
-// MT row blocks per CTA tile: 1, or 2 for a long-K GEMM, where the pair of
-// 128-row A blocks shares each staged B tile (a third less operand traffic
-// per FLOP; the two accumulators then fill TMEM, so the epilogue no longer
-// overlaps the next tile's MMAs, a small cost when K is long).
-template <int BN, int MT = 1> struct TcCfg {
-  static constexpr int STAGES = MT == 2 ? 3 : (BN == 256 ? 4 : 6);
-  static constexpr uint32_t A_BLOCK = BM * BK * 2;
-  static constexpr uint32_t A_BYTES = MT * A_BLOCK;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+// Shared-memory plan of a CTA tile of 128 rows × BN columns.
+//
+// PAIR: a cluster of two CTAs computes a 256 × BN tile with M = 256 MMAs
+// (tcgen05 cta_group::2) that the even CTA issues: each CTA stages its own
+// 128-row A block and half of the weight tile (BN/2 rows), the tensor cores
+// read B from both CTAs' shared memory, and each CTA's tensor memory holds
+// its 128 rows of the accumulator.  Per CTA a k-block stages 32 KB instead
+// of 48 KB for the same MMA work, and each weight tile is fetched once per
+// pair of row blocks.
+template <int BN, bool PAIR = false> struct TcCfg {
+  static constexpr int STAGES = PAIR ? 6 : (BN == 256 ? 4 : 6);
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;     // this CTA's share of the weight tile
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
@@ -97,13 +102,14 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 // epilogue that can take RMSNorm-1 statistics (kTileStats) a statistics warp.
 template <class Epi> constexpr int tc_threads() { return Epi::kTileStats ? 224 : 192; }
 
-template <int BN, class Epi, int MT = 1>
+template <int BN, class Epi, bool PAIR = false>
 __global__ void __launch_bounds__(224, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
               uint32_t a_box_bytes, int group_m, Epi epi, int* err) {
-  using C = TcCfg<BN, MT>;
-  static_assert(MT == 1 || (MT == 2 && BN * MT <= 512 && !Epi::kRowReduce && !Epi::kRowLse),
-                "row pairs: TMEM holds both accumulators; no row reductions");
+  using C = TcCfg<BN, PAIR>;
+  // The statistics warp's rows are read by every CTA's epilogue, which needs a
+  // cooperative launch; the CTA pairs' cluster launch does not take one.
+  static_assert(!PAIR || !Epi::kTileStats, "CTA pairs: no statistics warp");
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -117,9 +123,14 @@ __global__ void __launch_bounds__(224, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
-  const int m_units = (m_tiles + MT - 1) / MT;     // CTA tiles along M
+  constexpr int MU = PAIR ? 2 : 1;                  // row blocks per (pair or CTA) tile
+  const int m_units = (m_tiles + MU - 1) / MU;     // tiles along M
   const int tiles = m_units * n_tiles;
   const int kblocks = K / BK;
+  // PAIR: the cluster walks the tiles; rank 0 issues the MMAs
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int tile0 = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int tstep = PAIR ? (int)nclusters_x() : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -128,7 +139,7 @@ __global__ void __launch_bounds__(224, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], PAIR ? 8 : 4);     // PAIR: the epilogue warps of both CTAs, on rank 0's
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -136,9 +147,19 @@ __global__ void __launch_bounds__(224, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
+  if constexpr (PAIR) {
+    // both CTAs' barriers exist before either CTA's copies or commits reach them
+    __syncthreads();
+    cluster_sync();
+  }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -153,7 +174,7 @@ __global__ void __launch_bounds__(224, 1)
       uint32_t last_phase[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = 0, last_phase[s] = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < tiles; tile += tstep) {
         int mu, nt;
         tile_coords(tile, m_units, n_tiles, group_m, mu, nt);
         for (int kb = 0; kb < kblocks; ++kb) {
@@ -162,38 +183,46 @@ __global__ void __launch_bounds__(224, 1)
             break;
           }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
-          // the A box is shorter than the tile when M < 128; rows past it are never stored
-          mbar_arrive_expect_tx(&full[stage], MT * a_box_bytes + C::B_BYTES);
-#pragma unroll
-          for (int r = 0; r < MT; ++r)     // a block past M reads zeros
-            tma_load_2d(&tmA, sa + r * C::A_BLOCK, &full[stage], kb * BK, (mu * MT + r) * BM);
-          tma_load_2d(&tmB, sa + C::A_BYTES, &full[stage], kb * BK, nt * BN);
+          if constexpr (PAIR) {
+            // both CTAs' copies complete on rank 0's barrier, which counts them all
+            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (a_box_bytes + C::B_BYTES));
+            tma_load_2d_pair(&tmA, sa, fb, kb * BK, (mu * 2 + (int)rank) * BM);     // a block past M reads zeros
+            tma_load_2d_pair(&tmB, sa + C::A_BYTES, fb, kb * BK, nt * BN + (int)rank * (BN / 2));
+          } else {
+            // the A box is shorter than the tile when M < 128; rows past it are never stored
+            mbar_arrive_expect_tx(&full[stage], a_box_bytes + C::B_BYTES);
+            tma_load_2d(&tmA, sa, &full[stage], kb * BK, mu * BM);
+            tma_load_2d(&tmB, sa + C::A_BYTES, &full[stage], kb * BK, nt * BN);
+          }
           issued[stage] = 1;
           last_phase[stage] = phase;
           if (++stage == STAGES) stage = 0, phase ^= 1u;
         }
       }
-      // every copy issued must have landed before the CTA may exit
+      // every copy issued must have landed before the CTA may exit (PAIR:
+      // rank 0's barriers count both CTAs' copies, and the peer waits for
+      // rank 0 at the cluster barrier before it exits)
       for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) {
+        if (issued[s] && rank == 0) {
           volatile int no_abort = 0;
           mbar_wait(&full[s], last_phase[s], &no_abort, err);
         }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16(PAIR ? 2 * BM : BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++local) {
-        // MT == 1: two accumulators in turn; MT == 2: one pair of accumulators
-        const int acc = MT == 2 ? 0 : (local & 1);
-        const uint32_t acc_phase = (MT == 2 ? local : (local >> 1)) & 1;
+      for (int tile = tile0; ok && tile < tiles; tile += tstep, ++local) {
+        // two accumulators in turn
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;   // row block r of the tile at + r·BN
+        const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
             ok = false;
@@ -202,19 +231,29 @@ __global__ void __launch_bounds__(224, 1)
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t b0 = a0 + C::A_BYTES;
+          if constexpr (PAIR) {
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
+            for (int k = 0; k < BK / 16; ++k)
+              mma2_bf16_ss(d_tmem, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), idesc,
+                           (kb | k) != 0);
+            mma_commit_pair(&empty[stage]);     // frees the stage in both CTAs
+          } else {
 #pragma unroll
-            for (int r = 0; r < MT; ++r)
-              mma_bf16_ss(d_tmem + r * BN, desc_kmajor_sw128(a0 + r * C::A_BLOCK + k * 32),
-                          desc_kmajor_sw128(b0 + k * 32), idesc, (kb | k) != 0);
-          mma_commit(&empty[stage]);
+            for (int k = 0; k < BK / 16; ++k)
+              mma_bf16_ss(d_tmem, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), idesc,
+                          (kb | k) != 0);
+            mma_commit(&empty[stage]);
+          }
           if (++stage == STAGES) stage = 0, phase ^= 1u;
         }
-        if (ok) mma_commit(&tfull[acc]);
+        if (ok) {
+          if constexpr (PAIR) mma_commit_pair(&tfull[acc]);
+          else mma_commit(&tfull[acc]);
+        }
       }
       // all MMAs must be done before TMEM is released
-      mma_commit(drain);
+      if constexpr (PAIR) mma_commit_pair(drain);     // arrives on both CTAs' drain; rank 0 waits
+      else mma_commit(drain);
       volatile int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, err);
     }
@@ -253,9 +292,12 @@ __global__ void __launch_bounds__(224, 1)
     float* stage = reinterpret_cast<float*>(smem + C::OFF_EPI) + (warp - 2) * 32 * C::EPI_STRIDE;
     const int sub_row = lane >> 3, sub_col = 4 * (lane & 7);
     int local = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
-      const int acc = MT == 2 ? 0 : (local & 1);
-      const uint32_t acc_phase = (MT == 2 ? local : (local >> 1)) & 1;
+    // PAIR: this CTA's epilogue frees an accumulator on rank 0's barrier
+    const uint32_t tempty_cl[2] = {PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : 0u,
+                                   PAIR ? mapa_shared(smem_u32(&tempty[1]), 0) : 0u};
+    for (int tile = tile0; tile < tiles; tile += tstep, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag, err)) break;
       tc_fence_after();
       int mu, nt;
@@ -263,7 +305,7 @@ __global__ void __launch_bounds__(224, 1)
       if constexpr (Epi::kTileStats) {
         // the row scales of this tile's group, from every CTA's statistics warp
         if (epi.a.ts.x) {
-          const int g = mu * MT * BM / kStatRows;
+          const int g = mu * BM / kStatRows;
           if (g > stats_ready) {
             bool ok = true;
             if (lane == 0) ok = wait_count(epi.a.ts.done + g, (int)gridDim.x, abort_flag, err);
@@ -272,10 +314,10 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
       }
-      for (int r = 0; r < MT; ++r) {
-        const int mt = mu * MT + r;
+      {
+        const int mt = PAIR ? mu * 2 + (int)rank : mu;
         const int row0 = mt * BM + quad * 32;
-        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + (acc + r) * BN;
+        const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * BN;
         float rsum[8];
         float lm[8], ls[8];        // running (max, Σ exp) of each row (kRowLse)
         typename Epi::RowAux ra[8];
@@ -298,16 +340,30 @@ __global__ void __launch_bounds__(224, 1)
             if (row < M) ra[i] = epi.row_aux(row);
           }
         }
+        // the global inputs of chunk c0 are requested while chunk c0 - 32 is
+        // computed and stored, so their latency overlaps that chunk's stores
+        typename Epi::Aux ax_next[8];
+        {
+          const int col = nt * BN + sub_col;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = row0 + sub_row + 4 * i;
+            if (row < M && col < N) ax_next[i] = epi.aux(row, col, ra[i]);
+          }
+        }
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t r0[16], r1[16];
           tmem_ld16(taddr + c0, r0);
           tmem_ld16(taddr + c0 + 16, r1);
           tmem_wait_ld();
-          if (c0 + 32 == BN && r == MT - 1) {   // the accumulator(s) free once the last columns are in registers
+          if (c0 + 32 == BN) {   // the accumulator is free once its last columns are in registers
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (lane == 0) {
+              if constexpr (PAIR) mbar_arrive_cluster(tempty_cl[acc]);
+              else mbar_arrive(&tempty[acc]);
+            }
           }
           float* my = stage + lane * C::EPI_STRIDE;
 #pragma unroll
@@ -321,12 +377,15 @@ __global__ void __launch_bounds__(224, 1)
           }
           __syncwarp();
           const int col = nt * BN + c0 + sub_col;
-          // all global inputs of the chunk first, then compute and store
           typename Epi::Aux ax[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int row = row0 + sub_row + 4 * i;
-            if (row < M && col < N) ax[i] = epi.aux(row, col, ra[i]);
+          for (int i = 0; i < 8; ++i) ax[i] = ax_next[i];
+          if (c0 + 32 < BN) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int row = row0 + sub_row + 4 * i;
+              if (row < M && col + 32 < N) ax_next[i] = epi.aux(row, col + 32, ra[i]);
+            }
           }
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -375,11 +434,15 @@ __global__ void __launch_bounds__(224, 1)
     }
   }
 
+  // Teardown (PAIR: every MMA of the pair has completed, rank 0's issuer
+  // waited on its drain, before either CTA releases the pair's tensor memory)
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -399,36 +462,61 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BN, class Epi, int MT = 1>
+template <int BN, class Epi, bool PAIR = false>
 cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& epi, cudaStream_t s,
                 int* n_tiles_out = nullptr) {
-  using C = TcCfg<BN, MT>;
+  using C = TcCfg<BN, PAIR>;
+  constexpr int MU = PAIR ? 2 : 1;
   if (n_tiles_out) *n_tiles_out = (N + BN - 1) / BN;
   if (M <= 0 || N <= 0) return cudaSuccess;
+  if (PAIR && M < BM) return cudaErrorInvalidValue;
   CUtensorMap ta, tbm;
   const uint32_t a_rows = M >= BM ? BM : (uint32_t)((M + 7) / 8 * 8);
   cudaError_t e = make_tmap_2d_bf16(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)K, BK, a_rows);
   if (e != cudaSuccess) return e;
-  e = make_tmap_2d_bf16(&tbm, B, (uint64_t)N, (uint64_t)K, (uint64_t)K, BK, BN);
+  e = make_tmap_2d_bf16(&tbm, B, (uint64_t)N, (uint64_t)K, (uint64_t)K, BK, PAIR ? BN / 2 : BN);
   if (e != cudaSuccess) return e;
   static bool attr_set[64] = {false};
+  static int max_clusters[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(k_gemm_tc<BN, Epi, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(k_gemm_tc<BN, Epi, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM);
     if (e != cudaSuccess) return e;
+    if constexpr (PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
+      cfg.blockDim = dim3(tc_threads<Epi>(), 1, 1);
+      cfg.dynamicSmemBytes = C::SMEM;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<BN, Epi, PAIR>, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorNotSupported;
+      max_clusters[dev] = n;
+    }
     attr_set[dev] = true;
   }
-  const int m_units = ((M + BM - 1) / BM + MT - 1) / MT;
+  const int m_units = ((M + BM - 1) / BM + MU - 1) / MU;
   const int tiles = m_units * ((N + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
   // Short K with a B panel beyond what L2 keeps: group up to 48 row blocks (48
-  // MB of A at K = 4096), m fastest inside a group, so each B tile is read
-  // from HBM once per group rather than once per row block.  Otherwise n
-  // fastest.  (Measured on the W1/W3 GEMM of 32768 tokens: groups of 32, 48
-  // and 64 row blocks ran at 1775-1790, 1835 and 1622 TFLOP/s.)
+  // MB of A at K = 4096; 32 on CTA pairs), m fastest inside a group, so each B
+  // tile is read from HBM once per group rather than once per row block.
+  // Otherwise n fastest.  (Measured on the W1/W3 GEMM of 32768 tokens: single
+  // CTAs with groups of 32, 48 and 64 row blocks ran at 1775-1790, 1835 and
+  // 1622 TFLOP/s; CTA pairs with 16, 32, 48, 64 and 96 at 1715, 1793, 1775,
+  // 1759 and 1673 TFLOP/s, reading 12.6, 6.6, 8.0, 10.5 and 16.3 GB from DRAM.)
   const size_t b_bytes = (size_t)N * K * 2;
-  const int gmax = 48 / MT;                        // CTA tiles along M per group
+  const int gmax = (PAIR ? 32 : 48) / MU;          // tiles along M per group
   const int group_m =
       (K <= 8192 && b_bytes > (size_t(48) << 20) && m_units > 1) ? (m_units < gmax ? m_units : gmax) : 0;
   if constexpr (Epi::kTileStats) {
@@ -444,13 +532,39 @@ cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& ep
       attr[0].val.cooperative = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, Epi, MT>, ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
+      return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, Epi>, ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
                                 device_error_word());
     }
   }
-  k_gemm_tc<BN, Epi, MT><<<grid, tc_threads<Epi>(), C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
+  if constexpr (PAIR) {
+    const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(tc_threads<Epi>());
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, Epi, PAIR>, ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
+                              device_error_word());
+  }
+  k_gemm_tc<BN, Epi><<<grid, tc_threads<Epi>(), C::SMEM, s>>>(ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
                                                                    device_error_word());
   return cudaGetLastError();
+}
+
+// CTA pairs when the 256-row tiles fill at least two waves of pairs (one
+// cluster per two SMs).  Measured on the prefill of 32768 tokens at d = 4096
+// against single-CTA tiles: Wo 1445-1463 -> 1671-1680 TFLOP/s, W2 (single CTAs
+// with two row blocks each) 1698-1712 -> 1832-1844, W1/W3 1758-1775 -> 1780-1789.
+bool pair_fits(int M, int N) {
+  const long tiles = (long)((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
+  return M >= 2 * BM && tiles >= 2L * sm_count();
 }
 
 // Narrow N tiles when the grid would not fill the GPU.
@@ -523,25 +637,24 @@ cudaError_t make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t planes, u
 
 cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
                         cudaStream_t s) {
+  // single CTAs: the statistics warp needs the cooperative launch
   return run_auto(A, B, M, N, K, EpiQKV<bf16, true>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
 }
 cudaError_t gemm_tc_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
                        cudaStream_t s, int* row_parts) {
   // one Σh² partial per row and column tile
+  if (pair_fits(M, N)) return run<256, EpiWo<bf16, true>, true>(A, B, M, N, K, EpiWo<bf16, true>{e, D.d}, s, row_parts);
   return run_auto(A, B, M, N, K, EpiWo<bf16, true>{e, D.d}, s, row_parts);
 }
 cudaError_t gemm_tc_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
                         cudaStream_t s) {
+  if (pair_fits(M, N))
+    return run<256, EpiW13<bf16, true>, true>(A, B, M, N, K, EpiW13<bf16, true>{e, D.d, D.f, D.eps}, s);
   return run_auto(A, B, M, N, K, EpiW13<bf16, true>{e, D.d, D.f, D.eps}, s);
 }
 cudaError_t gemm_tc_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
                        cudaStream_t s) {
-  // long K: pairs of row blocks share each weight tile, when the row blocks
-  // pair up exactly and the pairs still fill several waves
-  const int m_tiles = (M + BM - 1) / BM;
-  const long pairs = (long)(m_tiles / 2) * ((N + 255) / 256);
-  if (K >= 8192 && m_tiles % 2 == 0 && pairs >= 4L * sm_count())
-    return run<256, EpiW2<true>, 2>(A, B, M, N, K, EpiW2<true>{e, D.d}, s);
+  if (pair_fits(M, N)) return run<256, EpiW2<true>, true>(A, B, M, N, K, EpiW2<true>{e, D.d}, s);
   return run_auto(A, B, M, N, K, EpiW2<true>{e, D.d}, s);
 }
 cudaError_t gemm_tc_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, cudaStream_t s) {
@@ -553,7 +666,7 @@ cudaError_t gemm_tc_lse(const void* A, const void* B, int M, int N, int K, const
 }
 cudaError_t gemm_tc_f32out(const void* A, const void* B, float* Cp, int M, int N, int K, int bn, int mt,
                            cudaStream_t s) {
-  if (mt == 2) return run<256, EpiF32, 2>(A, B, M, N, K, EpiF32{Cp, N}, s);
+  if (mt == 2) return run<256, EpiF32, true>(A, B, M, N, K, EpiF32{Cp, N}, s);
   if (bn == 256) return run<256>(A, B, M, N, K, EpiF32{Cp, N}, s);
   return run<128>(A, B, M, N, K, EpiF32{Cp, N}, s);
 }

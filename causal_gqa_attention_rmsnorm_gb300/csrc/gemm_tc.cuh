@@ -31,7 +31,7 @@ cudaError_t gemm_tc_w13(const void* A, const void* B, int M, int N, int K, const
 cudaError_t gemm_tc_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
                        cudaStream_t s);
 // Plain C = A·Bᵀ in fp32 with the same main loop (test hook); mt = 2 takes the
-// row-pair tiles (two 128-row A blocks per 256-column weight tile).
+// CTA-pair tiles (256 rows over two CTAs, M = 256 MMAs).
 cudaError_t gemm_tc_f32out(const void* A, const void* B, float* C, int M, int N, int K, int bn, int mt,
                            cudaStream_t s);
 

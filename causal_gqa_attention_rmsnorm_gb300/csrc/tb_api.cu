@@ -633,11 +633,12 @@ TB_API int32_t tbx_decode_chunk_keys(int32_t dtype, int32_t B, int32_t Hkv, int3
 }
 
 // Test hook (not part of the public header): C[M, N] = A[M, K]·B[N, K]ᵀ in
-// fp32 through the bf16 tcgen05 main loop, N-tile width bn (128 or 256).
+// fp32 through the bf16 tcgen05 main loop, N-tile width bn (128 or 256); mt = 2
+// takes 256-row tiles on CTA pairs (bn 256, M ≥ 128).
 TB_API tb_status tbx_gemm_bf16(const void* A, const void* B, float* Cp, int32_t M, int32_t N, int32_t K, int32_t bn,
                                int32_t mt, void* stream) {
   if (!A || !B || !Cp || M < 0 || N <= 0 || K <= 0 || K % 64 || N % 4 || (bn != 128 && bn != 256) ||
-      (mt != 1 && mt != 2) || (mt == 2 && bn != 256))
+      (mt != 1 && mt != 2) || (mt == 2 && (bn != 256 || M < 128)))
     return fail(TB_ERR_INVALID_ARG, "tbx_gemm_bf16: bad arguments");
   TB_TRY(gemm_tc_f32out(A, B, Cp, M, N, K, bn, mt, (cudaStream_t)stream));
   return TB_OK;

@@ -1,7 +1,7 @@
 """Bit-for-bit reproducibility: the same call on the same inputs gives the same
 bytes.  The one cross-CTA reduction of the block, the second norm's row sums
-Σh², adds its partials in a fixed order (the last producer of a row group
-sums them), so no output depends on which CTA finished first."""
+Σh², is stored as per-tile partials that its consumer adds in index order, so
+no output depends on which CTA finished first."""
 import pytest
 import torch
 
@@ -26,6 +26,9 @@ def _prefill_twice(s, seed):
     # tile GEMM (more than 64 tokens)
     ("tile", workloads.BlockShape("det_tile", "prefill", "bf16", B=2, T=300, d=1024, H=8, Hkv=2, dh=128, f=2048,
                                   rope_base=1e4, eps=1e-6, gains="normal")),
+    # 8192 tokens at d = 4096: the Wo, W1/W3 and W2 GEMMs on CTA pairs, attention on CTA pairs
+    ("pair", workloads.BlockShape("det_pair", "prefill", "bf16", B=1, T=8192, d=4096, H=32, Hkv=8, dh=128,
+                                  f=4096, rope_base=5e5, eps=1e-5, gains="normal")),
     # few-token GEMM (K-split partials, then the partial-sum epilogue)
     ("skinny", workloads.BlockShape("det_few", "prefill", "bf16", B=3, T=7, d=2048, H=16, Hkv=4, dh=128, f=1024,
                                     rope_base=1e4, eps=1e-6, gains="normal")),

@@ -13,11 +13,15 @@ pytestmark = pytest.mark.gpu
     (32, 6144, 4096, 128, 1),      # decode-shaped (M = 32)
     (1000, 768, 768, 256, 1),      # ragged M, N multiple of 256 with K 768
     (4096, 2304, 768, 256, 1),     # many tiles per CTA (persistent loop, accumulator ping-pong)
-    # row pairs (the long-K W2 tiles): two 128-row A blocks share each weight tile
-    (256, 256, 64, 256, 2),        # one pair, one k-block
-    (1000, 512, 8192, 256, 2),     # 8 row blocks, the last one ragged (104 rows): the last pair part zero-filled
-    (300, 768, 8192, 256, 2),      # 3 row blocks: the second pair's second block lies wholly past M
-    (4096, 1280, 14336, 256, 2),   # 16 pairs x 5 column tiles over 152 CTAs, K of the W2 shape
+    # CTA pairs: a 256-row tile over two CTAs, each staging half of the weight tile
+    (256, 256, 64, 256, 2),        # one pair tile, one k-block
+    (300, 512, 1024, 256, 2),      # 3 row blocks: the second pair's odd CTA lies wholly past M
+    (300, 768, 8192, 256, 2),      # the same with long K
+    (1000, 768, 4096, 256, 2),     # ragged last block (104 rows), K of the Wo shape
+    (1000, 512, 8192, 256, 2),     # 8 row blocks, the last one ragged
+    (2048, 7168, 4096, 256, 2),    # 56 MB weight panel: grouped raster, several tiles per cluster
+    (4096, 4096, 256, 256, 2),     # 16 x 16 pair tiles with four k-blocks each: short main loops
+    (4096, 1280, 14336, 256, 2),   # 16 pair tiles x 5 column tiles over 76 clusters, K of the W2 shape
 ])
 def test_gemm_bf16_matches_fp32_product(M, N, K, bn, mt):
     from causal_gqa_attention_rmsnorm_gb300 import binding

@@ -38,6 +38,10 @@ SMALL = {
     # bf16, 46 tokens in all: the few-token (K-split) GEMMs in a prefill
     "bf16_few_tokens": workloads.BlockShape("bf16_few_tokens", "prefill", "bf16", B=2, T=23, d=512, H=8, Hkv=2,
                                             dh=64, f=1024, rope_base=1e4, eps=1e-6, gains="normal"),
+    # bf16, GQA 8/2, dh 128: the CTA-pair attention with two KV groups of four heads, several query
+    # blocks and a ragged last one, two sequences
+    "bf16_gqa4_dh128": workloads.BlockShape("bf16_gqa4_dh128", "prefill", "bf16", B=2, T=520, d=1024, H=8,
+                                            Hkv=2, dh=128, f=1024, rope_base=5e5, eps=1e-5, gains="normal"),
     # bf16, GQA 8/1 (largest group), one token per sequence
     "bf16_t1": workloads.BlockShape("bf16_t1", "prefill", "bf16", B=3, T=1, d=1024, H=8, Hkv=1, dh=128,
                                     f=1536, rope_base=1e4, eps=1e-6, gains="normal"),

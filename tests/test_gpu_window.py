@@ -20,6 +20,9 @@ GQA = workloads.BlockShape("win_gqa", "prefill", "bf16", B=2, T=300, d=256, H=4,
 MHA = workloads.BlockShape("win_mha", "prefill", "bf16", B=1, T=333, d=512, H=4, Hkv=4, dh=128, f=1024,
                            rope_base=5e5, eps=1e-5, gains="normal")
 F32 = workloads.CONFIGS["tiny_fp32"].with_(name="win_f32", B=2, T=37)
+# GQA with groups of four heads at dh 128: the CTA-pair attention kernel
+PAIR = workloads.BlockShape("win_pair", "prefill", "bf16", B=2, T=333, d=1024, H=8, Hkv=2, dh=128, f=1024,
+                            rope_base=5e5, eps=1e-5, gains="normal")
 
 
 def _prefill_vs_oracle(s, seed=3):
@@ -41,6 +44,11 @@ def test_prefill_window_gqa_head_pairs(W):
 @pytest.mark.parametrize("W", [1, 50, 128, 256])
 def test_prefill_window_mha_block_pairs(W):
     _prefill_vs_oracle(MHA.with_(window=W))
+
+
+@pytest.mark.parametrize("W", [1, 37, 64, 65, 127, 128, 129, 200, 1000])
+def test_prefill_window_gqa_cta_pairs(W):
+    _prefill_vs_oracle(PAIR.with_(window=W))
 
 
 @pytest.mark.parametrize("W", [1, 5, 36, 37])
