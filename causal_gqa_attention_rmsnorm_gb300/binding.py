@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.tbx_skinny_split_count.restype = c_int32
         L.tbx_decode_chunk_keys.argtypes = [c_int32, c_int32, c_int32, c_int32, c_int32]
         L.tbx_decode_chunk_keys.restype = c_int32
+        L.tbx_set_stat_poll_ns.argtypes = [ctypes.c_uint64]
+        L.tbx_set_stat_poll_ns.restype = ctypes.c_uint64
         L.tb_embed.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, ctypes.c_int64, c_void_p, c_void_p]
         L.tb_lm_head_packed_bytes.argtypes = [P(tb_head_cfg)]
         L.tb_lm_head_packed_bytes.restype = c_size_t
@@ -362,6 +364,13 @@ def tbx_gemm_bf16(A: torch.Tensor, B: torch.Tensor, bn: int = 256, mt: int = 1, 
     _check("tbx_gemm_bf16", lib().tbx_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, bn, mt,
                                                 _stream(stream)))
     return C
+
+
+def tbx_set_stat_poll_ns(ns: int) -> int:
+    """Test hook: how long a prefill QKV tile epilogue polls for its row group's
+    RMSNorm-1 statistics before forming its rows' scales itself; returns the
+    previous value."""
+    return int(lib().tbx_set_stat_poll_ns(int(ns)))
 
 
 def tbx_trace_enable(slots: int) -> None:

@@ -188,8 +188,10 @@ struct QKVStats {
 // RMSNorm-1 statistics formed inside the tile QKV GEMM (prefill): one extra
 // warp per CTA computes r for its share of each group of kStatRows rows, in
 // group order, and counts the finished group in done[group] (zeroed before the
-// launch); a tile's epilogue waits, bounded, until its group's count reaches
-// the grid size.  The launch is cooperative, so every CTA it waits on runs.
+// launch).  A tile's epilogue polls its group's count for a bounded time; if
+// the group is not complete by then (a CTA of the grid not yet resident), the
+// epilogue warps form r for their own rows with the same function, which gives
+// the same bits, so no launch guarantee is needed.
 // x == nullptr: r comes from the row-statistics kernel.
 constexpr int kStatRows = 2048;
 struct TileStats {
@@ -200,7 +202,10 @@ struct TileStats {
   int* done = nullptr;       // [ceil(M / kStatRows)] arrival counts
   int32_t* lens_set = nullptr;   // prefill with a cache: lens[b] = T
   int T = 0;
+  unsigned long long poll_ns = 0;   // how long an epilogue polls for its group before forming r itself
 };
+// The poll limit the prefill passes (stat_poll_ns(); a test hook may shorten it).
+unsigned long long stat_poll_ns();
 struct QKVArgs {
   const float* r;          // [M] RMSNorm-1 inverse RMS of each token
   const float2* rope;      // [max_pos, dh/2]

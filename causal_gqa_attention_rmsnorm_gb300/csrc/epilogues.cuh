@@ -120,7 +120,7 @@ struct EpiQKV {
   int H, Hkv, dh, dh_shift;             // dh = 1 << dh_shift
   struct RowAux { float r; int b, t, qt, kt; };
   struct Aux { float2 c0, c1; };
-  __device__ __forceinline__ RowAux row_aux(int row) const {
+  __device__ __forceinline__ RowAux row_aux_nor(int row) const {
     RowAux ra;
     if (a.pos) {
       ra.b = row; ra.t = a.pos[row]; ra.qt = 0;
@@ -128,7 +128,19 @@ struct EpiQKV {
       ra.b = row / a.T; ra.t = row - ra.b * a.T; ra.qt = ra.t;
     }
     ra.kt = a.kv_dense ? ra.qt : ra.t;
+    ra.r = 0.f;
+    return ra;
+  }
+  __device__ __forceinline__ RowAux row_aux(int row) const {
+    RowAux ra = row_aux_nor(row);
     ra.r = __ldcg(a.r + row);       // L2: with a.ts.x set, another CTA of this kernel wrote it
+    return ra;
+  }
+  // The row inputs with the row scale r given (the tile GEMM's epilogue when
+  // it formed r itself).
+  __device__ __forceinline__ RowAux row_aux_r(int row, float r) const {
+    RowAux ra = row_aux_nor(row);
+    ra.r = r;
     return ra;
   }
   // The tile GEMM's statistics warp: Σx² of token row m over its 32 lanes

@@ -107,9 +107,6 @@ __global__ void __launch_bounds__(224, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
               uint32_t a_box_bytes, int group_m, Epi epi, int* err) {
   using C = TcCfg<BN, PAIR>;
-  // The statistics warp's rows are read by every CTA's epilogue, which needs a
-  // cooperative launch; the CTA pairs' cluster launch does not take one.
-  static_assert(!PAIR || !Epi::kTileStats, "CTA pairs: no statistics warp");
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -302,15 +299,21 @@ __global__ void __launch_bounds__(224, 1)
       tc_fence_after();
       int mu, nt;
       tile_coords(tile, m_units, n_tiles, group_m, mu, nt);
+      // kTileStats: the row scales of this tile's group come from every CTA's
+      // statistics warp.  A group is complete once all CTAs counted it, and each
+      // statistics warp takes the groups in order, so a complete group means that
+      // all earlier ones are.  If the group is still incomplete after a bounded
+      // poll (a CTA of the grid not resident yet), the warp forms r for its own
+      // rows with the same function, hence the same bits.
+      bool own_stats = false;
       if constexpr (Epi::kTileStats) {
-        // the row scales of this tile's group, from every CTA's statistics warp
         if (epi.a.ts.x) {
-          const int g = mu * BM / kStatRows;
+          const int g = (PAIR ? mu * 2 + (int)rank : mu) * BM / kStatRows;
           if (g > stats_ready) {
-            bool ok = true;
-            if (lane == 0) ok = wait_count(epi.a.ts.done + g, (int)gridDim.x, abort_flag, err);
-            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-            stats_ready = g;
+            int ready = 0;
+            if (lane == 0) ready = poll_count(epi.a.ts.done + g, (int)gridDim.x, epi.a.ts.poll_ns) ? 1 : 0;
+            if (__shfl_sync(0xffffffffu, ready, 0)) stats_ready = g;
+            else own_stats = true;
           }
         }
       }
@@ -322,10 +325,19 @@ __global__ void __launch_bounds__(224, 1)
         float lm[8], ls[8];        // running (max, Σ exp) of each row (kRowLse)
         typename Epi::RowAux ra[8];
         // kRowSumIn: lane l forms the input row sum of row row0 + l, and each
-        // lane takes those of its rows from the lane that owns them
+        // lane takes those of its rows from the lane that owns them; likewise
+        // the row scale r of the warp's own rows when it forms them (kTileStats)
         float rs_in = 0.f;
         if constexpr (Epi::kRowSumIn) {
           if (row0 + lane < M) rs_in = epi.row_sum_in(row0 + lane);
+        }
+        if constexpr (Epi::kTileStats) {
+          if (own_stats) {
+            for (int j = 0; j < 32 && row0 + j < M; ++j) {
+              const float rj = epi.tile_row_scale(row0 + j, lane);
+              if (lane == j) rs_in = rj;
+            }
+          }
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -336,6 +348,9 @@ __global__ void __launch_bounds__(224, 1)
           if constexpr (Epi::kRowSumIn) {
             const float ss = __shfl_sync(0xffffffffu, rs_in, sub_row + 4 * i);
             if (row < M) ra[i] = epi.row_aux_with(ss);
+          } else if constexpr (Epi::kTileStats) {
+            const float rr = __shfl_sync(0xffffffffu, rs_in, sub_row + 4 * i);
+            if (row < M) ra[i] = own_stats ? epi.row_aux_r(row, rr) : epi.row_aux(row);
           } else {
             if (row < M) ra[i] = epi.row_aux(row);
           }
@@ -519,23 +534,6 @@ cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& ep
   const int gmax = (PAIR ? 32 : 48) / MU;          // tiles along M per group
   const int group_m =
       (K <= 8192 && b_bytes > (size_t(48) << 20) && m_units > 1) ? (m_units < gmax ? m_units : gmax) : 0;
-  if constexpr (Epi::kTileStats) {
-    if (epi.a.ts.x) {
-      // cooperative: every epilogue waits on the statistics warps of all CTAs
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(grid);
-      cfg.blockDim = dim3(tc_threads<Epi>());
-      cfg.dynamicSmemBytes = C::SMEM;
-      cfg.stream = s;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeCooperative;
-      attr[0].val.cooperative = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, Epi>, ta, tbm, M, N, K, a_rows * BK * 2, group_m, epi,
-                                device_error_word());
-    }
-  }
   if constexpr (PAIR) {
     const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
     cudaLaunchConfig_t cfg = {};
@@ -637,8 +635,9 @@ cudaError_t make_tmap_3d_u8(CUtensorMap* m, const void* base, uint64_t planes, u
 
 cudaError_t gemm_tc_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
                         cudaStream_t s) {
-  // single CTAs: the statistics warp needs the cooperative launch
-  return run_auto(A, B, M, N, K, EpiQKV<bf16, true>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
+  const EpiQKV<bf16, true> epi{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)};
+  if (pair_fits(M, N)) return run<256, EpiQKV<bf16, true>, true>(A, B, M, N, K, epi, s);
+  return run_auto(A, B, M, N, K, epi, s);
 }
 cudaError_t gemm_tc_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
                        cudaStream_t s, int* row_parts) {

@@ -77,10 +77,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Wait until the counter at p (in global memory, written by other CTAs of the
-// grid) reaches target, reading it with acquire semantics; same limit and
-// abort protocol as mbar_wait.
-__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort, int* err) {
+// Poll the counter at p (global memory, written by other CTAs) until it
+// reaches target, for at most limit_ns; false when it did not.  No error is
+// raised: the caller has another way to its result.
+__device__ __forceinline__ bool poll_count(const int* p, int target, uint64_t limit_ns) {
   auto load = [p]() {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -88,17 +88,10 @@ __device__ __forceinline__ bool wait_count(const int* p, int target, volatile in
   };
   if (load() >= target) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     __nanosleep(128);
     if (load() >= target) return true;
-    if ((it & 15u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        atomicOr(err, TB_DEVERR_TIMEOUT);
-        return false;
-      }
-    }
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 

@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <vector>
 
 #include "common.cuh"
@@ -37,6 +38,11 @@ tb_status report(tb_status st, const char* fmt, ...) {
   va_end(ap);
   return st;
 }
+
+namespace {
+std::atomic<unsigned long long> g_stat_poll_ns{200000};
+}  // namespace
+unsigned long long stat_poll_ns() { return g_stat_poll_ns.load(); }
 
 // Device address of the error word on the current device.
 int* device_error_word() {
@@ -387,7 +393,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
   QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr, paged_of(kv, err)};
   if (tile_stats) {
     TB_TRY(cudaMemsetAsync(W.stat_done, 0, (size_t)(M + kStatRows - 1) / kStatRows * sizeof(int), s));
-    qa.ts = TileStats{x, cfg->d, cfg->eps, W.r, W.stat_done, kv ? kv->lens : nullptr, T};
+    qa.ts = TileStats{x, cfg->d, cfg->eps, W.r, W.stat_done, kv ? kv->lens : nullptr, T, stat_poll_ns()};
   } else {
     rec.stage("rms");
     TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
@@ -409,17 +415,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
     TB_TRY(gemm_simt_w2(dt, W.a, P.w2, M, cfg->d, cfg->f, D, ya, s));
   } else {
     rec.stage("qkv");
-    cudaError_t e = mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s);
-    if (e == cudaErrorCooperativeLaunchTooLarge && tile_stats) {
-      // fewer SMs than the cooperative grid needs (e.g. a limited share of
-      // the GPU): the row-statistics kernel first, then the plain launch
-      (void)cudaGetLastError();
-      qa.ts = TileStats();
-      TB_TRY(launch_row_stats(dt, x, M, cfg->d, cfg->eps, W.r, T, kv ? kv->lens : nullptr, nullptr, nullptr, 0,
-                              nullptr, err, s));
-      e = mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s);
-    }
-    TB_TRY(e);
+    TB_TRY(mm_qkv(W, x, P.wqkv, M, nqkv, cfg->d, D, qa, s));
     if (i8_cache) {
       rec.stage("quant");
       TB_TRY(launch_quantize_kv(*kv, W.k, W.v, T, nullptr, s));
@@ -631,6 +627,13 @@ TB_API int32_t tbx_decode_chunk_keys(int32_t dtype, int32_t B, int32_t Hkv, int3
   if (B <= 0 || Hkv <= 0 || T_max <= 0 || sms <= 0) return -1;
   return decode_chunk_keys_sms(dtype, B, Hkv, T_max, sms);
 }
+
+// Test hook (not part of the public header): how long a QKV tile epilogue
+// polls for its row group's RMSNorm-1 statistics before it forms its rows'
+// scales itself (default 200 us: far longer than the statistics warps of a
+// resident grid take); 0 makes nearly every epilogue form its own, which must
+// give the same bytes.  Returns the previous value.
+TB_API uint64_t tbx_set_stat_poll_ns(uint64_t ns) { return g_stat_poll_ns.exchange(ns); }
 
 // Test hook (not part of the public header): C[M, N] = A[M, K]·B[N, K]ᵀ in
 // fp32 through the bf16 tcgen05 main loop, N-tile width bn (128 or 256); mt = 2

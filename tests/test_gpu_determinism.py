@@ -42,6 +42,30 @@ def test_prefill_is_bit_reproducible(name, shape):
         assert torch.equal(y, ys[0]), name
 
 
+@pytest.mark.parametrize("name,shape", [
+    # CTA-pair QKV GEMM (8192 tokens at d = 4096)
+    ("pair", workloads.BlockShape("det_stats_pair", "prefill", "bf16", B=1, T=8192, d=4096, H=32, Hkv=8, dh=128,
+                                  f=4096, rope_base=5e5, eps=1e-5, gains="normal")),
+    # single-CTA QKV GEMM, several row groups of the statistics warps
+    ("single", workloads.BlockShape("det_stats_one", "prefill", "bf16", B=2, T=3000, d=1024, H=8, Hkv=2, dh=128,
+                                    f=2048, rope_base=1e4, eps=1e-6, gains="normal")),
+])
+def test_prefill_statistics_fallback_is_bit_identical(name, shape):
+    """A QKV tile epilogue whose row group's RMSNorm-1 statistics are not ready
+    in time forms its rows' scales itself, with the statistics warp's function:
+    the output must be the same bytes.  A zero poll limit sends nearly every
+    early tile that way."""
+    from causal_gqa_attention_rmsnorm_gb300 import binding
+    ys = _prefill_twice(shape, seed=5)
+    prev = binding.tbx_set_stat_poll_ns(0)
+    try:
+        yf = _prefill_twice(shape, seed=5)
+    finally:
+        binding.tbx_set_stat_poll_ns(prev)
+    for y in yf:
+        assert torch.equal(y, ys[0]), name
+
+
 @pytest.mark.parametrize("cache", ["bf16", "int8"])
 def test_decode_is_bit_reproducible(cache):
     import causal_gqa_attention_rmsnorm_gb300 as tb
