@@ -50,7 +50,7 @@ template <int NT> struct SkCfg {
 template <int NT>
 __global__ void __launch_bounds__(192)
     k_gemm_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N,
-                  int tiles, int kblocks, int splits, float* __restrict__ part, int* err, int blocked) {
+                  int tiles, int kblocks, int splits, float* __restrict__ part, int* err) {
   using C = SkCfg<NT>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -124,8 +124,7 @@ __global__ void __launch_bounds__(192)
           }
           uint8_t* sw = smem + st * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
-          if (blocked) tma_load_2d_hint(&tmW, sw, &full[st], 0, (tile * kblocks + kb0 + j) * kRows, pol);
-          else tma_load_2d_hint(&tmW, sw, &full[st], (kb0 + j) * kBK, tile * kRows, pol);
+          tma_load_2d_hint(&tmW, sw, &full[st], (kb0 + j) * kBK, tile * kRows, pol);
           if (dep) {
             tma_load_2d(&tmX, sw + C::W_BYTES, &full[st], (kb0 + j) * kBK, 0);
           } else {
@@ -294,10 +293,7 @@ template <int NT, class Epi>
 cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi& epi, float* part, cudaStream_t s) {
   using C = SkCfg<NT>;
   CUtensorMap tw, tx;
-  static const int blocked = [] { const char* v = getenv("TB_EXP_BLOCKED"); return v ? atoi(v) : 0; }();
-  const bool blk = blocked && N % kRows == 0;
-  cudaError_t e = blk ? make_tmap_2d_bf16(&tw, W, (uint64_t)N * K / kBK, (uint64_t)kBK, (uint64_t)kBK, kBK, kRows)
-                      : make_tmap_2d_bf16(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBK, kRows);
+  cudaError_t e = make_tmap_2d_bf16(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBK, kRows);
   if (e != cudaSuccess) return e;
   e = make_tmap_2d_bf16(&tx, X, (uint64_t)M, (uint64_t)K, (uint64_t)K, kBK, NT);
   if (e != cudaSuccess) return e;
@@ -313,7 +309,7 @@ cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi&
   const int splits = split_count(tiles, kblocks);
   const int items = tiles * splits, slots = 2 * sm_count();
   e = launch_pdl(k_gemm_skinny<NT>, dim3(items < slots ? items : slots), dim3(192), C::SMEM, s, tw, tx, M, N, tiles,
-                 kblocks, splits, part, device_error_word(), blk ? 1 : 0);
+                 kblocks, splits, part, device_error_word());
   if (e != cudaSuccess) return e;
   return launch_pdl(k_splitk_epilogue<Epi>, dim3((N / 4 + 255) / 256, M), dim3(32 * kEpiWarps), 0, s,
                     (const float*)part, splits, M, N, epi);
