@@ -171,9 +171,10 @@ __device__ __forceinline__ float ordered_sum(const float* part, int n) {
 
 // GEMM epilogue argument bundles.
 
-// RMSNorm-1 statistics and the decode step's bookkeeping taken by the QKV
-// GEMM's partial-sum epilogue (few-token decode): every CTA of a token row
-// forms the row's Σx² and reads its position from lens.  x == nullptr: r and
+// RMSNorm-1 statistics and the decode step's bookkeeping taken by the
+// few-token QKV GEMM's epilogue: each CTA forms Σx² of every token over its K
+// range, the cluster adds them, and the token's reducer reads its position
+// from lens.  x == nullptr: r and
 // the positions come from the row-statistics kernel instead.
 struct QKVStats {
   const void* x = nullptr;   // [M, d] block input (the block's dtype)
@@ -256,7 +257,7 @@ cudaError_t gemm_tc_logits(const void* A, const void* B, int M, int N, int K, co
 // (max, Σ exp) pair and the target's logit (ceil(N / 256) pairs per row).
 cudaError_t gemm_tc_lse(const void* A, const void* B, int M, int N, int K, const LseArgs& e, cudaStream_t s);
 int lse_tile_cols();
-cudaError_t gemm_skinny_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, float* part,
+cudaError_t gemm_skinny_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e,
                                cudaStream_t s);
 cudaError_t gemm_simt_logits(int dtype, const void* A, const void* B, int M, int N, int K, const LogitsArgs& e,
                              cudaStream_t s);
@@ -284,21 +285,20 @@ cudaError_t gemm_simt_w13(int dtype, const void* A, const void* B, int M, int N,
 cudaError_t gemm_simt_w2(int dtype, const void* A, const void* B, int M, int N, int K, const Dims& D,
                          const W2Args& e, cudaStream_t s);
 
-// gemm_skinny.cu (bf16, M ≤ skinny_max_tokens(): K-split tcgen05 GEMM plus a
-// partial-sum epilogue kernel; `part` holds skinny_part_floats(M, N) floats)
+// gemm_skinny.cu (bf16, M ≤ skinny_max_tokens(): K-split tcgen05 GEMM whose
+// split is reduced inside a cluster, with the fused epilogue)
 int skinny_max_tokens();
-size_t skinny_part_floats(int M, int max_n);
-// K ranges per weight tile for `tiles` 128-row weight tiles of `kblocks` K
-// blocks over `slots` resident CTAs (-1 for a non-positive argument)
+// K ranges per weight tile (the cluster size) for `tiles` 128-row weight tiles
+// of `kblocks` K blocks over `slots` resident CTAs (-1 for a non-positive argument)
 int skinny_split_count(int tiles, int kblocks, int slots);
 cudaError_t gemm_skinny_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
-                            float* part, cudaStream_t s);
+                            cudaStream_t s);
 cudaError_t gemm_skinny_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
-                           float* part, cudaStream_t s, int* row_parts);
+                           cudaStream_t s, int* row_parts);
 cudaError_t gemm_skinny_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
-                            float* part, cudaStream_t s);
+                            cudaStream_t s);
 cudaError_t gemm_skinny_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
-                           float* part, cudaStream_t s);
+                           cudaStream_t s);
 
 // attn_simt.cu (fp32 path)
 cudaError_t attn_prefill_simt(int dtype, const void* q, const void* k, const void* v, void* o, int B,

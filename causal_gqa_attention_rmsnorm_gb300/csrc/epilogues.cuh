@@ -187,49 +187,61 @@ struct EpiQKV {
     s = warp_sum(s);
     return 1.0f / sqrtf(s / (float)d + a.ts.eps);
   }
-  // Few-token decode with a.st.x set: this thread's share (16-byte vectors
-  // tid, tid + nthreads, ...) of Σx² over token row m ("Transformer block"
-  // page, RMSNorm: mean of squares, eps inside the root).
-  __device__ __forceinline__ float row_stats_partial(int m, int tid, int nthreads) const {
-    const int d = a.st.d;
-    const T* xr = (const T*)a.st.x + (size_t)m * d;
+  // Few-token decode with a.st.x set, one warp: Σx² of token rows t_first,
+  // t_first + t_step, ... (below M, at most TPW of them) over columns
+  // [k0, k1), k0 and k1 multiples of 64; each row's 16-byte vectors are taken
+  // by lanes lane, lane + 32, ..., then summed across the warp in a fixed
+  // order.  The loads of all the rows are issued together.  The cluster adds
+  // the ranges in order, and the root is taken as the "Transformer block"
+  // page's RMSNorm has it: mean of squares, eps inside the root.
+  template <int TPW>
+  __device__ __forceinline__ void row_stats_ranges(int t_first, int t_step, int M, int k0, int k1, int lane,
+                                                   float (&ss)[TPW]) const {
     constexpr int V = 16 / sizeof(T);
-    float s = 0.f;
-    if (d % V == 0) {
-      const uint4* p = reinterpret_cast<const uint4*>(xr);
-      for (int i = tid; i < d / V; i += nthreads) {
-        Vec16<T> v;
-        v.raw = __ldg(p + i);
+    const int nv = (k1 - k0) / V;
 #pragma unroll
-        for (int j = 0; j < V; ++j) {
-          const float f = v.get(j);
-          s = fmaf(f, f, s);
+    for (int j = 0; j < TPW; ++j) ss[j] = 0.f;
+    for (int i = lane; i < nv; i += 32) {
+      Vec16<T> v[TPW];
+#pragma unroll
+      for (int j = 0; j < TPW; ++j) {
+        const int t = t_first + j * t_step;
+        if (t < M) v[j].raw = __ldg(reinterpret_cast<const uint4*>((const T*)a.st.x + (size_t)t * a.st.d + k0) + i);
+      }
+#pragma unroll
+      for (int j = 0; j < TPW; ++j) {
+        if (t_first + j * t_step < M) {
+#pragma unroll
+          for (int e = 0; e < V; ++e) {
+            const float f = v[j].get(e);
+            ss[j] = fmaf(f, f, ss[j]);
+          }
         }
       }
-    } else {
-      for (int i = tid; i < d; i += nthreads) {
-        const float f = to_f(xr[i]);
-        s = fmaf(f, f, s);
-      }
     }
-    return s;
+#pragma unroll
+    for (int j = 0; j < TPW; ++j) ss[j] = warp_sum(ss[j]);
   }
-  // The row inputs from Σx² and lens; the row's first CTA (first) publishes
-  // the position, flags a full cache, and zeroes the step's work counter.
-  __device__ __forceinline__ RowAux row_aux_stats(int m, float ssq, bool first) const {
+  // The row inputs of decode token m from lens (the scale r follows from Σx²).
+  __device__ __forceinline__ RowAux row_aux_pos(int m) const {
     RowAux ra;
     const int p = a.st.lens[m];
     ra.b = m;
     ra.t = (p >= 0 && p < a.st.T_max) ? p : -1;
     ra.qt = 0;
     ra.kt = a.kv_dense ? ra.qt : ra.t;
+    ra.r = 0.f;
+    return ra;
+  }
+  // The scale r from Σx²; the token's first reducer (first) publishes the
+  // position, flags a full cache, and zeroes the step's work counter.
+  __device__ __forceinline__ void row_stats_finish(RowAux& ra, int m, float ssq, bool first) const {
     ra.r = 1.0f / sqrtf(ssq / (float)a.st.d + a.st.eps);
     if (first) {
       a.st.pos_out[m] = ra.t;
       if (ra.t < 0) atomicOr(a.st.err, TB_DEVERR_CACHE_FULL);
       if (m == 0 && a.st.zero_word) *a.st.zero_word = 0;
     }
-    return ra;
   }
   __device__ __forceinline__ Aux aux(int, int col, const RowAux& ra) const {
     Aux x;

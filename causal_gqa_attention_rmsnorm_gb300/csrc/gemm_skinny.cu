@@ -1,23 +1,28 @@
 // bf16 GEMM for few tokens (M ≤ 64, e.g. the decode step's one token per
-// sequence) on the 5th-generation tensor cores, split over K.
+// sequence) on the 5th-generation tensor cores, split over K, with the split
+// reduced inside a thread-block cluster.
 //
 // With M tokens and N outputs, C = X·Wᵀ is bound by streaming the weight
 // matrix W [N, K] from HBM.  The product is computed transposed, Cᵀ = W·Xᵀ, so
 // that 128 weight rows form the MMA's M dimension and the (padded) tokens its N
-// dimension: no MMA lane is wasted on padding rows.  A work item is one
-// 128-row weight tile over one contiguous range of K; persistent CTAs, two per
-// SM, walk the items with one continuous stage ring, so every SM streams
-// weights from the first cycle to the last.
+// dimension: no MMA lane is wasted on padding rows.  The `splits` CTAs of one
+// 128-row weight tile form a cluster, CTA rank r taking K range r:
 //   warp 0      TMA: the weight tile [128, 64] and the token tile [NT, 64]
-//               of each K block into a ring of shared-memory stages;
+//               of each K block of the range into a ring of shared-memory
+//               stages (the first weight stages before the wait for the
+//               previous kernel, which they do not depend on);
 //   warp 1      MMA issuer: D[128, NT] += W_blk · X_blkᵀ (tcgen05, fp32 in
 //               tensor memory);
-//   warps 2..5  drain: each warp's 32 TMEM lanes are 32 output features; the
-//               fp32 partial sums go to part[split][token][feature] while the
-//               next item accumulates into the other TMEM buffer.
-// A second kernel adds the K-range partials (from L2) and applies the block's
-// fused epilogue, the same functors as the large GEMMs, to 4 outputs per
-// thread.
+//   warps 2..5  epilogue: the accumulator to shared memory as
+//               part[token][feature] (the stage ring is free by then); after a
+//               cluster barrier, the tokens [r·tpr, (r+1)·tpr) summed over the
+//               cluster's partials in rank order through distributed shared
+//               memory, then the block's fused epilogue (the functors of the
+//               tile GEMM), one warp per token and four features per lane.
+// No partial sums go through global memory and no second kernel runs.  With
+// RMSNorm-1's statistics (the decode QKV epilogue) each CTA also forms Σx² of
+// every token over its own K range while its MMAs run, and the same reduction
+// adds those in rank order.
 #include "epilogues.cuh"
 #include "gemm_tc.cuh"
 #include "sm100_ptx.cuh"
@@ -30,56 +35,59 @@ using namespace ptx;
 constexpr int kRows = 128;       // weight rows per CTA: the MMA's M
 constexpr int kBK = 64;          // K per stage (one 128-byte swizzle row)
 constexpr int kMaxTok = 64;
-constexpr int kMaxItems = 1024;  // (weight tile, K range) items; sizes the partial buffer
 
+// Shared-memory plan: the stage ring, whose first NT × 128 floats hold the
+// partial tile after the main loop, then the barriers and Σx² partials.
 template <int NT> struct SkCfg {
   static constexpr int STAGES = NT <= 32 ? 5 : 4;           // two CTAs per SM
   static constexpr uint32_t W_BYTES = kRows * kBK * 2;       // 16 KB
-  static constexpr uint32_t X_BYTES = NT * kBK * 2;          // a multiple of 1 KB
+  static constexpr uint32_t X_BYTES = NT * kBK * 2;
   static constexpr uint32_t STAGE_BYTES = W_BYTES + X_BYTES;
   static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
-  static constexpr size_t SMEM = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t ACC_COLS = 64;                   // two accumulators of NT ≤ 64 columns
-  static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
+  static constexpr uint32_t OFF_SSQ = OFF_BAR + 128;         // NT floats: Σx² over this CTA's K range
+  static constexpr uint32_t OFF_RA = OFF_SSQ + 256;          // the row inputs of the tokens this CTA reduces
+  static constexpr uint32_t RA_BYTES = 2048;
+  static constexpr uint32_t OFF_MISC = OFF_RA + RA_BYTES;    // TMEM address, abort flag
+  static constexpr size_t SMEM = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = NT <= 32 ? 32 : 64;
+  static_assert(NT * kRows * 4 <= OFF_BAR, "the partial tile reuses the stage ring");
 };
 
-// Persistent: CTA c takes work items c, c + gridDim.x, ...; item w is weight
-// tile w % tiles over K range w / tiles.  The stage ring runs on across items
-// and the accumulators alternate, so one item's drain overlaps the next
-// item's loads and MMAs.
-template <int NT>
-__global__ void __launch_bounds__(192)
+template <int NT, class Epi>
+__global__ void __launch_bounds__(192, 2)
     k_gemm_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N,
-                  int tiles, int kblocks, int splits, float* __restrict__ part, int* err) {
+                  int kblocks, int splits, Epi epi, int* err) {
   using C = SkCfg<NT>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;     // [2]
-  uint64_t* tempty = tfull + 2;         // [2]
-  uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* drain = tfull + 1;
+  float* ssq_s = reinterpret_cast<float*>(smem + C::OFF_SSQ);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* part_s = reinterpret_cast<float*>(smem);             // [NT][kRows] after the main loop
+  using RowAux = typename Epi::RowAux;
+  static_assert(sizeof(RowAux) * NT <= C::RA_BYTES, "row inputs");
+  RowAux* ra_s = reinterpret_cast<RowAux*>(smem + C::OFF_RA);
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int items = tiles * splits;
-  auto krange = [&](int sp, int& kb0, int& nkb) {
-    kb0 = (int)((long long)kblocks * sp / splits);
-    nkb = (int)((long long)kblocks * (sp + 1) / splits) - kb0;   // ≥ 1: splits ≤ kblocks
-  };
+  const int tile = blockIdx.x / splits;
+  const int rank = (int)cluster_ctarank();                    // blockIdx.x % splits
+  const int kb0 = (int)((long long)kblocks * rank / splits);
+  const int nkb = (int)((long long)kblocks * (rank + 1) / splits) - kb0;   // ≥ 1: splits ≤ kblocks
+  const int tpr = (M + splits - 1) / splits;                   // tokens each CTA of the cluster reduces
+  const int t0 = min(M, rank * tpr), t1 = min(M, t0 + tpr);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
-    }
+    mbar_init(tfull, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -101,196 +109,187 @@ __global__ void __launch_bounds__(192)
       // tiles are requested before the wait for the previous kernel, so they
       // stream while it drains; their token tiles follow the wait.
       const uint64_t pol = policy_evict_first();   // weights are read once per call
-      int held_kb[STAGES];
-      int held = 0;
       bool dep = false;
       auto release = [&]() {
         pdl_wait();
         dep = true;
-        for (int h = 0; h < held; ++h)       // stage h holds the h-th K block issued
-          tma_load_2d(&tmX, smem + h * C::STAGE_BYTES + C::W_BYTES, &full[h], held_kb[h] * kBK, 0);
+        const int held = nkb < STAGES ? nkb : STAGES;
+        for (int h = 0; h < held; ++h)
+          tma_load_2d(&tmX, smem + h * C::STAGE_BYTES + C::W_BYTES, &full[h], (kb0 + h) * kBK, 0);
       };
-      int i = 0;                                  // running K-block count: stage i % STAGES
-      bool ok = true;
-      for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-        const int tile = w % tiles;
-        int kb0, nkb;
-        krange(w / tiles, kb0, nkb);
-        for (int j = 0; j < nkb; ++j, ++i) {
-          const int st = i % STAGES;
-          if (!mbar_wait(&empty[st], ((i / STAGES) & 1) ^ 1u, abort_flag, err)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sw = smem + st * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
-          tma_load_2d_hint(&tmW, sw, &full[st], (kb0 + j) * kBK, tile * kRows, pol);
-          if (dep) {
-            tma_load_2d(&tmX, sw + C::W_BYTES, &full[st], (kb0 + j) * kBK, 0);
-          } else {
-            held_kb[held++] = kb0 + j;
-            if (held == STAGES) release();
-          }
-        }
+      int j = 0;
+      for (; j < nkb; ++j) {
+        const int st = j % STAGES;
+        if (!mbar_wait(&empty[st], ((j / STAGES) & 1) ^ 1u, abort_flag, err)) break;
+        uint8_t* sw = smem + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+        tma_load_2d_hint(&tmW, sw, &full[st], (kb0 + j) * kBK, tile * kRows, pol);
+        if (dep) tma_load_2d(&tmX, sw + C::W_BYTES, &full[st], (kb0 + j) * kBK, 0);
+        else if (j + 1 == STAGES) release();
       }
       if (!dep) release();
       // every copy issued must land before the CTA may exit (earlier copies
       // into the same stages were consumed, hence complete)
       volatile int no_abort = 0;
-      for (int t = i - STAGES < 0 ? 0 : i - STAGES; t < i; ++t)
+      for (int t = j - STAGES < 0 ? 0 : j - STAGES; t < j; ++t)
         mbar_wait(&full[t % STAGES], (t / STAGES) & 1, &no_abort, err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kRows, NT);
-      int i = 0, local = 0;
       bool ok = true;
-      for (int w = blockIdx.x; ok && w < items; w += gridDim.x, ++local) {
-        int kb0, nkb;
-        krange(w / tiles, kb0, nkb);
-        const int acc = local & 1;
-        if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1u, abort_flag, err)) break;
-        tc_fence_after();
-        const uint32_t d = tmem + acc * C::ACC_COLS;
-        for (int j = 0; j < nkb; ++j, ++i) {
-          const int st = i % STAGES;
-          if (!mbar_wait(&full[st], (i / STAGES) & 1, abort_flag, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t w0 = smem_u32(smem + st * C::STAGE_BYTES), x0 = w0 + C::W_BYTES;
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_ss(d, desc_kmajor_sw128(w0 + k * 32), desc_kmajor_sw128(x0 + k * 32), idesc, (j | k) != 0);
-          mma_commit(&empty[st]);
+      for (int j = 0; j < nkb; ++j) {
+        const int st = j % STAGES;
+        if (!mbar_wait(&full[st], (j / STAGES) & 1, abort_flag, err)) {
+          ok = false;
+          break;
         }
-        if (ok) mma_commit(&tfull[acc]);
+        tc_fence_after();
+        const uint32_t w0 = smem_u32(smem + st * C::STAGE_BYTES), x0 = w0 + C::W_BYTES;
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          mma_bf16_ss(tmem, desc_kmajor_sw128(w0 + k * 32), desc_kmajor_sw128(x0 + k * 32), idesc, (j | k) != 0);
+        mma_commit(&empty[st]);
       }
+      if (ok) mma_commit(tfull);
+      // all MMAs must be done before TMEM is released
       mma_commit(drain);
       volatile int no_abort = 0;
       mbar_wait(drain, 0, &no_abort, err);
     }
   } else {
-    // lane l of warp w holds output feature 32·(w%4) + l of the tile for all
-    // NT tokens; the accumulator is released as soon as it is in registers
+    pdl_wait();
+    const int ew = warp - 2;                 // 0..3
+    // While the MMAs run: the row inputs of the tokens this CTA will reduce,
+    // one thread per token (positions; the second norm's scale from the Σh²
+    // partials; ...), and with RMSNorm-1's statistics Σx² of every token
+    // over this CTA's K range.
+    for (int t = t0 + (int)threadIdx.x - 64; t < t1; t += 128) {
+      bool have = false;
+      if constexpr (Epi::kRowStats) {
+        if (epi.a.st.x) {
+          ra_s[t - t0] = epi.row_aux_pos(t);
+          have = true;
+        }
+      }
+      if (!have) ra_s[t - t0] = epi.row_aux(t);
+    }
+    if constexpr (Epi::kRowStats) {
+      if (epi.a.st.x) {
+        constexpr int TPW = NT / 4;
+        float ss[TPW];
+        epi.template row_stats_ranges<TPW>(ew, 4, M, kb0 * kBK, (kb0 + nkb) * kBK, lane, ss);
+#pragma unroll
+        for (int j = 0; j < TPW; ++j)
+          if (lane == 0 && ew + 4 * j < M) ssq_s[ew + 4 * j] = ss[j];
+      }
+    }
+    // lane l of warp w holds output feature 32·(w%4) + l of the tile for all NT tokens
     const int quad = warp & 3;
-    int local = 0;
-    for (int w = blockIdx.x; w < items; w += gridDim.x, ++local) {
-      const int acc = local & 1;
-      if (!mbar_wait_warp(&tfull[acc], (local >> 1) & 1, abort_flag, err)) break;
+    if (mbar_wait_warp(tfull, 0, abort_flag, err)) {
       tc_fence_after();
       uint32_t u[NT];
 #pragma unroll
       for (int c = 0; c < NT; c += 16)
-        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + acc * C::ACC_COLS + c,
-                  *reinterpret_cast<uint32_t(*)[16]>(u + c));
+        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + c, *reinterpret_cast<uint32_t(*)[16]>(u + c));
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      const int n = (w % tiles) * kRows + quad * 32 + lane;
-      if (n < N) {
-        float* dst = part + (size_t)(w / tiles) * M * N + n;
+      const int f = quad * 32 + lane;
 #pragma unroll
-        for (int m = 0; m < NT; ++m)
-          if (m < M) dst[(size_t)m * N] = __uint_as_float(u[m]);
+      for (int t = 0; t < NT; ++t) part_s[t * kRows + f] = __uint_as_float(u[t]);
+    }
+  }
+
+  // the partials of every CTA of the cluster are in shared memory
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync();
+
+  if (warp >= 2) {
+    const int col = tile * kRows + 4 * lane;
+    const uint32_t part_base = smem_u32(part_s) + 16u * lane, ssq_base = smem_u32(ssq_s);
+    constexpr int kMaxSplits = 8;
+    for (int m = t0 + (warp - 2); m < t1; m += 4) {
+      // the epilogue's global inputs first (they do not depend on the sums),
+      // then this token's four columns from every CTA of the cluster
+      RowAux ra = ra_s[m - t0];
+      typename Epi::Aux ax{};
+      if (col < N) ax = epi.aux(m, col, ra);
+      float4 p[kMaxSplits];
+      float q[kMaxSplits];
+#pragma unroll
+      for (int r = 0; r < kMaxSplits; ++r) {
+        if (r < splits) {
+          p[r] = ld_dsmem_f4(mapa_shared(part_base + (uint32_t)(m * kRows * 4), (uint32_t)r));
+          q[r] = 0.f;
+          if constexpr (Epi::kRowStats) {
+            if (epi.a.st.x) q[r] = ld_dsmem_f32(mapa_shared(ssq_base + (uint32_t)(m * 4), (uint32_t)r));
+          }
+        }
+      }
+      // summed in rank order
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float ss = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxSplits; ++r) {
+        if (r < splits) {
+          acc.x += p[r].x;
+          acc.y += p[r].y;
+          acc.z += p[r].z;
+          acc.w += p[r].w;
+          ss += q[r];
+        }
+      }
+      if constexpr (Epi::kRowStats) {
+        // the token's reducer in the cluster of tile 0 publishes its position and flags
+        if (epi.a.st.x) epi.row_stats_finish(ra, m, ss, tile == 0 && lane == 0);
+      }
+      if constexpr (Epi::kRowDone) {
+        if (tile == 0 && lane == 0) epi.row_done(m);
+      }
+      float rsum = 0.f;
+      if (col < N) {
+        float v[4] = {acc.x, acc.y, acc.z, acc.w};
+        rsum = epi(m, col, v, ra, ax);
+      }
+      if constexpr (Epi::kRowReduce) {
+        // this tile's share of the token's row sum is partial `tile`
+        const RowSum& rs = epi.row_sums();
+        rsum = warp_sum(rsum);
+        if (lane == 0) rs.part[(size_t)m * rs.stride + tile] = rsum;
       }
     }
   }
 
+  // no CTA leaves (and frees its shared memory) while another still reads it
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-// Sum of the K-range partials of 4 consecutive outputs of one token, then the
-// fused epilogue.  Rows (tokens) are blockIdx.y, so a row reduction (Σh² of
-// the Wo epilogue) is one partial per warp.  With RMSNorm-1 statistics in the
-// QKV epilogue (kRowStats, a.st.x set) every CTA of row m first forms the
-// row's Σx² itself (the row is a few KB, read from L2 by each of the row's
-// CTAs) in a fixed order: per thread, per warp, then warps in order.
-constexpr int kEpiWarps = 8;                 // warps per CTA of the partial-sum epilogue (256 threads)
+}  // namespace
 
-template <class Epi>
-__global__ void __launch_bounds__(256)
-    k_splitk_epilogue(const float* __restrict__ part, int splits, int M, int N, Epi epi) {
-  pdl_trigger();
-  pdl_wait();
-  const int m = blockIdx.y;
-  const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  float r = 0.f;
-  typename Epi::RowAux ra_stats{};
-  bool have_stats = false;
-  if constexpr (Epi::kRowStats) {
-    if (epi.a.st.x) {
-      __shared__ float s_part[kEpiWarps];
-      __shared__ typename Epi::RowAux s_ra;
-      const float ss = warp_sum(epi.row_stats_partial(m, threadIdx.x, blockDim.x));
-      if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float t = 0.f;
-        for (int w = 0; w < kEpiWarps; ++w) t += s_part[w];
-        s_ra = epi.row_aux_stats(m, t, blockIdx.x == 0);
-      }
-      __syncthreads();
-      ra_stats = s_ra;
-      have_stats = true;
-    }
-  }
-  if constexpr (Epi::kRowDone) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) epi.row_done(m);
-  }
-  if (col < N) {
-    // the first eight partials are requested before the epilogue's own inputs
-    // (which may depend on one another), so all of them are in flight together
-    constexpr int U = 8;
-    float4 a[U];
-    const float* p = part + (size_t)m * N + col;
-    const size_t stride = (size_t)M * N;
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      a[u] = u < splits ? *reinterpret_cast<const float4*>(p + (size_t)u * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const auto ra = have_stats ? ra_stats : epi.row_aux(m);
-    const auto ax = epi.aux(m, col, ra);
-    int sp = U;
-    for (; sp + U <= splits; sp += U) {
-      float4 t[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) t[u] = *reinterpret_cast<const float4*>(p + (size_t)(sp + u) * stride);
-#pragma unroll
-      for (int u = 0; u < U; ++u) a[u] = make_float4(a[u].x + t[u].x, a[u].y + t[u].y, a[u].z + t[u].z, a[u].w + t[u].w);
-    }
-    for (int u = 0; sp < splits; ++sp, ++u) {
-      const float4 t = *reinterpret_cast<const float4*>(p + (size_t)sp * stride);
-      a[u] = make_float4(a[u].x + t.x, a[u].y + t.y, a[u].z + t.z, a[u].w + t.w);
-    }
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      v[0] += a[u].x;
-      v[1] += a[u].y;
-      v[2] += a[u].z;
-      v[3] += a[u].w;
-    }
-    r = epi(m, col, v, ra, ax);
-  }
-  if constexpr (Epi::kRowReduce) {
-    // each warp's share of row m is one partial
-    const RowSum& rs = epi.row_sums();
-    r = warp_sum(r);
-    if ((threadIdx.x & 31) == 0) rs.part[(size_t)m * rs.stride + blockIdx.x * kEpiWarps + (threadIdx.x >> 5)] = r;
-  }
+// K ranges per weight tile (the cluster size): the largest power of two that
+// one wave of the resident CTAs (two per SM) allows, at most 8 (a portable
+// cluster), with at least 4 K blocks (64 KB of weights) per CTA.  (Measured on
+// the decode QKV GEMM, 48 tiles at 152 SMs: clusters of 4, 6 and 8 took 18.6,
+// 25.0 and 22.9 us.)
+int skinny_split_count(int tiles, int kblocks, int slots) {
+  if (tiles <= 0 || kblocks <= 0 || slots <= 0) return -1;
+  int lim = slots / tiles;
+  if (lim > kblocks / 4) lim = kblocks / 4;
+  int sp = 1;
+  while (2 * sp <= lim && 2 * sp <= 8) sp *= 2;
+  return sp;
 }
 
-int split_count(int tiles, int kblocks) { return skinny_split_count(tiles, kblocks, 2 * sm_count()); }
+namespace {
 
 template <int NT, class Epi>
-cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi& epi, float* part, cudaStream_t s) {
+cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi& epi, cudaStream_t s) {
   using C = SkCfg<NT>;
   CUtensorMap tw, tx;
   cudaError_t e = make_tmap_2d_bf16(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBK, kRows);
@@ -301,81 +300,67 @@ cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi&
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(k_gemm_skinny<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    e = cudaFuncSetAttribute(k_gemm_skinny<NT, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const int tiles = (N + kRows - 1) / kRows, kblocks = K / kBK;
-  const int splits = split_count(tiles, kblocks);
-  const int items = tiles * splits, slots = 2 * sm_count();
-  e = launch_pdl(k_gemm_skinny<NT>, dim3(items < slots ? items : slots), dim3(192), C::SMEM, s, tw, tx, M, N, tiles,
-                 kblocks, splits, part, device_error_word());
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k_splitk_epilogue<Epi>, dim3((N / 4 + 255) / 256, M), dim3(32 * kEpiWarps), 0, s,
-                    (const float*)part, splits, M, N, epi);
+  const int sp = skinny_split_count(tiles, kblocks, 2 * sm_count());
+  // a cluster of sp CTAs per weight tile, launched as a programmatic
+  // dependent of the previous kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles * sp);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = sp;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_gemm_skinny<NT, Epi>, tw, tx, M, N, kblocks, sp, epi, device_error_word());
 }
 
 template <class Epi>
-cudaError_t run(const void* X, const void* W, int M, int N, int K, const Epi& epi, float* part, cudaStream_t s) {
+cudaError_t run(const void* X, const void* W, int M, int N, int K, const Epi& epi, cudaStream_t s) {
   if (M <= 0 || N <= 0) return cudaSuccess;
-  if (M > kMaxTok || K % kBK != 0 || N % 4 != 0 || !part) return cudaErrorInvalidValue;
-  if (M <= 16) return run_nt<16>(X, W, M, N, K, epi, part, s);
-  if (M <= 32) return run_nt<32>(X, W, M, N, K, epi, part, s);
-  if (M <= 48) return run_nt<48>(X, W, M, N, K, epi, part, s);
-  return run_nt<64>(X, W, M, N, K, epi, part, s);
+  if (M > kMaxTok || K % kBK != 0 || N % 4 != 0) return cudaErrorInvalidValue;
+  if (M <= 16) return run_nt<16>(X, W, M, N, K, epi, s);
+  if (M <= 32) return run_nt<32>(X, W, M, N, K, epi, s);
+  if (M <= 48) return run_nt<48>(X, W, M, N, K, epi, s);
+  return run_nt<64>(X, W, M, N, K, epi, s);
 }
 
 }  // namespace
 
-// K ranges per weight tile.  Items are equal in size, so the time is the
-// number of item waves over the resident CTAs (two per SM): take the split
-// count whose item count fills its last wave best (fewest splits on a tie),
-// with at least 4 K blocks (64 KB of weights) per item and at most kMaxItems
-// items.  The partials (items × 128 × M floats) stay in L2 between the two
-// kernels.
-int skinny_split_count(int tiles, int kblocks, int slots) {
-  if (tiles <= 0 || kblocks <= 0 || slots <= 0) return -1;
-  int spmax = kblocks / 4;
-  if (spmax > kMaxItems / tiles) spmax = kMaxItems / tiles;
-  int best = 1;
-  double best_fill = 0.0;
-  for (int sp = 1; sp <= spmax; ++sp) {
-    const long long items = (long long)tiles * sp, waves = (items + slots - 1) / slots;
-    const double fill = (double)items / (double)(waves * slots);
-    if (fill > best_fill + 1e-3) best = sp, best_fill = fill;
-  }
-  return best;
-}
-
 int skinny_max_tokens() { return kMaxTok; }
 
-size_t skinny_part_floats(int M, int max_n) {
-  const size_t tiles = (size_t)(max_n + kRows - 1) / kRows;
-  return (size_t)M * kRows * (tiles > (size_t)kMaxItems ? tiles : (size_t)kMaxItems);
-}
-
 cudaError_t gemm_skinny_qkv(const void* A, const void* B, int M, int N, int K, const Dims& D, const QKVArgs& e,
-                            float* part, cudaStream_t s) {
-  return run(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, part, s);
+                            cudaStream_t s) {
+  return run(A, B, M, N, K, EpiQKV<bf16>{e, D.H, D.Hkv, D.dh, log2_dh(D.dh)}, s);
 }
 cudaError_t gemm_skinny_wo(const void* A, const void* B, int M, int N, int K, const Dims& D, const WoArgs& e,
-                           float* part, cudaStream_t s, int* row_parts) {
-  // one Σh² partial per row and epilogue warp (128 columns)
-  if (row_parts) *row_parts = (N / 4 + 255) / 256 * kEpiWarps;
-  return run(A, B, M, N, K, EpiWo<bf16>{e, D.d}, part, s);
+                           cudaStream_t s, int* row_parts) {
+  // one Σh² partial per row and 128-column weight tile
+  if (row_parts) *row_parts = (N + kRows - 1) / kRows;
+  return run(A, B, M, N, K, EpiWo<bf16>{e, D.d}, s);
 }
 cudaError_t gemm_skinny_w13(const void* A, const void* B, int M, int N, int K, const Dims& D, const W13Args& e,
-                            float* part, cudaStream_t s) {
-  return run(A, B, M, N, K, EpiW13<bf16>{e, D.d, D.f, D.eps}, part, s);
+                            cudaStream_t s) {
+  return run(A, B, M, N, K, EpiW13<bf16>{e, D.d, D.f, D.eps}, s);
 }
 cudaError_t gemm_skinny_w2(const void* A, const void* B, int M, int N, int K, const Dims& D, const W2Args& e,
-                           float* part, cudaStream_t s) {
-  return run(A, B, M, N, K, EpiW2<>{e, D.d}, part, s);
+                           cudaStream_t s) {
+  return run(A, B, M, N, K, EpiW2<>{e, D.d}, s);
 }
 
-cudaError_t gemm_skinny_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e, float* part,
+cudaError_t gemm_skinny_logits(const void* A, const void* B, int M, int N, int K, const LogitsArgs& e,
                                cudaStream_t s) {
-  return run(A, B, M, N, K, EpiLogits{e}, part, s);
+  return run(A, B, M, N, K, EpiLogits{e}, s);
 }
 
 }  // namespace tb

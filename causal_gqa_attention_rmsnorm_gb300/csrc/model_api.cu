@@ -28,13 +28,11 @@ tb_status check_head(const tb_head_cfg* c) {
   return TB_OK;
 }
 
-// Workspace of the head: row scales, one chunk of logits, few-row GEMM
-// partials, and for the fused loss the (max, Σ exp) pairs and target logits
-// of one chunk.
+// Workspace of the head: row scales, one chunk of logits, and for the fused
+// loss the (max, Σ exp) pairs and target logits of one chunk.
 struct HeadWork {
   float* r;
   float* chunk;
-  float* part;
   float2* lse;
   float* tgt;
   int n_parts;
@@ -51,8 +49,6 @@ HeadWork carve_head(const tb_head_cfg* c, int rc, void* base) {
   HeadWork w{};
   w.r = (float*)take((size_t)rc * 4);
   w.chunk = (float*)take((size_t)rc * c->V * 4);
-  w.part = c->dtype == TB_BF16 ? (float*)take(skinny_part_floats(std::min(rc, skinny_max_tokens()), c->V) * 4)
-                               : nullptr;
   w.n_parts = (c->V + lse_tile_cols() - 1) / lse_tile_cols();
   if (c->dtype == TB_BF16) {
     w.lse = (float2*)take((size_t)rc * w.n_parts * sizeof(float2));
@@ -147,7 +143,7 @@ tb_status tb_lm_head(const tb_head_cfg* cfg, const void* packed, const void* x, 
       if (cfg->dtype == TB_F32)
         e = gemm_simt_logits(cfg->dtype, xa, packed, rows, cfg->V, cfg->d, la, s);
       else if (rows <= skinny_max_tokens())
-        e = gemm_skinny_logits(xa, packed, rows, cfg->V, cfg->d, la, W.part, s);
+        e = gemm_skinny_logits(xa, packed, rows, cfg->V, cfg->d, la, s);
       else
         e = gemm_tc_logits(xa, packed, rows, cfg->V, cfg->d, la, s);
     }

@@ -148,7 +148,7 @@ struct Work {
   float* part;
   int nchunk_max;
   int chunk;                 // keys per decode work item
-  float* skpart;             // K-split partial sums of the few-token GEMMs (bf16, M ≤ 64)
+  bool few;                  // bf16 with M ≤ 64 tokens: the few-token GEMM
   size_t total;
 };
 
@@ -165,9 +165,8 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
   const size_t M = (size_t)B * (mode == 0 ? T : 1);
   const size_t hd = (size_t)c->H * c->dh, kvd = (size_t)c->Hkv * c->dh;
   w.r = (float*)take(M * 4);
-  // partials per row: one per column tile (tile GEMM, ≥ 128 columns), per
-  // 128-column epilogue warp (few-token epilogue: 8 per 1024 columns) or per
-  // 64 columns (fp32 GEMM)
+  // partials per row: one per column tile (tile GEMM, ≥ 128 columns; few-token
+  // GEMM, 128 columns) or per 64 columns (fp32 GEMM)
   w.ssq_stride = (c->d + 63) / 64 + 8;
   w.ssq_part = (float*)take(M * w.ssq_stride * 4);
   w.pos = (int32_t*)take((size_t)B * 4);
@@ -187,12 +186,7 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
     w.nchunk_max = (T + w.chunk - 1) / w.chunk;
     w.part = (float*)take(decode_part_floats(B, c->H, c->dh, w.nchunk_max) * 4);
   }
-  if (c->dtype == TB_BF16 && M <= (size_t)skinny_max_tokens()) {
-    int max_n = (c->H + 2 * c->Hkv) * c->dh;
-    if (c->d > max_n) max_n = c->d;
-    if (2 * c->f > max_n) max_n = 2 * c->f;
-    w.skpart = (float*)take(skinny_part_floats((int)M, max_n) * 4);
-  }
+  w.few = c->dtype == TB_BF16 && M <= (size_t)skinny_max_tokens();
   w.total = off;
   return w;
 }
@@ -201,20 +195,19 @@ Work carve(const tb_block_cfg* c, int B, int T, int mode, void* base) {
 // with every SM; more tokens to the persistent tile GEMM.
 cudaError_t mm_qkv(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D,
                    const QKVArgs& e, cudaStream_t s) {
-  return W.skpart ? gemm_skinny_qkv(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_qkv(A, Bw, M, N, K, D, e, s);
+  return W.few ? gemm_skinny_qkv(A, Bw, M, N, K, D, e, s) : gemm_tc_qkv(A, Bw, M, N, K, D, e, s);
 }
 cudaError_t mm_wo(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D, const WoArgs& e,
                   cudaStream_t s, int* row_parts) {
-  return W.skpart ? gemm_skinny_wo(A, Bw, M, N, K, D, e, W.skpart, s, row_parts)
-                  : gemm_tc_wo(A, Bw, M, N, K, D, e, s, row_parts);
+  return W.few ? gemm_skinny_wo(A, Bw, M, N, K, D, e, s, row_parts) : gemm_tc_wo(A, Bw, M, N, K, D, e, s, row_parts);
 }
 cudaError_t mm_w13(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D,
                    const W13Args& e, cudaStream_t s) {
-  return W.skpart ? gemm_skinny_w13(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_w13(A, Bw, M, N, K, D, e, s);
+  return W.few ? gemm_skinny_w13(A, Bw, M, N, K, D, e, s) : gemm_tc_w13(A, Bw, M, N, K, D, e, s);
 }
 cudaError_t mm_w2(const Work& W, const void* A, const void* Bw, int M, int N, int K, const Dims& D, const W2Args& e,
                   cudaStream_t s) {
-  return W.skpart ? gemm_skinny_w2(A, Bw, M, N, K, D, e, W.skpart, s) : gemm_tc_w2(A, Bw, M, N, K, D, e, s);
+  return W.few ? gemm_skinny_w2(A, Bw, M, N, K, D, e, s) : gemm_tc_w2(A, Bw, M, N, K, D, e, s);
 }
 
 // The int8 layout's own rules (dh 128, contiguous, 32-row stages, scales).
@@ -389,7 +382,7 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
   // The tile GEMM path (bf16, more tokens than the few-token GEMM takes) forms
   // RMSNorm-1's statistics inside the QKV GEMM; the other paths run the
   // row-statistics kernel first.
-  const bool tile_stats = dt == TB_BF16 && !W.skpart;
+  const bool tile_stats = dt == TB_BF16 && !W.few;
   QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr, paged_of(kv, err)};
   if (tile_stats) {
     TB_TRY(cudaMemsetAsync(W.stat_done, 0, (size_t)(M + kStatRows - 1) / kStatRows * sizeof(int), s));
@@ -472,7 +465,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
   // the step's counters are formed in the QKV GEMM's partial-sum epilogue,
   // and the cache lengths advance in the Wo one; otherwise the row-statistics
   // kernel does all of it first.
-  const bool fused_stats = dt == TB_BF16 && W.skpart;
+  const bool fused_stats = dt == TB_BF16 && W.few;
   if (!fused_stats) {
     rec.stage("rms");
     TB_TRY(launch_row_stats(dt, x, B, cfg->d, cfg->eps, W.r, 1, nullptr, kv->lens, W.pos, kv->T_max, W.counter,

@@ -1,6 +1,7 @@
 """Host-side selection rules of the library, checked without a GPU through
-its test hooks: the few-token GEMM's K-split count and the decode work-item
-size.  Each hook takes the SM count, so the GB300's 152 SMs can be given here."""
+its test hooks: the few-token GEMM's K-split count (its cluster size) and the
+decode work-item size.  Each hook takes the SM count, so the GB300's 152 SMs
+can be given here."""
 import itertools
 import random
 
@@ -9,7 +10,7 @@ import pytest
 from causal_gqa_attention_rmsnorm_gb300 import binding
 
 SMS = 152
-MAX_ITEMS = 1024       # the few-token GEMM's partial buffer holds this many items
+MAX_CLUSTER = 8        # a portable thread-block cluster
 
 
 @pytest.fixture(scope="module")
@@ -17,40 +18,35 @@ def lib():
     return binding.lib()
 
 
-def fill(tiles, sp, slots):
-    items = tiles * sp
-    waves = -(-items // slots)
-    return items / (waves * slots)
-
-
 @pytest.mark.parametrize("name,N,K,expect", [
-    ("qkv", (32 + 2 * 8) * 128, 4096, 6),
-    ("wo", 4096, 4096, 9),
-    ("w13", 2 * 14336, 4096, 4),
-    ("w2", 4096, 14336, 19),
+    ("qkv", (32 + 2 * 8) * 128, 4096, 4),
+    ("wo", 4096, 4096, 8),
+    ("w13", 2 * 14336, 4096, 1),
+    ("w2", 4096, 14336, 8),
 ])
 def test_split_counts_of_the_decode_gemms(lib, name, N, K, expect):
     """The counts the decode step of the GQA block uses at 152 SMs."""
     assert lib.tbx_skinny_split_count(N // 128, K // 64, 2 * SMS) == expect
 
 
-def test_split_count_fills_its_last_wave_best(lib):
-    """Against the stated rule: among the allowed counts (at least four K
-    blocks per item, at most MAX_ITEMS items) the result fills its last wave
-    as well as the best one, up to the rule's tie margin of 1e-3."""
+def test_split_count_rule(lib):
+    """Against the stated rule: the largest power of two that one wave of the
+    resident CTAs allows, at most a portable cluster, at least four K blocks
+    per CTA, and never fewer than one."""
     rng = random.Random(0)
-    cases = [(t, kb, s) for t, kb, s in itertools.product([1, 3, 16, 32, 48, 224, 1002], [4, 7, 64, 224, 448],
+    cases = [(t, kb, s) for t, kb, s in itertools.product([1, 3, 16, 32, 48, 224, 1002], [1, 4, 7, 64, 224, 448],
                                                            [2, 304, 160])]
     cases += [(rng.randint(1, 1100), rng.randint(1, 600), rng.randint(1, 400)) for _ in range(300)]
     for tiles, kblocks, slots in cases:
         sp = lib.tbx_skinny_split_count(tiles, kblocks, slots)
-        spmax = min(kblocks // 4, MAX_ITEMS // tiles)
-        if spmax < 1:
-            assert sp == 1
-            continue
-        assert 1 <= sp <= spmax
-        best = max(fill(tiles, s, slots) for s in range(1, spmax + 1))
-        assert fill(tiles, sp, slots) >= best - 1e-3 - 1e-12
+        assert 1 <= sp <= MAX_CLUSTER
+        lim = min(slots // tiles, MAX_CLUSTER, kblocks // 4)
+        assert sp & (sp - 1) == 0                     # a power of two
+        assert sp == 1 or sp <= lim
+        assert 2 * sp > lim or 2 * sp > MAX_CLUSTER   # the largest one
+        if sp > 1:
+            assert tiles * sp <= slots          # one wave
+            assert kblocks // sp >= 4
 
 
 def test_split_count_rejects_empty_shapes(lib):
