@@ -38,8 +38,9 @@ constexpr int kMaxTok = 64;
 
 // Shared-memory plan: the stage ring, whose first NT × 128 floats hold the
 // partial tile after the main loop, then the barriers and Σx² partials.
-template <int NT> struct SkCfg {
-  static constexpr int STAGES = NT <= 32 ? 5 : 4;           // two CTAs per SM
+template <int NT, int CPS = 2> struct SkCfg {
+  // CPS CTAs per SM: two with a 4-5 stage ring, or three with a 3-stage one
+  static constexpr int STAGES = CPS == 3 ? 3 : (NT <= 32 ? 5 : 4);
   static constexpr uint32_t W_BYTES = kRows * kBK * 2;       // 16 KB
   static constexpr uint32_t X_BYTES = NT * kBK * 2;
   static constexpr uint32_t STAGE_BYTES = W_BYTES + X_BYTES;
@@ -53,11 +54,11 @@ template <int NT> struct SkCfg {
   static_assert(NT * kRows * 4 <= OFF_BAR, "the partial tile reuses the stage ring");
 };
 
-template <int NT, class Epi>
-__global__ void __launch_bounds__(192, 2)
+template <int NT, class Epi, int CPS>
+__global__ void __launch_bounds__(192, CPS)
     k_gemm_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M, int N,
                   int kblocks, int splits, Epi epi, int* err) {
-  using C = SkCfg<NT>;
+  using C = SkCfg<NT, CPS>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -288,24 +289,19 @@ int skinny_split_count(int tiles, int kblocks, int slots) {
 
 namespace {
 
-template <int NT, class Epi>
-cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi& epi, cudaStream_t s) {
-  using C = SkCfg<NT>;
-  CUtensorMap tw, tx;
-  cudaError_t e = make_tmap_2d_bf16(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBK, kRows);
-  if (e != cudaSuccess) return e;
-  e = make_tmap_2d_bf16(&tx, X, (uint64_t)M, (uint64_t)K, (uint64_t)K, kBK, NT);
-  if (e != cudaSuccess) return e;
+template <int NT, class Epi, int CPS>
+cudaError_t launch_nt(const CUtensorMap& tw, const CUtensorMap& tx, int M, int N, int tiles, int kblocks, int sp,
+                      const Epi& epi, cudaStream_t s) {
+  using C = SkCfg<NT, CPS>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(k_gemm_skinny<NT, Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_gemm_skinny<NT, Epi, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int tiles = (N + kRows - 1) / kRows, kblocks = K / kBK;
-  const int sp = skinny_split_count(tiles, kblocks, 2 * sm_count());
   // a cluster of sp CTAs per weight tile, launched as a programmatic
   // dependent of the previous kernel
   cudaLaunchConfig_t cfg = {};
@@ -322,7 +318,27 @@ cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi&
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemm_skinny<NT, Epi>, tw, tx, M, N, kblocks, sp, epi, device_error_word());
+  return cudaLaunchKernelEx(&cfg, k_gemm_skinny<NT, Epi, CPS>, tw, tx, M, N, kblocks, sp, epi, device_error_word());
+}
+
+template <int NT, class Epi>
+cudaError_t run_nt(const void* X, const void* W, int M, int N, int K, const Epi& epi, cudaStream_t s) {
+  CUtensorMap tw, tx;
+  cudaError_t e = make_tmap_2d_bf16(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kBK, kRows);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d_bf16(&tx, X, (uint64_t)M, (uint64_t)K, (uint64_t)K, kBK, NT);
+  if (e != cudaSuccess) return e;
+  const int tiles = (N + kRows - 1) / kRows, kblocks = K / kBK;
+  // Three CTAs per SM (3-stage rings) when that allows a larger split in one
+  // wave: more weight bytes in flight over the GPU (decode W1/W3: 224 tiles,
+  // one CTA each on two per SM, two each on three per SM).  Measured on the
+  // decode step of 32 tokens at d = 4096: 266.6 -> 263.8 us as a graph.
+  const int sp2 = skinny_split_count(tiles, kblocks, 2 * sm_count());
+  if constexpr (NT <= 32) {
+    const int sp3 = skinny_split_count(tiles, kblocks, 3 * sm_count());
+    if (sp3 > sp2) return launch_nt<NT, Epi, 3>(tw, tx, M, N, tiles, kblocks, sp3, epi, s);
+  }
+  return launch_nt<NT, Epi, 2>(tw, tx, M, N, tiles, kblocks, sp2, epi, s);
 }
 
 template <class Epi>

@@ -25,8 +25,21 @@ def lib():
     ("w2", 4096, 14336, 8),
 ])
 def test_split_counts_of_the_decode_gemms(lib, name, N, K, expect):
-    """The counts the decode step of the GQA block uses at 152 SMs."""
+    """The counts for two CTAs per SM at 152 SMs."""
     assert lib.tbx_skinny_split_count(N // 128, K // 64, 2 * SMS) == expect
+
+
+@pytest.mark.parametrize("name,N,K,two,three", [
+    ("qkv", (32 + 2 * 8) * 128, 4096, 4, 8),
+    ("wo", 4096, 4096, 8, 8),
+    ("w13", 2 * 14336, 4096, 1, 2),
+    ("w2", 4096, 14336, 8, 8),
+])
+def test_decode_gemms_take_three_ctas_per_sm_for_a_larger_split(lib, name, N, K, two, three):
+    """The launcher runs three CTAs per SM when that allows a larger split in
+    one wave: the decode QKV and W1/W3 GEMMs; Wo and W2 keep two."""
+    assert lib.tbx_skinny_split_count(N // 128, K // 64, 2 * SMS) == two
+    assert lib.tbx_skinny_split_count(N // 128, K // 64, 3 * SMS) == three
 
 
 def test_split_count_rule(lib):
