@@ -155,7 +155,8 @@ class KVCache:
     Paged (block_table given): k, v page pools [num_pages, Hkv, page_size, dh]
     and block_table int32 [B, T_max / page_size].  int8 (k, v of torch.int8):
     codes [B, Hkv, T_max, dh] with fp32 row scales k_scale, v_scale
-    [B, Hkv, T_max].  lens int32 [B]."""
+    [B, Hkv, T_max], or paged: code pools [num_pages, Hkv, page_size, dh] and
+    scale pools [num_pages, Hkv, page_size].  lens int32 [B]."""
     k: torch.Tensor
     v: torch.Tensor
     lens: torch.Tensor
@@ -188,7 +189,7 @@ class KVCache:
             for name, t in (("k_scale", self.k_scale), ("v_scale", self.v_scale)):
                 if t is None:
                     raise ValueError(f"an int8 cache needs {name}")
-                _need(t, name, torch.float32, (B, Hkv, T_max))
+                _need(t, name, torch.float32, (B, Hkv, T_max) if bt is None else (npages, Hkv, ps))
             ks, vs = self.k_scale.data_ptr(), self.v_scale.data_ptr()
         return tb_kvcache(self.k.data_ptr(), self.v.data_ptr(), self.lens.data_ptr(), B, Hkv, T_max, dh, dt,
                           None if bt is None else bt.data_ptr(), ps, npages, ks, vs)

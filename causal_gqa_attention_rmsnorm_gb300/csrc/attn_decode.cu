@@ -731,7 +731,8 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
     k_decode_i8(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                 const float* __restrict__ kscale, const float* __restrict__ vscale, const bf16* __restrict__ q,
                 const int32_t* __restrict__ pos_arr, int B, int Hkv, int T_max, float* __restrict__ part,
-                int nchunk_max, int chunk, int* __restrict__ counter, int window, float scale_log2, int* err) {
+                int nchunk_max, int chunk, int* __restrict__ counter, int window, PagedKV pg, float scale_log2,
+                int* err) {
   pdl_trigger();
   pdl_wait();
   constexpr int DH = 128, S = kQSlots;
@@ -812,10 +813,23 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
       uint8_t* dst = smem + pw * C::WARP_BYTES + sl * C::SLOT;
       float* sc = reinterpret_cast<float*>(smem + C::OFF_SC + bi * C::SC);
       mbar_arrive_expect_tx(&full[bi], C::TX);
-      const int key = pkey0 + pst * kQKeys, plane = pb * Hkv + pkvh;
-      tma_load_3d_hint(&tmK, dst, &full[bi], 0, key, plane, pol);
-      tma_load_3d_hint(&tmV, dst + C::BOX, &full[bi], 0, key, plane, pol);
-      const size_t srow = (size_t)plane * T_max + key;
+      const int key = pkey0 + pst * kQKeys;
+      int plane = pb * Hkv + pkvh, y = key;
+      size_t srow = (size_t)plane * T_max + key;
+      if (pg.bt) {       // paged: a 32-key stage lies inside one page (page_size a multiple of 32)
+        const int page = pg.bt[(size_t)pb * pg.max_pages + key / pg.ps];
+        y = key % pg.ps;
+        if (page < 0 || page >= pg.num_pages) {
+          atomicOr(err, TB_DEVERR_BAD_PAGE);
+          plane = pg.num_pages * Hkv;   // outside the pool: the code copies read zeros
+          srow = 0;                     // and the scales come from the pool's first row
+        } else {
+          plane = page * Hkv + pkvh;
+          srow = (size_t)plane * pg.ps + y;
+        }
+      }
+      tma_load_3d_hint(&tmK, dst, &full[bi], 0, y, plane, pol);
+      tma_load_3d_hint(&tmV, dst + C::BOX, &full[bi], 0, y, plane, pol);
       bulk_load_hint(sc, kscale + srow, kQKeys * 4, &full[bi], pol);
       bulk_load_hint(sc + kQKeys, vscale + srow, kQKeys * 4, &full[bi], pol);
       ++pst;
@@ -1047,13 +1061,15 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
 template <int G>
 cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
                           const int32_t* pos, int B, int Hkv, int T_max, float* part, int nchunk_max, int chunk,
-                          int* counter, int window, void* o, cudaStream_t s) {
+                          int* counter, int window, const PagedKV& pg, void* o, cudaStream_t s) {
   using C = QCfg;
   CUtensorMap tk, tv;
-  const uint64_t planes = (uint64_t)B * Hkv;
-  cudaError_t e = make_tmap_3d_u8(&tk, kc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kQKeys);
+  // contiguous: (sequence, KV head) planes of T_max rows; paged: (page, KV head) planes of page_size rows
+  const uint64_t planes = pg.bt ? (uint64_t)pg.num_pages * Hkv : (uint64_t)B * Hkv;
+  const uint64_t rows = pg.bt ? (uint64_t)pg.ps : (uint64_t)T_max;
+  cudaError_t e = make_tmap_3d_u8(&tk, kc, planes, rows, 128, 128, rows * 128, 128, kQKeys);
   if (e != cudaSuccess) return e;
-  e = make_tmap_3d_u8(&tv, vc, planes, (uint64_t)T_max, 128, 128, (uint64_t)T_max * 128, 128, kQKeys);
+  e = make_tmap_3d_u8(&tv, vc, planes, rows, 128, 128, rows * 128, 128, kQKeys);
   if (e != cudaSuccess) return e;
   const size_t smem = C::OFF_PRE + (size_t)(2 * B + 1) * 4 + 1024;
   if (smem > 232448) return cudaErrorInvalidValue;
@@ -1067,7 +1083,7 @@ cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const f
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
   e = launch_pdl(k_decode_i8<G>, dim3(sm_count()), dim3(kQWarps * 32), smem, s, tk, tv, ks, vs, (const bf16*)q, pos, B,
-                 Hkv, T_max, part, nchunk_max, chunk, counter, window, scale_log2, device_error_word());
+                 Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, scale_log2, device_error_word());
   if (e != cudaSuccess) return e;
   return launch_pdl(k_decode_combine<bf16, 128>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
                     nchunk_max, chunk, window, kQKeys, (bf16*)o);
@@ -1185,17 +1201,17 @@ int decode_chunk_keys_sms(int dtype, int B, int Hkv, int T_max, int sms) {
 
 cudaError_t attn_decode_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
                            const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max, int chunk,
-                           int* work_counter, int window, void* o, cudaStream_t s) {
-  if (chunk % kQKeys) return cudaErrorInvalidValue;
+                           int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s) {
+  if (chunk % kQKeys || (pg.bt && pg.ps % kQKeys)) return cudaErrorInvalidValue;
   switch (H / Hkv) {
     case 1: return run_stream_i8<1>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
-                                         window, o, s);
+                                         window, pg, o, s);
     case 2: return run_stream_i8<2>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
-                                         window, o, s);
+                                         window, pg, o, s);
     case 4: return run_stream_i8<4>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
-                                         window, o, s);
+                                         window, pg, o, s);
     case 8: return run_stream_i8<8>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
-                                         window, o, s);
+                                         window, pg, o, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -326,6 +326,6 @@ cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc
 // scales ks, vs [B, Hkv, T_max]; bf16 q and o.
 cudaError_t attn_decode_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
                            const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max,
-                           int chunk, int* work_counter, int window, void* o, cudaStream_t s);
+                           int chunk, int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s);
 
 }  // namespace tb

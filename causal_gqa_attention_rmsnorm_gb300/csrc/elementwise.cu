@@ -179,11 +179,15 @@ __device__ __forceinline__ void quantize_row128(const bf16* __restrict__ x, int8
 }
 
 // k and v rows [B, Hkv, rows, 128] -> cache rows start[b] + r of codes
-// [B, Hkv, T_max, 128] and scales [B, Hkv, T_max].  A sequence whose start is
-// negative (a skipped decode row) or whose rows would pass T_max is left alone.
+// [B, Hkv, T_max, 128] and scales [B, Hkv, T_max], or, paged (pg.bt set), of
+// the page pools [num_pages, Hkv, page_size, 128] and [num_pages, Hkv,
+// page_size] at the pages the block table names.  A sequence whose start is
+// negative (a skipped decode row) or whose rows would pass T_max is left
+// alone; a page id outside the pool is never written through and sets
+// TB_DEVERR_BAD_PAGE.
 __global__ void k_quantize_kv(const bf16* __restrict__ kn, const bf16* __restrict__ vn, int rows,
                               const int32_t* __restrict__ start, int Hkv, int T_max, int8_t* __restrict__ kq,
-                              float* __restrict__ ks, int8_t* __restrict__ vq, float* __restrict__ vs) {
+                              float* __restrict__ ks, int8_t* __restrict__ vq, float* __restrict__ vs, PagedKV pg) {
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -192,7 +196,14 @@ __global__ void k_quantize_kv(const bf16* __restrict__ kn, const bf16* __restric
   const int t0 = start ? start[b] : 0;
   if (t0 < 0 || t0 + rows > T_max) return;
   const size_t src = (((size_t)b * Hkv + h) * rows + r) * 128;
-  const size_t row = ((size_t)b * Hkv + h) * T_max + t0 + r;
+  size_t row;
+  if (pg.bt) {
+    const long long pr = paged_row(pg, Hkv, b, h, t0 + r);
+    if (pr < 0) return;
+    row = (size_t)pr;
+  } else {
+    row = ((size_t)b * Hkv + h) * T_max + t0 + r;
+  }
   quantize_row128(kn + src, kq + row * 128, ks + row, lane);
   quantize_row128(vn + src, vq + row * 128, vs + row, lane);
 }
@@ -257,8 +268,18 @@ cudaError_t launch_quantize_kv(const tb_kvcache& kv, const void* k_new, const vo
   if (kv.B > 65535 || kv.Hkv > 65535) return cudaErrorInvalidValue;
   const int warps = std::min(rows, 8);
   const dim3 grid((unsigned)((rows + warps - 1) / warps), kv.Hkv, kv.B);
+  PagedKV pg;
+  if (kv.block_table) {
+    pg.k = kv.k;
+    pg.v = kv.v;
+    pg.bt = kv.block_table;
+    pg.ps = kv.page_size;
+    pg.max_pages = kv.T_max / kv.page_size;
+    pg.num_pages = kv.num_pages;
+    pg.err = device_error_word();
+  }
   return launch_pdl(k_quantize_kv, grid, dim3(32 * warps), 0, s, (const bf16*)k_new, (const bf16*)v_new, rows,
-                    start, kv.Hkv, kv.T_max, (int8_t*)kv.k, kv.k_scale, (int8_t*)kv.v, kv.v_scale);
+                    start, kv.Hkv, kv.T_max, (int8_t*)kv.k, kv.k_scale, (int8_t*)kv.v, kv.v_scale, pg);
 }
 
 cudaError_t launch_kv_append(int dtype, const tb_kvcache& kv, const void* k_new, const void* v_new, int n,

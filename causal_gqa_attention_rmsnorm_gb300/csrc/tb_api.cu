@@ -213,8 +213,9 @@ cudaError_t mm_w2(const Work& W, const void* A, const void* Bw, int M, int N, in
 // The int8 layout's own rules (dh 128, contiguous, 32-row stages, scales).
 tb_status check_i8(const tb_kvcache* kv) {
   if (kv->dh != 128) return fail(TB_ERR_UNSUPPORTED, "an int8 cache needs dh 128 (dh=%d)", kv->dh);
-  if (kv->block_table) return fail(TB_ERR_UNSUPPORTED, "an int8 cache is contiguous (no block table)");
   if (kv->T_max % 32) return fail(TB_ERR_UNSUPPORTED, "an int8 cache needs T_max a multiple of 32 (%d)", kv->T_max);
+  if (kv->block_table && kv->page_size % 32)
+    return fail(TB_ERR_UNSUPPORTED, "a paged int8 cache needs page_size a multiple of 32 (%d)", kv->page_size);
   if (!kv->k_scale || !kv->v_scale || !aligned16(kv->k_scale) || !aligned16(kv->v_scale))
     return fail(TB_ERR_INVALID_ARG, "an int8 cache needs 16-byte aligned k_scale and v_scale");
   return TB_OK;
@@ -383,7 +384,8 @@ tb_status tb_block_prefill(const tb_block_cfg* cfg, const void* packed, const vo
   // RMSNorm-1's statistics inside the QKV GEMM; the other paths run the
   // row-statistics kernel first.
   const bool tile_stats = dt == TB_BF16 && !W.few;
-  QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr, paged_of(kv, err)};
+  // (an int8 cache, paged or not, gets its codes from the quantiser, never the rows)
+  QKVArgs qa{W.r, P.rope, W.q, kbuf, vbuf, T, kv_stride, nullptr, i8_cache ? PagedKV() : paged_of(kv, err)};
   if (tile_stats) {
     TB_TRY(cudaMemsetAsync(W.stat_done, 0, (size_t)(M + kStatRows - 1) / kStatRows * sizeof(int), s));
     qa.ts = TileStats{x, cfg->d, cfg->eps, W.r, W.stat_done, kv ? kv->lens : nullptr, T, stat_poll_ns()};
@@ -472,11 +474,11 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
                             err, s));
   }
   const PagedKV pg = paged_of(kv, err);
-  // an int8 cache gets the new rows through the workspace and the quantiser
+  // an int8 cache (paged or not) gets the new rows through the workspace and the quantiser
   const bool i8 = kv->dtype == TB_I8;
-  void* knew = pg.bt ? nullptr : (i8 ? W.k : kv->k);
-  void* vnew = pg.bt ? nullptr : (i8 ? W.v : kv->v);
-  QKVArgs qa{W.r, P.rope, W.q, knew, vnew, 1, i8 ? 1 : kv->T_max, W.pos, pg, i8};
+  void* knew = i8 ? W.k : (pg.bt ? nullptr : kv->k);
+  void* vnew = i8 ? W.v : (pg.bt ? nullptr : kv->v);
+  QKVArgs qa{W.r, P.rope, W.q, knew, vnew, 1, i8 ? 1 : kv->T_max, W.pos, i8 ? PagedKV() : pg, i8};
   WoArgs wa{x, W.h, W.hb, RowSum{W.ssq_part, W.ssq_stride, 0}};
   if (fused_stats) {
     qa.st = QKVStats{x, cfg->d, cfg->eps, kv->lens, W.pos, kv->T_max, W.counter, err};
@@ -505,7 +507,7 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
       TB_TRY(launch_quantize_kv(*kv, W.k, W.v, 1, W.pos, s));
       rec.stage("attn");
       TB_TRY(attn_decode_i8(W.q, kv->k, kv->v, kv->k_scale, kv->v_scale, W.pos, B, cfg->H, cfg->Hkv, kv->T_max,
-                            W.part, W.nchunk_max, W.chunk, W.counter, cfg->window, W.o, s));
+                            W.part, W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s));
     } else {
       rec.stage("attn");
       TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,

@@ -103,7 +103,7 @@ typedef struct {
   const void *g_attn, *wq, *wk, *wv, *wo, *g_mlp, *w1, *w3, *w2;
 } tb_block_weights;
 
-/* KV cache of post-RoPE keys and values, in one of three layouts.
+/* KV cache of post-RoPE keys and values, in one of four layouts.
  *  Contiguous (block_table == NULL, dtype == cfg.dtype):
  *    k, v  : device, cfg.dtype, [B, Hkv, T_max, dh] each, row-major.
  *  Paged (block_table != NULL), the cache allocated per sequence in fixed-size
@@ -123,6 +123,10 @@ typedef struct {
  *    q = round-half-even(x / s) clamped to [-127, 127], s and x / s evaluated
  *    in fp32 (a zero row: s = 0, q = 0); it reads back as q·s.  Only a bf16
  *    block with dh = 128 and T_max a multiple of 32 takes an int8 cache.
+ *  Paged int8 (dtype == TB_I8, block_table != NULL): the int8 layout in page
+ *  pools, k, v codes [num_pages, Hkv, page_size, dh] and k_scale, v_scale
+ *  [num_pages, Hkv, page_size], with the paged layout's block table and
+ *  page_size a multiple of 32.
  *    Prefill attends over the unquantised rows and stores their codes; a
  *    decode step stores the new token's codes first, then attends over the
  *    dequantised rows, its own included.

@@ -134,8 +134,9 @@ def test_append_argument_checks(lib):
 
 
 def test_int8_cache_checks(lib):
-    """An int8 cache takes a bf16 block with dh 128, a contiguous layout, T_max a
-    multiple of 16 and both scale arrays; anything else is refused before a launch."""
+    """An int8 cache takes a bf16 block with dh 128, T_max a multiple of 32, both
+    scale arrays and, paged, a page size that is a multiple of 32; anything else
+    is refused before a launch."""
     c = cfg(d=512, H=4, Hkv=2, dh=128)
     decode = lambda kv, cc=c: lib.tb_block_decode(ctypes.byref(cc), FAKE, FAKE, FAKE + 4096, 0, ctypes.byref(kv),
                                                   FAKE, 1 << 30, None)
@@ -145,7 +146,9 @@ def test_int8_cache_checks(lib):
     assert decode(i8(ks=None)) == 1 and b"k_scale" in lib.tb_last_error_message()
     assert decode(i8(vs=FAKE + 4)) == 1                       # misaligned scales
     assert decode(i8(T_max=240)) == 2                         # T_max not a multiple of 32
-    assert decode(i8(bt=FAKE, ps=16, np=8)) == 2              # no paged int8 layout
+    assert decode(i8(bt=FAKE, ps=16, np=8)) == 2              # paged: page_size not a multiple of 32
+    assert b"page_size" in lib.tb_last_error_message()
+    assert lib.tb_kvcache_append(ctypes.byref(i8(bt=FAKE, ps=48, np=8, T_max=96)), FAKE, FAKE, 3, None) == 2
     assert decode(i8(), cfg(d=512, H=4, Hkv=2, dh=128, dtype=tb.TB_F32)) == 2   # fp32 block
     assert decode(i8(dh=64), cfg()) == 2                      # dh 64
     # append: bf16 rows into the int8 layout, same rules

@@ -263,3 +263,117 @@ def test_int8_decode_full_workload_sampled_sequences():
     for b, g, r in zip(sampled, got, refs):
         e = errors(g, r)
         assert e["finite"] and e["rel_l2"] <= 1e-2 and e["max_abs"] <= bound, (b, e, bound)
+
+
+# ---- paged int8 caches: the int8 layout in page pools ------------------------
+
+def _paged_copy(kv, ps, seed):
+    """The rows of a contiguous int8 cache in shuffled page pools (a few spare
+    pages, zero codes and NaN scales outside the table)."""
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    B, Hkv, T_max, dh = kv.k.shape
+    per = T_max // ps
+    num_pages = B * per + 3
+    perm = np.random.default_rng(seed).permutation(num_pages)[:B * per].reshape(B, per)
+    codes = lambda: torch.zeros((num_pages, Hkv, ps, dh), dtype=torch.int8, device="cuda")
+    scales = lambda: torch.full((num_pages, Hkv, ps), float("nan"), dtype=torch.float32, device="cuda")
+    pk, pv, pks, pvs = codes(), codes(), scales(), scales()
+    for b in range(B):
+        for p in range(per):
+            sl = slice(p * ps, (p + 1) * ps)
+            pk[perm[b, p]], pv[perm[b, p]] = kv.k[b, :, sl], kv.v[b, :, sl]
+            pks[perm[b, p]], pvs[perm[b, p]] = kv.k_scale[b, :, sl], kv.v_scale[b, :, sl]
+    return tb.KVCache(pk, pv, kv.lens.clone(), torch.tensor(perm, dtype=torch.int32, device="cuda"), pks, pvs)
+
+
+def _assert_same_rows(paged, contig, n_of):
+    """Every sequence's first n_of[b] rows, gathered through the block table,
+    equal the contiguous cache's: codes and scales bit for bit."""
+    bt = paged.block_table.cpu().numpy()
+    ps = paged.k.shape[2]
+    for b, n in enumerate(n_of):
+        for name, pc, cc in (("k", paged.k, contig.k), ("v", paged.v, contig.v),
+                             ("k_scale", paged.k_scale, contig.k_scale), ("v_scale", paged.v_scale, contig.v_scale)):
+            pool, want = pc.cpu().numpy(), cc[b, :, :n].cpu().numpy()
+            if pool.ndim == 3:                   # scale pools: one value per row
+                pool, want = pool[..., None], want[..., None]
+            got = oracle.gather_paged(pool, bt[b], ps, n)
+            np.testing.assert_array_equal(got, want, err_msg=f"{name} b={b}")
+
+
+@pytest.mark.parametrize("ps", [32, 128])
+@pytest.mark.parametrize("W", [0, 100])
+def test_paged_int8_decode_equals_contiguous(ps, W):
+    """Same kernels, same arithmetic: a decode step over the paged pools gives
+    the contiguous int8 cache's output and appended rows bit for bit."""
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    T_max = 512
+    lens = [0, 31, 32, 300, 510]
+    s = BASE.with_(B=len(lens), window=W, T=T_max)
+    inp = workloads.make_block_inputs(s, seed=41)
+    contig, _ = _int8_cache(s, 41, lens, T_max)
+    paged = _paged_copy(contig, ps, seed=ps + W)
+    cfg = block_config(s, max_pos=T_max)
+    dev = to_device(inp)
+    packed = tb.tb_pack_weights(cfg, dev)
+    for x in (dev["x"], workloads.make_block_inputs(s, seed=42)["x"].cuda()):     # two steps
+        y_c = tb.tb_block_decode(cfg, packed, x, contig)
+        y_p = tb.tb_block_decode(cfg, packed, x, paged)
+        assert tb.tb_get_device_error(clear=True) == 0
+        assert torch.equal(y_p, y_c)
+        assert torch.equal(paged.lens, contig.lens)
+    _assert_same_rows(paged, contig, [n + 2 for n in lens])
+
+
+def test_paged_int8_prefill_and_append_equal_contiguous():
+    """Prefill into paged int8 pools, then append rows: the pools hold the
+    contiguous int8 cache's codes and scales, and the outputs are equal."""
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    T, T_max, ps = 200, 256, 64
+    s = BASE.with_(mode="prefill", B=2, T=T, window=0)
+    inp = workloads.make_block_inputs(s, seed=13)
+    cfg = block_config(s, max_pos=T_max)
+    dev = to_device(inp)
+    packed = tb.tb_pack_weights(cfg, dev)
+    contig = tb.KVCache.empty_int8(s.B, s.Hkv, T_max, s.dh)
+    paged = _paged_copy(contig, ps, seed=5)
+    y_c = tb.tb_block_prefill(cfg, packed, dev["x"], kv=contig)
+    y_p = tb.tb_block_prefill(cfg, packed, dev["x"], kv=paged)
+    assert tb.tb_get_device_error(clear=True) == 0
+    assert torch.equal(y_p, y_c)
+    g = torch.Generator().manual_seed(6)
+    kn = torch.randn(s.B, s.Hkv, 40, s.dh, generator=g).to(torch.bfloat16).cuda()
+    vn = torch.randn(s.B, s.Hkv, 40, s.dh, generator=g).to(torch.bfloat16).cuda()
+    tb.tb_kvcache_append(contig, kn, vn)
+    tb.tb_kvcache_append(paged, kn, vn)
+    assert tb.tb_get_device_error(clear=True) == 0
+    assert paged.lens.tolist() == contig.lens.tolist() == [T + 40] * s.B
+    _assert_same_rows(paged, contig, [T + 40] * s.B)
+
+
+def test_paged_int8_bad_page_is_flagged():
+    """A block-table entry outside the pool is never dereferenced by the
+    quantiser or the attention: the step sets TB_DEVERR_BAD_PAGE and the
+    context stays usable."""
+    import causal_gqa_attention_rmsnorm_gb300 as tb
+    T_max, ps = 256, 64
+    lens = [10, 100, 200, 70]
+    s = BASE.with_(T=T_max)
+    inp = workloads.make_block_inputs(s, seed=2)
+    contig, _ = _int8_cache(s, 2, lens, T_max)
+    paged = _paged_copy(contig, ps, seed=3)
+    good = paged.block_table.clone()
+    bad = good.clone()
+    bad[2, 1] = 10 ** 6                          # sequence 2's second page: outside the pool
+    bad[1, 1] = -1                               # sequence 1's new row lands in a bad page
+    paged.block_table.copy_(bad)
+    cfg = block_config(s, max_pos=T_max)
+    dev = to_device(inp)
+    packed = tb.tb_pack_weights(cfg, dev)
+    tb.tb_block_decode(cfg, packed, dev["x"], paged)
+    assert tb.tb_get_device_error(clear=True) & tb.TB_DEVERR_BAD_PAGE
+    paged.block_table.copy_(good)
+    paged.lens.copy_(torch.tensor(lens, dtype=torch.int32))
+    y_p = tb.tb_block_decode(cfg, packed, dev["x"], paged)
+    assert tb.tb_get_device_error(clear=True) == 0
+    assert torch.isfinite(y_p).all()
