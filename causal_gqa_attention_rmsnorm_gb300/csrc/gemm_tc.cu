@@ -556,13 +556,16 @@ cudaError_t run(const void* A, const void* B, int M, int N, int K, const Epi& ep
   return cudaGetLastError();
 }
 
-// CTA pairs when the 256-row tiles fill at least two waves of pairs (one
+// CTA pairs when the 256-row tiles fill at least two waves of clusters (one
 // cluster per two SMs).  Measured on the prefill of 32768 tokens at d = 4096
 // against single-CTA tiles: Wo 1445-1463 -> 1671-1680 TFLOP/s, W2 (single CTAs
-// with two row blocks each) 1698-1712 -> 1832-1844, W1/W3 1758-1775 -> 1780-1789.
+// with two row blocks each) 1698-1712 -> 1832-1844, W1/W3 1758-1775 ->
+// 1780-1789; on 4096 tokens (256 tiles of Wo and of W2): Wo 1165 -> 1325, W2
+// 1367 -> 1586.  With 96 tiles (768 columns, 8192 tokens) Wo ran slower on pairs
+// (277 -> 220), so fewer tiles keep single CTAs.
 bool pair_fits(int M, int N) {
   const long tiles = (long)((M + 2 * BM - 1) / (2 * BM)) * ((N + 255) / 256);
-  return M >= 2 * BM && tiles >= 2L * sm_count();
+  return M >= 2 * BM && tiles >= (long)sm_count();
 }
 
 // Narrow N tiles when the grid would not fill the GPU.
