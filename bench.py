@@ -35,8 +35,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Token count up to which each bf16 GEMM runs as a K-split kernel plus a
-# partial-sum epilogue kernel (two launches instead of one).
+# Token count up to which each bf16 GEMM runs as the few-token GEMM (one
+# launch each, its K split reduced inside a cluster).
 FEW_TOKENS = 64
 
 
@@ -46,10 +46,17 @@ METRIC = "prefill tokens/s per block (attention TFLOP/s, GEMM TFLOP/s; decode KV
 
 def decode_launches(B: int) -> int:
     """Kernels one bf16 decode step launches: the two attention kernels and
-    the four GEMMs, each with its partial-sum epilogue when the batch takes the
-    few-token GEMM (whose QKV epilogue also forms the row statistics); above
-    that, the tile GEMMs and the row-statistics kernel."""
-    return 2 + 4 * 2 if B <= FEW_TOKENS else 3 + 4
+    the four GEMMs (the few-token GEMM, whose QKV instance also forms the row
+    statistics, when the batch takes it; above that, the tile GEMMs and the
+    row-statistics kernel)."""
+    return 2 + 4 if B <= FEW_TOKENS else 3 + 4
+
+
+def prefill_launches(tokens: int) -> int:
+    """Kernels one bf16 prefill launches: the four GEMMs and the attention (the
+    tile QKV GEMM forms the row statistics); with few tokens the
+    row-statistics kernel runs first."""
+    return 5 if tokens > FEW_TOKENS else 6
 
 
 def load_peaks():
@@ -339,7 +346,7 @@ def bench_prefill(args, s, world, peaks):
         del xs, ys
     del ws
     return {"ms_total": ms_total, "stages": stages, "clocks": clk, "e2e": e2e,
-            "launches_per_step": 6 if s.B * s.T > FEW_TOKENS else 10}
+            "launches_per_step": prefill_launches(s.B * s.T)}
 
 
 # DRAM bytes (read + write) per launch of a kernel at the benchmark workload,
@@ -510,6 +517,7 @@ def bench_window(args, world, peaks):
     ms, st = timed(lambda: tb.tb_block_prefill(cfg, packed, dev["x"], y=y, ws=ws))
     assert torch.isfinite(y).all().item()
     fl = acc.causal_attn_flops(s.B, s.H, s.dh, s.T, W)
+    pre_tokens = s.B * s.T
     pre = {"workload": s.name, "ms_per_step": ms, "tok_s": world * s.B * s.T / (ms * 1e-3),
            "attn_ms": st["attn"], "attn_flops": fl, "attn_tflops": fl / (st["attn"] * 1e-3) / 1e12,
            "attn_frac_bf16": fl / (st["attn"] * 1e-3) / 1e12 / peaks["bf16_tflops"]}
@@ -536,7 +544,8 @@ def bench_window(args, world, peaks):
     dec = {"workload": s.name, "step_ms": ms, "tok_s": world * s.B / (ms * 1e-3), "attn_ms": st["attn"],
            "kv_bytes": kv_bytes, "kv_gbs": kv_bytes / (st["attn"] * 1e-3) / 1e9,
            "kv_frac_hbm": kv_bytes / (st["attn"] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
-    return {"window": W, "prefill": pre, "decode": dec, "gpu_launches": (6 + decode_launches(s.B)) * n}
+    return {"window": W, "prefill": pre, "decode": dec,
+            "gpu_launches": (prefill_launches(pre_tokens) + decode_launches(s.B)) * n}
 
 
 def bench_paged(args, world, peaks):
@@ -773,7 +782,8 @@ def bench_stack(args, world, peaks):
     dms = ev[0].elapsed_time(ev[1]) / m
     dec = {"workload": sd.name, "layers": L, "step_ms": dms, "tok_s": world * sd.B / (dms * 1e-3)}
     return {"prefill": pre, "decode": dec,
-            "gpu_launches": n * (1 + 6 * L + 3 * (tokens + 4095) // 4096) + m * (1 + decode_launches(sd.B) * L + 3)}
+            "gpu_launches": n * (1 + prefill_launches(tokens) * L + 3 * (tokens + 4095) // 4096)
+                            + m * (1 + decode_launches(sd.B) * L + 2)}
 
 
 def ctypes_cfg(cfg):

@@ -464,8 +464,8 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
 
   StageRecorder rec(s);
   // Few tokens on the bf16 path: RMSNorm-1's statistics, the positions and
-  // the step's counters are formed in the QKV GEMM's partial-sum epilogue,
-  // and the cache lengths advance in the Wo one; otherwise the row-statistics
+  // the step's counters are formed in the few-token QKV GEMM's epilogue, and
+  // the cache lengths advance in the Wo one; otherwise the row-statistics
   // kernel does all of it first.
   const bool fused_stats = dt == TB_BF16 && W.few;
   if (!fused_stats) {

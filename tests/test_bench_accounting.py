@@ -48,8 +48,15 @@ def test_roofline_entry_for_a_bandwidth_stage():
 
 
 def test_decode_launch_counts():
-    # the decode attention and its merge, and four GEMMs each followed by its
-    # partial-sum epilogue (the QKV one forms the row statistics) when the batch
-    # takes the few-token GEMM; above that, row statistics and four tile GEMMs
-    assert bench.decode_launches(32) == 2 + 4 * 2
+    # the decode attention and its merge, and the four few-token GEMMs (the QKV
+    # one forms the row statistics) when the batch takes them; above that, row
+    # statistics and four tile GEMMs
+    assert bench.decode_launches(32) == 2 + 4
     assert bench.decode_launches(bench.FEW_TOKENS + 1) == 3 + 4
+
+
+def test_prefill_launch_counts():
+    # four GEMMs and the attention (the tile QKV GEMM forms the row
+    # statistics); with few tokens the row-statistics kernel first
+    assert bench.prefill_launches(4 * 8192) == 5
+    assert bench.prefill_launches(bench.FEW_TOKENS) == 6

@@ -29,7 +29,7 @@ def _prefill_twice(s, seed):
     # 8192 tokens at d = 4096: the Wo, W1/W3 and W2 GEMMs on CTA pairs, attention on CTA pairs
     ("pair", workloads.BlockShape("det_pair", "prefill", "bf16", B=1, T=8192, d=4096, H=32, Hkv=8, dh=128,
                                   f=4096, rope_base=5e5, eps=1e-5, gains="normal")),
-    # few-token GEMM (K-split partials, then the partial-sum epilogue)
+    # few-token GEMM (K split over the CTAs of a cluster, reduced in distributed shared memory)
     ("skinny", workloads.BlockShape("det_few", "prefill", "bf16", B=3, T=7, d=2048, H=16, Hkv=4, dh=128, f=1024,
                                     rope_base=1e4, eps=1e-6, gains="normal")),
     # fp32 SIMT GEMM
