@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
     k_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const bf16* __restrict__ q, const int32_t* __restrict__ pos_arr, int B, int Hkv,
                  float* __restrict__ part, int nchunk_max, int chunk, int* __restrict__ counter, int window,
-                 PagedKV pg, float scale_log2, int* err) {
+                 PagedKV pg, float scale_log2, int* err, L2Prefetch pf) {
   pdl_trigger();
   pdl_wait();
   using C = MCfg<DH>;
@@ -602,6 +602,10 @@ __global__ void __launch_bounds__(kMWarps * 32, 1)
       --pidx;
     }
   }
+  // this warp's share of the next kernel's weights, pulled into L2 while the
+  // other warps finish their last items
+  if (ok && lane == 0 && pf.bytes)
+    prefetch_l2_part(pf.p, pf.bytes, blockIdx.x * kMWarps + warp, gridDim.x * kMWarps);
   // copies issued but not consumed (only after an aborted wait) must land before the CTA exits
   issued = __shfl_sync(0xffffffffu, issued, 0);
   if (!ok && lane == 0) {
@@ -732,7 +736,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
                 const float* __restrict__ kscale, const float* __restrict__ vscale, const bf16* __restrict__ q,
                 const int32_t* __restrict__ pos_arr, int B, int Hkv, int T_max, float* __restrict__ part,
                 int nchunk_max, int chunk, int* __restrict__ counter, int window, PagedKV pg, float scale_log2,
-                int* err) {
+                int* err, L2Prefetch pf) {
   pdl_trigger();
   pdl_wait();
   constexpr int DH = 128, S = kQSlots;
@@ -1051,6 +1055,8 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
       }
     }
   }
+  if (ok && lane == 0 && pf.bytes)     // this warp's share of the next kernel's weights, into L2
+    prefetch_l2_part(pf.p, pf.bytes, blockIdx.x * kQWarps + warp, gridDim.x * kQWarps);
   issued = __shfl_sync(0xffffffffu, issued, 0);
   if (!ok && lane == 0) {      // copies issued but not consumed must land before the CTA exits
     volatile int no_abort = 0;
@@ -1061,7 +1067,8 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
 template <int G>
 cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
                           const int32_t* pos, int B, int Hkv, int T_max, float* part, int nchunk_max, int chunk,
-                          int* counter, int window, const PagedKV& pg, void* o, cudaStream_t s) {
+                          int* counter, int window, const PagedKV& pg, void* o, cudaStream_t s,
+                          const L2Prefetch& pf) {
   using C = QCfg;
   CUtensorMap tk, tv;
   // contiguous: (sequence, KV head) planes of T_max rows; paged: (page, KV head) planes of page_size rows
@@ -1083,7 +1090,7 @@ cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const f
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
   e = launch_pdl(k_decode_i8<G>, dim3(sm_count()), dim3(kQWarps * 32), smem, s, tk, tv, ks, vs, (const bf16*)q, pos, B,
-                 Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, scale_log2, device_error_word());
+                 Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, scale_log2, device_error_word(), pf);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_decode_combine<bf16, 128>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
                     nchunk_max, chunk, window, kQKeys, (bf16*)o);
@@ -1092,7 +1099,7 @@ cudaError_t run_stream_i8(const void* q, const void* kc, const void* vc, const f
 template <int DH, int G>
 cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv, int T_max,
                        float* part, int nchunk_max, int chunk, int* counter, int window, const PagedKV& pg, void* o,
-                       cudaStream_t s) {
+                       cudaStream_t s, const L2Prefetch& pf) {
   using C = MCfg<DH>;
   CUtensorMap tk, tv;
   // planes of rows: (sequence, KV head) planes of T_max rows, or (page, KV head) planes of page_size rows
@@ -1117,7 +1124,7 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
   e = launch_pdl(k_decode_mma<DH, G>, dim3(sm_count()), dim3(kMWarps * 32), smem, s, tk, tv, (const bf16*)q, pos, B,
-                 Hkv, part, nchunk_max, chunk, counter, window, pg, scale_log2, device_error_word());
+                 Hkv, part, nchunk_max, chunk, counter, window, pg, scale_log2, device_error_word(), pf);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_decode_combine<bf16, DH>, dim3(Hkv * G, B), dim3(256), 0, s, (const float*)part, pos, Hkv * G,
                     nchunk_max, chunk, window, kMKeys, (bf16*)o);
@@ -1126,16 +1133,16 @@ cudaError_t run_stream(const void* q, const void* kc, const void* vc, const int3
 template <int DH>
 cudaError_t stream_by_g(int G, const void* q, const void* kc, const void* vc, const int32_t* pos, int B, int Hkv,
                         int T_max, float* part, int nchunk_max, int chunk, int* counter, int window, const PagedKV& pg,
-                        void* o, cudaStream_t s) {
+                        void* o, cudaStream_t s, const L2Prefetch& pf) {
   switch (G) {
     case 1: return run_stream<DH, 1>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, o,
-                                         s);
+                                         s, pf);
     case 2: return run_stream<DH, 2>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, o,
-                                         s);
+                                         s, pf);
     case 4: return run_stream<DH, 4>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, o,
-                                         s);
+                                         s, pf);
     case 8: return run_stream<DH, 8>(q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, counter, window, pg, o,
-                                         s);
+                                         s, pf);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1201,17 +1208,18 @@ int decode_chunk_keys_sms(int dtype, int B, int Hkv, int T_max, int sms) {
 
 cudaError_t attn_decode_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
                            const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max, int chunk,
-                           int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s) {
+                           int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s,
+                           const L2Prefetch& pf) {
   if (chunk % kQKeys || (pg.bt && pg.ps % kQKeys)) return cudaErrorInvalidValue;
   switch (H / Hkv) {
     case 1: return run_stream_i8<1>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
-                                         window, pg, o, s);
+                                         window, pg, o, s, pf);
     case 2: return run_stream_i8<2>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
-                                         window, pg, o, s);
+                                         window, pg, o, s, pf);
     case 4: return run_stream_i8<4>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
-                                         window, pg, o, s);
+                                         window, pg, o, s, pf);
     case 8: return run_stream_i8<8>(q, kc, vc, ks, vs, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter,
-                                         window, pg, o, s);
+                                         window, pg, o, s, pf);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1222,14 +1230,16 @@ size_t decode_part_floats(int B, int H, int dh, int nchunk_max) {
 
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos, int B,
                         int H, int Hkv, int dh, int T_max, float* part, int nchunk_max, int chunk, int* work_counter,
-                        int window, const PagedKV& pg, void* o, cudaStream_t s) {
+                        int window, const PagedKV& pg, void* o, cudaStream_t s, const L2Prefetch& pf) {
   const int G = H / Hkv;
   if (dtype == TB_F32) return by_dh<float>(dh, G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, window, pg, o, s);
   if (chunk % kMKeys) return cudaErrorInvalidValue;
   if (dh == 128)
-    return stream_by_g<128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter, window, pg, o, s);
+    return stream_by_g<128>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter, window, pg, o, s,
+                            pf);
   if (dh == 64)
-    return stream_by_g<64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter, window, pg, o, s);
+    return stream_by_g<64>(G, q, kc, vc, pos, B, Hkv, T_max, part, nchunk_max, chunk, work_counter, window, pg, o, s,
+                           pf);
   return cudaErrorInvalidValue;
 }
 

@@ -130,6 +130,13 @@ struct PagedKV {
   int* err = nullptr;
 };
 
+// A byte range that a kernel pulls into L2 after its own work, for the next
+// kernel on the stream (p 16-byte aligned; bytes 0: none).
+struct L2Prefetch {
+  const void* p = nullptr;
+  unsigned long long bytes = 0;
+};
+
 // Row offset (in rows of dh values) of key t of (sequence b, KV head h) in a
 // paged pool, or -1 for a bad page id (flagged in the error word).
 __device__ __forceinline__ long long paged_row(const PagedKV& p, int Hkv, int b, int h, int t) {
@@ -321,11 +328,13 @@ int decode_chunk_keys_sms(int dtype, int B, int Hkv, int T_max, int sms);   // t
 size_t decode_part_floats(int B, int H, int dh, int nchunk_max);
 cudaError_t attn_decode(int dtype, const void* q, const void* kc, const void* vc, const int32_t* pos,
                         int B, int H, int Hkv, int dh, int T_max, float* part, int nchunk_max, int chunk,
-                        int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s);
+                        int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s,
+                        const L2Prefetch& pf = L2Prefetch());
 // Decode over an int8 cache (dh 128): codes kc, vc [B, Hkv, T_max, 128], row
 // scales ks, vs [B, Hkv, T_max]; bf16 q and o.
 cudaError_t attn_decode_i8(const void* q, const void* kc, const void* vc, const float* ks, const float* vs,
                            const int32_t* pos, int B, int H, int Hkv, int T_max, float* part, int nchunk_max,
-                           int chunk, int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s);
+                           int chunk, int* work_counter, int window, const PagedKV& pg, void* o, cudaStream_t s,
+                           const L2Prefetch& pf = L2Prefetch());
 
 }  // namespace tb

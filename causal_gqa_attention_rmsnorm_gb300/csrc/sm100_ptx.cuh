@@ -103,6 +103,24 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
   return __all_sync(0xffffffffu, ok);
 }
 
+// Pull [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
+// Part i of n of the 16-byte units of [p, p + bytes), pulled into L2 in pieces
+// of at most 64 KB.
+__device__ __forceinline__ void prefetch_l2_part(const void* p, unsigned long long bytes, int i, int n) {
+  const unsigned long long units = bytes >> 4, per = (units + (unsigned long long)n - 1) / (unsigned long long)n;
+  unsigned long long u = per * (unsigned long long)i;
+  const unsigned long long end = u + per < units ? u + per : units;
+  for (; u < end; u += 4096) {
+    const unsigned long long len = end - u < 4096 ? end - u : 4096;
+    prefetch_l2_bulk(static_cast<const uint8_t*>(p) + (u << 4), (uint32_t)(len << 4));
+  }
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

@@ -502,16 +502,21 @@ tb_status tb_block_decode(const tb_block_cfg* cfg, const void* packed, const voi
   } else {
     rec.stage("qkv");
     TB_TRY(mm_qkv(W, x, P.wqkv, B, nqkv, cfg->d, D, qa, s));
+    // The attention kernels end by pulling Wo's weights into L2, so that the
+    // Wo GEMM that follows reads them from there: the last items of the
+    // attention leave HBM idle, the GEMM's first loads would wait on it.
+    L2Prefetch wo_pf;
+    if (!((uintptr_t)P.wo & 15u)) wo_pf = L2Prefetch{P.wo, (unsigned long long)cfg->d * cfg->H * cfg->dh * 2ull};
     if (i8) {
       rec.stage("quant");
       TB_TRY(launch_quantize_kv(*kv, W.k, W.v, 1, W.pos, s));
       rec.stage("attn");
       TB_TRY(attn_decode_i8(W.q, kv->k, kv->v, kv->k_scale, kv->v_scale, W.pos, B, cfg->H, cfg->Hkv, kv->T_max,
-                            W.part, W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s));
+                            W.part, W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s, wo_pf));
     } else {
       rec.stage("attn");
       TB_TRY(attn_decode(dt, W.q, kv->k, kv->v, W.pos, B, cfg->H, cfg->Hkv, cfg->dh, kv->T_max, W.part,
-                         W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s));
+                         W.nchunk_max, W.chunk, W.counter, cfg->window, pg, W.o, s, wo_pf));
     }
     rec.stage("wo");
     TB_TRY(mm_wo(W, W.o, P.wo, B, cfg->d, cfg->H * cfg->dh, D, wa, s, &ga.ssq.n));
