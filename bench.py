@@ -355,15 +355,12 @@ def bench_prefill(args, s, world, peaks):
             "launches_per_step": prefill_launches(s.B * s.T)}
 
 
-# DRAM bytes (read + write) per launch of a kernel at the benchmark workload,
-# from one ncu capture of the current kernel (see profiles/): the W13 GEMM was
-# captured at B = 1 (543.6 MB read + 222.6 MB write) and every term (A once,
-# the weight panel once per 32-row-block group, the output once) grows with the
-# row count, so a B = 4 launch moves 4x that.
 # DRAM read + write of one launch of the stage's kernel, from a one-pass ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum) of the benchmark's own
-# launch (profiles/gemm_w13_gqa_8k.md).
-NCU_TRAFFIC = {("gqa_8k", "w13"): 5.901e9 + 930.05e6}
+# launches: the mean of the two timed W1/W3 launches in
+# profiles/prefill_gqa_8k_launches.md.  The reads vary from box to box
+# (profiles/gemm_w13_gqa_8k.md).
+NCU_TRAFFIC = {("gqa_8k", "w13"): (4454309888 + 4500537856 + 927719936 + 928212736) / 2}
 
 
 def roofline_entry(stages, work, peaks, peak_src, workload):
