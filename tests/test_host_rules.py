@@ -3,6 +3,7 @@ its test hooks: the few-token GEMM's K-split count (its cluster size) and the
 decode work-item size.  Each hook takes the SM count, so the GB300's 152 SMs
 can be given here."""
 import itertools
+import os
 import random
 
 import pytest
@@ -15,6 +16,8 @@ MAX_CLUSTER = 8        # a portable thread-block cluster
 
 @pytest.fixture(scope="module")
 def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        pytest.skip("libtb.so not built")
     return binding.lib()
 
 
